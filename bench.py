@@ -1,0 +1,443 @@
+#!/usr/bin/env python
+"""Benchmark of one decode step of the paged KV-cache path on GB300.
+
+A step is the whole hot path for one attention layer of a decode batch:
+copy-on-write block copies (when the workload has any), slot mapping of the
+new tokens, the slot-mapped KV write, and paged decode attention (partition
+kernel + split-K reduce).  Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle, timed on host cores
+
+Under torchrun every rank runs its own replica of the workload on its own GPU
+(weak scaling, no collective on the data path); the value is the sum of all
+ranks' bytes over the slowest rank's time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention KV GB/s (% of GB300 HBM peak); decode tokens/s per layer"
+DEFAULT_WORKLOAD = "qwen3_0_6b"
+KERNEL_SRC = ["paged_kv_cache_115_gb300/csrc/pkv_attention.cuh",
+              "paged_kv_cache_115_gb300/csrc/pkv_device.cuh"]
+
+
+def kernel_src_sha() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SRC:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def read_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+def read_traffic():
+    """DRAM bytes per attention launch from the committed ncu summary, valid
+    only while the kernel source is unchanged since the capture."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "attention_traffic.json")) as f:
+            t = json.load(f)
+    except OSError:
+        return None
+    if t.get("kernel_src_sha") != kernel_src_sha():
+        return None
+    return t
+
+
+def workload_desc(w) -> dict:
+    import numpy as np
+    return {
+        "workload": w.name,
+        "num_seqs": w.num_seqs,
+        "num_q_heads": w.num_q_heads,
+        "num_kv_heads": w.num_kv_heads,
+        "head_dim": w.head_dim,
+        "block_size": w.block_size,
+        "num_blocks": w.num_blocks,
+        "context_lens": {"min": int(w.context_lens.min()), "max": int(w.context_lens.max()),
+                         "mean": float(np.mean(w.context_lens)), "sum": int(w.context_lens.sum())},
+        "copy_pairs": int(len(w.copy_pairs)),
+        "new_tokens": int((w.positions >= 0).sum()),
+        "step": ("kv_block_copy + " if len(w.copy_pairs) else "")
+        + "slot_mapping + paged_kv_write + paged_attention_decode (partition + split-K reduce)",
+    }
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.lines = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle baseline (the only place bench.py runs the oracle)
+# ---------------------------------------------------------------------------
+def _cpu_sample(name: str, seed: int, budget_s: float) -> dict:
+    import numpy as np
+    import torch
+    import oracle
+    from paged_kv_cache_115_gb300 import accounting, workloads as wl
+
+    full = wl.build(name, seed=seed)
+    order = list(range(full.num_seqs))
+    done_bytes, done_tokens, done_seqs, elapsed = 0, 0, 0, 0.0
+    H_kv, D = full.num_kv_heads, full.head_dim
+    eb = full.elem_bytes
+    for s in order:
+        L = int(full.context_lens[s])
+        sub = wl.build_decode("sample", [L], full.num_q_heads, H_kv, D, full.block_size,
+                              full.dtype, seed=seed + s)
+        t = wl.materialize(sub, seed=seed + s, canary=False)
+
+        def st(x):
+            x = x.contiguous()
+            return x.view(torch.int16).numpy().view(np.uint16) if x.dtype == torch.bfloat16 \
+                else x.numpy()
+        q, kc, vc = st(t["q"]), st(t["k_cache"]), st(t["v_cache"])
+        t0 = time.perf_counter()
+        slots = oracle.slot_mapping(sub.block_tables, sub.positions, sub.block_size)
+        kc, vc = oracle.kv_write(kc, vc, st(t["k_new"]), st(t["v_new"]), slots)
+        oracle.paged_attention_decode(q, kc, vc, sub.block_tables, sub.context_lens, sub.scale,
+                                      sub.dtype)
+        elapsed += time.perf_counter() - t0
+        done_bytes += accounting.attention_kv_bytes([L], H_kv, D, eb)
+        done_tokens += 1
+        done_seqs += 1
+        if elapsed >= budget_s:
+            break
+    return {"bytes": done_bytes, "seconds": elapsed, "seqs": done_seqs,
+            "of_seqs": full.num_seqs, "tokens": int(sum(full.context_lens[:done_seqs]))}
+
+
+def run_cpu_baseline(name: str, seed: int, budget_s: float) -> dict:
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[k] = "1"
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    code = ("import json,sys; sys.path.insert(0, %r); import bench; "
+            "print(json.dumps(bench._cpu_sample(%r, %d, %f)))" % (ROOT, name, seed, budget_s))
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
+                       cwd=ROOT, timeout=max(600, budget_s * 20))
+    if r.returncode != 0:
+        raise RuntimeError("cpu baseline failed: " + r.stderr[-2000:])
+    res = json.loads(r.stdout.strip().splitlines()[-1])
+    gbs = res["bytes"] / res["seconds"] / 1e9
+    return {
+        "value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+        "seconds": res["seconds"],
+        "decode_tokens_per_s_per_layer": res["seqs"] / res["seconds"],
+        "sample": (f"fp64 numpy oracle (slot mapping + KV write + attention), single-threaded, "
+                   f"on the first {res['seqs']} of {res['of_seqs']} sequences of {name} "
+                   f"({res['tokens']} cached tokens, {res['bytes'] / 1e6:.1f} MB of KV)"),
+    }
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def run_gpu(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
+    torch.cuda.set_device(dev)
+
+    from paged_kv_cache_115_gb300 import accounting, build, workloads as wl
+    if rank == 0 or world == 1:
+        build.build()
+    if world > 1:
+        dist.barrier()
+    from paged_kv_cache_115_gb300 import ops
+
+    w = wl.build(args.workload, seed=args.seed + rank)
+    t = wl.materialize(w, device=dev, seed=args.seed + rank, canary=False, values_device="cuda")
+    kv_bytes = accounting.attention_kv_bytes(w.context_lens, w.num_kv_heads, w.head_dim,
+                                             w.elem_bytes)
+    stream = torch.cuda.current_stream(dev)
+    ws_bytes = ops.attention_workspace_bytes(w.num_seqs, w.num_q_heads, w.num_kv_heads,
+                                             w.head_dim, w.block_size, w.max_context_len,
+                                             t["q"].dtype)
+    workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    out = torch.empty_like(t["q"])
+    slots = torch.empty(w.num_seqs, dtype=torch.int64, device=dev)
+    has_copy = len(w.copy_pairs) > 0
+    max_len = w.max_context_len
+
+    def attention():
+        ops.paged_attention_decode(t["q"], t["k_cache"], t["v_cache"], t["block_tables"],
+                                   t["context_lens"], w.scale, out=out, max_context_len=max_len,
+                                   workspace=workspace)
+
+    def prologue():
+        if has_copy:
+            ops.kv_block_copy(t["k_cache"], t["v_cache"], t["copy_pairs"])
+        ops.slot_mapping(t["block_tables"], t["positions"], w.block_size, w.num_blocks, out=slots)
+        ops.paged_kv_write(t["k_new"], t["v_new"], slots, t["k_cache"], t["v_cache"])
+
+    # kernels launched per step (ours only)
+    attn_launches = ops.attention_launch_count(w.num_seqs, w.num_q_heads, w.num_kv_heads,
+                                               w.head_dim, w.block_size, max_len, t["q"].dtype)
+    launches_per_step = (1 if has_copy else 0) + 2 + attn_launches
+
+    for _ in range(max(args.warmup, 3)):
+        prologue()
+        attention()
+    torch.cuda.synchronize(dev)
+    assert ops.get_device_error(dev) == 0
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(dev.index) if rank == 0 else None
+    time.sleep(0.2 if clocks else 0)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    start.record(stream)
+    for i in range(K):
+        prologue()
+        ev[i][0].record(stream)
+        attention()
+        ev[i][1].record(stream)
+    stop.record(stream)
+    torch.cuda.synchronize(dev)
+    clock_info = clocks.stop() if clocks else None
+    if world > 1:
+        dist.barrier()
+    total_ms = start.elapsed_time(stop)
+    attn_ms = [a.elapsed_time(b) for a, b in ev]
+    attn_avg_ms = sum(attn_ms) / K
+    assert ops.get_device_error(dev) == 0
+
+    # ---- end to end through the public API with host buffers
+    pin = {k: t[k].cpu().pin_memory() for k in ("q", "k_new", "v_new", "block_tables",
+                                                 "context_lens", "positions")}
+    if has_copy:
+        pin["copy_pairs"] = t["copy_pairs"].cpu().pin_memory()
+    host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    h2d = sum(v.numel() * v.element_size() for v in pin.values())
+    d2h = host_out.numel() * host_out.element_size()
+    e2e_steps = max(1, min(K, 200))
+
+    def e2e_step():
+        for k, v in pin.items():
+            t[k].copy_(v, non_blocking=True)
+        prologue()
+        attention()
+        host_out.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+
+    # ---- max over ranks
+    vals = torch.tensor([total_ms, e2e_ms, attn_avg_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
+    total_ms, e2e_ms, attn_avg_ms = vals.tolist()
+    ms_step = total_ms / K
+    value = world * kv_bytes / (ms_step * 1e-3) / 1e9
+    e2e_value = world * kv_bytes / (e2e_ms * 1e-3) / 1e9
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return None
+
+    peaks, peak_src = read_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    achieved = kv_bytes / (attn_avg_ms * 1e-3) / 1e9
+    traffic = read_traffic()
+    cfg = workload_desc(w)
+    cfg["l2"] = (f"inputs larger than L2: {kv_bytes / 1e6:.0f} MB of KV read per step "
+                 f"vs 129 MB L2; no flush between steps")
+    cfg["parallelism"] = f"replicas x{world}" if world > 1 else "single GPU"
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": w.dtype,
+        "data": "synthetic: seeded N(0,1) q/k/v rounded to bf16; block tables from a seeded "
+                "shuffled free list; lengths drawn per the workload recipe",
+        "config": cfg,
+        "hbm_frac": value / world / hbm,
+        "decode_tokens_per_s_per_layer": world * w.num_seqs / (ms_step * 1e-3),
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "pkv_attention_decode (partition + split-K reduce)",
+            "achieved": achieved,
+            "peak": hbm,
+            "peak_source": f"{peak_src} hbm_gbs (copy, read+write)",
+            "unit": "GB/s",
+            "frac": achieved / hbm,
+            "algorithmic_bytes_per_launch": kv_bytes,
+            "avg_launch_ms": attn_avg_ms,
+            "traffic": traffic["bytes_per_launch"] if traffic else None,
+        },
+        "e2e": {"value": e2e_value, "unit": "GB/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "decode_tokens_per_s_per_layer": world * w.num_seqs / (e2e_ms * 1e-3)},
+        "gpu_launches": launches_per_step * K,
+        "clocks": clock_info,
+    }
+    if not args.no_cpu_baseline:
+        try:
+            line["cpu_baseline"] = run_cpu_baseline(args.workload, args.seed, args.cpu_budget)
+        except Exception as e:  # report, do not hide the GPU number
+            line["cpu_baseline"] = {"value": None, "error": str(e)[:300], "kind": "oracle"}
+    if world > 1:
+        dist.destroy_process_group()
+    return line
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the CPU oracle as it stands
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return None
+    from paged_kv_cache_115_gb300 import workloads as wl
+    w = wl.build(args.workload, seed=args.seed)
+    per_step = max(1.0, args.cpu_budget / max(1, args.steps))
+    for _ in range(args.warmup):
+        _cpu_sample(args.workload, args.seed, min(per_step, 1.0))
+    tot_bytes, tot_s, seqs = 0, 0.0, 0
+    for _ in range(args.steps):
+        r = _cpu_sample(args.workload, args.seed, per_step)
+        tot_bytes += r["bytes"]
+        tot_s += r["seconds"]
+        seqs += r["seqs"]
+    value = tot_bytes / tot_s / 1e9
+    cfg = workload_desc(w)
+    sample = (f"fp64 numpy oracle on the first sequences of {args.workload}, about "
+              f"{per_step:.0f} s of CPU work per step, {seqs} sequences in all")
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_s / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (same recipe as the GPU arm)", "config": cfg,
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["gpu", "reference"], default="gpu")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-budget", type=float, default=15.0,
+                    help="seconds of CPU work for the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.impl == "reference":
+        # the oracle runs single-threaded: set before numpy / torch load
+        for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+            os.environ[k] = "1"
+    if args.warmup < 3 and args.impl == "gpu":
+        args.warmup = 3
+    line = run_reference(args) if args.impl == "reference" else run_gpu(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

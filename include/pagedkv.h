@@ -1,0 +1,199 @@
+/*
+ * pagedkv.h — C ABI of the GB300 (sm_103a) paged KV-cache decode path.
+ *
+ * The library implements the device side of PagedAttention-style KV-cache
+ * management as the pages on the subject describe it:
+ *
+ *   "19.2 KV Cache 系统化管理" (book chapter 19.2): §19.2.2 block table and
+ *      copy-on-write, §19.2.3 the block pool layout, write_slot /
+ *      append_token and the block-wise online-softmax attention;
+ *   "推理与 KV Cache 02:分页、共享与回收如何协作", section
+ *      "从一个位置找到缓存块": logical block = floor(t/K), offset = t mod K,
+ *      token slot = physical_block * K + offset;
+ *   "KV Cache：长上下文为什么吃显存，PagedAttention 怎么救", §01 (the new
+ *      token's query attends to K_{1:t}, V_{1:t}) and §02 (GQA ratio).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Every pointer argument except `code` in pkv_get_device_error is a DEVICE
+ *   pointer to contiguous row-major memory owned by the caller.  The library
+ *   allocates nothing and frees nothing.
+ * - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *   Every compute call is asynchronous on that stream and returns once the
+ *   work is enqueued.
+ * - KV pool layout: k_cache and v_cache are [num_blocks, block_size,
+ *   num_kv_heads, head_dim] (the pool of §19.2.3, its head axis holding the KV
+ *   heads); seen as [num_blocks * block_size, num_kv_heads, head_dim] they are
+ *   indexed by token slot.
+ * - `dtype` is the storage type of q, k, v, the pools and out alike.
+ * - Arguments are validated on the host before anything is launched; a bad
+ *   argument returns PKV_ERR_INVALID_ARGUMENT or PKV_ERR_UNSUPPORTED and
+ *   launches nothing.  A failed launch returns PKV_ERR_CUDA.
+ * - Values that live on the device (block ids, slots, lengths, copy pairs)
+ *   are checked by the kernels: an out-of-range value is never dereferenced;
+ *   the offending element is skipped (attention treats an out-of-range block
+ *   as zeros) and a code is recorded in a per-device error word that
+ *   pkv_get_device_error reads.  No kernel traps.
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(PKV_BUILD) && defined(__GNUC__)
+#define PKV_API __attribute__((visibility("default")))
+#else
+#define PKV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PKV_OK = 0,
+  PKV_ERR_INVALID_ARGUMENT = 1,   /* null pointer, bad size, bad alignment  */
+  PKV_ERR_UNSUPPORTED = 2,        /* shape/dtype this build does not handle */
+  PKV_ERR_WORKSPACE_TOO_SMALL = 3,
+  PKV_ERR_CUDA = 4,               /* a CUDA runtime call or launch failed   */
+  PKV_ERR_DEVICE_CHECK = 5        /* returned by pkv_get_device_error only  */
+} pkv_status;
+
+typedef enum { PKV_F32 = 0, PKV_BF16 = 1 } pkv_dtype;
+
+/* Codes recorded in the device error word (first one wins). */
+enum {
+  PKV_DEVERR_NONE = 0,
+  PKV_DEVERR_BLOCK_ID = 1,     /* block-table entry outside [0, num_blocks)          */
+  PKV_DEVERR_SLOT = 2,         /* slot outside [-1, num_blocks * block_size)          */
+  PKV_DEVERR_COPY_PAIR = 3,    /* copy pair id outside [0, num_blocks)               */
+  PKV_DEVERR_CONTEXT_LEN = 4,  /* context_lens[s] < 0, > max_context_len or beyond the
+                                  table row (the length is clamped)                  */
+  PKV_DEVERR_POSITION = 5,     /* position beyond the block-table row                */
+  PKV_DEVERR_TIMEOUT = 6       /* a pipeline wait gave up after about a second       */
+};
+
+/* Human-readable name of a status.  Never NULL. */
+PKV_API const char* pkv_status_string(pkv_status status);
+
+/* Message of the last failure on the calling thread ("" if none). */
+PKV_API const char* pkv_last_error_message(void);
+
+/* ABI version: (major << 16) | minor. */
+PKV_API int32_t pkv_version(void);
+
+/*
+ * a1 — slot mapping ("推理与 KV Cache 02", 从一个位置找到缓存块).
+ *   slot_mapping[s] = block_tables[s][positions[s] / block_size] * block_size
+ *                     + positions[s] % block_size
+ * block_tables: int32 [num_seqs, max_blocks_per_seq]; positions: int32
+ * [num_seqs]; slot_mapping: int64 [num_seqs] (output).  A negative position
+ * gives slot -1 (padding).  A position past the table row or a block id
+ * outside [0, num_blocks) gives -1 and records a device error.
+ */
+PKV_API pkv_status pkv_slot_mapping(const int32_t* block_tables, int32_t max_blocks_per_seq,
+                            const int32_t* positions, int32_t num_seqs,
+                            int32_t block_size, int64_t num_blocks,
+                            int64_t* slot_mapping, void* stream);
+
+/*
+ * a2 — slot-mapped KV append ("19.2 KV Cache 系统化管理" §19.2.3, write_slot).
+ *   k_cache.view(-1, H_kv, D)[slot_mapping[i]] = k[i]; same for v.
+ * k, v: [num_tokens, num_kv_heads, head_dim]; slot_mapping: int64
+ * [num_tokens].  Slot -1 skips the token.  Bit-exact copy of the rows.
+ * Duplicate slots in one call: which token wins is unspecified.
+ */
+PKV_API pkv_status pkv_kv_write(const void* k, const void* v, const int64_t* slot_mapping,
+                        int64_t num_tokens, void* k_cache, void* v_cache,
+                        int64_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                        int32_t head_dim, pkv_dtype dtype, void* stream);
+
+/*
+ * a5 — copy-on-write block copy ("19.2 KV Cache 系统化管理" §19.2.2, 写时复制:
+ * allocate a new block and copy the shared block's contents into it).
+ *   for each i: k_cache[pairs[i][1]] = k_cache[pairs[i][0]]; same for v_cache.
+ * src_dst_pairs: int64 [num_pairs, 2].  Bit-exact.  A destination that is
+ * also a source or another destination in the same call is unspecified.
+ */
+PKV_API pkv_status pkv_kv_block_copy(void* k_cache, void* v_cache, const int64_t* src_dst_pairs,
+                             int64_t num_pairs, int64_t num_blocks, int32_t block_size,
+                             int32_t num_kv_heads, int32_t head_dim, pkv_dtype dtype,
+                             void* stream);
+
+/* Optional tuning of pkv_attention_decode (pass NULL for the defaults). */
+typedef struct {
+  int32_t kernel;        /* 0 = automatic, 1 = TMA + tensor-core kernel
+                            (bf16, block_size % 16 == 0, head_dim 64 or 128,
+                            G <= 8), 2 = CUDA-core kernel (any supported shape) */
+  int32_t num_splits;    /* kernel 1: CTAs sharing the token range of one KV-head
+                            group (0 = SM count x CTAs per SM).  kernel 2:
+                            tokens per partition (0 = automatic).              */
+  int32_t reserved[6];   /* must be zero */
+} pkv_attention_config;
+
+/*
+ * Workspace bytes pkv_attention_decode needs for these sizes (written to
+ * *bytes).  Depends on the current device's SM count and on `config`.
+ */
+PKV_API pkv_status pkv_attention_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
+                                         int32_t num_kv_heads, int32_t head_dim,
+                                         int32_t block_size, int32_t max_context_len,
+                                         pkv_dtype dtype, const pkv_attention_config* config,
+                                         size_t* bytes);
+
+/*
+ * Number of kernel launches pkv_attention_decode makes for these sizes
+ * (written to *launches): one partition launch per batch of sequences plus
+ * one split-K reduce launch per batch when any sequence may be split.
+ */
+PKV_API pkv_status pkv_attention_launch_count(int32_t num_seqs, int32_t num_q_heads,
+                                              int32_t num_kv_heads, int32_t head_dim,
+                                              int32_t block_size, int32_t max_context_len,
+                                              pkv_dtype dtype, const pkv_attention_config* config,
+                                              int32_t* launches);
+
+/*
+ * a3 + a4 — decode attention over the paged cache with GQA and split-K
+ * ("19.2 KV Cache 系统化管理" §19.2.3 paged_attention; "KV Cache：长上下文为什么
+ * 吃显存" §01, §02).
+ *   For each sequence s and query head h, with G = num_q_heads / num_kv_heads,
+ *   j = h / G, L = context_lens[s] and token t in block
+ *   block_tables[s][t / block_size] at offset t % block_size:
+ *     out[s][h] = sum_t softmax_t(scale * q[s][h] . K_j[t]) * V_j[t]
+ *   accumulated in fp32 with an online (running max / running sum) softmax.
+ *   Long contexts are split across CTAs; partial (max, sum, output) states are
+ *   merged by a second kernel with the same rescaling identity.
+ * q: [num_seqs, num_q_heads, head_dim]; block_tables: int32 [num_seqs,
+ * max_blocks_per_seq]; context_lens: int32 [num_seqs] (tokens read, including
+ * the one appended this step); out: [num_seqs, num_q_heads, head_dim].
+ * max_context_len: host-side upper bound of context_lens (sizes the split;
+ * longer sequences are clamped to it and flagged).  A sequence of length 0
+ * gets a zero output.  Entries of a table row past ceil(L / block_size) are
+ * never read.  workspace: device scratch of at least
+ * pkv_attention_workspace_bytes bytes, 256-byte aligned; no initial contents
+ * are required; it must not be shared with a call that overlaps on the GPU.
+ * Supported: num_q_heads % num_kv_heads == 0, G <= 16, head_dim in {32, 64,
+ * 128, 256} (64 or 128 for the tensor-core kernel), 1 <= block_size <= 1024.
+ */
+PKV_API pkv_status pkv_attention_decode(const void* q, const void* k_cache, const void* v_cache,
+                                const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                const int32_t* context_lens, int32_t max_context_len,
+                                int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                                float scale, void* out, void* workspace,
+                                size_t workspace_bytes, pkv_dtype dtype,
+                                const pkv_attention_config* config, void* stream);
+
+/*
+ * Synchronises `stream`, copies the current device's error word into *code
+ * (a PKV_DEVERR_* value) and clears it.  Returns PKV_ERR_DEVICE_CHECK when
+ * the word was non-zero, PKV_OK when it was zero.
+ */
+PKV_API pkv_status pkv_get_device_error(int32_t* code, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

@@ -1,0 +1,567 @@
+// libpagedkv: C ABI (include/pagedkv.h) over the sm_103a kernels.
+//
+// Host side only: argument validation, launch planning, TMA tensor-map
+// encoding and kernel launches.  Nothing here allocates device memory.
+#include <cudaTypedefs.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "pkv_attention.cuh"
+#include "pkv_copy.cuh"
+#include "pkv_device.cuh"
+
+namespace {
+
+thread_local std::string g_last_msg;
+
+pkv_status fail(pkv_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_msg = buf;
+  return st;
+}
+
+#define PKV_CUDA(call)                                                                 \
+  do {                                                                                 \
+    cudaError_t e_ = (call);                                                           \
+    if (e_ != cudaSuccess) return fail(PKV_ERR_CUDA, "%s: %s", #call, cudaGetErrorString(e_)); \
+  } while (0)
+
+#define PKV_CHECK(cond, st, ...)                  \
+  do {                                            \
+    if (!(cond)) return fail((st), __VA_ARGS__);  \
+  } while (0)
+
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+inline size_t elem_bytes(pkv_dtype d) { return d == PKV_BF16 ? 2 : 4; }
+inline bool dtype_ok(pkv_dtype d) { return d == PKV_F32 || d == PKV_BF16; }
+inline int log2_exact(int64_t x) {
+  if (x <= 0 || (x & (x - 1))) return -1;
+  int l = 0;
+  while ((int64_t(1) << l) < x) ++l;
+  return l;
+}
+
+// ---- per-device facts --------------------------------------------------------
+constexpr int kMaxDevices = 64;
+struct DeviceFacts {
+  std::once_flag once;
+  int sm_count = 0;
+  cudaError_t err = cudaSuccess;
+};
+DeviceFacts g_dev[kMaxDevices];
+
+pkv_status device_facts(int* dev_out, int* sm_count) {
+  int dev = 0;
+  PKV_CUDA(cudaGetDevice(&dev));
+  PKV_CHECK(dev >= 0 && dev < kMaxDevices, PKV_ERR_UNSUPPORTED, "device ordinal %d too large", dev);
+  DeviceFacts& f = g_dev[dev];
+  std::call_once(f.once, [&] {
+    f.err = cudaDeviceGetAttribute(&f.sm_count, cudaDevAttrMultiProcessorCount, dev);
+  });
+  if (f.err != cudaSuccess) return fail(PKV_ERR_CUDA, "SM count: %s", cudaGetErrorString(f.err));
+  *dev_out = dev;
+  *sm_count = f.sm_count;
+  return PKV_OK;
+}
+
+// Opt a kernel into large dynamic shared memory once per device.
+template <typename Kernel>
+pkv_status set_smem_once(Kernel k, int bytes, std::once_flag (&flags)[kMaxDevices],
+                         cudaError_t (&errs)[kMaxDevices], int dev) {
+  std::call_once(flags[dev], [&] {
+    errs[dev] = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  });
+  if (errs[dev] != cudaSuccess)
+    return fail(PKV_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(errs[dev]));
+  return PKV_OK;
+}
+
+// ---- driver entry point for tensor maps -------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+pkv_status get_encode(PFN_cuTensorMapEncodeTiled_v12000* fn) {
+  std::call_once(g_encode_once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  PKV_CHECK(g_encode != nullptr, PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  *fn = g_encode;
+  return PKV_OK;
+}
+
+// Launch with programmatic stream serialization: the kernel may be scheduled
+// while the previous kernel in the stream finishes; it waits for that
+// kernel's results (griddepcontrol.wait) before touching global memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// ---- attention planning -------------------------------------------------------
+enum { KIND_TC = 1, KIND_SIMT = 2 };
+
+struct AttnPlan {
+  int kind = 0;
+  int hpc = 0, groups = 0, n_per_group = 0;  // tensor-core kernel
+  int ps = 0;                                // CUDA-core kernel: tokens per partition
+  int pmax = 1;
+  int seq_batch = 0;
+  size_t ws_bytes = 0;
+};
+
+bool tc_shape_ok(int G, int D, int K, int64_t num_blocks, pkv_dtype dt) {
+  return dt == PKV_BF16 && (D == 64 || D == 128) && G >= 1 && G <= 8 && K % 16 == 0 &&
+         num_blocks * K < (int64_t(1) << 31) - 64;
+}
+
+bool simt_shape_ok(int G, int D) {
+  return (D == 32 || D == 64 || D == 128 || D == 256) && G >= 1 && G <= 16;
+}
+
+int tc_hpc(int H_kv) {
+  for (int h : {8, 4, 2, 1})
+    if (H_kv % h == 0) return h;
+  return 1;
+}
+
+pkv_status plan_attention(int S, int H_q, int H_kv, int D, int K, int max_len, int64_t num_blocks,
+                          pkv_dtype dt, const pkv_attention_config* cfg, bool tma_aligned,
+                          AttnPlan* plan) {
+  PKV_CHECK(S >= 0 && H_q > 0 && H_kv > 0 && D > 0 && K > 0 && K <= 1024 && max_len >= 0,
+            PKV_ERR_INVALID_ARGUMENT, "bad attention sizes");
+  PKV_CHECK(H_q % H_kv == 0, PKV_ERR_INVALID_ARGUMENT, "num_q_heads %% num_kv_heads != 0");
+  PKV_CHECK(dtype_ok(dt), PKV_ERR_INVALID_ARGUMENT, "bad dtype");
+  pkv_attention_config c = {};
+  if (cfg) c = *cfg;
+  for (int r : c.reserved) PKV_CHECK(r == 0, PKV_ERR_INVALID_ARGUMENT, "reserved config fields must be 0");
+  PKV_CHECK(c.kernel >= 0 && c.kernel <= 2 && c.num_splits >= 0, PKV_ERR_INVALID_ARGUMENT,
+            "bad attention config");
+  const int G = H_q / H_kv;
+  const bool tc_ok = tc_shape_ok(G, D, K, num_blocks, dt) && tma_aligned;
+  AttnPlan p;
+  if (c.kernel == 1 || (c.kernel == 0 && tc_ok)) {
+    PKV_CHECK(tc_ok, PKV_ERR_UNSUPPORTED,
+              "tensor-core kernel needs bf16, head_dim 64/128, G <= 8, block_size %% 16 == 0 "
+              "and a 16-byte aligned pool");
+    int dev, sms;
+    pkv_status st = device_facts(&dev, &sms);
+    if (st != PKV_OK) return st;
+    p.kind = KIND_TC;
+    p.hpc = tc_hpc(H_kv);
+    p.groups = H_kv / p.hpc;
+    const int total = sms;   // one CTA per SM (shared memory bound)
+    p.n_per_group = c.num_splits ? c.num_splits : (total / p.groups > 0 ? total / p.groups : 1);
+    const int max_chunks = (int)ceil_div(max_len, pkv::kTcChunk);
+    p.pmax = std::max(1, std::min(p.n_per_group, max_chunks));
+    p.seq_batch = std::min(S, pkv::kTcMaxSeqs);
+  } else {
+    PKV_CHECK(simt_shape_ok(G, D), PKV_ERR_UNSUPPORTED,
+              "unsupported shape: head_dim must be 32/64/128/256 and G <= 16");
+    p.kind = KIND_SIMT;
+    p.ps = c.num_splits ? c.num_splits : 512;
+    PKV_CHECK(p.ps >= 1 && p.ps <= pkv::kSimtMaxPS, PKV_ERR_INVALID_ARGUMENT,
+              "tokens per partition must be in [1, %d]", pkv::kSimtMaxPS);
+    p.pmax = std::max<int>(1, (int)ceil_div(max_len, p.ps));
+    PKV_CHECK(p.pmax <= 2147483647 / 2, PKV_ERR_UNSUPPORTED, "too many partitions");
+    p.seq_batch = std::min(S, 65535);
+  }
+  const size_t sb = (size_t)std::max(p.seq_batch, 1);
+  p.ws_bytes = align256(sb * 4) + align256(sb * p.pmax * H_q * sizeof(float2)) +
+               align256(sb * p.pmax * H_q * (size_t)D * sizeof(float));
+  *plan = p;
+  return PKV_OK;
+}
+
+pkv::Workspace carve_workspace(void* ws, const AttnPlan& p, int H_q, int D) {
+  const size_t sb = (size_t)std::max(p.seq_batch, 1);
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  pkv::Workspace w;
+  w.nparts = reinterpret_cast<int*>(b);
+  b += align256(sb * 4);
+  w.ml = reinterpret_cast<float2*>(b);
+  b += align256(sb * p.pmax * H_q * sizeof(float2));
+  w.o = reinterpret_cast<float*>(b);
+  w.pmax = p.pmax;
+  return w;
+}
+
+// ---- tensor-core kernel dispatch ------------------------------------------------
+template <int D, int HPC>
+struct TcInst {
+  // as many stages as fit in ~192 KiB of shared memory, between 2 and 8
+  static constexpr int STAGE_BYTES = 2 * HPC * (D / 64) * pkv::kBoxBytes;
+  static constexpr int NS_FIT = 196608 / STAGE_BYTES;
+  static constexpr int NS = NS_FIT < 2 ? 2 : (NS_FIT > 8 ? 8 : NS_FIT);
+  using C = pkv::TcCfg<D, HPC, NS>;
+  static std::once_flag flags[kMaxDevices];
+  static cudaError_t errs[kMaxDevices];
+  static pkv_status launch(const pkv::TcParams& prm, int n, int groups, cudaStream_t st, int dev) {
+    auto k = pkv::attn_tc_kernel<D, HPC, NS>;
+    pkv_status s = set_smem_once(k, C::SMEM, flags, errs, dev);
+    if (s != PKV_OK) return s;
+    PKV_CUDA(launch_pdl(k, dim3(n, groups), dim3(C::THREADS), (size_t)C::SMEM, st, prm));
+    return PKV_OK;
+  }
+};
+template <int D, int HPC> std::once_flag TcInst<D, HPC>::flags[kMaxDevices];
+template <int D, int HPC> cudaError_t TcInst<D, HPC>::errs[kMaxDevices];
+
+template <int D>
+pkv_status launch_tc_d(int hpc, const pkv::TcParams& prm, int n, int groups, cudaStream_t st,
+                       int dev) {
+  switch (hpc) {
+    case 8: return TcInst<D, 8>::launch(prm, n, groups, st, dev);
+    case 4: return TcInst<D, 4>::launch(prm, n, groups, st, dev);
+    case 2: return TcInst<D, 2>::launch(prm, n, groups, st, dev);
+    default: return TcInst<D, 1>::launch(prm, n, groups, st, dev);
+  }
+}
+
+pkv_status encode_pool_map(CUtensorMap* map, const void* pool, int64_t num_blocks, int K, int H_kv,
+                           int D) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  pkv_status st = get_encode(&enc);
+  if (st != PKV_OK) return st;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H_kv, (cuuint64_t)(num_blocks * K)};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H_kv * D * 2};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)pkv::kTcChunk};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pool), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  PKV_CHECK(r == CUDA_SUCCESS, PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return PKV_OK;
+}
+
+// ---- CUDA-core kernel dispatch --------------------------------------------------
+template <typename T, int D, int GMAX>
+pkv_status launch_simt_t(const void* q, const void* kc, const void* vc, const int32_t* bt, int maxB,
+                         const int32_t* lens, int max_len, int S, int H_q, int H_kv, int K,
+                         int64_t nb, float sl, void* out, pkv::Workspace ws, int ps, int pmax,
+                         cudaStream_t st) {
+  PKV_CUDA(launch_pdl(pkv::attn_simt_kernel<T, D, GMAX>, dim3(pmax, H_kv, S),
+                      dim3(pkv::kSimtThreads), 0, st, static_cast<const T*>(q),
+                      static_cast<const T*>(kc), static_cast<const T*>(vc), bt, maxB, lens, max_len,
+                      H_q, H_kv, H_q / H_kv, K, (long long)nb, sl, static_cast<T*>(out), ws, ps));
+  return PKV_OK;
+}
+
+template <typename T, int D>
+pkv_status launch_simt_d(int G, const void* q, const void* kc, const void* vc, const int32_t* bt,
+                         int maxB, const int32_t* lens, int max_len, int S, int H_q, int H_kv,
+                         int K, int64_t nb, float sl, void* out, pkv::Workspace ws, int ps,
+                         int pmax, cudaStream_t st) {
+  if (G <= 2)
+    return launch_simt_t<T, D, 2>(q, kc, vc, bt, maxB, lens, max_len, S, H_q, H_kv, K, nb, sl, out,
+                                  ws, ps, pmax, st);
+  if (G <= 8)
+    return launch_simt_t<T, D, 8>(q, kc, vc, bt, maxB, lens, max_len, S, H_q, H_kv, K, nb, sl, out,
+                                  ws, ps, pmax, st);
+  return launch_simt_t<T, D, 16>(q, kc, vc, bt, maxB, lens, max_len, S, H_q, H_kv, K, nb, sl, out,
+                                 ws, ps, pmax, st);
+}
+
+template <typename T>
+pkv_status launch_simt(int D, int G, const void* q, const void* kc, const void* vc,
+                       const int32_t* bt, int maxB, const int32_t* lens, int max_len, int S,
+                       int H_q, int H_kv, int K, int64_t nb, float sl, void* out,
+                       pkv::Workspace ws, int ps, int pmax, cudaStream_t st) {
+  switch (D) {
+    case 32:
+      return launch_simt_d<T, 32>(G, q, kc, vc, bt, maxB, lens, max_len, S, H_q, H_kv, K, nb, sl,
+                                  out, ws, ps, pmax, st);
+    case 64:
+      return launch_simt_d<T, 64>(G, q, kc, vc, bt, maxB, lens, max_len, S, H_q, H_kv, K, nb, sl,
+                                  out, ws, ps, pmax, st);
+    case 128:
+      return launch_simt_d<T, 128>(G, q, kc, vc, bt, maxB, lens, max_len, S, H_q, H_kv, K, nb, sl,
+                                   out, ws, ps, pmax, st);
+    default:
+      return launch_simt_d<T, 256>(G, q, kc, vc, bt, maxB, lens, max_len, S, H_q, H_kv, K, nb, sl,
+                                   out, ws, ps, pmax, st);
+  }
+}
+
+// Widest vector (16/8/4/2 bytes) that divides the row and every base pointer.
+int vec_width(int64_t row_bytes, std::initializer_list<const void*> ptrs) {
+  for (int w : {16, 8, 4, 2}) {
+    if (row_bytes % w) continue;
+    bool ok = true;
+    for (const void* p : ptrs) ok = ok && aligned(p, w);
+    if (ok) return w;
+  }
+  return 0;
+}
+
+}  // namespace
+
+// =============================================================================
+// C ABI
+// =============================================================================
+extern "C" {
+
+const char* pkv_status_string(pkv_status s) {
+  switch (s) {
+    case PKV_OK: return "PKV_OK";
+    case PKV_ERR_INVALID_ARGUMENT: return "PKV_ERR_INVALID_ARGUMENT";
+    case PKV_ERR_UNSUPPORTED: return "PKV_ERR_UNSUPPORTED";
+    case PKV_ERR_WORKSPACE_TOO_SMALL: return "PKV_ERR_WORKSPACE_TOO_SMALL";
+    case PKV_ERR_CUDA: return "PKV_ERR_CUDA";
+    case PKV_ERR_DEVICE_CHECK: return "PKV_ERR_DEVICE_CHECK";
+  }
+  return "PKV_UNKNOWN_STATUS";
+}
+
+const char* pkv_last_error_message(void) { return g_last_msg.c_str(); }
+
+int32_t pkv_version(void) { return (1 << 16) | 0; }
+
+pkv_status pkv_slot_mapping(const int32_t* block_tables, int32_t max_blocks_per_seq,
+                            const int32_t* positions, int32_t num_seqs, int32_t block_size,
+                            int64_t num_blocks, int64_t* slot_mapping, void* stream) {
+  PKV_CHECK(num_seqs >= 0 && max_blocks_per_seq >= 1 && block_size >= 1 && num_blocks >= 1,
+            PKV_ERR_INVALID_ARGUMENT, "bad slot-mapping sizes");
+  if (num_seqs == 0) return PKV_OK;
+  PKV_CHECK(block_tables && positions && slot_mapping, PKV_ERR_INVALID_ARGUMENT, "null pointer");
+  PKV_CHECK(num_blocks <= INT64_MAX / block_size, PKV_ERR_INVALID_ARGUMENT, "pool too large");
+  const int threads = 256;
+  PKV_CUDA(launch_pdl(pkv::slot_mapping_kernel, dim3((num_seqs + threads - 1) / threads),
+                      dim3(threads), 0, as_stream(stream), block_tables, max_blocks_per_seq,
+                      positions, num_seqs, block_size, log2_exact(block_size), num_blocks,
+                      slot_mapping));
+  return PKV_OK;
+}
+
+pkv_status pkv_kv_write(const void* k, const void* v, const int64_t* slot_mapping,
+                        int64_t num_tokens, void* k_cache, void* v_cache, int64_t num_blocks,
+                        int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                        pkv_dtype dtype, void* stream) {
+  PKV_CHECK(num_tokens >= 0 && num_blocks >= 1 && block_size >= 1 && num_kv_heads >= 1 &&
+                head_dim >= 1 && dtype_ok(dtype),
+            PKV_ERR_INVALID_ARGUMENT, "bad kv_write sizes");
+  if (num_tokens == 0) return PKV_OK;
+  PKV_CHECK(k && v && slot_mapping && k_cache && v_cache, PKV_ERR_INVALID_ARGUMENT, "null pointer");
+  PKV_CHECK(num_tokens <= 2147483647, PKV_ERR_UNSUPPORTED, "too many tokens");
+  const int64_t row = (int64_t)num_kv_heads * head_dim * elem_bytes(dtype);
+  const int vw = vec_width(row, {k, v, k_cache, v_cache});
+  PKV_CHECK(vw > 0, PKV_ERR_INVALID_ARGUMENT, "misaligned kv_write buffers");
+  const int threads = 128;
+  const int64_t nvec = row / vw;
+  const int64_t chunks = ceil_div(nvec, threads);
+  PKV_CHECK(chunks <= 65535, PKV_ERR_UNSUPPORTED, "token row too wide");
+  dim3 grid((unsigned)num_tokens, (unsigned)chunks, 2);
+  const int64_t slots = num_blocks * block_size;
+  auto* kb = static_cast<const uint8_t*>(k);
+  auto* vb = static_cast<const uint8_t*>(v);
+  auto* kc = static_cast<uint8_t*>(k_cache);
+  auto* vc = static_cast<uint8_t*>(v_cache);
+  cudaStream_t st = as_stream(stream);
+  switch (vw) {
+    case 16: PKV_CUDA(launch_pdl(pkv::kv_write_kernel<16>, grid, dim3(threads), 0, st, kb, vb, slot_mapping, kc, vc, slots, row)); break;
+    case 8: PKV_CUDA(launch_pdl(pkv::kv_write_kernel<8>, grid, dim3(threads), 0, st, kb, vb, slot_mapping, kc, vc, slots, row)); break;
+    case 4: PKV_CUDA(launch_pdl(pkv::kv_write_kernel<4>, grid, dim3(threads), 0, st, kb, vb, slot_mapping, kc, vc, slots, row)); break;
+    default: PKV_CUDA(launch_pdl(pkv::kv_write_kernel<2>, grid, dim3(threads), 0, st, kb, vb, slot_mapping, kc, vc, slots, row)); break;
+  }
+  return PKV_OK;
+}
+
+pkv_status pkv_kv_block_copy(void* k_cache, void* v_cache, const int64_t* src_dst_pairs,
+                             int64_t num_pairs, int64_t num_blocks, int32_t block_size,
+                             int32_t num_kv_heads, int32_t head_dim, pkv_dtype dtype,
+                             void* stream) {
+  PKV_CHECK(num_pairs >= 0 && num_blocks >= 1 && block_size >= 1 && num_kv_heads >= 1 &&
+                head_dim >= 1 && dtype_ok(dtype),
+            PKV_ERR_INVALID_ARGUMENT, "bad block-copy sizes");
+  if (num_pairs == 0) return PKV_OK;
+  PKV_CHECK(k_cache && v_cache && src_dst_pairs, PKV_ERR_INVALID_ARGUMENT, "null pointer");
+  PKV_CHECK(num_pairs <= 2147483647, PKV_ERR_UNSUPPORTED, "too many pairs");
+  const int64_t blk = (int64_t)block_size * num_kv_heads * head_dim * elem_bytes(dtype);
+  const int vw = vec_width(blk, {k_cache, v_cache});
+  PKV_CHECK(vw > 0, PKV_ERR_INVALID_ARGUMENT, "misaligned pools");
+  constexpr int threads = 256, unroll = 4;
+  const int64_t chunks = ceil_div(blk / vw, threads * unroll);
+  PKV_CHECK(chunks <= 65535, PKV_ERR_UNSUPPORTED, "block too large");
+  dim3 grid((unsigned)num_pairs, (unsigned)chunks, 2);
+  auto* kc = static_cast<uint8_t*>(k_cache);
+  auto* vc = static_cast<uint8_t*>(v_cache);
+  cudaStream_t st = as_stream(stream);
+  switch (vw) {
+    case 16: PKV_CUDA(launch_pdl(pkv::block_copy_kernel<16, unroll>, grid, dim3(threads), 0, st, kc, vc, src_dst_pairs, num_blocks, blk)); break;
+    case 8: PKV_CUDA(launch_pdl(pkv::block_copy_kernel<8, unroll>, grid, dim3(threads), 0, st, kc, vc, src_dst_pairs, num_blocks, blk)); break;
+    case 4: PKV_CUDA(launch_pdl(pkv::block_copy_kernel<4, unroll>, grid, dim3(threads), 0, st, kc, vc, src_dst_pairs, num_blocks, blk)); break;
+    default: PKV_CUDA(launch_pdl(pkv::block_copy_kernel<2, unroll>, grid, dim3(threads), 0, st, kc, vc, src_dst_pairs, num_blocks, blk)); break;
+  }
+  return PKV_OK;
+}
+
+pkv_status pkv_attention_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
+                                         int32_t num_kv_heads, int32_t head_dim,
+                                         int32_t block_size, int32_t max_context_len,
+                                         pkv_dtype dtype, const pkv_attention_config* config,
+                                         size_t* bytes) {
+  PKV_CHECK(bytes != nullptr, PKV_ERR_INVALID_ARGUMENT, "null bytes pointer");
+  AttnPlan plan;
+  // the tensor-core plan assumes an aligned pool; a misaligned pool takes the
+  // CUDA-core plan, whose workspace is never larger for the same sizes
+  pkv_status st = plan_attention(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                                 max_context_len, 1, dtype, config, true, &plan);
+  if (st != PKV_OK) return st;
+  AttnPlan alt;
+  pkv_attention_config c2 = {};
+  if (config) c2 = *config;
+  if (plan.kind == KIND_TC && c2.kernel == 0) {
+    c2.kernel = 2;
+    c2.num_splits = 0;
+    if (plan_attention(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_context_len,
+                       1, dtype, &c2, true, &alt) == PKV_OK)
+      plan.ws_bytes = std::max(plan.ws_bytes, alt.ws_bytes);
+  }
+  *bytes = plan.ws_bytes;
+  return PKV_OK;
+}
+
+pkv_status pkv_attention_launch_count(int32_t num_seqs, int32_t num_q_heads,
+                                      int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                      int32_t max_context_len, pkv_dtype dtype,
+                                      const pkv_attention_config* config, int32_t* launches) {
+  PKV_CHECK(launches != nullptr, PKV_ERR_INVALID_ARGUMENT, "null launches pointer");
+  AttnPlan plan;
+  pkv_status st = plan_attention(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                                 max_context_len, 1, dtype, config, true, &plan);
+  if (st != PKV_OK) return st;
+  const int batches = num_seqs == 0 ? 0 : (int)ceil_div(num_seqs, plan.seq_batch);
+  *launches = batches * (plan.pmax > 1 ? 2 : 1);
+  return PKV_OK;
+}
+
+pkv_status pkv_attention_decode(const void* q, const void* k_cache, const void* v_cache,
+                                const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                const int32_t* context_lens, int32_t max_context_len,
+                                int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                                float scale, void* out, void* workspace, size_t workspace_bytes,
+                                pkv_dtype dtype, const pkv_attention_config* config,
+                                void* stream) {
+  PKV_CHECK(num_seqs >= 0 && max_blocks_per_seq >= 1 && num_blocks >= 1,
+            PKV_ERR_INVALID_ARGUMENT, "bad attention sizes");
+  const bool tma_aligned = aligned(k_cache, 16) && aligned(v_cache, 16);
+  AttnPlan plan;
+  pkv_status st = plan_attention(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                                 max_context_len, num_blocks, dtype, config, tma_aligned, &plan);
+  if (st != PKV_OK) return st;
+  if (num_seqs == 0) return PKV_OK;
+  PKV_CHECK(q && k_cache && v_cache && block_tables && context_lens && out && workspace,
+            PKV_ERR_INVALID_ARGUMENT, "null pointer");
+  PKV_CHECK(workspace_bytes >= plan.ws_bytes, PKV_ERR_WORKSPACE_TOO_SMALL,
+            "workspace %zu bytes < %zu needed", workspace_bytes, plan.ws_bytes);
+  PKV_CHECK(aligned(workspace, 256), PKV_ERR_INVALID_ARGUMENT, "workspace must be 256-byte aligned");
+  const size_t eb = elem_bytes(dtype);
+  PKV_CHECK(aligned(q, eb) && aligned(out, eb) && aligned(k_cache, eb) && aligned(v_cache, eb),
+            PKV_ERR_INVALID_ARGUMENT, "misaligned q/out/pool");
+  PKV_CHECK((int64_t)max_blocks_per_seq * block_size <= 2147483647, PKV_ERR_UNSUPPORTED,
+            "table row too long");
+  const double log2e = 1.4426950408889634;
+  const float sl = (float)((double)scale * log2e);
+  cudaStream_t strm = as_stream(stream);
+  pkv::Workspace ws = carve_workspace(workspace, plan, num_q_heads, head_dim);
+  const int D = head_dim, H_q = num_q_heads, H_kv = num_kv_heads;
+
+  pkv::TcParams prm;
+  int dev = 0;
+  if (plan.kind == KIND_TC) {
+    int sms;
+    st = device_facts(&dev, &sms);
+    if (st != PKV_OK) return st;
+    memset(&prm, 0, sizeof(prm));
+    st = encode_pool_map(&prm.tmap_k, k_cache, num_blocks, block_size, H_kv, D);
+    if (st != PKV_OK) return st;
+    st = encode_pool_map(&prm.tmap_v, v_cache, num_blocks, block_size, H_kv, D);
+    if (st != PKV_OK) return st;
+  }
+  for (int s0 = 0; s0 < num_seqs; s0 += plan.seq_batch) {
+    const int S = std::min(plan.seq_batch, num_seqs - s0);
+    const uint8_t* qb = static_cast<const uint8_t*>(q) + (size_t)s0 * H_q * D * eb;
+    uint8_t* ob = static_cast<uint8_t*>(out) + (size_t)s0 * H_q * D * eb;
+    const int32_t* btb = block_tables + (size_t)s0 * max_blocks_per_seq;
+    const int32_t* lb = context_lens + s0;
+    if (plan.kind == KIND_TC) {
+      prm.q = reinterpret_cast<const __nv_bfloat16*>(qb);
+      prm.out = reinterpret_cast<__nv_bfloat16*>(ob);
+      prm.block_tables = btb;
+      prm.context_lens = lb;
+      prm.ws = ws;
+      prm.num_blocks = num_blocks;
+      prm.max_blocks_per_seq = max_blocks_per_seq;
+      prm.num_seqs = S;
+      prm.max_len = max_context_len;
+      prm.H_q = H_q;
+      prm.G = H_q / H_kv;
+      prm.block_size = block_size;
+      prm.scale_log2 = sl;
+      st = D == 64 ? launch_tc_d<64>(plan.hpc, prm, plan.n_per_group, plan.groups, strm, dev)
+                   : launch_tc_d<128>(plan.hpc, prm, plan.n_per_group, plan.groups, strm, dev);
+    } else if (dtype == PKV_BF16) {
+      st = launch_simt<__nv_bfloat16>(D, H_q / H_kv, qb, k_cache, v_cache, btb, max_blocks_per_seq,
+                                      lb, max_context_len, S, H_q, H_kv, block_size, num_blocks,
+                                      sl, ob, ws, plan.ps, plan.pmax, strm);
+    } else {
+      st = launch_simt<float>(D, H_q / H_kv, qb, k_cache, v_cache, btb, max_blocks_per_seq, lb,
+                              max_context_len, S, H_q, H_kv, block_size, num_blocks, sl, ob, ws,
+                              plan.ps, plan.pmax, strm);
+    }
+    if (st != PKV_OK) return st;
+    if (plan.pmax > 1) {
+      if (dtype == PKV_BF16) {
+        PKV_CUDA(launch_pdl(pkv::attn_reduce_kernel<__nv_bfloat16>, dim3(S), dim3(128), 0, strm, ws,
+                            H_q, D, reinterpret_cast<__nv_bfloat16*>(ob)));
+      } else {
+        PKV_CUDA(launch_pdl(pkv::attn_reduce_kernel<float>, dim3(S), dim3(128), 0, strm, ws, H_q,
+                            D, reinterpret_cast<float*>(ob)));
+      }
+    }
+  }
+  return PKV_OK;
+}
+
+pkv_status pkv_get_device_error(int32_t* code, void* stream) {
+  PKV_CHECK(code != nullptr, PKV_ERR_INVALID_ARGUMENT, "null code pointer");
+  PKV_CUDA(cudaStreamSynchronize(as_stream(stream)));
+  int h = 0;
+  PKV_CUDA(cudaMemcpyFromSymbol(&h, pkv::g_error_word, sizeof(int)));
+  *code = h;
+  if (h != 0) {
+    const int zero = 0;
+    PKV_CUDA(cudaMemcpyToSymbol(pkv::g_error_word, &zero, sizeof(int)));
+    return fail(PKV_ERR_DEVICE_CHECK, "device check failed with code %d", h);
+  }
+  return PKV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,599 @@
+// Decode attention over the paged KV cache: partition kernels and the split-K
+// reduce.
+//
+// What is computed ("19.2 KV Cache 系统化管理" §19.2.3 paged_attention;
+// "KV Cache：长上下文为什么吃显存" §01/§02): for sequence s and query head h
+// (KV head j = h / G), out = softmax(scale * q . K_j[0:L]) V_j[0:L], with K/V
+// rows found through the block table (token t -> block bt[s][t / K], offset
+// t % K).  Scores and weights are kept in the base-2 domain
+// (x = scale * log2(e) * q.k, weight = 2^(x - max)), which is the same
+// softmax.  Every kernel keeps the running maximum m, the running sum l and
+// the unnormalised output o of the page's block loop; partial states of one
+// (s, h) are merged by attn_reduce_kernel with
+//   M = max m_p,  l = sum l_p 2^(m_p - M),  out = sum o_p 2^(m_p - M) / l.
+//
+// Workspace layout (per launch batch of sequences, Pmax partials per seq):
+//   int    nparts[S]                   partials written for s (0: empty seq,
+//                                      1: output already final)
+//   float2 ml[S][Pmax][H_q]            (m, l) of each partial
+//   float  o [S][Pmax][H_q][D]         unnormalised partial outputs
+#pragma once
+
+#include "pkv_device.cuh"
+
+namespace pkv {
+
+struct Workspace {
+  int* nparts;
+  float2* ml;
+  float* o;
+  int pmax;
+};
+
+// ===========================================================================
+// CUDA-core partition kernel (fp32 or bf16, any block size, G <= 16).
+// grid = (Pmax, H_kv, S), block = 128 threads; CTA (p, j, s) covers tokens
+// [p*PS, min((p+1)*PS, L)) of sequence s for the G query heads of KV head j.
+// Each warp takes every 4th token; the four warps' states are merged in
+// shared memory.
+// ===========================================================================
+constexpr int kSimtThreads = 128;
+constexpr int kSimtMaxPS = 1024;
+
+template <typename T, int D, int GMAX>
+__global__ void __launch_bounds__(kSimtThreads)
+attn_simt_kernel(const T* __restrict__ q, const T* __restrict__ k_cache,
+                 const T* __restrict__ v_cache, const int32_t* __restrict__ block_tables,
+                 int max_blocks_per_seq, const int32_t* __restrict__ context_lens, int max_len,
+                 int H_q, int H_kv, int G, int K, long long num_blocks, float scale_log2,
+                 T* __restrict__ out, Workspace ws, int PS) {
+  constexpr int E = D / 32;   // elements of a row per lane
+  __shared__ int s_bt[kSimtMaxPS + 2];
+  __shared__ float s_m[4][GMAX], s_l[4][GMAX];
+  __shared__ float s_o[GMAX][D];
+
+  pdl_wait_primary();
+  pdl_launch_dependents();
+
+  const int p = blockIdx.x, j = blockIdx.y, s = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int L = effective_len(context_lens[s], max_len, max_blocks_per_seq * K);
+  const int np = (L + PS - 1) / PS;
+  if (p == 0 && j == 0 && threadIdx.x == 0) ws.nparts[s] = np;
+  if (L == 0) {
+    if (p == 0) {
+      for (int i = threadIdx.x; i < G * D; i += blockDim.x)
+        out[((int64_t)s * H_q + j * G) * D + i] = from_f32<T>(0.f);
+    }
+    return;
+  }
+  if (p >= np) return;
+  const int t0 = p * PS, t1 = min(t0 + PS, L);
+  const int lb0 = t0 / K, nlb = (t1 - 1) / K - lb0 + 1;
+  for (int i = threadIdx.x; i < nlb; i += blockDim.x) {
+    int phys = block_tables[(int64_t)s * max_blocks_per_seq + lb0 + i];
+    if (phys < 0 || phys >= num_blocks) {
+      record_error(PKV_DEVERR_BLOCK_ID);
+      phys = -1;
+    }
+    s_bt[i] = phys;
+  }
+  for (int i = threadIdx.x; i < GMAX * D; i += blockDim.x) (&s_o[0][0])[i] = 0.f;
+
+  float qr[GMAX][E];
+#pragma unroll
+  for (int n = 0; n < GMAX; ++n)
+#pragma unroll
+    for (int e = 0; e < E; ++e)
+      qr[n][e] = n < G ? to_f32(q[((int64_t)s * H_q + j * G + n) * D + lane + 32 * e]) : 0.f;
+  __syncthreads();
+
+  float m[GMAX], l[GMAX], o[GMAX][E];
+#pragma unroll
+  for (int n = 0; n < GMAX; ++n) {
+    m[n] = -INFINITY;
+    l[n] = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) o[n][e] = 0.f;
+  }
+  for (int t = t0 + warp; t < t1; t += 4) {
+    const int lbi = t / K - lb0;
+    const int phys = s_bt[lbi];
+    const int off = t - (t / K) * K;
+    float kr[E], vr[E];
+    if (phys >= 0) {
+      const int64_t row = (((int64_t)phys * K + off) * H_kv + j) * D;
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        kr[e] = to_f32(k_cache[row + lane + 32 * e]);
+        vr[e] = to_f32(v_cache[row + lane + 32 * e]);
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < E; ++e) kr[e] = vr[e] = 0.f;
+    }
+#pragma unroll
+    for (int n = 0; n < GMAX; ++n) {
+      if (n >= G) break;
+      float d = 0.f;
+#pragma unroll
+      for (int e = 0; e < E; ++e) d = fmaf(qr[n][e], kr[e], d);
+      const float x = warp_sum(d) * scale_log2;
+      const float mn = fmaxf(m[n], x);
+      const float a = exp2f(m[n] - mn);
+      const float w = exp2f(x - mn);
+      l[n] = l[n] * a + w;
+#pragma unroll
+      for (int e = 0; e < E; ++e) o[n][e] = fmaf(o[n][e], a, w * vr[e]);
+      m[n] = mn;
+    }
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int n = 0; n < GMAX; ++n) {
+      s_m[warp][n] = m[n];
+      s_l[warp][n] = l[n];
+    }
+  }
+  __syncthreads();
+  float M[GMAX], Lsum[GMAX], f[GMAX];
+#pragma unroll
+  for (int n = 0; n < GMAX; ++n) {
+    M[n] = fmaxf(fmaxf(s_m[0][n], s_m[1][n]), fmaxf(s_m[2][n], s_m[3][n]));
+    Lsum[n] = 0.f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w)
+      Lsum[n] += s_m[w][n] == -INFINITY ? 0.f : s_l[w][n] * exp2f(s_m[w][n] - M[n]);
+    f[n] = m[n] == -INFINITY ? 0.f : exp2f(m[n] - M[n]);
+  }
+  for (int w = 0; w < 4; ++w) {
+    if (warp == w) {
+#pragma unroll
+      for (int n = 0; n < GMAX; ++n)
+#pragma unroll
+        for (int e = 0; e < E; ++e) s_o[n][lane + 32 * e] += o[n][e] * f[n];
+    }
+    __syncthreads();
+  }
+  if (np == 1) {
+    for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
+      const int n = i / D, d = i - n * D;
+      out[((int64_t)s * H_q + j * G + n) * D + d] = from_f32<T>(s_o[n][d] / Lsum[n]);
+    }
+  } else {
+    const int64_t base = ((int64_t)s * ws.pmax + p) * H_q + j * G;
+    for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
+      const int n = i / D, d = i - n * D;
+      ws.o[(base + n) * D + d] = s_o[n][d];
+    }
+    if (threadIdx.x < G) ws.ml[base + threadIdx.x] = make_float2(M[threadIdx.x], Lsum[threadIdx.x]);
+  }
+}
+
+// ===========================================================================
+// Split-K reduce: one CTA per sequence, one warp per query head at a time.
+// ===========================================================================
+template <typename T>
+__global__ void __launch_bounds__(128)
+attn_reduce_kernel(Workspace ws, int H_q, int D, T* __restrict__ out) {
+  pdl_wait_primary();
+  pdl_launch_dependents();
+  const int s = blockIdx.x;
+  int np = ws.nparts[s];
+  if (np <= 1) return;
+  if (np > ws.pmax) {   // cannot happen with lengths clamped to the bound; never read past it
+    record_error(PKV_DEVERR_CONTEXT_LEN);
+    np = ws.pmax;
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int h = warp; h < H_q; h += 4) {
+    const int64_t base = (int64_t)s * ws.pmax * H_q + h;   // + p * H_q
+    float M = -INFINITY;
+    for (int p = lane; p < np; p += 32) M = fmaxf(M, ws.ml[base + (int64_t)p * H_q].x);
+    M = warp_max(M);
+    float Lsum = 0.f;
+    for (int p = lane; p < np; p += 32) {
+      const float2 ml = ws.ml[base + (int64_t)p * H_q];
+      Lsum += ml.y * exp2f(ml.x - M);
+    }
+    Lsum = warp_sum(Lsum);
+    const float inv = 1.f / Lsum;
+    for (int d0 = 0; d0 < D; d0 += 32) {
+      const int d = d0 + lane;
+      float acc = 0.f;
+      for (int p0 = 0; p0 < np; p0 += 32) {
+        const int pl = p0 + lane;
+        const float w = pl < np ? exp2f(ws.ml[base + (int64_t)pl * H_q].x - M) : 0.f;
+        const int cnt = min(32, np - p0);
+        for (int u = 0; u < cnt; ++u) {
+          const float wu = __shfl_sync(0xffffffffu, w, u);
+          if (d < D) acc = fmaf(wu, ws.o[(base + (int64_t)(p0 + u) * H_q) * D + d], acc);
+        }
+      }
+      if (d < D) out[((int64_t)s * H_q + h) * D + d] = from_f32<T>(acc * inv);
+    }
+  }
+}
+
+// ===========================================================================
+// TMA + tensor-core partition kernel (bf16, K % 16 == 0, D in {64, 128},
+// G <= 8).
+//
+// Work decomposition: the token range of the batch is cut into chunks of 16
+// tokens (one tensor-core M tile).  Chunks are numbered sequence-major; with
+// T chunks and n CTAs per KV-head group, CTA i owns chunks
+// [floor(i T / n), floor((i+1) T / n)) — equal work per CTA whatever the
+// length mix.  A run of chunks of one sequence inside a CTA is a split-K
+// partition; its (m, l, o) goes to the workspace unless the CTA holds the
+// whole sequence, in which case it writes the final output.
+//
+// Roles: warp HPC is the producer; one elected pass of its lanes issues the
+// TMA loads of a stage (16 tokens x HPC heads, K and V, one box per head and
+// 64-column half) completing on the stage's "full" mbarrier.  Warps
+// 0..HPC-1 are consumers, warp w owning KV head (group * HPC + w): it waits
+// on "full", computes S^T = K_tile Q^T and O^T += V^T P^T with
+// mma.m16n8k16 (tokens x heads, the q-group padded to 8 columns), does the
+// online softmax on the 16 x 8 score tile with warp shuffles, and arrives
+// on the stage's "empty" mbarrier.
+//
+// Shared-memory tiles use the 128-byte swizzle, so the 8 rows an ldmatrix
+// phase reads (8 tokens, same 16-byte column) land in 8 distinct bank groups.
+// ===========================================================================
+constexpr int kTcChunk = 16;
+constexpr int kTcMaxSeqs = 2048;
+constexpr int kBoxBytes = kTcChunk * 128;
+
+struct TcParams {
+  CUtensorMap tmap_k;
+  CUtensorMap tmap_v;
+  const __nv_bfloat16* q;
+  __nv_bfloat16* out;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  Workspace ws;
+  long long num_blocks;
+  int max_blocks_per_seq;
+  int num_seqs;
+  int max_len;
+  int H_q;
+  int G;
+  int block_size;
+  float scale_log2;
+};
+
+template <int D, int HPC, int NS>
+struct TcCfg {
+  static constexpr int NH = D / 64;
+  static constexpr int NBOX = 2 * HPC * NH;
+  static constexpr int KPART = HPC * NH * kBoxBytes;
+  static constexpr int STAGE = 2 * KPART;
+  static constexpr int THREADS = (HPC + 1) * 32;
+  static constexpr int BAR_OFF = NS * STAGE;
+  static constexpr int CSTART_OFF = BAR_OFF + 2 * NS * 8 + 16;
+  static constexpr int SMEM = CSTART_OFF + (kTcMaxSeqs + 1) * 4 + 1024;  // + alignment slack
+  static_assert(NBOX <= 32, "one TMA box per producer lane");
+};
+
+// Largest CTA index i whose range starts at or before chunk c.
+__device__ __forceinline__ int cta_of_chunk(long long c, long long T, int n) {
+  return (int)(((c + 1) * (long long)n - 1) / T);
+}
+
+// Largest s in [0, S) with cstart[s] <= c (c < cstart[S]).
+__device__ __forceinline__ int seq_of_chunk(const int* cstart, int S, int c) {
+  int lo = 0, hi = S;   // invariant: cstart[lo] <= c < cstart[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (cstart[mid] <= c) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+template <int D, int HPC, int NS>
+__global__ void __launch_bounds__(TcCfg<D, HPC, NS>::THREADS, 1)
+attn_tc_kernel(const __grid_constant__ TcParams p) {
+  using C = TcCfg<D, HPC, NS>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t bar_full = smem_u32(smem + C::BAR_OFF);   // + 8 * stage
+  const uint32_t bar_empty = bar_full + 8 * NS;
+  int* cstart = reinterpret_cast<int*>(smem + C::CSTART_OFF);
+  __shared__ int s_wsum[32];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int S = p.num_seqs;
+  const int K = p.block_size;
+  const int row_tokens = p.max_blocks_per_seq * K;
+
+  if (tid == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(bar_full + 8 * i, 1);
+      mbar_init(bar_empty + 8 * i, HPC);
+    }
+    fence_barrier_init();
+  }
+  pdl_wait_primary();
+
+  // ---- chunk prefix sums over the batch: cstart[s] = sum_{s'<s} ceil(L/16)
+  {
+    const int per = (S + C::THREADS - 1) / C::THREADS;
+    const int a = min(S, tid * per), b = min(S, a + per);
+    int local = 0;
+    for (int s = a; s < b; ++s)
+      local += (effective_len(p.context_lens[s], p.max_len, row_tokens) + kTcChunk - 1) / kTcChunk;
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) s_wsum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      int w = lane < (C::THREADS / 32) ? s_wsum[lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += v;
+      }
+      s_wsum[lane] = w;   // inclusive warp totals
+    }
+    __syncthreads();
+    int run = (warp ? s_wsum[warp - 1] : 0) + incl - local;
+    for (int s = a; s < b; ++s) {
+      cstart[s] = run;
+      run += (effective_len(p.context_lens[s], p.max_len, row_tokens) + kTcChunk - 1) / kTcChunk;
+    }
+    if (tid == C::THREADS - 1) cstart[S] = run;
+    __syncthreads();
+  }
+  pdl_launch_dependents();
+
+  const long long T = cstart[S];
+  const int n = gridDim.x, cta = blockIdx.x, group = blockIdx.y;
+  const int head0 = group * HPC;
+  const int G = p.G, H_q = p.H_q;
+  const int cb = (int)((long long)cta * T / n);
+  const int ce = (int)((long long)(cta + 1) * T / n);
+
+  // ---- bookkeeping: partial counts and zero outputs of empty sequences
+  for (int s = tid; s < S; s += C::THREADS) {
+    const int a = cstart[s], b = cstart[s + 1];
+    if (a == b) {
+      const int owner = a < T ? cta_of_chunk(a, T, n) : n - 1;
+      if (owner == cta) {
+        if (group == 0) p.ws.nparts[s] = 0;
+        __nv_bfloat16* o = p.out + ((int64_t)s * H_q + head0 * G) * D;
+        for (int i = 0; i < HPC * G * D; ++i) o[i] = __float2bfloat16_rn(0.f);
+      }
+    } else if (group == 0) {
+      const int first = cta_of_chunk(a, T, n);
+      if (first == cta) p.ws.nparts[s] = cta_of_chunk(b - 1, T, n) - first + 1;
+    }
+  }
+  if (cb >= ce) return;
+
+  if (warp == HPC) {
+    // =================== producer ===================
+    if (lane == 0) {
+      prefetch_tensormap(&p.tmap_k);
+      prefetch_tensormap(&p.tmap_v);
+    }
+    const uint64_t policy = l2_policy_evict_first();
+    int k = 0;
+    bool ok = true;
+    for (int c0 = cb; c0 < ce && ok; c0 += 32) {
+      // block-table entries of the next 32 chunks, one per lane
+      int row = 0;
+      const int c = c0 + lane;
+      if (c < ce) {
+        const int s = seq_of_chunk(cstart, S, c);
+        const int tok = (c - cstart[s]) * kTcChunk;
+        const int lb = tok / K;
+        const long long phys = p.block_tables[(int64_t)s * p.max_blocks_per_seq + lb];
+        if (phys < 0 || phys >= p.num_blocks) {
+          record_error(PKV_DEVERR_BLOCK_ID);
+          row = -2 * kTcChunk;          // whole box out of bounds: zero fill
+        } else {
+          row = (int)(phys * K + (tok - lb * K));
+        }
+      }
+      const int cnt = min(32, ce - c0);
+      for (int b = 0; b < cnt; ++b, ++k) {
+        const int r = __shfl_sync(0xffffffffu, row, b);
+        const int stage = k % NS;
+        const uint32_t parity = ((k / NS) & 1) ^ 1;
+        if (!mbar_wait_bounded(bar_empty + 8 * stage, parity)) {
+          record_error(PKV_DEVERR_TIMEOUT);
+          ok = false;
+          break;
+        }
+        if (lane == 0) mbar_arrive_expect_tx(bar_full + 8 * stage, C::STAGE);
+        __syncwarp();
+        if (lane < C::NBOX) {
+          const int kv = lane / (HPC * C::NH);
+          const int rem = lane - kv * (HPC * C::NH);
+          const int h = rem / C::NH, half = rem - h * C::NH;
+          const uint32_t dst = smem_u32(smem + stage * C::STAGE + kv * C::KPART +
+                                        (h * C::NH + half) * kBoxBytes);
+          tma_load_3d(dst, kv ? &p.tmap_v : &p.tmap_k, bar_full + 8 * stage, half * 64,
+                      head0 + h, r, policy);
+        }
+        __syncwarp();
+      }
+    }
+    if (!ok) {
+      // do not leave the CTA while our own copies may still land in smem
+      for (int kk = max(0, k - NS); kk < k; ++kk)
+        mbar_wait_bounded(bar_full + 8 * (kk % NS), (kk / NS) & 1);
+    }
+    return;
+  }
+
+  // =================== consumers ===================
+  const int w = warp;                 // KV head head0 + w
+  const int j = head0 + w;
+  const int g = lane >> 2, tq = lane & 3;
+  const float sl = p.scale_log2;
+
+  uint32_t qf[D / 16][2];
+  float o[D / 16][4];
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  int s = seq_of_chunk(cstart, S, cb);
+  int len_s = 0;
+  int k = 0;
+  for (int c = cb; c < ce; ++c, ++k) {
+    while (c >= cstart[s + 1]) ++s;
+    const int a = cstart[s], b = cstart[s + 1];
+    if (c == cb || c == a) {
+      // ---- new partition: load the q-group as the B fragments of Q^T
+      len_s = effective_len(p.context_lens[s], p.max_len, row_tokens);
+      const __nv_bfloat16* qrow = p.q + ((int64_t)s * H_q + j * G + g) * D;
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        if (g < G) {
+          qf[ks][0] = __ldg(reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 2 * tq));
+          qf[ks][1] = __ldg(reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 8 + 2 * tq));
+        } else {
+          qf[ks][0] = qf[ks][1] = 0u;
+        }
+      }
+#pragma unroll
+      for (int mt = 0; mt < D / 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+      m0 = m1 = -INFINITY;
+      l0 = l1 = 0.f;
+    }
+    const int valid = min(kTcChunk, len_s - (c - a) * kTcChunk);
+    const int stage = k % NS;
+    if (!mbar_wait_bounded(bar_full + 8 * stage, (k / NS) & 1)) {
+      record_error(PKV_DEVERR_TIMEOUT);
+      return;
+    }
+    uint8_t* kt = smem + stage * C::STAGE + w * C::NH * kBoxBytes;
+    uint8_t* vt = kt + C::KPART;
+    if (valid < kTcChunk) {
+      // rows past the sequence end may hold anything (stale slots, NaN):
+      // give them zero V so that 0-weight x V stays 0 in the tensor core
+      const int nvec = (kTcChunk - valid) * C::NH * 8;
+      for (int i = lane; i < nvec; i += 32) {
+        const int r = valid + i / (C::NH * 8);
+        const int rem = i % (C::NH * 8);
+        const int half = rem >> 3, ch = rem & 7;
+        *reinterpret_cast<uint4*>(vt + half * kBoxBytes + r * 128 + ch * 16) =
+            make_uint4(0u, 0u, 0u, 0u);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+    }
+    // ---- S^T[16 tok x 8 heads] = K_tile[16 x D] . Q^T[D x 8]
+    float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+    {
+      const int r = (lane & 7) + ((lane >> 3) & 1) * 8;
+      const int chs = lane >> 4;
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        const int half = ks >> 2;
+        const int ch = ((ks & 3) << 1) + chs;
+        const uint32_t addr = smem_u32(kt + half * kBoxBytes) + r * 128 + ((ch ^ (r & 7)) << 4);
+        uint32_t a0, a1, a2, a3;
+        ldmatrix_x4(addr, a0, a1, a2, a3);
+        mma_bf16_16816(sacc, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+      }
+    }
+    // ---- online softmax on (tok g / g+8) x (head 2tq / 2tq+1)
+    float x0 = sacc[0] * sl, x1 = sacc[1] * sl, x2 = sacc[2] * sl, x3 = sacc[3] * sl;
+    if (g >= valid) x0 = x1 = -INFINITY;
+    if (g + 8 >= valid) x2 = x3 = -INFINITY;
+    float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+    }
+    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+    const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
+    const float p0 = exp2f(x0 - mn0), p1 = exp2f(x1 - mn1);
+    const float p2 = exp2f(x2 - mn0), p3 = exp2f(x3 - mn1);
+    l0 = l0 * al0 + (p0 + p2);
+    l1 = l1 * al1 + (p1 + p3);
+    m0 = mn0;
+    m1 = mn1;
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) {
+      o[mt][0] *= al0;
+      o[mt][1] *= al1;
+      o[mt][2] *= al0;
+      o[mt][3] *= al1;
+    }
+    const uint32_t pb0 = movmatrix_trans(pack_bf16x2(p0, p1));
+    const uint32_t pb1 = movmatrix_trans(pack_bf16x2(p2, p3));
+    // ---- O^T[D x 8] += V^T[D x 16 tok] . P^T[16 tok x 8]
+    {
+      const int r = (lane & 7) + (lane >> 4) * 8;
+      const int chs = (lane >> 3) & 1;
+#pragma unroll
+      for (int mt = 0; mt < D / 16; ++mt) {
+        const int half = mt >> 2;
+        const int ch = ((mt & 3) << 1) + chs;
+        const uint32_t addr = smem_u32(vt + half * kBoxBytes) + r * 128 + ((ch ^ (r & 7)) << 4);
+        uint32_t a0, a1, a2, a3;
+        ldmatrix_x4_trans(addr, a0, a1, a2, a3);
+        mma_bf16_16816(o[mt], a0, a1, a2, a3, pb0, pb1);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_empty + 8 * stage);
+
+    if (c == ce - 1 || c == b - 1) {
+      // ---- end of partition: write the final output or a partial state
+      float lt0 = l0, lt1 = l1;
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        lt0 += __shfl_xor_sync(0xffffffffu, lt0, off);
+        lt1 += __shfl_xor_sync(0xffffffffu, lt1, off);
+      }
+      const int first = cta_of_chunk(a, T, n);
+      const int np = cta_of_chunk(b - 1, T, n) - first + 1;
+      const int part = cta - first;
+      const int n0 = 2 * tq, n1 = 2 * tq + 1;
+      if (np == 1) {
+        const float i0 = 1.f / lt0, i1 = 1.f / lt1;
+        __nv_bfloat16* orow = p.out + ((int64_t)s * H_q + j * G) * D;
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+          const int d0 = mt * 16 + g;
+          if (n0 < G) {
+            orow[n0 * D + d0] = __float2bfloat16_rn(o[mt][0] * i0);
+            orow[n0 * D + d0 + 8] = __float2bfloat16_rn(o[mt][2] * i0);
+          }
+          if (n1 < G) {
+            orow[n1 * D + d0] = __float2bfloat16_rn(o[mt][1] * i1);
+            orow[n1 * D + d0 + 8] = __float2bfloat16_rn(o[mt][3] * i1);
+          }
+        }
+      } else if (part < p.ws.pmax) {
+        const int64_t base = ((int64_t)s * p.ws.pmax + part) * H_q + j * G;
+        float* ob = p.ws.o + base * D;
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+          const int d0 = mt * 16 + g;
+          if (n0 < G) {
+            ob[n0 * D + d0] = o[mt][0];
+            ob[n0 * D + d0 + 8] = o[mt][2];
+          }
+          if (n1 < G) {
+            ob[n1 * D + d0] = o[mt][1];
+            ob[n1 * D + d0 + 8] = o[mt][3];
+          }
+        }
+        if (g == 0) {
+          if (n0 < G) p.ws.ml[base + n0] = make_float2(m0, lt0);
+          if (n1 < G) p.ws.ml[base + n1] = make_float2(m1, lt1);
+        }
+      }
+    }
+  }
+}
+
+}  // namespace pkv

@@ -1,0 +1,99 @@
+// Integer and data-movement kernels: slot mapping, slot-mapped KV append and
+// the copy-on-write block copy.  All of them are bit-exact byte moves or
+// integer arithmetic; every device-side index is range-checked before use.
+#pragma once
+
+#include "pkv_device.cuh"
+
+namespace pkv {
+
+// a1: slot of each sequence's new token ("推理与 KV Cache 02", 从一个位置找到
+// 缓存块: logical block = t / K, offset = t % K, slot = block * K + offset).
+// K need not be a power of two; when it is, the compiler's division by a
+// run-time value is replaced by the shift the host passes in (log2_bs >= 0).
+__global__ void slot_mapping_kernel(const int32_t* __restrict__ block_tables,
+                                    int32_t max_blocks_per_seq,
+                                    const int32_t* __restrict__ positions, int32_t num_seqs,
+                                    int32_t block_size, int32_t log2_bs, int64_t num_blocks,
+                                    int64_t* __restrict__ slot_mapping) {
+  const int s = blockIdx.x * blockDim.x + threadIdx.x;
+  if (s >= num_seqs) return;
+  const int t = positions[s];
+  int64_t slot = -1;
+  if (t >= 0) {
+    const int lb = log2_bs >= 0 ? (t >> log2_bs) : (t / block_size);
+    const int off = log2_bs >= 0 ? (t & (block_size - 1)) : (t - lb * block_size);
+    if (lb >= max_blocks_per_seq) {
+      record_error(PKV_DEVERR_POSITION);
+    } else {
+      const int64_t phys = block_tables[(int64_t)s * max_blocks_per_seq + lb];
+      if (phys < 0 || phys >= num_blocks) {
+        record_error(PKV_DEVERR_BLOCK_ID);
+      } else {
+        slot = phys * block_size + off;
+      }
+    }
+  }
+  slot_mapping[s] = slot;
+}
+
+template <int VW>
+struct VecT;
+template <> struct VecT<16> { using T = uint4; };
+template <> struct VecT<8>  { using T = uint2; };
+template <> struct VecT<4>  { using T = uint32_t; };
+template <> struct VecT<2>  { using T = uint16_t; };
+
+// a2: k_cache.view(-1, row)[slot[i]] = k[i] (and v).  grid = (tokens,
+// vector chunks of a row, 2 for K/V); one thread moves VW bytes.
+template <int VW>
+__global__ void kv_write_kernel(const uint8_t* __restrict__ k, const uint8_t* __restrict__ v,
+                                const int64_t* __restrict__ slot_mapping,
+                                uint8_t* __restrict__ k_cache, uint8_t* __restrict__ v_cache,
+                                int64_t num_slots, int64_t row_bytes) {
+  using V = typename VecT<VW>::T;
+  const int64_t i = blockIdx.x;
+  const int64_t e = (int64_t)blockIdx.y * blockDim.x + threadIdx.x;
+  if (e * VW >= row_bytes) return;
+  const int64_t slot = slot_mapping[i];
+  if (slot < 0 || slot >= num_slots) {
+    if (slot != -1 && e == 0 && blockIdx.z == 0) record_error(PKV_DEVERR_SLOT);
+    return;
+  }
+  const uint8_t* src = (blockIdx.z ? v : k) + i * row_bytes + e * VW;
+  uint8_t* dst = (blockIdx.z ? v_cache : k_cache) + slot * row_bytes + e * VW;
+  *reinterpret_cast<V*>(dst) = __ldg(reinterpret_cast<const V*>(src));
+}
+
+// a5: copy whole blocks, K and V.  grid = (pairs, chunks of a block, 2);
+// each thread moves UNROLL vectors, all loads before all stores.
+template <int VW, int UNROLL>
+__global__ void block_copy_kernel(uint8_t* __restrict__ k_cache, uint8_t* __restrict__ v_cache,
+                                  const int64_t* __restrict__ pairs, int64_t num_blocks,
+                                  int64_t block_bytes) {
+  using V = typename VecT<VW>::T;
+  const int64_t p = blockIdx.x;
+  const int64_t src = pairs[2 * p], dst = pairs[2 * p + 1];
+  if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+    if (threadIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) record_error(PKV_DEVERR_COPY_PAIR);
+    return;
+  }
+  uint8_t* base = blockIdx.z ? v_cache : k_cache;
+  const V* s = reinterpret_cast<const V*>(base + src * block_bytes);
+  V* d = reinterpret_cast<V*>(base + dst * block_bytes);
+  const int64_t nvec = block_bytes / VW;
+  const int64_t first = (int64_t)blockIdx.y * blockDim.x * UNROLL + threadIdx.x;
+  V buf[UNROLL];
+#pragma unroll
+  for (int u = 0; u < UNROLL; ++u) {
+    const int64_t e = first + (int64_t)u * blockDim.x;
+    if (e < nvec) buf[u] = s[e];
+  }
+#pragma unroll
+  for (int u = 0; u < UNROLL; ++u) {
+    const int64_t e = first + (int64_t)u * blockDim.x;
+    if (e < nvec) d[e] = buf[u];
+  }
+}
+
+}  // namespace pkv

@@ -1,0 +1,240 @@
+"""Thin torch-facing binding of libpagedkv (include/pagedkv.h).
+
+Argument marshalling only: every function checks devices / dtypes / shapes,
+passes raw device pointers and the current CUDA stream to the C ABI, and
+raises if the library reports an error.  All compute runs in the library's
+CUDA kernels; there is no CPU path.  Importing this module loads the shared
+library and raises ImportError when it has not been built.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+_LIB_PATH = _build.LIB_PATH
+
+if not os.path.exists(_LIB_PATH):
+    raise ImportError(
+        f"libpagedkv is not built ({_LIB_PATH} missing); run "
+        "`python -c 'import __graft_entry__ as g; g.build()'` on a machine with nvcc")
+
+_lib = ctypes.CDLL(_LIB_PATH)
+
+PKV_OK = 0
+PKV_ERR_DEVICE_CHECK = 5
+PKV_F32, PKV_BF16 = 0, 1
+
+DEVICE_ERRORS = {
+    0: "none", 1: "block id out of range", 2: "slot out of range", 3: "copy pair out of range",
+    4: "context length out of range", 5: "position beyond block-table row", 6: "pipeline timeout",
+}
+
+c_i32, c_i64, c_vp, c_sz, c_f = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_float
+
+
+class AttentionConfig(ctypes.Structure):
+    _fields_ = [("kernel", c_i32), ("num_splits", c_i32), ("reserved", c_i32 * 6)]
+
+
+def _sig(name, restype, *argtypes):
+    f = getattr(_lib, name)
+    f.restype = restype
+    f.argtypes = list(argtypes)
+    return f
+
+
+_status_string = _sig("pkv_status_string", ctypes.c_char_p, c_i32)
+_last_msg = _sig("pkv_last_error_message", ctypes.c_char_p)
+_version = _sig("pkv_version", c_i32)
+_slot_mapping = _sig("pkv_slot_mapping", c_i32, c_vp, c_i32, c_vp, c_i32, c_i32, c_i64, c_vp, c_vp)
+_kv_write = _sig("pkv_kv_write", c_i32, c_vp, c_vp, c_vp, c_i64, c_vp, c_vp, c_i64, c_i32, c_i32,
+                 c_i32, c_i32, c_vp)
+_block_copy = _sig("pkv_kv_block_copy", c_i32, c_vp, c_vp, c_vp, c_i64, c_i64, c_i32, c_i32, c_i32,
+                   c_i32, c_vp)
+_ws_bytes = _sig("pkv_attention_workspace_bytes", c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, c_i32,
+                 c_i32, ctypes.POINTER(AttentionConfig), ctypes.POINTER(c_sz))
+_launch_count = _sig("pkv_attention_launch_count", c_i32, c_i32, c_i32, c_i32, c_i32, c_i32,
+                     c_i32, c_i32, ctypes.POINTER(AttentionConfig), ctypes.POINTER(c_i32))
+_attention = _sig("pkv_attention_decode", c_i32, c_vp, c_vp, c_vp, c_vp, c_i32, c_vp, c_i32, c_i32,
+                  c_i32, c_i32, c_i32, c_i32, c_i64, c_f, c_vp, c_vp, c_sz, c_i32,
+                  ctypes.POINTER(AttentionConfig), c_vp)
+_dev_error = _sig("pkv_get_device_error", c_i32, ctypes.POINTER(c_i32), c_vp)
+
+EXPORTED = ("pkv_status_string", "pkv_last_error_message", "pkv_version", "pkv_slot_mapping",
+            "pkv_kv_write", "pkv_kv_block_copy", "pkv_attention_workspace_bytes",
+            "pkv_attention_launch_count", "pkv_attention_decode", "pkv_get_device_error")
+
+
+class PagedKVError(RuntimeError):
+    pass
+
+
+def _check(status: int, what: str) -> None:
+    if status != PKV_OK:
+        raise PagedKVError(f"{what}: {_status_string(status).decode()} "
+                           f"({_last_msg().decode()})")
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return PKV_BF16
+    if t.dtype == torch.float32:
+        return PKV_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _stream(device: torch.device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype=None, dim=None) -> None:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if dim is not None and t.dim() != dim:
+        raise ValueError(f"{name} must have {dim} dims, got {t.dim()}")
+
+
+def _ptr(t: torch.Tensor) -> ctypes.c_void_p:
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def version() -> int:
+    return int(_version())
+
+
+def slot_mapping(block_tables: torch.Tensor, positions: torch.Tensor, block_size: int,
+                 num_blocks: int, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """int64 slot of each sequence's token at ``positions`` (-1 for padding)."""
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(positions, "positions", torch.int32, 1)
+    S = positions.shape[0]
+    if out is None:
+        out = torch.empty(S, dtype=torch.int64, device=positions.device)
+    _need(out, "out", torch.int64, 1)
+    _check(_slot_mapping(_ptr(block_tables), block_tables.shape[1], _ptr(positions), S,
+                         block_size, num_blocks, _ptr(out), _stream(positions.device)),
+           "pkv_slot_mapping")
+    return out
+
+
+def paged_kv_write(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
+                   k_cache: torch.Tensor, v_cache: torch.Tensor) -> None:
+    """k_cache.view(-1, H_kv, D)[slot_mapping[i]] = k[i] (same for v), in place."""
+    _need(k_cache, "k_cache", None, 4)
+    _need(v_cache, "v_cache", k_cache.dtype, 4)
+    if v_cache.shape != k_cache.shape:
+        raise ValueError("k_cache and v_cache shapes differ")
+    nb, K, H, D = k_cache.shape
+    _need(k, "k", k_cache.dtype, 3)
+    _need(v, "v", k_cache.dtype, 3)
+    _need(slot_mapping, "slot_mapping", torch.int64, 1)
+    T = k.shape[0]
+    if tuple(k.shape) != (T, H, D) or tuple(v.shape) != (T, H, D) or slot_mapping.shape[0] != T:
+        raise ValueError("k/v/slot_mapping shapes do not match the pool")
+    _check(_kv_write(_ptr(k), _ptr(v), _ptr(slot_mapping), T, _ptr(k_cache), _ptr(v_cache), nb, K,
+                     H, D, _dtype_code(k_cache), _stream(k_cache.device)), "pkv_kv_write")
+
+
+def kv_block_copy(k_cache: torch.Tensor, v_cache: torch.Tensor,
+                  src_dst_pairs: torch.Tensor) -> None:
+    """Copy-on-write block copy: block dst <- block src for each row of pairs."""
+    _need(k_cache, "k_cache", None, 4)
+    _need(v_cache, "v_cache", k_cache.dtype, 4)
+    _need(src_dst_pairs, "src_dst_pairs", torch.int64, 2)
+    nb, K, H, D = k_cache.shape
+    _check(_block_copy(_ptr(k_cache), _ptr(v_cache), _ptr(src_dst_pairs), src_dst_pairs.shape[0],
+                       nb, K, H, D, _dtype_code(k_cache), _stream(k_cache.device)),
+           "pkv_kv_block_copy")
+
+
+def _cfg(kernel: int, num_splits: int) -> AttentionConfig:
+    c = AttentionConfig()
+    c.kernel = kernel
+    c.num_splits = num_splits
+    return c
+
+
+def attention_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                              max_context_len, dtype: torch.dtype, kernel: int = 0,
+                              num_splits: int = 0) -> int:
+    out = c_sz(0)
+    cfg = _cfg(kernel, num_splits)
+    code = PKV_BF16 if dtype == torch.bfloat16 else PKV_F32
+    _check(_ws_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_context_len,
+                     code, ctypes.byref(cfg), ctypes.byref(out)), "pkv_attention_workspace_bytes")
+    return int(out.value)
+
+
+def attention_launch_count(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                           max_context_len, dtype: torch.dtype, kernel: int = 0,
+                           num_splits: int = 0) -> int:
+    """Kernel launches one paged_attention_decode call makes for these sizes."""
+    out = c_i32(0)
+    cfg = _cfg(kernel, num_splits)
+    code = PKV_BF16 if dtype == torch.bfloat16 else PKV_F32
+    _check(_launch_count(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                         max_context_len, code, ctypes.byref(cfg), ctypes.byref(out)),
+           "pkv_attention_launch_count")
+    return int(out.value)
+
+
+def paged_attention_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                           block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                           out: Optional[torch.Tensor] = None,
+                           max_context_len: Optional[int] = None,
+                           workspace: Optional[torch.Tensor] = None,
+                           kernel: int = 0, num_splits: int = 0) -> torch.Tensor:
+    """Decode attention over the paged cache (GQA, split-K).
+
+    ``max_context_len`` is a host-side bound on ``context_lens``; when omitted
+    it is read from the device (one synchronising copy).  ``workspace`` is a
+    uint8 CUDA tensor of at least :func:`attention_workspace_bytes` bytes;
+    when omitted one is allocated with torch.
+    """
+    _need(q, "q", None, 3)
+    _need(k_cache, "k_cache", q.dtype, 4)
+    _need(v_cache, "v_cache", q.dtype, 4)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(context_lens, "context_lens", torch.int32, 1)
+    S, H_q, D = q.shape
+    nb, K, H_kv, D2 = k_cache.shape
+    if D2 != D or v_cache.shape != k_cache.shape or context_lens.shape[0] != S \
+            or block_tables.shape[0] != S:
+        raise ValueError("shape mismatch between q, caches, tables and lengths")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", q.dtype, 3)
+    if max_context_len is None:
+        max_context_len = int(context_lens.max().item()) if S else 0
+    need = attention_workspace_bytes(S, H_q, H_kv, D, K, max_context_len, q.dtype, kernel,
+                                     num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _need(workspace, "workspace", torch.uint8, 1)
+    cfg = _cfg(kernel, num_splits)
+    _check(_attention(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                      block_tables.shape[1], _ptr(context_lens), max_context_len, S, H_q, H_kv, D,
+                      K, nb, float(scale), _ptr(out), _ptr(workspace), workspace.numel(),
+                      _dtype_code(q), ctypes.byref(cfg), _stream(q.device)),
+           "pkv_attention_decode")
+    return out
+
+
+def get_device_error(device=None) -> int:
+    """Synchronise, read and clear the library's device error word (0 = none)."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    code = c_i32(0)
+    st = _dev_error(ctypes.byref(code), _stream(dev))
+    if st not in (PKV_OK, PKV_ERR_DEVICE_CHECK):
+        _check(st, "pkv_get_device_error")
+    return int(code.value)
