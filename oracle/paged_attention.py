@@ -48,14 +48,18 @@ __all__ = [
 def decode(x: np.ndarray, dtype: str) -> np.ndarray:
     """Exact conversion of stored values to float64.
 
-    ``"f32"``: IEEE binary32 values, widened exactly.
+    ``"f32"``: IEEE binary32 values (float32, or their uint32 bit patterns),
+    widened exactly.
     ``"bf16"``: bfloat16 bit patterns (uint16).  A bfloat16 number is the upper
     half of the binary32 number with the same sign, exponent and leading seven
     mantissa bits, so shifting the pattern into the high 16 bits of a 32-bit
     word gives that binary32 number exactly.
     """
     if dtype == "f32":
-        return np.asarray(x, dtype=np.float32).astype(np.float64)
+        a = np.asarray(x)
+        if a.dtype == np.uint32:
+            a = a.view(np.float32)
+        return a.astype(np.float32).astype(np.float64)
     if dtype == "bf16":
         bits = np.asarray(x).view(np.uint16).astype(np.uint32) << np.uint32(16)
         return bits.view(np.float32).astype(np.float64)

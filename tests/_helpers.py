@@ -10,12 +10,13 @@ F32_ATOL = 1e-5
 
 
 def storage(t: torch.Tensor) -> np.ndarray:
-    """CPU numpy view of a tensor's raw storage (uint16 bits for bf16)."""
+    """CPU numpy view of a tensor's raw storage: uint16 bits for bf16, uint32
+    bits for fp32 (so that NaN canaries compare bit for bit)."""
     t = t.detach().cpu().contiguous()
     if t.dtype == torch.bfloat16:
         return t.view(torch.int16).numpy().view(np.uint16)
     if t.dtype == torch.float32:
-        return t.numpy()
+        return t.view(torch.int32).numpy().view(np.uint32)
     return t.numpy()
 
 

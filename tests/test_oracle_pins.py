@@ -93,6 +93,8 @@ def pin_decode():
     assert np.isnan(oracle.decode(np.array([0x7FC1], np.uint16), "bf16")[0])
     f = np.array([1.5, -2.25e-30, 3.4e38], dtype=np.float32)
     assert np.array_equal(oracle.decode(f, "f32"), f.astype(np.float64))
+    assert np.array_equal(oracle.decode(f.view(np.uint32), "f32"), f.astype(np.float64))
+    assert oracle.decode(np.array([0x3F800000], np.uint32), "f32")[0] == 1.0
 
 
 # --------------------------------------------------------------------------
