@@ -351,11 +351,15 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
   pdl_launch_dependents();
 
   const long long T = cstart[S];
-  const int n = gridDim.x, cta = blockIdx.x, group = blockIdx.y;
+  // Split over at most T CTAs so that every working CTA owns >= 1 chunk and a
+  // sequence's partial index (CTA - first CTA of the sequence) stays below
+  // min(n, chunks of the sequence) <= Pmax.  CTAs past n only do bookkeeping.
+  const int n = (int)(T < (long long)gridDim.x ? (T > 0 ? T : 1) : (long long)gridDim.x);
+  const int cta = blockIdx.x, group = blockIdx.y;
   const int head0 = group * HPC;
   const int G = p.G, H_q = p.H_q;
-  const int cb = (int)((long long)cta * T / n);
-  const int ce = (int)((long long)(cta + 1) * T / n);
+  const int cb = cta < n ? (int)((long long)cta * T / n) : 0;
+  const int ce = cta < n ? (int)((long long)(cta + 1) * T / n) : 0;
 
   // ---- bookkeeping: partial counts and zero outputs of empty sequences
   for (int s = tid; s < S; s += C::THREADS) {
