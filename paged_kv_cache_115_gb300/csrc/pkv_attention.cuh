@@ -530,8 +530,14 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
       o[mt][2] *= al0;
       o[mt][3] *= al1;
     }
-    const uint32_t pb0 = movmatrix_trans(pack_bf16x2(p0, p1));
-    const uint32_t pb1 = movmatrix_trans(pack_bf16x2(p2, p3));
+    // P enters the tensor core as bf16: split it into hi + lo bf16 terms so
+    // that the product carries ~16 significant bits of each weight (a single
+    // bf16 rounding of P costs up to 2^-9 relative per weight)
+    uint32_t ph01, pl01, ph23, pl23;
+    split_bf16x2(p0, p1, ph01, pl01);
+    split_bf16x2(p2, p3, ph23, pl23);
+    const uint32_t pb0 = movmatrix_trans(ph01), pb1 = movmatrix_trans(ph23);
+    const uint32_t pc0 = movmatrix_trans(pl01), pc1 = movmatrix_trans(pl23);
     // ---- O^T[D x 8] += V^T[D x 16 tok] . P^T[16 tok x 8]
     {
       const int r = (lane & 7) + (lane >> 4) * 8;
@@ -544,6 +550,7 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
         uint32_t a0, a1, a2, a3;
         ldmatrix_x4_trans(addr, a0, a1, a2, a3);
         mma_bf16_16816(o[mt], a0, a1, a2, a3, pb0, pb1);
+        mma_bf16_16816(o[mt], a0, a1, a2, a3, pc0, pc1);
       }
     }
     __syncwarp();

@@ -142,6 +142,16 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// (a, b) -> bf16 pairs hi = rn(a, b) and lo = rn(a - hi.a, b - hi.b), so that
+// hi + lo represents a and b to about 16 significant bits.
+__device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  const float2 hf = __bfloat1622float2(h);
+  __nv_bfloat162 l = __floats2bfloat162_rn(a - hf.x, b - hf.y);
+  hi = *reinterpret_cast<uint32_t*>(&h);
+  lo = *reinterpret_cast<uint32_t*>(&l);
+}
+
 // Programmatic dependent launch: let the next kernel in the stream start its
 // prologue / wait for the previous kernel's memory to be visible.
 __device__ __forceinline__ void pdl_launch_dependents() {
