@@ -201,6 +201,26 @@ def run_cpu_baseline(name: str, seed: int, budget_s: float) -> dict:
 
 
 # ---------------------------------------------------------------------------
+# multi-rank helpers (one process per GPU; no collective on the data path)
+# ---------------------------------------------------------------------------
+def max_over_ranks(values, device):
+    """Element-wise maximum of per-rank timings (the slowest rank sets the
+    job's time).  A no-op without an initialised process group."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def rank_seed(base_seed: int, rank: int) -> int:
+    """Each rank draws its own replica of the workload (weak scaling)."""
+    return base_seed + rank
+
+
+# ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
 def run_gpu(args):
@@ -224,8 +244,9 @@ def run_gpu(args):
         dist.barrier()
     from paged_kv_cache_115_gb300 import ops
 
-    w = wl.build(args.workload, seed=args.seed + rank)
-    t = wl.materialize(w, device=dev, seed=args.seed + rank, canary=False, values_device="cuda")
+    w = wl.build(args.workload, seed=rank_seed(args.seed, rank))
+    t = wl.materialize(w, device=dev, seed=rank_seed(args.seed, rank), canary=False,
+                       values_device="cuda")
     kv_bytes = accounting.attention_kv_bytes(w.context_lens, w.num_kv_heads, w.head_dim,
                                              w.elem_bytes)
     stream = torch.cuda.current_stream(dev)
@@ -316,10 +337,7 @@ def run_gpu(args):
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
 
     # ---- max over ranks
-    vals = torch.tensor([total_ms, e2e_ms, attn_avg_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
-    total_ms, e2e_ms, attn_avg_ms = vals.tolist()
+    total_ms, e2e_ms, attn_avg_ms = max_over_ranks([total_ms, e2e_ms, attn_avg_ms], dev)
     ms_step = total_ms / K
     value = world * kv_bytes / (ms_step * 1e-3) / 1e9
     e2e_value = world * kv_bytes / (e2e_ms * 1e-3) / 1e9
