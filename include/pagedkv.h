@@ -186,6 +186,37 @@ PKV_API pkv_status pkv_attention_decode(const void* q, const void* k_cache, cons
                                 const pkv_attention_config* config, void* stream);
 
 /*
+ * pkv_attention_decode without a caller-provided workspace.
+ *
+ * The pages have no counterpart to this call; it exists for callers that
+ * cannot allocate device memory when they run attention.  Examples: an
+ * inference engine that handed nearly all free HBM to its KV-cache pool at
+ * start-up, so a cudaMalloc at decode time would fail; and code that must
+ * not enter the CUDA allocator on the decode path at all, because cudaMalloc
+ * and cudaFree can synchronise the device.  Here the split-K scratch lives in
+ * a fixed array inside the library (PKV_NOALLOC_SCRATCH_BYTES, 64 MiB, held
+ * on every GPU that loads the library until the process exits).  The call
+ * allocates nothing.
+ *
+ * Arguments and results are those of pkv_attention_decode.  Sizes whose
+ * scratch (pkv_attention_workspace_bytes) exceeds PKV_NOALLOC_SCRATCH_BYTES
+ * are rejected with PKV_ERR_WORKSPACE_TOO_SMALL before anything is launched.
+ * The first call on a device looks up that device's copy of the array
+ * (cudaGetSymbolAddress) with the device current; make that first call
+ * before any stream capture.  All calls on a device share the one array:
+ * calls that overlap on the GPU (different streams, no ordering between
+ * them) race on it and give undefined results.  No initial contents are
+ * needed; whatever a previous call left there is overwritten before use.
+ */
+#define PKV_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+PKV_API pkv_status pkv_attention_decode_noalloc(
+    const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+    int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t max_context_len,
+    int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+    int32_t block_size, int64_t num_blocks, float scale, void* out, pkv_dtype dtype,
+    const pkv_attention_config* config, void* stream);
+
+/*
  * Synchronises `stream`, copies the current device's error word into *code
  * (a PKV_DEVERR_* value) and clears it.  Returns PKV_ERR_DEVICE_CHECK when
  * the word was non-zero, PKV_OK when it was zero.

@@ -320,6 +320,32 @@ int vec_width(int64_t row_bytes, std::initializer_list<const void*> ptrs) {
   return 0;
 }
 
+// ---- fixed scratch for pkv_attention_decode_noalloc ---------------------------
+// In host code this name is only a host-side stand-in for the array; the
+// device address is looked up per device with cudaGetSymbolAddress.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[PKV_NOALLOC_SCRATCH_BYTES];
+
+struct NoAllocScratch {
+  std::once_flag once;
+  void* ptr = nullptr;
+  cudaError_t err = cudaSuccess;
+};
+NoAllocScratch g_noalloc[kMaxDevices];
+
+// Device address of this device's copy of the scratch array (set up once per
+// device, with that device current).
+pkv_status noalloc_scratch(void** ptr) {
+  int dev = 0;
+  PKV_CUDA(cudaGetDevice(&dev));
+  PKV_CHECK(dev >= 0 && dev < kMaxDevices, PKV_ERR_UNSUPPORTED, "device ordinal %d too large", dev);
+  NoAllocScratch& sc = g_noalloc[dev];
+  std::call_once(sc.once, [&] { sc.err = cudaGetSymbolAddress(&sc.ptr, g_noalloc_scratch); });
+  if (sc.err != cudaSuccess || sc.ptr == nullptr)
+    return fail(PKV_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(sc.err));
+  *ptr = sc.ptr;
+  return PKV_OK;
+}
+
 }  // namespace
 
 // =============================================================================
@@ -548,6 +574,31 @@ pkv_status pkv_attention_decode(const void* q, const void* k_cache, const void* 
     }
   }
   return PKV_OK;
+}
+
+pkv_status pkv_attention_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                        const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                        const int32_t* context_lens, int32_t max_context_len,
+                                        int32_t num_seqs, int32_t num_q_heads,
+                                        int32_t num_kv_heads, int32_t head_dim,
+                                        int32_t block_size, int64_t num_blocks, float scale,
+                                        void* out, pkv_dtype dtype,
+                                        const pkv_attention_config* config, void* stream) {
+  size_t need = 0;
+  pkv_status st = pkv_attention_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                                block_size, max_context_len, dtype, config, &need);
+  if (st != PKV_OK) return st;
+  PKV_CHECK(need <= PKV_NOALLOC_SCRATCH_BYTES, PKV_ERR_WORKSPACE_TOO_SMALL,
+            "these sizes need %zu bytes of scratch; the fixed scratch holds %u bytes "
+            "(use pkv_attention_decode with a larger workspace)",
+            need, (unsigned)PKV_NOALLOC_SCRATCH_BYTES);
+  void* scratch = nullptr;
+  st = noalloc_scratch(&scratch);
+  if (st != PKV_OK) return st;
+  return pkv_attention_decode(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                              max_context_len, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                              block_size, num_blocks, scale, out, scratch,
+                              PKV_NOALLOC_SCRATCH_BYTES, dtype, config, stream);
 }
 
 pkv_status pkv_get_device_error(int32_t* code, void* stream) {

@@ -64,11 +64,18 @@ _launch_count = _sig("pkv_attention_launch_count", c_i32, c_i32, c_i32, c_i32, c
 _attention = _sig("pkv_attention_decode", c_i32, c_vp, c_vp, c_vp, c_vp, c_i32, c_vp, c_i32, c_i32,
                   c_i32, c_i32, c_i32, c_i32, c_i64, c_f, c_vp, c_vp, c_sz, c_i32,
                   ctypes.POINTER(AttentionConfig), c_vp)
+_attention_noalloc = _sig("pkv_attention_decode_noalloc", c_i32, c_vp, c_vp, c_vp, c_vp, c_i32,
+                          c_vp, c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, c_i64, c_f, c_vp, c_i32,
+                          ctypes.POINTER(AttentionConfig), c_vp)
 _dev_error = _sig("pkv_get_device_error", c_i32, ctypes.POINTER(c_i32), c_vp)
+
+# bytes of the library's fixed attention scratch (PKV_NOALLOC_SCRATCH_BYTES)
+NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 EXPORTED = ("pkv_status_string", "pkv_last_error_message", "pkv_version", "pkv_slot_mapping",
             "pkv_kv_write", "pkv_kv_block_copy", "pkv_attention_workspace_bytes",
-            "pkv_attention_launch_count", "pkv_attention_decode", "pkv_get_device_error")
+            "pkv_attention_launch_count", "pkv_attention_decode",
+            "pkv_attention_decode_noalloc", "pkv_get_device_error")
 
 
 class PagedKVError(RuntimeError):
@@ -227,6 +234,39 @@ def paged_attention_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
                       K, nb, float(scale), _ptr(out), _ptr(workspace), workspace.numel(),
                       _dtype_code(q), ctypes.byref(cfg), _stream(q.device)),
            "pkv_attention_decode")
+    return out
+
+
+def paged_attention_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor,
+                                   v_cache: torch.Tensor, block_tables: torch.Tensor,
+                                   context_lens: torch.Tensor, scale: float,
+                                   out: torch.Tensor, max_context_len: int,
+                                   kernel: int = 0, num_splits: int = 0) -> torch.Tensor:
+    """Same result as :func:`paged_attention_decode`, for callers that cannot
+    allocate device memory at this point (an engine whose KV pool took the free
+    HBM, or a decode path that must stay out of the CUDA allocator).  The
+    split-K scratch is the library's fixed in-module array, so ``out`` must be
+    given, ``max_context_len`` must be a host value, and nothing here (torch
+    included) allocates.  Sizes needing more than NOALLOC_SCRATCH_BYTES of
+    scratch raise.  Calls that overlap on the GPU share that scratch and race.
+    """
+    _need(q, "q", None, 3)
+    _need(k_cache, "k_cache", q.dtype, 4)
+    _need(v_cache, "v_cache", q.dtype, 4)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(context_lens, "context_lens", torch.int32, 1)
+    _need(out, "out", q.dtype, 3)
+    S, H_q, D = q.shape
+    nb, K, H_kv, D2 = k_cache.shape
+    if D2 != D or v_cache.shape != k_cache.shape or context_lens.shape[0] != S \
+            or block_tables.shape[0] != S or out.shape != q.shape:
+        raise ValueError("shape mismatch between q, caches, tables, lengths and out")
+    cfg = _cfg(kernel, num_splits)
+    _check(_attention_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                              block_tables.shape[1], _ptr(context_lens), int(max_context_len), S,
+                              H_q, H_kv, D, K, nb, float(scale), _ptr(out), _dtype_code(q),
+                              ctypes.byref(cfg), _stream(q.device)),
+           "pkv_attention_decode_noalloc")
     return out
 
 
