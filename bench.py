@@ -31,7 +31,10 @@ sys.path.insert(0, ROOT)
 
 METRIC = "paged decode attention KV GB/s (% of GB300 HBM peak); decode tokens/s per layer"
 DEFAULT_WORKLOAD = "qwen3_0_6b"
-KERNEL_SRC = ["paged_kv_cache_115_gb300/csrc/pkv_attention.cuh",
+# sources of the dominant kernel (attn_tc_kernel); a recorded DRAM-traffic
+# figure is used only while these files are unchanged
+KERNEL_SRC = ["paged_kv_cache_115_gb300/csrc/pkv_attention_tc.cuh",
+              "paged_kv_cache_115_gb300/csrc/pkv_attention_common.cuh",
               "paged_kv_cache_115_gb300/csrc/pkv_device.cuh"]
 
 

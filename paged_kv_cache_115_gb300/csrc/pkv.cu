@@ -10,7 +10,9 @@
 #include <mutex>
 #include <string>
 
-#include "pkv_attention.cuh"
+#include "pkv_attention_simt.cuh"
+#include "pkv_attention_tc.cuh"
+#include "pkv_reduce.cuh"
 #include "pkv_copy.cuh"
 #include "pkv_device.cuh"
 
@@ -309,6 +311,22 @@ pkv_status launch_simt(int D, int G, const void* q, const void* kc, const void* 
   }
 }
 
+// ---- split-K reduce dispatch -----------------------------------------------------
+template <typename T>
+pkv_status launch_reduce(int D, pkv::Workspace ws, int S, int H_q, void* out, cudaStream_t st) {
+  const int64_t pairs = (int64_t)S * H_q;
+  const dim3 grid((unsigned)ceil_div(pairs, pkv::kReduceWarps));
+  const dim3 block(pkv::kReduceWarps * 32);
+  T* o = static_cast<T*>(out);
+  switch (D) {
+    case 32: PKV_CUDA(launch_pdl(pkv::attn_reduce_kernel<T, 32>, grid, block, 0, st, ws, S, H_q, o)); break;
+    case 64: PKV_CUDA(launch_pdl(pkv::attn_reduce_kernel<T, 64>, grid, block, 0, st, ws, S, H_q, o)); break;
+    case 128: PKV_CUDA(launch_pdl(pkv::attn_reduce_kernel<T, 128>, grid, block, 0, st, ws, S, H_q, o)); break;
+    default: PKV_CUDA(launch_pdl(pkv::attn_reduce_kernel<T, 256>, grid, block, 0, st, ws, S, H_q, o)); break;
+  }
+  return PKV_OK;
+}
+
 // Widest vector (16/8/4/2 bytes) that divides the row and every base pointer.
 int vec_width(int64_t row_bytes, std::initializer_list<const void*> ptrs) {
   for (int w : {16, 8, 4, 2}) {
@@ -564,13 +582,10 @@ pkv_status pkv_attention_decode(const void* q, const void* k_cache, const void* 
     }
     if (st != PKV_OK) return st;
     if (plan.pmax > 1) {
-      if (dtype == PKV_BF16) {
-        PKV_CUDA(launch_pdl(pkv::attn_reduce_kernel<__nv_bfloat16>, dim3(S), dim3(128), 0, strm, ws,
-                            H_q, D, reinterpret_cast<__nv_bfloat16*>(ob)));
-      } else {
-        PKV_CUDA(launch_pdl(pkv::attn_reduce_kernel<float>, dim3(S), dim3(128), 0, strm, ws, H_q,
-                            D, reinterpret_cast<float*>(ob)));
-      }
+      st = dtype == PKV_BF16
+               ? launch_reduce<__nv_bfloat16>(D, ws, S, H_q, ob, strm)
+               : launch_reduce<float>(D, ws, S, H_q, ob, strm);
+      if (st != PKV_OK) return st;
     }
   }
   return PKV_OK;

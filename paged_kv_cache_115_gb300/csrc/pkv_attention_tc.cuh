@@ -1,219 +1,9 @@
-// Decode attention over the paged KV cache: partition kernels and the split-K
-// reduce.
-//
-// What is computed ("19.2 KV Cache 系统化管理" §19.2.3 paged_attention;
-// "KV Cache：长上下文为什么吃显存" §01/§02): for sequence s and query head h
-// (KV head j = h / G), out = softmax(scale * q . K_j[0:L]) V_j[0:L], with K/V
-// rows found through the block table (token t -> block bt[s][t / K], offset
-// t % K).  Scores and weights are kept in the base-2 domain
-// (x = scale * log2(e) * q.k, weight = 2^(x - max)), which is the same
-// softmax.  Every kernel keeps the running maximum m, the running sum l and
-// the unnormalised output o of the page's block loop; partial states of one
-// (s, h) are merged by attn_reduce_kernel with
-//   M = max m_p,  l = sum l_p 2^(m_p - M),  out = sum o_p 2^(m_p - M) / l.
-//
-// Workspace layout (per launch batch of sequences, Pmax partials per seq):
-//   int    nparts[S]                   partials written for s (0: empty seq,
-//                                      1: output already final)
-//   float2 ml[S][Pmax][H_q]            (m, l) of each partial
-//   float  o [S][Pmax][H_q][D]         unnormalised partial outputs
+// TMA + tensor-core decode-attention partition kernel (bf16).
 #pragma once
 
-#include "pkv_device.cuh"
+#include "pkv_attention_common.cuh"
 
 namespace pkv {
-
-struct Workspace {
-  int* nparts;
-  float2* ml;
-  float* o;
-  int pmax;
-};
-
-// ===========================================================================
-// CUDA-core partition kernel (fp32 or bf16, any block size, G <= 16).
-// grid = (Pmax, H_kv, S), block = 128 threads; CTA (p, j, s) covers tokens
-// [p*PS, min((p+1)*PS, L)) of sequence s for the G query heads of KV head j.
-// Each warp takes every 4th token; the four warps' states are merged in
-// shared memory.
-// ===========================================================================
-constexpr int kSimtThreads = 128;
-constexpr int kSimtMaxPS = 1024;
-
-template <typename T, int D, int GMAX>
-__global__ void __launch_bounds__(kSimtThreads)
-attn_simt_kernel(const T* __restrict__ q, const T* __restrict__ k_cache,
-                 const T* __restrict__ v_cache, const int32_t* __restrict__ block_tables,
-                 int max_blocks_per_seq, const int32_t* __restrict__ context_lens, int max_len,
-                 int H_q, int H_kv, int G, int K, long long num_blocks, float scale_log2,
-                 T* __restrict__ out, Workspace ws, int PS) {
-  constexpr int E = D / 32;   // elements of a row per lane
-  __shared__ int s_bt[kSimtMaxPS + 2];
-  __shared__ float s_m[4][GMAX], s_l[4][GMAX];
-  __shared__ float s_o[GMAX][D];
-
-  pdl_wait_primary();
-  pdl_launch_dependents();
-
-  const int p = blockIdx.x, j = blockIdx.y, s = blockIdx.z;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int L = effective_len(context_lens[s], max_len, max_blocks_per_seq * K);
-  const int np = (L + PS - 1) / PS;
-  if (p == 0 && j == 0 && threadIdx.x == 0) ws.nparts[s] = np;
-  if (L == 0) {
-    if (p == 0) {
-      for (int i = threadIdx.x; i < G * D; i += blockDim.x)
-        out[((int64_t)s * H_q + j * G) * D + i] = from_f32<T>(0.f);
-    }
-    return;
-  }
-  if (p >= np) return;
-  const int t0 = p * PS, t1 = min(t0 + PS, L);
-  const int lb0 = t0 / K, nlb = (t1 - 1) / K - lb0 + 1;
-  for (int i = threadIdx.x; i < nlb; i += blockDim.x) {
-    int phys = block_tables[(int64_t)s * max_blocks_per_seq + lb0 + i];
-    if (phys < 0 || phys >= num_blocks) {
-      record_error(PKV_DEVERR_BLOCK_ID);
-      phys = -1;
-    }
-    s_bt[i] = phys;
-  }
-  for (int i = threadIdx.x; i < GMAX * D; i += blockDim.x) (&s_o[0][0])[i] = 0.f;
-
-  float qr[GMAX][E];
-#pragma unroll
-  for (int n = 0; n < GMAX; ++n)
-#pragma unroll
-    for (int e = 0; e < E; ++e)
-      qr[n][e] = n < G ? to_f32(q[((int64_t)s * H_q + j * G + n) * D + lane + 32 * e]) : 0.f;
-  __syncthreads();
-
-  float m[GMAX], l[GMAX], o[GMAX][E];
-#pragma unroll
-  for (int n = 0; n < GMAX; ++n) {
-    m[n] = -INFINITY;
-    l[n] = 0.f;
-#pragma unroll
-    for (int e = 0; e < E; ++e) o[n][e] = 0.f;
-  }
-  for (int t = t0 + warp; t < t1; t += 4) {
-    const int lbi = t / K - lb0;
-    const int phys = s_bt[lbi];
-    const int off = t - (t / K) * K;
-    float kr[E], vr[E];
-    if (phys >= 0) {
-      const int64_t row = (((int64_t)phys * K + off) * H_kv + j) * D;
-#pragma unroll
-      for (int e = 0; e < E; ++e) {
-        kr[e] = to_f32(k_cache[row + lane + 32 * e]);
-        vr[e] = to_f32(v_cache[row + lane + 32 * e]);
-      }
-    } else {
-#pragma unroll
-      for (int e = 0; e < E; ++e) kr[e] = vr[e] = 0.f;
-    }
-#pragma unroll
-    for (int n = 0; n < GMAX; ++n) {
-      if (n >= G) break;
-      float d = 0.f;
-#pragma unroll
-      for (int e = 0; e < E; ++e) d = fmaf(qr[n][e], kr[e], d);
-      const float x = warp_sum(d) * scale_log2;
-      const float mn = fmaxf(m[n], x);
-      const float a = exp2f(m[n] - mn);
-      const float w = exp2f(x - mn);
-      l[n] = l[n] * a + w;
-#pragma unroll
-      for (int e = 0; e < E; ++e) o[n][e] = fmaf(o[n][e], a, w * vr[e]);
-      m[n] = mn;
-    }
-  }
-  if (lane == 0) {
-#pragma unroll
-    for (int n = 0; n < GMAX; ++n) {
-      s_m[warp][n] = m[n];
-      s_l[warp][n] = l[n];
-    }
-  }
-  __syncthreads();
-  float M[GMAX], Lsum[GMAX], f[GMAX];
-#pragma unroll
-  for (int n = 0; n < GMAX; ++n) {
-    M[n] = fmaxf(fmaxf(s_m[0][n], s_m[1][n]), fmaxf(s_m[2][n], s_m[3][n]));
-    Lsum[n] = 0.f;
-#pragma unroll
-    for (int w = 0; w < 4; ++w)
-      Lsum[n] += s_m[w][n] == -INFINITY ? 0.f : s_l[w][n] * exp2f(s_m[w][n] - M[n]);
-    f[n] = m[n] == -INFINITY ? 0.f : exp2f(m[n] - M[n]);
-  }
-  for (int w = 0; w < 4; ++w) {
-    if (warp == w) {
-#pragma unroll
-      for (int n = 0; n < GMAX; ++n)
-#pragma unroll
-        for (int e = 0; e < E; ++e) s_o[n][lane + 32 * e] += o[n][e] * f[n];
-    }
-    __syncthreads();
-  }
-  if (np == 1) {
-    for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
-      const int n = i / D, d = i - n * D;
-      out[((int64_t)s * H_q + j * G + n) * D + d] = from_f32<T>(s_o[n][d] / Lsum[n]);
-    }
-  } else {
-    const int64_t base = ((int64_t)s * ws.pmax + p) * H_q + j * G;
-    for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
-      const int n = i / D, d = i - n * D;
-      ws.o[(base + n) * D + d] = s_o[n][d];
-    }
-    if (threadIdx.x < G) ws.ml[base + threadIdx.x] = make_float2(M[threadIdx.x], Lsum[threadIdx.x]);
-  }
-}
-
-// ===========================================================================
-// Split-K reduce: one CTA per sequence, one warp per query head at a time.
-// ===========================================================================
-template <typename T>
-__global__ void __launch_bounds__(128)
-attn_reduce_kernel(Workspace ws, int H_q, int D, T* __restrict__ out) {
-  pdl_wait_primary();
-  pdl_launch_dependents();
-  const int s = blockIdx.x;
-  int np = ws.nparts[s];
-  if (np <= 1) return;
-  if (np > ws.pmax) {   // cannot happen with lengths clamped to the bound; never read past it
-    record_error(PKV_DEVERR_CONTEXT_LEN);
-    np = ws.pmax;
-  }
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int h = warp; h < H_q; h += 4) {
-    const int64_t base = (int64_t)s * ws.pmax * H_q + h;   // + p * H_q
-    float M = -INFINITY;
-    for (int p = lane; p < np; p += 32) M = fmaxf(M, ws.ml[base + (int64_t)p * H_q].x);
-    M = warp_max(M);
-    float Lsum = 0.f;
-    for (int p = lane; p < np; p += 32) {
-      const float2 ml = ws.ml[base + (int64_t)p * H_q];
-      Lsum += ml.y * exp2f(ml.x - M);
-    }
-    Lsum = warp_sum(Lsum);
-    const float inv = 1.f / Lsum;
-    for (int d0 = 0; d0 < D; d0 += 32) {
-      const int d = d0 + lane;
-      float acc = 0.f;
-      for (int p0 = 0; p0 < np; p0 += 32) {
-        const int pl = p0 + lane;
-        const float w = pl < np ? exp2f(ws.ml[base + (int64_t)pl * H_q].x - M) : 0.f;
-        const int cnt = min(32, np - p0);
-        for (int u = 0; u < cnt; ++u) {
-          const float wu = __shfl_sync(0xffffffffu, w, u);
-          if (d < D) acc = fmaf(wu, ws.o[(base + (int64_t)(p0 + u) * H_q) * D + d], acc);
-        }
-      }
-      if (d < D) out[((int64_t)s * H_q + h) * D + d] = from_f32<T>(acc * inv);
-    }
-  }
-}
 
 // ===========================================================================
 // TMA + tensor-core partition kernel (bf16, K % 16 == 0, D in {64, 128},
