@@ -82,7 +82,8 @@ def workload_desc(w) -> dict:
         "copy_pairs": int(len(w.copy_pairs)),
         "new_tokens": int((w.positions >= 0).sum()),
         "step": ("kv_block_copy + " if len(w.copy_pairs) else "")
-        + "slot_mapping + paged_kv_write + paged_attention_decode (partition + split-K reduce)",
+        + "paged_kv_append (slot mapping + KV write, fused) + paged_attention_decode "
+          "(partition + split-K reduce)",
     }
 
 
@@ -270,13 +271,14 @@ def run_gpu(args):
     def prologue():
         if has_copy:
             ops.kv_block_copy(t["k_cache"], t["v_cache"], t["copy_pairs"])
-        ops.slot_mapping(t["block_tables"], t["positions"], w.block_size, w.num_blocks, out=slots)
-        ops.paged_kv_write(t["k_new"], t["v_new"], slots, t["k_cache"], t["v_cache"])
+        # slot mapping + KV write of the new tokens, one fused launch
+        ops.paged_kv_append(t["k_new"], t["v_new"], t["block_tables"], t["positions"],
+                            t["k_cache"], t["v_cache"], slots)
 
     # kernels launched per step (ours only)
     attn_launches = ops.attention_launch_count(w.num_seqs, w.num_q_heads, w.num_kv_heads,
                                                w.head_dim, w.block_size, max_len, t["q"].dtype)
-    launches_per_step = (1 if has_copy else 0) + 2 + attn_launches
+    launches_per_step = (1 if has_copy else 0) + 1 + attn_launches
 
     for _ in range(max(args.warmup, 3)):
         prologue()

@@ -110,6 +110,23 @@ PKV_API pkv_status pkv_kv_write(const void* k, const void* v, const int64_t* slo
                         int32_t head_dim, pkv_dtype dtype, void* stream);
 
 /*
+ * a1 + a2 in one launch — slot mapping and KV append fused.
+ *   For token i (block-table row i): slot = block_tables[i][positions[i] /
+ *   block_size] * block_size + positions[i] % block_size, then
+ *   k_cache.view(-1, H_kv, D)[slot] = k[i] and the same for v.
+ * Same results as pkv_slot_mapping followed by pkv_kv_write; a negative
+ * position skips the token; out-of-range positions / block ids skip it and
+ * record a device error.  slot_mapping_out (int64 [num_tokens]) may be NULL;
+ * when given it receives the slots (-1 for skipped tokens).
+ */
+PKV_API pkv_status pkv_kv_append(const void* k, const void* v, const int32_t* block_tables,
+                                 int32_t max_blocks_per_seq, const int32_t* positions,
+                                 int32_t num_tokens, void* k_cache, void* v_cache,
+                                 int64_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                                 int32_t head_dim, pkv_dtype dtype, int64_t* slot_mapping_out,
+                                 void* stream);
+
+/*
  * a5 — copy-on-write block copy ("19.2 KV Cache 系统化管理" §19.2.2, 写时复制:
  * allocate a new block and copy the shared block's contents into it).
  *   for each i: k_cache[pairs[i][1]] = k_cache[pairs[i][0]]; same for v_cache.
@@ -215,6 +232,16 @@ PKV_API pkv_status pkv_attention_decode_noalloc(
     int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
     int32_t block_size, int64_t num_blocks, float scale, void* out, pkv_dtype dtype,
     const pkv_attention_config* config, void* stream);
+
+/*
+ * Self test of the failure path (the pages have no counterpart): launches one
+ * CTA that waits on an mbarrier nothing ever arrives on, with the same
+ * bounded wait the attention pipeline uses, limited to `limit_cycles`
+ * (1 .. 2^31 SM cycles).  The wait gives up, records PKV_DEVERR_TIMEOUT and
+ * the kernel exits; the context stays usable.  Read the code with
+ * pkv_get_device_error.
+ */
+PKV_API pkv_status pkv_selftest_wait_timeout(int64_t limit_cycles, void* stream);
 
 /*
  * Synchronises `stream`, copies the current device's error word into *code

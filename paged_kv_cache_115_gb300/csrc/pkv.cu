@@ -436,6 +436,48 @@ pkv_status pkv_kv_write(const void* k, const void* v, const int64_t* slot_mappin
   return PKV_OK;
 }
 
+pkv_status pkv_kv_append(const void* k, const void* v, const int32_t* block_tables,
+                         int32_t max_blocks_per_seq, const int32_t* positions, int32_t num_tokens,
+                         void* k_cache, void* v_cache, int64_t num_blocks, int32_t block_size,
+                         int32_t num_kv_heads, int32_t head_dim, pkv_dtype dtype,
+                         int64_t* slot_mapping_out, void* stream) {
+  PKV_CHECK(num_tokens >= 0 && max_blocks_per_seq >= 1 && num_blocks >= 1 && block_size >= 1 &&
+                num_kv_heads >= 1 && head_dim >= 1 && dtype_ok(dtype),
+            PKV_ERR_INVALID_ARGUMENT, "bad kv_append sizes");
+  if (num_tokens == 0) return PKV_OK;
+  PKV_CHECK(k && v && block_tables && positions && k_cache && v_cache, PKV_ERR_INVALID_ARGUMENT,
+            "null pointer");
+  PKV_CHECK(num_blocks <= INT64_MAX / block_size, PKV_ERR_INVALID_ARGUMENT, "pool too large");
+  const int64_t row = (int64_t)num_kv_heads * head_dim * elem_bytes(dtype);
+  const int vw = vec_width(row, {k, v, k_cache, v_cache});
+  PKV_CHECK(vw > 0, PKV_ERR_INVALID_ARGUMENT, "misaligned kv_append buffers");
+  const int threads = 128;
+  const int64_t chunks = ceil_div(row / vw, threads);
+  PKV_CHECK(chunks <= 65535, PKV_ERR_UNSUPPORTED, "token row too wide");
+  dim3 grid((unsigned)num_tokens, (unsigned)chunks, 2);
+  auto* kb = static_cast<const uint8_t*>(k);
+  auto* vb = static_cast<const uint8_t*>(v);
+  auto* kc = static_cast<uint8_t*>(k_cache);
+  auto* vc = static_cast<uint8_t*>(v_cache);
+  const int l2 = log2_exact(block_size);
+  cudaStream_t st = as_stream(stream);
+  switch (vw) {
+    case 16: PKV_CUDA(launch_pdl(pkv::kv_append_kernel<16>, grid, dim3(threads), 0, st, kb, vb, block_tables, max_blocks_per_seq, positions, block_size, l2, num_blocks, kc, vc, row, slot_mapping_out)); break;
+    case 8: PKV_CUDA(launch_pdl(pkv::kv_append_kernel<8>, grid, dim3(threads), 0, st, kb, vb, block_tables, max_blocks_per_seq, positions, block_size, l2, num_blocks, kc, vc, row, slot_mapping_out)); break;
+    case 4: PKV_CUDA(launch_pdl(pkv::kv_append_kernel<4>, grid, dim3(threads), 0, st, kb, vb, block_tables, max_blocks_per_seq, positions, block_size, l2, num_blocks, kc, vc, row, slot_mapping_out)); break;
+    default: PKV_CUDA(launch_pdl(pkv::kv_append_kernel<2>, grid, dim3(threads), 0, st, kb, vb, block_tables, max_blocks_per_seq, positions, block_size, l2, num_blocks, kc, vc, row, slot_mapping_out)); break;
+  }
+  return PKV_OK;
+}
+
+pkv_status pkv_selftest_wait_timeout(int64_t limit_cycles, void* stream) {
+  PKV_CHECK(limit_cycles >= 1 && limit_cycles <= (int64_t(1) << 31), PKV_ERR_INVALID_ARGUMENT,
+            "limit_cycles must be in [1, 2^31]");
+  pkv::selftest_wait_timeout_kernel<<<1, 32, 0, as_stream(stream)>>>((long long)limit_cycles);
+  PKV_CUDA(cudaGetLastError());
+  return PKV_OK;
+}
+
 pkv_status pkv_kv_block_copy(void* k_cache, void* v_cache, const int64_t* src_dst_pairs,
                              int64_t num_pairs, int64_t num_blocks, int32_t block_size,
                              int32_t num_kv_heads, int32_t head_dim, pkv_dtype dtype,

@@ -16,6 +16,8 @@ __global__ void slot_mapping_kernel(const int32_t* __restrict__ block_tables,
                                     const int32_t* __restrict__ positions, int32_t num_seqs,
                                     int32_t block_size, int32_t log2_bs, int64_t num_blocks,
                                     int64_t* __restrict__ slot_mapping) {
+  pdl_wait_primary();
+  pdl_launch_dependents();
   const int s = blockIdx.x * blockDim.x + threadIdx.x;
   if (s >= num_seqs) return;
   const int t = positions[s];
@@ -52,6 +54,8 @@ __global__ void kv_write_kernel(const uint8_t* __restrict__ k, const uint8_t* __
                                 uint8_t* __restrict__ k_cache, uint8_t* __restrict__ v_cache,
                                 int64_t num_slots, int64_t row_bytes) {
   using V = typename VecT<VW>::T;
+  pdl_wait_primary();
+  pdl_launch_dependents();
   const int64_t i = blockIdx.x;
   const int64_t e = (int64_t)blockIdx.y * blockDim.x + threadIdx.x;
   if (e * VW >= row_bytes) return;
@@ -65,6 +69,61 @@ __global__ void kv_write_kernel(const uint8_t* __restrict__ k, const uint8_t* __
   *reinterpret_cast<V*>(dst) = __ldg(reinterpret_cast<const V*>(src));
 }
 
+// a1 + a2 fused: the slot of token i comes from its sequence's block-table
+// row and position (as in slot_mapping_kernel) and the K/V rows are stored
+// there (as in kv_write_kernel).  grid = (tokens, vector chunks, 2).  The
+// slot is also written to `slots` (when non-null) by one thread per token.
+template <int VW>
+__global__ void kv_append_kernel(const uint8_t* __restrict__ k, const uint8_t* __restrict__ v,
+                                 const int32_t* __restrict__ block_tables,
+                                 int32_t max_blocks_per_seq, const int32_t* __restrict__ positions,
+                                 int32_t block_size, int32_t log2_bs, int64_t num_blocks,
+                                 uint8_t* __restrict__ k_cache, uint8_t* __restrict__ v_cache,
+                                 int64_t row_bytes, int64_t* __restrict__ slots) {
+  using V = typename VecT<VW>::T;
+  pdl_wait_primary();
+  pdl_launch_dependents();
+  const int64_t i = blockIdx.x;
+  const int64_t e = (int64_t)blockIdx.y * blockDim.x + threadIdx.x;
+  const bool leader = e == 0 && blockIdx.z == 0;
+  const int t = positions[i];
+  int64_t slot = -1;
+  if (t >= 0) {
+    const int lb = log2_bs >= 0 ? (t >> log2_bs) : (t / block_size);
+    const int off = log2_bs >= 0 ? (t & (block_size - 1)) : (t - lb * block_size);
+    if (lb >= max_blocks_per_seq) {
+      if (leader) record_error(PKV_DEVERR_POSITION);
+    } else {
+      const int64_t phys = block_tables[i * max_blocks_per_seq + lb];
+      if (phys < 0 || phys >= num_blocks) {
+        if (leader) record_error(PKV_DEVERR_BLOCK_ID);
+      } else {
+        slot = phys * block_size + off;
+      }
+    }
+  }
+  if (leader && slots != nullptr) slots[i] = slot;
+  if (slot < 0 || e * VW >= row_bytes) return;
+  const uint8_t* src = (blockIdx.z ? v : k) + i * row_bytes + e * VW;
+  uint8_t* dst = (blockIdx.z ? v_cache : k_cache) + slot * row_bytes + e * VW;
+  *reinterpret_cast<V*>(dst) = __ldg(reinterpret_cast<const V*>(src));
+}
+
+// Failure-path self test: one CTA waits on an mbarrier that nothing ever
+// arrives on; the bounded wait must give up after `limit` cycles and record
+// PKV_DEVERR_TIMEOUT, leaving the context usable.
+__global__ void selftest_wait_timeout_kernel(long long limit) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t b = smem_u32(&bar);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  const bool ok = mbar_wait_bounded(b, 0, limit);
+  if (!ok && threadIdx.x == 0) record_error(PKV_DEVERR_TIMEOUT);
+}
+
 // a5: copy whole blocks, K and V.  grid = (pairs, chunks of a block, 2);
 // each thread moves UNROLL vectors, all loads before all stores.
 template <int VW, int UNROLL>
@@ -72,6 +131,8 @@ __global__ void block_copy_kernel(uint8_t* __restrict__ k_cache, uint8_t* __rest
                                   const int64_t* __restrict__ pairs, int64_t num_blocks,
                                   int64_t block_bytes) {
   using V = typename VecT<VW>::T;
+  pdl_wait_primary();
+  pdl_launch_dependents();
   const int64_t p = blockIdx.x;
   const int64_t src = pairs[2 * p], dst = pairs[2 * p + 1];
   if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {

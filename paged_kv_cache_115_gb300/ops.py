@@ -55,6 +55,9 @@ _version = _sig("pkv_version", c_i32)
 _slot_mapping = _sig("pkv_slot_mapping", c_i32, c_vp, c_i32, c_vp, c_i32, c_i32, c_i64, c_vp, c_vp)
 _kv_write = _sig("pkv_kv_write", c_i32, c_vp, c_vp, c_vp, c_i64, c_vp, c_vp, c_i64, c_i32, c_i32,
                  c_i32, c_i32, c_vp)
+_kv_append = _sig("pkv_kv_append", c_i32, c_vp, c_vp, c_vp, c_i32, c_vp, c_i32, c_vp, c_vp, c_i64,
+                  c_i32, c_i32, c_i32, c_i32, c_vp, c_vp)
+_selftest_timeout = _sig("pkv_selftest_wait_timeout", c_i32, c_i64, c_vp)
 _block_copy = _sig("pkv_kv_block_copy", c_i32, c_vp, c_vp, c_vp, c_i64, c_i64, c_i32, c_i32, c_i32,
                    c_i32, c_vp)
 _ws_bytes = _sig("pkv_attention_workspace_bytes", c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, c_i32,
@@ -73,7 +76,7 @@ _dev_error = _sig("pkv_get_device_error", c_i32, ctypes.POINTER(c_i32), c_vp)
 NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 EXPORTED = ("pkv_status_string", "pkv_last_error_message", "pkv_version", "pkv_slot_mapping",
-            "pkv_kv_write", "pkv_kv_block_copy", "pkv_attention_workspace_bytes",
+            "pkv_kv_write", "pkv_kv_append", "pkv_kv_block_copy", "pkv_selftest_wait_timeout", "pkv_attention_workspace_bytes",
             "pkv_attention_launch_count", "pkv_attention_decode",
             "pkv_attention_decode_noalloc", "pkv_get_device_error")
 
@@ -150,6 +153,39 @@ def paged_kv_write(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
         raise ValueError("k/v/slot_mapping shapes do not match the pool")
     _check(_kv_write(_ptr(k), _ptr(v), _ptr(slot_mapping), T, _ptr(k_cache), _ptr(v_cache), nb, K,
                      H, D, _dtype_code(k_cache), _stream(k_cache.device)), "pkv_kv_write")
+
+
+def paged_kv_append(k: torch.Tensor, v: torch.Tensor, block_tables: torch.Tensor,
+                    positions: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                    slot_mapping_out: Optional[torch.Tensor] = None) -> None:
+    """Slot mapping and KV write in one launch: token i (block-table row i) goes
+    to the slot of ``positions[i]``; optionally stores the slots."""
+    _need(k_cache, "k_cache", None, 4)
+    _need(v_cache, "v_cache", k_cache.dtype, 4)
+    if v_cache.shape != k_cache.shape:
+        raise ValueError("k_cache and v_cache shapes differ")
+    nb, K, H, D = k_cache.shape
+    _need(k, "k", k_cache.dtype, 3)
+    _need(v, "v", k_cache.dtype, 3)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(positions, "positions", torch.int32, 1)
+    T = k.shape[0]
+    if tuple(k.shape) != (T, H, D) or tuple(v.shape) != (T, H, D) or positions.shape[0] != T \
+            or block_tables.shape[0] != T:
+        raise ValueError("k/v/positions/block_tables shapes do not match")
+    sp = None
+    if slot_mapping_out is not None:
+        _need(slot_mapping_out, "slot_mapping_out", torch.int64, 1)
+        sp = _ptr(slot_mapping_out)
+    _check(_kv_append(_ptr(k), _ptr(v), _ptr(block_tables), block_tables.shape[1],
+                      _ptr(positions), T, _ptr(k_cache), _ptr(v_cache), nb, K, H, D,
+                      _dtype_code(k_cache), sp, _stream(k_cache.device)), "pkv_kv_append")
+
+
+def selftest_wait_timeout(limit_cycles: int, device=None) -> None:
+    """Run the bounded-wait self test (records device error 6 when it gives up)."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    _check(_selftest_timeout(int(limit_cycles), _stream(dev)), "pkv_selftest_wait_timeout")
 
 
 def kv_block_copy(k_cache: torch.Tensor, v_cache: torch.Tensor,

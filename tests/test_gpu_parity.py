@@ -283,3 +283,57 @@ def test_full_size_step_sampled(ops, name):
         ref = oracle.paged_attention_decode_one(qn, okc, ovc, w.block_tables, w.context_lens,
                                                 w.scale, s, h, "bf16")
         check_attention(outf[s, h], ref, "bf16", f"{name} s={s} h={h}")
+
+
+# ---------------------------------------------------------------------------
+# fused slot mapping + KV write
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["tiny", "qwen3_0_6b", "prefix_cow"])
+def test_kv_append_matches_oracle(ops, name):
+    w = wl.build(name)
+    c = wl.materialize(w)
+    d = to_dev(c)
+    if len(w.copy_pairs):
+        ops.kv_block_copy(d["k_cache"], d["v_cache"], d["copy_pairs"])
+    slots = torch.full((w.num_seqs,), 7, dtype=torch.int64, device=DEV)
+    ops.paged_kv_append(d["k_new"], d["v_new"], d["block_tables"], d["positions"], d["k_cache"],
+                        d["v_cache"], slots)
+    torch.cuda.synchronize()
+    assert ops.get_device_error() == 0
+    oslots, okc, ovc = oracle_step_pool(w, c)
+    assert np.array_equal(slots.cpu().numpy(), oslots)
+    assert np.array_equal(storage(d["k_cache"]), okc)
+    assert np.array_equal(storage(d["v_cache"]), ovc)
+
+
+def test_kv_append_padding_and_device_checks(ops):
+    w = wl.build_decode("append_edge", [5, 0, 9, 3], 4, 2, 64, 4, "bf16", seed=3)
+    c = wl.materialize(w)
+    d = to_dev(c)
+    ops.paged_kv_append(d["k_new"], d["v_new"], d["block_tables"], d["positions"], d["k_cache"],
+                        d["v_cache"])                 # no slot output
+    assert ops.get_device_error() == 0
+    _, okc, ovc = oracle_step_pool(w, c)
+    assert np.array_equal(storage(d["k_cache"]), okc)
+    bad = d["block_tables"].clone()
+    bad[2, 2] = -5                                    # the block of position 8
+    slots = torch.empty(4, dtype=torch.int64, device=DEV)
+    before = d["k_cache"].clone()
+    ops.paged_kv_append(d["k_new"], d["v_new"], bad, d["positions"], d["k_cache"], d["v_cache"],
+                        slots)
+    assert ops.get_device_error() == 1
+    assert slots.cpu().tolist()[1] == -1 and slots.cpu().tolist()[2] == -1
+    assert torch.equal(before.view(torch.int16), d["k_cache"].view(torch.int16))
+
+
+# ---------------------------------------------------------------------------
+# failure path: a pipeline wait that can never complete gives up and reports
+# ---------------------------------------------------------------------------
+
+def test_bounded_wait_gives_up_and_context_survives(ops):
+    assert ops.get_device_error() == 0
+    ops.selftest_wait_timeout(20_000_000)             # ~10 ms of SM cycles
+    assert ops.get_device_error() == 6
+    assert ops.get_device_error() == 0                # the word was cleared
+    full_check(ops, wl.build("tiny"))                 # the context still works
