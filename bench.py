@@ -311,6 +311,39 @@ def run_gpu(args):
     attn_avg_ms = sum(attn_ms) / K
     assert ops.get_device_error(dev) == 0
 
+    # ---- each row of the step alone: events around the row only, L2 flushed
+    # (a 256 MB write) before every timed launch
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    row_fns = []
+    if has_copy:
+        row_fns.append(("kv_block_copy", lambda: ops.kv_block_copy(
+            t["k_cache"], t["v_cache"], t["copy_pairs"]),
+            accounting.block_copy_bytes(len(w.copy_pairs), w.block_size, w.num_kv_heads,
+                                        w.head_dim, w.elem_bytes)))
+    row_fns.append(("paged_kv_append", lambda: ops.paged_kv_append(
+        t["k_new"], t["v_new"], t["block_tables"], t["positions"], t["k_cache"], t["v_cache"],
+        slots), accounting.kv_write_bytes(int((w.positions >= 0).sum()), w.num_kv_heads,
+                                          w.head_dim, w.elem_bytes)))
+    row_fns.append(("paged_attention_decode", attention, kv_bytes))
+    rows = {}
+    R = max(5, min(50, K))
+    for name, fn, nbytes in row_fns:
+        times = []
+        for _ in range(R):
+            flush.fill_(1)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            times.append(a.elapsed_time(b))
+        med = statistics.median(times)
+        rows[name] = {"median_us": med * 1e3, "min_us": min(times) * 1e3,
+                      "algorithmic_bytes": nbytes, "GBps": nbytes / (med * 1e-3) / 1e9,
+                      "frac": None}
+    del flush
+    assert ops.get_device_error(dev) == 0
+
     # ---- end to end through the public API with host buffers
     pin = {k: t[k].cpu().pin_memory() for k in ("q", "k_new", "v_new", "block_tables",
                                                  "context_lens", "positions")}
@@ -355,6 +388,8 @@ def run_gpu(args):
     peaks, peak_src = read_peaks()
     hbm = float(peaks["hbm_gbs"])
     achieved = kv_bytes / (attn_avg_ms * 1e-3) / 1e9
+    for r in rows.values():
+        r["frac"] = r["GBps"] / hbm
     traffic = read_traffic()
     cfg = workload_desc(w)
     cfg["l2"] = (f"inputs larger than L2: {kv_bytes / 1e6:.0f} MB of KV read per step "
@@ -392,6 +427,7 @@ def run_gpu(args):
         "e2e": {"value": e2e_value, "unit": "GB/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "decode_tokens_per_s_per_layer": world * w.num_seqs / (e2e_ms * 1e-3)},
+        "rows": rows,
         "gpu_launches": launches_per_step * K,
         "clocks": clock_info,
     }
