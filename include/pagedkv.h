@@ -244,6 +244,81 @@ PKV_API pkv_status pkv_attention_decode_noalloc(
 PKV_API pkv_status pkv_selftest_wait_timeout(int64_t limit_cycles, void* stream);
 
 /*
+ * Quantized KV cache (one byte per element).
+ *
+ * "学习大模型推理的显存优化", section KV Cache 量化: FP8 e4m3 (1 sign, 4
+ * exponent, 3 mantissa bits, largest value 448); values are stored divided by
+ * a scale and multiplied back when read; the default scale is 1.0.
+ * "19.2 KV Cache 系统化管理" §19.2.4: INT8 with one scale per token,
+ * k_int8 = round(k / scale), scale = max|k| / 127.
+ *
+ * PKV_KV_FP8_E4M3: pools hold e4m3 codes; one scale per tensor (k_scale for
+ *   the K pool, v_scale for V); a value x is stored as e4m3(x / scale),
+ *   rounded to nearest even and saturated to +-448.
+ * PKV_KV_INT8_TOKEN: pools hold int8 codes; every token slot of a pool has
+ *   its own float scale (k_token_scales / v_token_scales, device arrays of
+ *   num_blocks * block_size floats) computed over the token's whole row (all
+ *   KV heads x head_dim): scale = max|x| / 127 (float32), code =
+ *   round_half_even(x / scale); an all-zero row gets scale 0 and codes 0.
+ */
+typedef enum { PKV_KV_PLAIN = 0, PKV_KV_FP8_E4M3 = 1, PKV_KV_INT8_TOKEN = 2 } pkv_kv_format;
+
+typedef struct {
+  int32_t format;          /* pkv_kv_format */
+  float k_scale;           /* FP8: scale of the K pool (must be finite and > 0) */
+  float v_scale;           /* FP8: scale of the V pool */
+  float* k_token_scales;   /* INT8: [num_blocks * block_size] device floats */
+  float* v_token_scales;   /* INT8: [num_blocks * block_size] device floats */
+} pkv_kv_quant;
+
+/*
+ * a1 + a2 into a quantized pool: as pkv_kv_append, but the new rows k, v
+ * (in_dtype: PKV_BF16 or PKV_F32) are quantized per `quant` before they are
+ * stored; for INT8 the token's scales are stored at the same slot.
+ */
+PKV_API pkv_status pkv_kv_append_quant(const void* k, const void* v, const int32_t* block_tables,
+                                       int32_t max_blocks_per_seq, const int32_t* positions,
+                                       int32_t num_tokens, void* k_cache, void* v_cache,
+                                       int64_t num_blocks, int32_t block_size,
+                                       int32_t num_kv_heads, int32_t head_dim,
+                                       pkv_dtype in_dtype, const pkv_kv_quant* quant,
+                                       int64_t* slot_mapping_out, void* stream);
+
+/*
+ * a5 on a quantized pool: copies the byte blocks of K and V and, for INT8,
+ * the blocks' per-token scales (so a copy is bit-exact in codes and scales).
+ */
+PKV_API pkv_status pkv_kv_block_copy_quant(void* k_cache, void* v_cache,
+                                           const int64_t* src_dst_pairs, int64_t num_pairs,
+                                           int64_t num_blocks, int32_t block_size,
+                                           int32_t num_kv_heads, int32_t head_dim,
+                                           const pkv_kv_quant* quant, void* stream);
+
+/* Workspace bytes of pkv_attention_decode_quant for these sizes. */
+PKV_API pkv_status pkv_attention_quant_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
+                                                       int32_t num_kv_heads, int32_t head_dim,
+                                                       int32_t block_size,
+                                                       int32_t max_context_len,
+                                                       pkv_dtype q_dtype,
+                                                       const pkv_kv_quant* quant,
+                                                       const pkv_attention_config* config,
+                                                       size_t* bytes);
+
+/*
+ * a3 + a4 over a quantized pool: the same attention as pkv_attention_decode
+ * with every cached value read back as code * scale (per tensor for FP8, per
+ * token slot for INT8).  q and out are q_dtype (PKV_BF16 or PKV_F32); the
+ * accumulation is fp32.
+ */
+PKV_API pkv_status pkv_attention_decode_quant(
+    const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+    int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t max_context_len,
+    int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+    int32_t block_size, int64_t num_blocks, float scale, void* out, void* workspace,
+    size_t workspace_bytes, pkv_dtype q_dtype, const pkv_kv_quant* quant,
+    const pkv_attention_config* config, void* stream);
+
+/*
  * Synchronises `stream`, copies the current device's error word into *code
  * (a PKV_DEVERR_* value) and clears it.  Returns PKV_ERR_DEVICE_CHECK when
  * the word was non-zero, PKV_OK when it was zero.

@@ -4,6 +4,7 @@
 // encoding and kernel launches.  Nothing here allocates device memory.
 #include <cudaTypedefs.h>
 
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -201,6 +202,20 @@ pkv_status plan_attention(int S, int H_q, int H_kv, int D, int K, int max_len, i
   return PKV_OK;
 }
 
+// Plan for a quantized pool: the CUDA-core kernel (head_dim 64 / 128, G <= 16).
+pkv_status plan_attention_quant(int S, int H_q, int H_kv, int D, int K, int max_len,
+                                pkv_dtype q_dt, const pkv_kv_quant* quant,
+                                const pkv_attention_config* cfg, AttnPlan* plan) {
+  pkv_attention_config c = {};
+  if (cfg) c = *cfg;
+  PKV_CHECK(c.kernel == 0 || c.kernel == 2, PKV_ERR_UNSUPPORTED,
+            "quantized pools use the CUDA-core kernel (config.kernel 0 or 2)");
+  PKV_CHECK(D == 64 || D == 128, PKV_ERR_UNSUPPORTED, "quantized pools need head_dim 64 or 128");
+  (void)quant;
+  c.kernel = 2;
+  return plan_attention(S, H_q, H_kv, D, K, max_len, 1, q_dt, &c, false, plan);
+}
+
 pkv::Workspace carve_workspace(void* ws, const AttnPlan& p, int H_q, int D) {
   const size_t sb = (size_t)std::max(p.seq_batch, 1);
   uint8_t* b = static_cast<uint8_t*>(ws);
@@ -263,52 +278,76 @@ pkv_status encode_pool_map(CUtensorMap* map, const void* pool, int64_t num_block
 }
 
 // ---- CUDA-core kernel dispatch --------------------------------------------------
-template <typename T, int D, int GMAX>
-pkv_status launch_simt_t(const void* q, const void* kc, const void* vc, const int32_t* bt, int maxB,
-                         const int32_t* lens, int max_len, int S, int H_q, int H_kv, int K,
-                         int64_t nb, float sl, void* out, pkv::Workspace ws, int ps, int pmax,
-                         cudaStream_t st) {
-  PKV_CUDA(launch_pdl(pkv::attn_simt_kernel<T, D, GMAX>, dim3(pmax, H_kv, S),
-                      dim3(pkv::kSimtThreads), 0, st, static_cast<const T*>(q),
-                      static_cast<const T*>(kc), static_cast<const T*>(vc), bt, maxB, lens, max_len,
-                      H_q, H_kv, H_q / H_kv, K, (long long)nb, sl, static_cast<T*>(out), ws, ps));
+struct SimtArgs {
+  const int32_t* bt;
+  int maxB;
+  const int32_t* lens;
+  int max_len, S, H_q, H_kv, K;
+  int64_t nb;
+  float sl;
+  pkv::Workspace ws;
+  int ps, pmax;
+};
+
+template <typename T, typename KV, int D, int GMAX>
+pkv_status launch_simt_t(const void* q, KV kv, void* out, const SimtArgs& a, cudaStream_t st) {
+  PKV_CUDA(launch_pdl(pkv::attn_simt_kernel<T, KV, D, GMAX>, dim3(a.pmax, a.H_kv, a.S),
+                      dim3(pkv::kSimtThreads), 0, st, static_cast<const T*>(q), kv, a.bt, a.maxB,
+                      a.lens, a.max_len, a.H_q, a.H_kv, a.H_q / a.H_kv, a.K, (long long)a.nb,
+                      a.sl, static_cast<T*>(out), a.ws, a.ps));
   return PKV_OK;
 }
 
-template <typename T, int D>
-pkv_status launch_simt_d(int G, const void* q, const void* kc, const void* vc, const int32_t* bt,
-                         int maxB, const int32_t* lens, int max_len, int S, int H_q, int H_kv,
-                         int K, int64_t nb, float sl, void* out, pkv::Workspace ws, int ps,
-                         int pmax, cudaStream_t st) {
-  if (G <= 2)
-    return launch_simt_t<T, D, 2>(q, kc, vc, bt, maxB, lens, max_len, S, H_q, H_kv, K, nb, sl, out,
-                                  ws, ps, pmax, st);
-  if (G <= 8)
-    return launch_simt_t<T, D, 8>(q, kc, vc, bt, maxB, lens, max_len, S, H_q, H_kv, K, nb, sl, out,
-                                  ws, ps, pmax, st);
-  return launch_simt_t<T, D, 16>(q, kc, vc, bt, maxB, lens, max_len, S, H_q, H_kv, K, nb, sl, out,
-                                 ws, ps, pmax, st);
+template <typename T, typename KV, int D>
+pkv_status launch_simt_d(int G, const void* q, KV kv, void* out, const SimtArgs& a,
+                         cudaStream_t st) {
+  if (G <= 2) return launch_simt_t<T, KV, D, 2>(q, kv, out, a, st);
+  if (G <= 8) return launch_simt_t<T, KV, D, 8>(q, kv, out, a, st);
+  return launch_simt_t<T, KV, D, 16>(q, kv, out, a, st);
+}
+
+template <typename T, typename KV>
+pkv_status launch_simt(int D, const void* q, KV kv, void* out, const SimtArgs& a,
+                       cudaStream_t st) {
+  const int G = a.H_q / a.H_kv;
+  switch (D) {
+    case 32: return launch_simt_d<T, KV, 32>(G, q, kv, out, a, st);
+    case 64: return launch_simt_d<T, KV, 64>(G, q, kv, out, a, st);
+    case 128: return launch_simt_d<T, KV, 128>(G, q, kv, out, a, st);
+    default: return launch_simt_d<T, KV, 256>(G, q, kv, out, a, st);
+  }
+}
+
+// Quantized pools: head_dim 64 or 128 only (fewer instantiations).
+template <typename T, typename KV>
+pkv_status launch_simt_q(int D, const void* q, KV kv, void* out, const SimtArgs& a,
+                         cudaStream_t st) {
+  const int G = a.H_q / a.H_kv;
+  if (D == 64) return launch_simt_d<T, KV, 64>(G, q, kv, out, a, st);
+  return launch_simt_d<T, KV, 128>(G, q, kv, out, a, st);
 }
 
 template <typename T>
-pkv_status launch_simt(int D, int G, const void* q, const void* kc, const void* vc,
-                       const int32_t* bt, int maxB, const int32_t* lens, int max_len, int S,
-                       int H_q, int H_kv, int K, int64_t nb, float sl, void* out,
-                       pkv::Workspace ws, int ps, int pmax, cudaStream_t st) {
-  switch (D) {
-    case 32:
-      return launch_simt_d<T, 32>(G, q, kc, vc, bt, maxB, lens, max_len, S, H_q, H_kv, K, nb, sl,
-                                  out, ws, ps, pmax, st);
-    case 64:
-      return launch_simt_d<T, 64>(G, q, kc, vc, bt, maxB, lens, max_len, S, H_q, H_kv, K, nb, sl,
-                                  out, ws, ps, pmax, st);
-    case 128:
-      return launch_simt_d<T, 128>(G, q, kc, vc, bt, maxB, lens, max_len, S, H_q, H_kv, K, nb, sl,
-                                   out, ws, ps, pmax, st);
-    default:
-      return launch_simt_d<T, 256>(G, q, kc, vc, bt, maxB, lens, max_len, S, H_q, H_kv, K, nb, sl,
-                                   out, ws, ps, pmax, st);
-  }
+pkv_status launch_simt_typed(const pkv_kv_quant* quant, int D, const void* q, const void* kc,
+                             const void* vc, void* out, const SimtArgs& a, cudaStream_t st) {
+  if (quant == nullptr)
+    return launch_simt<T>(D, q, pkv::KvPlain<T>{static_cast<const T*>(kc),
+                                                 static_cast<const T*>(vc)}, out, a, st);
+  if (quant->format == PKV_KV_FP8_E4M3)
+    return launch_simt_q<T>(D, q, pkv::KvFp8{static_cast<const uint8_t*>(kc),
+                                              static_cast<const uint8_t*>(vc), quant->k_scale,
+                                              quant->v_scale}, out, a, st);
+  return launch_simt_q<T>(D, q, pkv::KvInt8{static_cast<const int8_t*>(kc),
+                                             static_cast<const int8_t*>(vc),
+                                             quant->k_token_scales, quant->v_token_scales},
+                          out, a, st);
+}
+
+pkv_status launch_simt_any(pkv_dtype dt, const pkv_kv_quant* quant, int D, const void* q,
+                           const void* kc, const void* vc, void* out, const SimtArgs& a,
+                           cudaStream_t st) {
+  return dt == PKV_BF16 ? launch_simt_typed<__nv_bfloat16>(quant, D, q, kc, vc, out, a, st)
+                        : launch_simt_typed<float>(quant, D, q, kc, vc, out, a, st);
 }
 
 // ---- split-K reduce dispatch -----------------------------------------------------
@@ -327,15 +366,55 @@ pkv_status launch_reduce(int D, pkv::Workspace ws, int S, int H_q, void* out, cu
   return PKV_OK;
 }
 
-// Widest vector (16/8/4/2 bytes) that divides the row and every base pointer.
+// Widest vector (16/8/4/2/1 bytes) that divides the row and every base pointer.
 int vec_width(int64_t row_bytes, std::initializer_list<const void*> ptrs) {
-  for (int w : {16, 8, 4, 2}) {
+  for (int w : {16, 8, 4, 2, 1}) {
     if (row_bytes % w) continue;
     bool ok = true;
     for (const void* p : ptrs) ok = ok && aligned(p, w);
     if (ok) return w;
   }
   return 0;
+}
+
+// Copy whole blocks of `blk` bytes in both pools for every (src, dst) pair.
+pkv_status copy_blocks(void* k_cache, void* v_cache, const int64_t* pairs, int64_t num_pairs,
+                       int64_t num_blocks, int64_t blk, cudaStream_t st) {
+  PKV_CHECK(num_pairs <= 2147483647, PKV_ERR_UNSUPPORTED, "too many pairs");
+  const int vw = vec_width(blk, {k_cache, v_cache});
+  PKV_CHECK(vw > 0, PKV_ERR_INVALID_ARGUMENT, "misaligned pools");
+  constexpr int threads = 256, unroll = 4;
+  const int64_t chunks = ceil_div(blk / vw, threads * unroll);
+  PKV_CHECK(chunks <= 65535, PKV_ERR_UNSUPPORTED, "block too large");
+  dim3 grid((unsigned)num_pairs, (unsigned)chunks, 2);
+  auto* kc = static_cast<uint8_t*>(k_cache);
+  auto* vc = static_cast<uint8_t*>(v_cache);
+  switch (vw) {
+    case 16: PKV_CUDA(launch_pdl(pkv::block_copy_kernel<16, unroll>, grid, dim3(threads), 0, st, kc, vc, pairs, num_blocks, blk)); break;
+    case 8: PKV_CUDA(launch_pdl(pkv::block_copy_kernel<8, unroll>, grid, dim3(threads), 0, st, kc, vc, pairs, num_blocks, blk)); break;
+    case 4: PKV_CUDA(launch_pdl(pkv::block_copy_kernel<4, unroll>, grid, dim3(threads), 0, st, kc, vc, pairs, num_blocks, blk)); break;
+    case 2: PKV_CUDA(launch_pdl(pkv::block_copy_kernel<2, unroll>, grid, dim3(threads), 0, st, kc, vc, pairs, num_blocks, blk)); break;
+    default: PKV_CUDA(launch_pdl(pkv::block_copy_kernel<1, unroll>, grid, dim3(threads), 0, st, kc, vc, pairs, num_blocks, blk)); break;
+  }
+  return PKV_OK;
+}
+
+// Validates a quantized-pool description (token scales required for INT8).
+pkv_status check_quant(const pkv_kv_quant* q, bool need_token_scales) {
+  PKV_CHECK(q != nullptr, PKV_ERR_INVALID_ARGUMENT, "null quant description");
+  PKV_CHECK(q->format == PKV_KV_FP8_E4M3 || q->format == PKV_KV_INT8_TOKEN,
+            PKV_ERR_INVALID_ARGUMENT, "quant format must be FP8_E4M3 or INT8_TOKEN");
+  if (q->format == PKV_KV_FP8_E4M3) {
+    PKV_CHECK(std::isfinite(q->k_scale) && std::isfinite(q->v_scale) && q->k_scale > 0.f &&
+                  q->v_scale > 0.f,
+              PKV_ERR_INVALID_ARGUMENT, "FP8 scales must be finite and > 0");
+  } else if (need_token_scales) {
+    PKV_CHECK(q->k_token_scales && q->v_token_scales, PKV_ERR_INVALID_ARGUMENT,
+              "INT8 pools need per-token scale arrays");
+    PKV_CHECK(aligned(q->k_token_scales, 4) && aligned(q->v_token_scales, 4),
+              PKV_ERR_INVALID_ARGUMENT, "misaligned token scales");
+  }
+  return PKV_OK;
 }
 
 // ---- fixed scratch for pkv_attention_decode_noalloc ---------------------------
@@ -415,7 +494,7 @@ pkv_status pkv_kv_write(const void* k, const void* v, const int64_t* slot_mappin
   PKV_CHECK(num_tokens <= 2147483647, PKV_ERR_UNSUPPORTED, "too many tokens");
   const int64_t row = (int64_t)num_kv_heads * head_dim * elem_bytes(dtype);
   const int vw = vec_width(row, {k, v, k_cache, v_cache});
-  PKV_CHECK(vw > 0, PKV_ERR_INVALID_ARGUMENT, "misaligned kv_write buffers");
+  PKV_CHECK(vw >= 2, PKV_ERR_INVALID_ARGUMENT, "misaligned kv_write buffers");
   const int threads = 128;
   const int64_t nvec = row / vw;
   const int64_t chunks = ceil_div(nvec, threads);
@@ -450,7 +529,7 @@ pkv_status pkv_kv_append(const void* k, const void* v, const int32_t* block_tabl
   PKV_CHECK(num_blocks <= INT64_MAX / block_size, PKV_ERR_INVALID_ARGUMENT, "pool too large");
   const int64_t row = (int64_t)num_kv_heads * head_dim * elem_bytes(dtype);
   const int vw = vec_width(row, {k, v, k_cache, v_cache});
-  PKV_CHECK(vw > 0, PKV_ERR_INVALID_ARGUMENT, "misaligned kv_append buffers");
+  PKV_CHECK(vw >= 2, PKV_ERR_INVALID_ARGUMENT, "misaligned kv_append buffers");
   const int threads = 128;
   const int64_t chunks = ceil_div(row / vw, threads);
   PKV_CHECK(chunks <= 65535, PKV_ERR_UNSUPPORTED, "token row too wide");
@@ -487,22 +566,71 @@ pkv_status pkv_kv_block_copy(void* k_cache, void* v_cache, const int64_t* src_ds
             PKV_ERR_INVALID_ARGUMENT, "bad block-copy sizes");
   if (num_pairs == 0) return PKV_OK;
   PKV_CHECK(k_cache && v_cache && src_dst_pairs, PKV_ERR_INVALID_ARGUMENT, "null pointer");
-  PKV_CHECK(num_pairs <= 2147483647, PKV_ERR_UNSUPPORTED, "too many pairs");
   const int64_t blk = (int64_t)block_size * num_kv_heads * head_dim * elem_bytes(dtype);
-  const int vw = vec_width(blk, {k_cache, v_cache});
-  PKV_CHECK(vw > 0, PKV_ERR_INVALID_ARGUMENT, "misaligned pools");
-  constexpr int threads = 256, unroll = 4;
-  const int64_t chunks = ceil_div(blk / vw, threads * unroll);
-  PKV_CHECK(chunks <= 65535, PKV_ERR_UNSUPPORTED, "block too large");
-  dim3 grid((unsigned)num_pairs, (unsigned)chunks, 2);
+  return copy_blocks(k_cache, v_cache, src_dst_pairs, num_pairs, num_blocks, blk,
+                     as_stream(stream));
+}
+
+pkv_status pkv_kv_append_quant(const void* k, const void* v, const int32_t* block_tables,
+                               int32_t max_blocks_per_seq, const int32_t* positions,
+                               int32_t num_tokens, void* k_cache, void* v_cache,
+                               int64_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                               int32_t head_dim, pkv_dtype in_dtype, const pkv_kv_quant* quant,
+                               int64_t* slot_mapping_out, void* stream) {
+  PKV_CHECK(num_tokens >= 0 && max_blocks_per_seq >= 1 && num_blocks >= 1 && block_size >= 1 &&
+                num_kv_heads >= 1 && head_dim >= 1 && dtype_ok(in_dtype),
+            PKV_ERR_INVALID_ARGUMENT, "bad kv_append_quant sizes");
+  pkv_status st = check_quant(quant, true);
+  if (st != PKV_OK) return st;
+  if (num_tokens == 0) return PKV_OK;
+  PKV_CHECK(k && v && block_tables && positions && k_cache && v_cache, PKV_ERR_INVALID_ARGUMENT,
+            "null pointer");
+  PKV_CHECK(num_blocks <= INT64_MAX / block_size, PKV_ERR_INVALID_ARGUMENT, "pool too large");
+  PKV_CHECK(aligned(k, elem_bytes(in_dtype)) && aligned(v, elem_bytes(in_dtype)),
+            PKV_ERR_INVALID_ARGUMENT, "misaligned k/v");
+  const int64_t row = (int64_t)num_kv_heads * head_dim;
+  const int l2 = log2_exact(block_size);
+  dim3 grid((unsigned)num_tokens, 2);
+  dim3 block(pkv::kQuantThreads);
+  cudaStream_t strm = as_stream(stream);
   auto* kc = static_cast<uint8_t*>(k_cache);
   auto* vc = static_cast<uint8_t*>(v_cache);
-  cudaStream_t st = as_stream(stream);
-  switch (vw) {
-    case 16: PKV_CUDA(launch_pdl(pkv::block_copy_kernel<16, unroll>, grid, dim3(threads), 0, st, kc, vc, src_dst_pairs, num_blocks, blk)); break;
-    case 8: PKV_CUDA(launch_pdl(pkv::block_copy_kernel<8, unroll>, grid, dim3(threads), 0, st, kc, vc, src_dst_pairs, num_blocks, blk)); break;
-    case 4: PKV_CUDA(launch_pdl(pkv::block_copy_kernel<4, unroll>, grid, dim3(threads), 0, st, kc, vc, src_dst_pairs, num_blocks, blk)); break;
-    default: PKV_CUDA(launch_pdl(pkv::block_copy_kernel<2, unroll>, grid, dim3(threads), 0, st, kc, vc, src_dst_pairs, num_blocks, blk)); break;
+  const float ks = quant->k_scale, vs = quant->v_scale;
+  float* kts = quant->k_token_scales;
+  float* vts = quant->v_token_scales;
+#define PKV_LAUNCH_AQ(TIN, FMT)                                                               \
+  PKV_CUDA(launch_pdl(pkv::kv_append_quant_kernel<TIN, FMT>, grid, block, 0, strm,            \
+                      static_cast<const TIN*>(k), static_cast<const TIN*>(v), block_tables,   \
+                      max_blocks_per_seq, positions, block_size, l2, num_blocks, kc, vc, row, \
+                      ks, vs, kts, vts, slot_mapping_out))
+  if (quant->format == PKV_KV_FP8_E4M3) {
+    if (in_dtype == PKV_BF16) PKV_LAUNCH_AQ(__nv_bfloat16, 1); else PKV_LAUNCH_AQ(float, 1);
+  } else {
+    if (in_dtype == PKV_BF16) PKV_LAUNCH_AQ(__nv_bfloat16, 2); else PKV_LAUNCH_AQ(float, 2);
+  }
+#undef PKV_LAUNCH_AQ
+  return PKV_OK;
+}
+
+pkv_status pkv_kv_block_copy_quant(void* k_cache, void* v_cache, const int64_t* src_dst_pairs,
+                                   int64_t num_pairs, int64_t num_blocks, int32_t block_size,
+                                   int32_t num_kv_heads, int32_t head_dim,
+                                   const pkv_kv_quant* quant, void* stream) {
+  PKV_CHECK(num_pairs >= 0 && num_blocks >= 1 && block_size >= 1 && num_kv_heads >= 1 &&
+                head_dim >= 1,
+            PKV_ERR_INVALID_ARGUMENT, "bad block-copy sizes");
+  pkv_status st = check_quant(quant, true);
+  if (st != PKV_OK) return st;
+  if (num_pairs == 0) return PKV_OK;
+  PKV_CHECK(k_cache && v_cache && src_dst_pairs, PKV_ERR_INVALID_ARGUMENT, "null pointer");
+  const int64_t blk = (int64_t)block_size * num_kv_heads * head_dim;
+  cudaStream_t strm = as_stream(stream);
+  st = copy_blocks(k_cache, v_cache, src_dst_pairs, num_pairs, num_blocks, blk, strm);
+  if (st != PKV_OK) return st;
+  if (quant->format == PKV_KV_INT8_TOKEN) {
+    PKV_CUDA(launch_pdl(pkv::token_scale_copy_kernel, dim3((unsigned)num_pairs), dim3(64), 0,
+                        strm, quant->k_token_scales, quant->v_token_scales, src_dst_pairs,
+                        num_blocks, block_size));
   }
   return PKV_OK;
 }
@@ -547,20 +675,28 @@ pkv_status pkv_attention_launch_count(int32_t num_seqs, int32_t num_q_heads,
   return PKV_OK;
 }
 
-pkv_status pkv_attention_decode(const void* q, const void* k_cache, const void* v_cache,
-                                const int32_t* block_tables, int32_t max_blocks_per_seq,
-                                const int32_t* context_lens, int32_t max_context_len,
-                                int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
-                                int32_t head_dim, int32_t block_size, int64_t num_blocks,
-                                float scale, void* out, void* workspace, size_t workspace_bytes,
-                                pkv_dtype dtype, const pkv_attention_config* config,
-                                void* stream) {
+}  // extern "C"
+
+namespace {
+
+pkv_status attention_impl(const void* q, const void* k_cache, const void* v_cache,
+                          const int32_t* block_tables, int32_t max_blocks_per_seq,
+                          const int32_t* context_lens, int32_t max_context_len, int32_t num_seqs,
+                          int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                          int32_t block_size, int64_t num_blocks, float scale, void* out,
+                          void* workspace, size_t workspace_bytes, pkv_dtype dtype,
+                          const pkv_attention_config* config, const pkv_kv_quant* quant,
+                          void* stream) {
   PKV_CHECK(num_seqs >= 0 && max_blocks_per_seq >= 1 && num_blocks >= 1,
             PKV_ERR_INVALID_ARGUMENT, "bad attention sizes");
   const bool tma_aligned = aligned(k_cache, 16) && aligned(v_cache, 16);
   AttnPlan plan;
-  pkv_status st = plan_attention(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                                 max_context_len, num_blocks, dtype, config, tma_aligned, &plan);
+  pkv_status st = quant ? plan_attention_quant(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                               block_size, max_context_len, dtype, quant, config,
+                                               &plan)
+                        : plan_attention(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                         block_size, max_context_len, num_blocks, dtype, config,
+                                         tma_aligned, &plan);
   if (st != PKV_OK) return st;
   if (num_seqs == 0) return PKV_OK;
   PKV_CHECK(q && k_cache && v_cache && block_tables && context_lens && out && workspace,
@@ -569,7 +705,9 @@ pkv_status pkv_attention_decode(const void* q, const void* k_cache, const void* 
             "workspace %zu bytes < %zu needed", workspace_bytes, plan.ws_bytes);
   PKV_CHECK(aligned(workspace, 256), PKV_ERR_INVALID_ARGUMENT, "workspace must be 256-byte aligned");
   const size_t eb = elem_bytes(dtype);
-  PKV_CHECK(aligned(q, eb) && aligned(out, eb) && aligned(k_cache, eb) && aligned(v_cache, eb),
+  const size_t pool_eb = quant ? 1 : eb;
+  PKV_CHECK(aligned(q, eb) && aligned(out, eb) && aligned(k_cache, pool_eb) &&
+                aligned(v_cache, pool_eb),
             PKV_ERR_INVALID_ARGUMENT, "misaligned q/out/pool");
   PKV_CHECK((int64_t)max_blocks_per_seq * block_size <= 2147483647, PKV_ERR_UNSUPPORTED,
             "table row too long");
@@ -613,14 +751,10 @@ pkv_status pkv_attention_decode(const void* q, const void* k_cache, const void* 
       prm.scale_log2 = sl;
       st = D == 64 ? launch_tc_d<64>(plan.hpc, prm, plan.n_per_group, plan.groups, strm, dev)
                    : launch_tc_d<128>(plan.hpc, prm, plan.n_per_group, plan.groups, strm, dev);
-    } else if (dtype == PKV_BF16) {
-      st = launch_simt<__nv_bfloat16>(D, H_q / H_kv, qb, k_cache, v_cache, btb, max_blocks_per_seq,
-                                      lb, max_context_len, S, H_q, H_kv, block_size, num_blocks,
-                                      sl, ob, ws, plan.ps, plan.pmax, strm);
     } else {
-      st = launch_simt<float>(D, H_q / H_kv, qb, k_cache, v_cache, btb, max_blocks_per_seq, lb,
-                              max_context_len, S, H_q, H_kv, block_size, num_blocks, sl, ob, ws,
-                              plan.ps, plan.pmax, strm);
+      const SimtArgs a{btb, max_blocks_per_seq, lb, max_context_len, S, H_q, H_kv,
+                       block_size, num_blocks, sl, ws, plan.ps, plan.pmax};
+      st = launch_simt_any(dtype, quant, D, qb, k_cache, v_cache, ob, a, strm);
     }
     if (st != PKV_OK) return st;
     if (plan.pmax > 1) {
@@ -630,6 +764,58 @@ pkv_status pkv_attention_decode(const void* q, const void* k_cache, const void* 
       if (st != PKV_OK) return st;
     }
   }
+  return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_attention_decode(const void* q, const void* k_cache, const void* v_cache,
+                                const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                const int32_t* context_lens, int32_t max_context_len,
+                                int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                                float scale, void* out, void* workspace, size_t workspace_bytes,
+                                pkv_dtype dtype, const pkv_attention_config* config,
+                                void* stream) {
+  return attention_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                        max_context_len, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                        block_size, num_blocks, scale, out, workspace, workspace_bytes, dtype,
+                        config, nullptr, stream);
+}
+
+pkv_status pkv_attention_decode_quant(const void* q, const void* k_cache, const void* v_cache,
+                                      const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                      const int32_t* context_lens, int32_t max_context_len,
+                                      int32_t num_seqs, int32_t num_q_heads,
+                                      int32_t num_kv_heads, int32_t head_dim,
+                                      int32_t block_size, int64_t num_blocks, float scale,
+                                      void* out, void* workspace, size_t workspace_bytes,
+                                      pkv_dtype q_dtype, const pkv_kv_quant* quant,
+                                      const pkv_attention_config* config, void* stream) {
+  pkv_status st = check_quant(quant, true);
+  if (st != PKV_OK) return st;
+  return attention_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                        max_context_len, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                        block_size, num_blocks, scale, out, workspace, workspace_bytes, q_dtype,
+                        config, quant, stream);
+}
+
+pkv_status pkv_attention_quant_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
+                                               int32_t num_kv_heads, int32_t head_dim,
+                                               int32_t block_size, int32_t max_context_len,
+                                               pkv_dtype q_dtype, const pkv_kv_quant* quant,
+                                               const pkv_attention_config* config,
+                                               size_t* bytes) {
+  PKV_CHECK(bytes != nullptr, PKV_ERR_INVALID_ARGUMENT, "null bytes pointer");
+  pkv_status st = check_quant(quant, false);
+  if (st != PKV_OK) return st;
+  AttnPlan plan;
+  st = plan_attention_quant(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                            max_context_len, q_dtype, quant, config, &plan);
+  if (st != PKV_OK) return st;
+  *bytes = plan.ws_bytes;
   return PKV_OK;
 }
 

@@ -1,4 +1,5 @@
-// CUDA-core decode-attention partition kernel (fp32 / bf16, any block size).
+// CUDA-core decode-attention partition kernel (fp32 / bf16 queries; bf16,
+// fp32, FP8 e4m3 or INT8 pools; any block size).
 #pragma once
 
 #include "pkv_attention_common.cuh"
@@ -15,10 +16,42 @@ namespace pkv {
 constexpr int kSimtThreads = 128;
 constexpr int kSimtMaxPS = 1024;
 
-template <typename T, int D, int GMAX>
+// K/V row loaders: element e of lane `lane` of the row starting at element
+// `row` (= (slot * H_kv + j) * D) of the pool, as float.
+template <typename T>
+struct KvPlain {          // pool stored in the query dtype
+  const T* k;
+  const T* v;
+  __device__ __forceinline__ float ld_k(int64_t i, int64_t) const { return to_f32(k[i]); }
+  __device__ __forceinline__ float ld_v(int64_t i, int64_t) const { return to_f32(v[i]); }
+};
+struct KvFp8 {            // e4m3 codes, one scale per tensor
+  const uint8_t* k;
+  const uint8_t* v;
+  float k_scale, v_scale;
+  __device__ __forceinline__ float ld_k(int64_t i, int64_t) const {
+    return e4m3_to_f32(k[i]) * k_scale;
+  }
+  __device__ __forceinline__ float ld_v(int64_t i, int64_t) const {
+    return e4m3_to_f32(v[i]) * v_scale;
+  }
+};
+struct KvInt8 {           // int8 codes, one scale per token slot
+  const int8_t* k;
+  const int8_t* v;
+  const float* k_ts;
+  const float* v_ts;
+  __device__ __forceinline__ float ld_k(int64_t i, int64_t slot) const {
+    return (float)k[i] * k_ts[slot];
+  }
+  __device__ __forceinline__ float ld_v(int64_t i, int64_t slot) const {
+    return (float)v[i] * v_ts[slot];
+  }
+};
+
+template <typename T, typename KV, int D, int GMAX>
 __global__ void __launch_bounds__(kSimtThreads)
-attn_simt_kernel(const T* __restrict__ q, const T* __restrict__ k_cache,
-                 const T* __restrict__ v_cache, const int32_t* __restrict__ block_tables,
+attn_simt_kernel(const T* __restrict__ q, KV kv, const int32_t* __restrict__ block_tables,
                  int max_blocks_per_seq, const int32_t* __restrict__ context_lens, int max_len,
                  int H_q, int H_kv, int G, int K, long long num_blocks, float scale_log2,
                  T* __restrict__ out, Workspace ws, int PS) {
@@ -77,11 +110,12 @@ attn_simt_kernel(const T* __restrict__ q, const T* __restrict__ k_cache,
     const int off = t - (t / K) * K;
     float kr[E], vr[E];
     if (phys >= 0) {
-      const int64_t row = (((int64_t)phys * K + off) * H_kv + j) * D;
+      const int64_t slot = (int64_t)phys * K + off;
+      const int64_t row = (slot * H_kv + j) * D;
 #pragma unroll
       for (int e = 0; e < E; ++e) {
-        kr[e] = to_f32(k_cache[row + lane + 32 * e]);
-        vr[e] = to_f32(v_cache[row + lane + 32 * e]);
+        kr[e] = kv.ld_k(row + lane + 32 * e, slot);
+        vr[e] = kv.ld_v(row + lane + 32 * e, slot);
       }
     } else {
 #pragma unroll

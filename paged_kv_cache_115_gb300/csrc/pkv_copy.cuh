@@ -45,6 +45,7 @@ template <> struct VecT<16> { using T = uint4; };
 template <> struct VecT<8>  { using T = uint2; };
 template <> struct VecT<4>  { using T = uint32_t; };
 template <> struct VecT<2>  { using T = uint16_t; };
+template <> struct VecT<1>  { using T = uint8_t; };
 
 // a2: k_cache.view(-1, row)[slot[i]] = k[i] (and v).  grid = (tokens,
 // vector chunks of a row, 2 for K/V); one thread moves VW bytes.
@@ -107,6 +108,90 @@ __global__ void kv_append_kernel(const uint8_t* __restrict__ k, const uint8_t* _
   const uint8_t* src = (blockIdx.z ? v : k) + i * row_bytes + e * VW;
   uint8_t* dst = (blockIdx.z ? v_cache : k_cache) + slot * row_bytes + e * VW;
   *reinterpret_cast<V*>(dst) = __ldg(reinterpret_cast<const V*>(src));
+}
+
+// a1 + a2 into a quantized pool.  grid = (tokens, 2 for K/V), 128 threads.
+// FMT 1: e4m3(x / scale) per element (per-tensor scale).  FMT 2: the token's
+// row (all heads) gets scale = max|x| / 127 and codes rint(x / scale), the
+// scale stored at the token's slot.  Divisions are IEEE float32 (__fdiv_rn).
+constexpr int kQuantThreads = 128;
+
+template <typename TIN, int FMT>
+__global__ void __launch_bounds__(kQuantThreads)
+kv_append_quant_kernel(const TIN* __restrict__ k, const TIN* __restrict__ v,
+                       const int32_t* __restrict__ block_tables, int32_t max_blocks_per_seq,
+                       const int32_t* __restrict__ positions, int32_t block_size,
+                       int32_t log2_bs, int64_t num_blocks, uint8_t* __restrict__ k_cache,
+                       uint8_t* __restrict__ v_cache, int64_t row_elems, float k_scale,
+                       float v_scale, float* __restrict__ k_ts, float* __restrict__ v_ts,
+                       int64_t* __restrict__ slots) {
+  __shared__ float s_red[kQuantThreads / 32];
+  pdl_wait_primary();
+  pdl_launch_dependents();
+  const int64_t i = blockIdx.x;
+  const int z = blockIdx.y;
+  const bool leader = threadIdx.x == 0 && z == 0;
+  const int t = positions[i];
+  int64_t slot = -1;
+  if (t >= 0) {
+    const int lb = log2_bs >= 0 ? (t >> log2_bs) : (t / block_size);
+    const int off = log2_bs >= 0 ? (t & (block_size - 1)) : (t - lb * block_size);
+    if (lb >= max_blocks_per_seq) {
+      if (leader) record_error(PKV_DEVERR_POSITION);
+    } else {
+      const int64_t phys = block_tables[i * max_blocks_per_seq + lb];
+      if (phys < 0 || phys >= num_blocks) {
+        if (leader) record_error(PKV_DEVERR_BLOCK_ID);
+      } else {
+        slot = phys * block_size + off;
+      }
+    }
+  }
+  if (leader && slots != nullptr) slots[i] = slot;
+  if (slot < 0) return;
+  const TIN* src = (z ? v : k) + i * row_elems;
+  uint8_t* dst = (z ? v_cache : k_cache) + slot * row_elems;
+  if constexpr (FMT == 1) {
+    const float sc = z ? v_scale : k_scale;
+    for (int64_t e = threadIdx.x; e < row_elems; e += blockDim.x)
+      dst[e] = f32_to_e4m3(__fdiv_rn(to_f32(src[e]), sc));
+  } else {
+    float amax = 0.f;
+    for (int64_t e = threadIdx.x; e < row_elems; e += blockDim.x)
+      amax = fmaxf(amax, fabsf(to_f32(src[e])));
+    amax = warp_max(amax);
+    if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = amax;
+    __syncthreads();
+    amax = s_red[0];
+#pragma unroll
+    for (int w = 1; w < kQuantThreads / 32; ++w) amax = fmaxf(amax, s_red[w]);
+    const float sc = amax == 0.f ? 0.f : __fdiv_rn(amax, 127.f);
+    int8_t* d8 = reinterpret_cast<int8_t*>(dst);
+    for (int64_t e = threadIdx.x; e < row_elems; e += blockDim.x) {
+      float c = sc == 0.f ? 0.f : rintf(__fdiv_rn(to_f32(src[e]), sc));
+      c = fminf(127.f, fmaxf(-127.f, c));
+      d8[e] = (int8_t)c;
+    }
+    if (threadIdx.x == 0) (z ? v_ts : k_ts)[slot] = sc;
+  }
+}
+
+// Per-token scales of copied blocks (INT8 pools): ts[dst*K + i] = ts[src*K + i].
+__global__ void token_scale_copy_kernel(float* __restrict__ k_ts, float* __restrict__ v_ts,
+                                        const int64_t* __restrict__ pairs, int64_t num_blocks,
+                                        int32_t block_size) {
+  pdl_wait_primary();
+  pdl_launch_dependents();
+  const int64_t p = blockIdx.x;
+  const int64_t src = pairs[2 * p], dst = pairs[2 * p + 1];
+  if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+    if (threadIdx.x == 0) record_error(PKV_DEVERR_COPY_PAIR);
+    return;
+  }
+  for (int i = threadIdx.x; i < block_size; i += blockDim.x) {
+    k_ts[dst * block_size + i] = k_ts[src * block_size + i];
+    v_ts[dst * block_size + i] = v_ts[src * block_size + i];
+  }
 }
 
 // Failure-path self test: one CTA waits on an mbarrier that nothing ever

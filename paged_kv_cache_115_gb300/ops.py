@@ -42,6 +42,15 @@ class AttentionConfig(ctypes.Structure):
     _fields_ = [("kernel", c_i32), ("num_splits", c_i32), ("reserved", c_i32 * 6)]
 
 
+class KvQuant(ctypes.Structure):
+    """pkv_kv_quant: format 1 = FP8 e4m3 (per-tensor scales), 2 = INT8 per token."""
+    _fields_ = [("format", c_i32), ("k_scale", c_f), ("v_scale", c_f),
+                ("k_token_scales", c_vp), ("v_token_scales", c_vp)]
+
+
+KV_FP8_E4M3, KV_INT8_TOKEN = 1, 2
+
+
 def _sig(name, restype, *argtypes):
     f = getattr(_lib, name)
     f.restype = restype
@@ -70,6 +79,17 @@ _attention = _sig("pkv_attention_decode", c_i32, c_vp, c_vp, c_vp, c_vp, c_i32, 
 _attention_noalloc = _sig("pkv_attention_decode_noalloc", c_i32, c_vp, c_vp, c_vp, c_vp, c_i32,
                           c_vp, c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, c_i64, c_f, c_vp, c_i32,
                           ctypes.POINTER(AttentionConfig), c_vp)
+_append_quant = _sig("pkv_kv_append_quant", c_i32, c_vp, c_vp, c_vp, c_i32, c_vp, c_i32, c_vp,
+                     c_vp, c_i64, c_i32, c_i32, c_i32, c_i32, ctypes.POINTER(KvQuant), c_vp,
+                     c_vp)
+_copy_quant = _sig("pkv_kv_block_copy_quant", c_i32, c_vp, c_vp, c_vp, c_i64, c_i64, c_i32, c_i32,
+                   c_i32, ctypes.POINTER(KvQuant), c_vp)
+_ws_quant = _sig("pkv_attention_quant_workspace_bytes", c_i32, c_i32, c_i32, c_i32, c_i32, c_i32,
+                 c_i32, c_i32, ctypes.POINTER(KvQuant), ctypes.POINTER(AttentionConfig),
+                 ctypes.POINTER(c_sz))
+_attention_quant = _sig("pkv_attention_decode_quant", c_i32, c_vp, c_vp, c_vp, c_vp, c_i32, c_vp,
+                        c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, c_i64, c_f, c_vp, c_vp, c_sz,
+                        c_i32, ctypes.POINTER(KvQuant), ctypes.POINTER(AttentionConfig), c_vp)
 _dev_error = _sig("pkv_get_device_error", c_i32, ctypes.POINTER(c_i32), c_vp)
 
 # bytes of the library's fixed attention scratch (PKV_NOALLOC_SCRATCH_BYTES)
@@ -78,7 +98,9 @@ NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 EXPORTED = ("pkv_status_string", "pkv_last_error_message", "pkv_version", "pkv_slot_mapping",
             "pkv_kv_write", "pkv_kv_append", "pkv_kv_block_copy", "pkv_selftest_wait_timeout", "pkv_attention_workspace_bytes",
             "pkv_attention_launch_count", "pkv_attention_decode",
-            "pkv_attention_decode_noalloc", "pkv_get_device_error")
+            "pkv_attention_decode_noalloc", "pkv_kv_append_quant", "pkv_kv_block_copy_quant",
+            "pkv_attention_quant_workspace_bytes", "pkv_attention_decode_quant",
+            "pkv_get_device_error")
 
 
 class PagedKVError(RuntimeError):
@@ -314,3 +336,122 @@ def get_device_error(device=None) -> int:
     if st not in (PKV_OK, PKV_ERR_DEVICE_CHECK):
         _check(st, "pkv_get_device_error")
     return int(code.value)
+
+
+# ---------------------------------------------------------------------------
+# quantized KV cache (FP8 e4m3 per-tensor scale, INT8 per-token scale)
+# ---------------------------------------------------------------------------
+
+def kv_quant(fmt: str, k_scale: float = 1.0, v_scale: float = 1.0,
+             k_token_scales: Optional[torch.Tensor] = None,
+             v_token_scales: Optional[torch.Tensor] = None) -> KvQuant:
+    """Describe a quantized pool: ``fmt`` "fp8" (scales per tensor) or "int8"
+    (float32 CUDA tensors of one scale per token slot)."""
+    qd = KvQuant()
+    if fmt == "fp8":
+        qd.format, qd.k_scale, qd.v_scale = KV_FP8_E4M3, float(k_scale), float(v_scale)
+    elif fmt == "int8":
+        for name, t in (("k_token_scales", k_token_scales), ("v_token_scales", v_token_scales)):
+            if t is None:
+                raise ValueError(f"int8 pools need {name}")
+            _need(t, name, torch.float32, 1)
+        qd.format = KV_INT8_TOKEN
+        qd.k_token_scales = k_token_scales.data_ptr()
+        qd.v_token_scales = v_token_scales.data_ptr()
+    else:
+        raise ValueError(f"unknown quantized format {fmt!r}")
+    return qd
+
+
+def _need_pool(t: torch.Tensor, name: str) -> None:
+    _need(t, name, None, 4)
+    if t.dtype not in (torch.uint8, torch.int8, getattr(torch, "float8_e4m3fn", torch.uint8)):
+        raise TypeError(f"{name} must hold one-byte codes (uint8 / int8 / float8_e4m3fn)")
+
+
+def paged_kv_append_quant(k: torch.Tensor, v: torch.Tensor, block_tables: torch.Tensor,
+                          positions: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                          quant: KvQuant,
+                          slot_mapping_out: Optional[torch.Tensor] = None) -> None:
+    """Slot mapping + quantized KV write in one launch (rows k, v in bf16/fp32)."""
+    _need_pool(k_cache, "k_cache")
+    _need_pool(v_cache, "v_cache")
+    nb, K, H, D = k_cache.shape
+    _need(k, "k", None, 3)
+    _need(v, "v", k.dtype, 3)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(positions, "positions", torch.int32, 1)
+    T = k.shape[0]
+    if tuple(k.shape) != (T, H, D) or tuple(v.shape) != (T, H, D) or positions.shape[0] != T \
+            or block_tables.shape[0] != T or v_cache.shape != k_cache.shape:
+        raise ValueError("k/v/positions/block_tables/pool shapes do not match")
+    sp = None
+    if slot_mapping_out is not None:
+        _need(slot_mapping_out, "slot_mapping_out", torch.int64, 1)
+        sp = _ptr(slot_mapping_out)
+    _check(_append_quant(_ptr(k), _ptr(v), _ptr(block_tables), block_tables.shape[1],
+                         _ptr(positions), T, _ptr(k_cache), _ptr(v_cache), nb, K, H, D,
+                         _dtype_code(k), ctypes.byref(quant), sp, _stream(k_cache.device)),
+           "pkv_kv_append_quant")
+
+
+def kv_block_copy_quant(k_cache: torch.Tensor, v_cache: torch.Tensor,
+                        src_dst_pairs: torch.Tensor, quant: KvQuant) -> None:
+    """Copy-on-write block copy of a quantized pool (codes and, for INT8, scales)."""
+    _need_pool(k_cache, "k_cache")
+    _need_pool(v_cache, "v_cache")
+    _need(src_dst_pairs, "src_dst_pairs", torch.int64, 2)
+    nb, K, H, D = k_cache.shape
+    _check(_copy_quant(_ptr(k_cache), _ptr(v_cache), _ptr(src_dst_pairs), src_dst_pairs.shape[0],
+                       nb, K, H, D, ctypes.byref(quant), _stream(k_cache.device)),
+           "pkv_kv_block_copy_quant")
+
+
+def attention_quant_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                                    max_context_len, q_dtype: torch.dtype, quant: KvQuant,
+                                    kernel: int = 0, num_splits: int = 0) -> int:
+    out = c_sz(0)
+    cfg = _cfg(kernel, num_splits)
+    code = PKV_BF16 if q_dtype == torch.bfloat16 else PKV_F32
+    _check(_ws_quant(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_context_len,
+                     code, ctypes.byref(quant), ctypes.byref(cfg), ctypes.byref(out)),
+           "pkv_attention_quant_workspace_bytes")
+    return int(out.value)
+
+
+def paged_attention_decode_quant(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                 block_tables: torch.Tensor, context_lens: torch.Tensor,
+                                 scale: float, quant: KvQuant,
+                                 out: Optional[torch.Tensor] = None,
+                                 max_context_len: Optional[int] = None,
+                                 workspace: Optional[torch.Tensor] = None,
+                                 kernel: int = 0, num_splits: int = 0) -> torch.Tensor:
+    """Decode attention over a quantized pool (values read back as code * scale)."""
+    _need(q, "q", None, 3)
+    _need_pool(k_cache, "k_cache")
+    _need_pool(v_cache, "v_cache")
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(context_lens, "context_lens", torch.int32, 1)
+    S, H_q, D = q.shape
+    nb, K, H_kv, D2 = k_cache.shape
+    if D2 != D or v_cache.shape != k_cache.shape or context_lens.shape[0] != S \
+            or block_tables.shape[0] != S:
+        raise ValueError("shape mismatch between q, caches, tables and lengths")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", q.dtype, 3)
+    if max_context_len is None:
+        max_context_len = int(context_lens.max().item()) if S else 0
+    need = attention_quant_workspace_bytes(S, H_q, H_kv, D, K, max_context_len, q.dtype, quant,
+                                           kernel, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _need(workspace, "workspace", torch.uint8, 1)
+    cfg = _cfg(kernel, num_splits)
+    _check(_attention_quant(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                            block_tables.shape[1], _ptr(context_lens), max_context_len, S, H_q,
+                            H_kv, D, K, nb, float(scale), _ptr(out), _ptr(workspace),
+                            workspace.numel(), _dtype_code(q), ctypes.byref(quant),
+                            ctypes.byref(cfg), _stream(q.device)),
+           "pkv_attention_decode_quant")
+    return out

@@ -1,0 +1,205 @@
+"""GPU parity of the quantized KV cache (FP8 e4m3 per-tensor scale, INT8 per
+token) against the oracle: quantized writes and copies bit-exact (codes and
+scales), attention within the tolerance of the plain path."""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import quant as Q
+import oracle
+from paged_kv_cache_115_gb300 import workloads as wl
+from tests._helpers import as_f64, check_attention, storage
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def ops():
+    from paged_kv_cache_115_gb300 import build
+    build.build()
+    from paged_kv_cache_115_gb300 import ops as o
+    o.get_device_error()
+    return o
+
+
+def f32_rows(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().float().numpy()
+
+
+def identity_tables(T, K, nb, rng):
+    """One token per row, each token in its own (shuffled) block at offset
+    t % K: row i holds position i % K in block perm[i]."""
+    perm = rng.permutation(nb)[:T]
+    bt = perm.reshape(T, 1).astype(np.int32)
+    pos = (np.arange(T) % K).astype(np.int32)
+    return bt, pos
+
+
+@pytest.mark.parametrize("scale", [1.0, 0.37, 3.0])
+def test_fp8_append_every_bf16_value(ops, scale):
+    # every finite bf16 bit pattern, as K rows; V rows the same values reversed
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    vals = (bits.astype(np.uint32) << 16).view(np.float32)
+    bits = bits[np.isfinite(vals)]
+    n = (len(bits) // 256) * 256
+    H, D = 2, 128
+    T = n // (H * D)
+    kb = torch.from_numpy(bits[:n].view(np.int16).reshape(T, H, D).copy()).view(torch.bfloat16)
+    vb = torch.from_numpy(bits[:n][::-1].view(np.int16).reshape(T, H, D).copy()).view(torch.bfloat16)
+    K, nb = 4, T + 3
+    rng = np.random.default_rng(0)
+    bt, pos = identity_tables(T, K, nb, rng)
+    kc = torch.full((nb, K, H, D), 0x7F, dtype=torch.uint8)
+    vc = torch.full((nb, K, H, D), 0x7F, dtype=torch.uint8)
+    dkc, dvc = kc.to(DEV), vc.to(DEV)
+    qd = ops.kv_quant("fp8", scale, scale * 2)
+    slots = torch.empty(T, dtype=torch.int64, device=DEV)
+    ops.paged_kv_append_quant(kb.to(DEV), vb.to(DEV), torch.from_numpy(bt).to(DEV),
+                              torch.from_numpy(pos).to(DEV), dkc, dvc, qd, slots)
+    assert ops.get_device_error() == 0
+    oslots = oracle.slot_mapping(bt, pos, K)
+    assert np.array_equal(slots.cpu().numpy(), oslots)
+    ek, ev = Q.kv_write_fp8(kc.numpy(), vc.numpy(), f32_rows(kb), f32_rows(vb), oslots,
+                            scale, scale * 2)
+    assert np.array_equal(dkc.cpu().numpy(), ek)
+    assert np.array_equal(dvc.cpu().numpy(), ev)
+
+
+@pytest.mark.parametrize("in_dtype", [torch.bfloat16, torch.float32])
+def test_int8_append_bit_exact(ops, in_dtype):
+    rng = np.random.default_rng(1)
+    T, H, D, K, nb = 200, 8, 128, 16, 230
+    mags = 10.0 ** rng.uniform(-4, 4, size=(T, 1, 1))
+    k = torch.from_numpy((rng.standard_normal((T, H, D)) * mags).astype(np.float32)).to(in_dtype)
+    v = torch.from_numpy((rng.standard_normal((T, H, D)) * mags).astype(np.float32)).to(in_dtype)
+    k[3] = 0.0                                   # all-zero row: scale 0, codes 0
+    v[7, 2, 5] = 1e4                             # one outlier dominates its row
+    bt, pos = identity_tables(T, K, nb, rng)
+    pos[5] = -1                                  # padding token
+    kc = torch.full((nb, K, H, D), 99, dtype=torch.int8)
+    vc = torch.full((nb, K, H, D), 99, dtype=torch.int8)
+    kts = torch.full((nb * K,), -5.0)
+    vts = torch.full((nb * K,), -5.0)
+    d = [x.to(DEV) for x in (kc, vc, kts, vts)]
+    qd = ops.kv_quant("int8", k_token_scales=d[2], v_token_scales=d[3])
+    ops.paged_kv_append_quant(k.to(DEV), v.to(DEV), torch.from_numpy(bt).to(DEV),
+                              torch.from_numpy(pos).to(DEV), d[0], d[1], qd)
+    assert ops.get_device_error() == 0
+    oslots = oracle.slot_mapping(bt, pos, K)
+    ek, ev, ekt, evt = Q.kv_write_int8(kc.numpy(), vc.numpy(), kts.numpy(), vts.numpy(),
+                                       f32_rows(k), f32_rows(v), oslots)
+    assert np.array_equal(d[0].cpu().numpy(), ek) and np.array_equal(d[1].cpu().numpy(), ev)
+    assert np.array_equal(d[2].cpu().numpy().view(np.uint32), ekt.view(np.uint32))
+    assert np.array_equal(d[3].cpu().numpy().view(np.uint32), evt.view(np.uint32))
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "int8"])
+def test_quant_block_copy(ops, fmt):
+    rng = np.random.default_rng(2)
+    nb, K, H, D = 12, 16, 8, 128
+    kc = torch.from_numpy(rng.integers(0, 256, size=(nb, K, H, D), dtype=np.uint8))
+    vc = torch.from_numpy(rng.integers(0, 256, size=(nb, K, H, D), dtype=np.uint8))
+    kts = torch.from_numpy(rng.standard_normal(nb * K).astype(np.float32))
+    vts = torch.from_numpy(rng.standard_normal(nb * K).astype(np.float32))
+    pairs = np.array([[0, 5], [3, 9], [11, 2]], dtype=np.int64)
+    d = [x.to(DEV) for x in (kc, vc, kts, vts)]
+    qd = ops.kv_quant(fmt, 1.0, 1.0, d[2], d[3]) if fmt == "int8" else ops.kv_quant(fmt)
+    ops.kv_block_copy_quant(d[0], d[1], torch.from_numpy(pairs).to(DEV), qd)
+    assert ops.get_device_error() == 0
+    ek, ev = oracle.kv_block_copy(kc.numpy(), vc.numpy(), pairs)
+    assert np.array_equal(d[0].cpu().numpy(), ek) and np.array_equal(d[1].cpu().numpy(), ev)
+    if fmt == "int8":
+        ekt, evt = oracle.kv_block_copy(kts.numpy().reshape(nb, K), vts.numpy().reshape(nb, K),
+                                        pairs)
+        assert np.array_equal(d[2].cpu().numpy(), ekt.reshape(-1))
+        assert np.array_equal(d[3].cpu().numpy(), evt.reshape(-1))
+    else:
+        assert np.array_equal(d[2].cpu().numpy(), kts.numpy())   # fp8: scales untouched
+
+
+def quant_problem(fmt, lens, H_q, H_kv, D, K, q_dtype, seed):
+    """A decode step whose pool already holds quantized history: codes drawn
+    directly (fp8: finite codes with |value| <= 8; int8: any code with a
+    random per-slot scale); slots without history hold NaN canaries (fp8 code
+    0x7F, int8 scale NaN)."""
+    w = wl.build_decode("quant", lens, H_q, H_kv, D, K, q_dtype, seed=seed)
+    rng = np.random.default_rng(seed)
+    nb, hist = w.num_blocks, w.history_mask
+    shape = (nb, K, H_kv, D)
+    c = wl.materialize(w, seed=seed, canary=False)
+    if fmt == "fp8":
+        vals = Q.e4m3_values()
+        ok = np.array([i for i in range(256) if np.isfinite(vals[i]) and abs(vals[i]) <= 8],
+                      np.uint8)
+        kc = rng.choice(ok, size=shape).astype(np.uint8)
+        vc = rng.choice(ok, size=shape).astype(np.uint8)
+        kc[~hist] = 0x7F
+        vc[~hist] = 0x7F
+        return w, c, kc, vc, None, None
+    kc = rng.integers(-127, 128, size=shape).astype(np.int8)
+    vc = rng.integers(-127, 128, size=shape).astype(np.int8)
+    kts = rng.uniform(0.002, 0.03, size=nb * K).astype(np.float32)
+    vts = rng.uniform(0.002, 0.03, size=nb * K).astype(np.float32)
+    kts[~hist.reshape(-1)] = np.nan
+    vts[~hist.reshape(-1)] = np.nan
+    return w, c, kc, vc, kts, vts
+
+
+SHAPES = [(128, 4, 16), (64, 2, 4), (128, 8, 32)]
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "int8"])
+@pytest.mark.parametrize("q_dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("D,G,K", SHAPES)
+@pytest.mark.parametrize("num_splits", [0, 64])
+def test_quant_step_matches_oracle(ops, fmt, q_dtype, D, G, K, num_splits):
+    H_kv = 2
+    lens = [1, 17, 0, 300, 64, 601]
+    w, c, kc, vc, kts, vts = quant_problem(fmt, lens, G * H_kv, H_kv, D, K, q_dtype,
+                                           seed=D + G + K)
+    dkc, dvc = torch.from_numpy(kc).to(DEV), torch.from_numpy(vc).to(DEV)
+    if fmt == "fp8":
+        qd = ops.kv_quant("fp8", 0.5, 1.5)
+        scales = dict(k_scale=0.5, v_scale=1.5)
+    else:
+        dkt, dvt = torch.from_numpy(kts.copy()).to(DEV), torch.from_numpy(vts.copy()).to(DEV)
+        qd = ops.kv_quant("int8", k_token_scales=dkt, v_token_scales=dvt)
+    d = {k: v.to(DEV) for k, v in c.items()}
+    ops.paged_kv_append_quant(d["k_new"], d["v_new"], d["block_tables"], d["positions"], dkc,
+                              dvc, qd)
+    out = ops.paged_attention_decode_quant(d["q"], dkc, dvc, d["block_tables"],
+                                           d["context_lens"], w.scale, qd,
+                                           max_context_len=w.max_context_len,
+                                           num_splits=num_splits)
+    torch.cuda.synchronize()
+    assert ops.get_device_error() == 0
+    slots = oracle.slot_mapping(w.block_tables, w.positions, w.block_size)
+    if fmt == "fp8":
+        okc, ovc = Q.kv_write_fp8(kc, vc, f32_rows(c["k_new"]), f32_rows(c["v_new"]), slots,
+                                  0.5, 1.5)
+        tok = {}
+    else:
+        okc, ovc, okt, ovt = Q.kv_write_int8(kc, vc, kts, vts, f32_rows(c["k_new"]),
+                                             f32_rows(c["v_new"]), slots)
+        scales = {}
+        tok = dict(k_tok_scales=okt, v_tok_scales=ovt)
+        assert np.array_equal(dkt.cpu().numpy().view(np.uint32), okt.view(np.uint32))
+    assert np.array_equal(dkc.cpu().numpy(), okc) and np.array_equal(dvc.cpu().numpy(), ovc)
+    ref = Q.paged_attention_decode_quant(storage(c["q"]), okc, ovc, w.block_tables,
+                                         w.context_lens, w.scale, q_dtype, fmt, **scales, **tok)
+    check_attention(as_f64(out), ref, q_dtype, f"{fmt} {q_dtype} D{D} G{G} K{K}")
+
+
+def test_quant_rejects_bad_descriptions(ops):
+    q = torch.zeros((1, 2, 128), dtype=torch.bfloat16, device=DEV)
+    kc = torch.zeros((2, 16, 1, 128), dtype=torch.uint8, device=DEV)
+    bt = torch.zeros((1, 1), dtype=torch.int32, device=DEV)
+    lens = torch.ones(1, dtype=torch.int32, device=DEV)
+    with pytest.raises(ops.PagedKVError, match="scales"):
+        ops.paged_attention_decode_quant(q, kc, kc, bt, lens, 0.1, ops.kv_quant("fp8", 0.0, 1.0))
+    bad = ops.KvQuant()
+    bad.format = 2                              # int8 without scale arrays
+    with pytest.raises(ops.PagedKVError, match="scale"):
+        ops.paged_attention_decode_quant(q, kc, kc, bt, lens, 0.1, bad)
