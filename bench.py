@@ -251,34 +251,79 @@ def run_gpu(args):
     w = wl.build(args.workload, seed=rank_seed(args.seed, rank))
     t = wl.materialize(w, device=dev, seed=rank_seed(args.seed, rank), canary=False,
                        values_device="cuda")
-    kv_bytes = accounting.attention_kv_bytes(w.context_lens, w.num_kv_heads, w.head_dim,
-                                             w.elem_bytes)
+    fmt = args.kv_format
     stream = torch.cuda.current_stream(dev)
-    ws_bytes = ops.attention_workspace_bytes(w.num_seqs, w.num_q_heads, w.num_kv_heads,
-                                             w.head_dim, w.block_size, w.max_context_len,
-                                             t["q"].dtype)
-    workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
     out = torch.empty_like(t["q"])
     slots = torch.empty(w.num_seqs, dtype=torch.int64, device=dev)
     has_copy = len(w.copy_pairs) > 0
     max_len = w.max_context_len
+    if fmt == "bf16":
+        kv_bytes = accounting.attention_kv_bytes(w.context_lens, w.num_kv_heads, w.head_dim,
+                                                 w.elem_bytes)
+        ws_bytes = ops.attention_workspace_bytes(w.num_seqs, w.num_q_heads, w.num_kv_heads,
+                                                 w.head_dim, w.block_size, max_len, t["q"].dtype)
+    else:
+        # one-byte pools of seeded random codes (finite e4m3 codes; int8 codes
+        # with per-slot scales); the bf16 pools are dropped
+        g = torch.Generator(device=dev)
+        g.manual_seed(rank_seed(args.seed, rank) + 7)
+        shape = t["k_cache"].shape
+        del t["k_cache"], t["v_cache"]
+        for name in ("k_cache", "v_cache"):
+            c = torch.randint(0, 256, shape, generator=g, device=dev, dtype=torch.int32)
+            c = torch.where((c & 0x7F) == 0x7F, c - 1, c).to(torch.uint8)
+            t[name] = c if fmt == "fp8" else c.view(torch.int8)
+        if fmt == "int8":
+            n = shape[0] * shape[1]
+            t["k_ts"] = torch.rand(n, generator=g, device=dev) * 0.02 + 0.001
+            t["v_ts"] = torch.rand(n, generator=g, device=dev) * 0.02 + 0.001
+            qd = ops.kv_quant("int8", k_token_scales=t["k_ts"], v_token_scales=t["v_ts"])
+        else:
+            qd = ops.kv_quant("fp8", 0.05, 0.05)
+        kv_bytes = accounting.attention_kv_bytes(w.context_lens, w.num_kv_heads, w.head_dim, 1)
+        if fmt == "int8":
+            kv_bytes += int(w.context_lens.sum()) * 2 * 4      # one K and one V scale per token
+        ws_bytes = ops.attention_quant_workspace_bytes(w.num_seqs, w.num_q_heads,
+                                                       w.num_kv_heads, w.head_dim, w.block_size,
+                                                       max_len, t["q"].dtype, qd)
+    workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
 
     def attention():
-        ops.paged_attention_decode(t["q"], t["k_cache"], t["v_cache"], t["block_tables"],
-                                   t["context_lens"], w.scale, out=out, max_context_len=max_len,
-                                   workspace=workspace)
+        if fmt == "bf16":
+            ops.paged_attention_decode(t["q"], t["k_cache"], t["v_cache"], t["block_tables"],
+                                       t["context_lens"], w.scale, out=out,
+                                       max_context_len=max_len, workspace=workspace)
+        else:
+            ops.paged_attention_decode_quant(t["q"], t["k_cache"], t["v_cache"],
+                                             t["block_tables"], t["context_lens"], w.scale, qd,
+                                             out=out, max_context_len=max_len,
+                                             workspace=workspace)
+
+    def copy_fn():
+        if fmt == "bf16":
+            ops.kv_block_copy(t["k_cache"], t["v_cache"], t["copy_pairs"])
+        else:
+            ops.kv_block_copy_quant(t["k_cache"], t["v_cache"], t["copy_pairs"], qd)
+
+    def append_fn():
+        # slot mapping + KV write of the new tokens in one fused launch
+        if fmt == "bf16":
+            ops.paged_kv_append(t["k_new"], t["v_new"], t["block_tables"], t["positions"],
+                                t["k_cache"], t["v_cache"], slots)
+        else:
+            ops.paged_kv_append_quant(t["k_new"], t["v_new"], t["block_tables"], t["positions"],
+                                      t["k_cache"], t["v_cache"], qd, slots)
 
     def prologue():
         if has_copy:
-            ops.kv_block_copy(t["k_cache"], t["v_cache"], t["copy_pairs"])
-        # slot mapping + KV write of the new tokens, one fused launch
-        ops.paged_kv_append(t["k_new"], t["v_new"], t["block_tables"], t["positions"],
-                            t["k_cache"], t["v_cache"], slots)
+            copy_fn()
+        append_fn()
 
     # kernels launched per step (ours only)
     attn_launches = ops.attention_launch_count(w.num_seqs, w.num_q_heads, w.num_kv_heads,
                                                w.head_dim, w.block_size, max_len, t["q"].dtype)
-    launches_per_step = (1 if has_copy else 0) + 1 + attn_launches
+    copy_launches = (1 if fmt != "int8" else 2) if has_copy else 0
+    launches_per_step = copy_launches + 1 + attn_launches
 
     for _ in range(max(args.warmup, 3)):
         prologue()
@@ -315,15 +360,14 @@ def run_gpu(args):
     # (a 256 MB write) before every timed launch
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     row_fns = []
+    pool_eb = w.elem_bytes if fmt == "bf16" else 1
+    n_new = int((w.positions >= 0).sum())
     if has_copy:
-        row_fns.append(("kv_block_copy", lambda: ops.kv_block_copy(
-            t["k_cache"], t["v_cache"], t["copy_pairs"]),
-            accounting.block_copy_bytes(len(w.copy_pairs), w.block_size, w.num_kv_heads,
-                                        w.head_dim, w.elem_bytes)))
-    row_fns.append(("paged_kv_append", lambda: ops.paged_kv_append(
-        t["k_new"], t["v_new"], t["block_tables"], t["positions"], t["k_cache"], t["v_cache"],
-        slots), accounting.kv_write_bytes(int((w.positions >= 0).sum()), w.num_kv_heads,
-                                          w.head_dim, w.elem_bytes)))
+        row_fns.append(("kv_block_copy", copy_fn,
+                        accounting.block_copy_bytes(len(w.copy_pairs), w.block_size,
+                                                    w.num_kv_heads, w.head_dim, pool_eb)))
+    row_fns.append(("paged_kv_append", append_fn,
+                    n_new * w.num_kv_heads * w.head_dim * 2 * (w.elem_bytes + pool_eb)))
     row_fns.append(("paged_attention_decode", attention, kv_bytes))
     rows = {}
     R = max(5, min(50, K))
@@ -406,7 +450,7 @@ def run_gpu(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": w.dtype,
+        "dtype": w.dtype if fmt == "bf16" else f"{w.dtype} q / {fmt} KV",
         "data": "synthetic: seeded N(0,1) q/k/v rounded to bf16; block tables from a seeded "
                 "shuffled free list; lengths drawn per the workload recipe",
         "config": cfg,
@@ -482,6 +526,9 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["gpu", "reference"], default="gpu")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--kv-format", choices=["bf16", "fp8", "int8"], default="bf16",
+                    help="KV pool storage: bf16, FP8 e4m3 (per-tensor scale) or INT8 "
+                         "(per-token scale)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of CPU work for the oracle baseline sample")

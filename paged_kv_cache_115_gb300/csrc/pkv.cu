@@ -202,16 +202,32 @@ pkv_status plan_attention(int S, int H_q, int H_kv, int D, int K, int max_len, i
   return PKV_OK;
 }
 
-// Plan for a quantized pool: the CUDA-core kernel (head_dim 64 / 128, G <= 16).
+// Plan for a quantized pool: the tensor-core kernel when the shape allows it
+// (bf16 queries, head_dim 128, G <= 8, block_size % 16 == 0, 16-byte aligned
+// pools and scales), else the CUDA-core kernel (head_dim 64 / 128, G <= 16).
 pkv_status plan_attention_quant(int S, int H_q, int H_kv, int D, int K, int max_len,
-                                pkv_dtype q_dt, const pkv_kv_quant* quant,
-                                const pkv_attention_config* cfg, AttnPlan* plan) {
+                                int64_t num_blocks, pkv_dtype q_dt, const pkv_kv_quant* quant,
+                                const pkv_attention_config* cfg, bool aligned_ok,
+                                AttnPlan* plan) {
   pkv_attention_config c = {};
   if (cfg) c = *cfg;
-  PKV_CHECK(c.kernel == 0 || c.kernel == 2, PKV_ERR_UNSUPPORTED,
-            "quantized pools use the CUDA-core kernel (config.kernel 0 or 2)");
+  PKV_CHECK(c.kernel >= 0 && c.kernel <= 2, PKV_ERR_INVALID_ARGUMENT, "bad attention config");
   PKV_CHECK(D == 64 || D == 128, PKV_ERR_UNSUPPORTED, "quantized pools need head_dim 64 or 128");
-  (void)quant;
+  PKV_CHECK(H_q > 0 && H_kv > 0 && H_q % H_kv == 0, PKV_ERR_INVALID_ARGUMENT,
+            "num_q_heads %% num_kv_heads != 0");
+  bool scales_ok = true;
+  if (quant->format == PKV_KV_INT8_TOKEN && quant->k_token_scales && quant->v_token_scales)
+    scales_ok = aligned(quant->k_token_scales, 16) && aligned(quant->v_token_scales, 16);
+  const bool tc_ok = q_dt == PKV_BF16 && D == 128 && tc_shape_ok(H_q / H_kv, D, K, num_blocks,
+                                                                  PKV_BF16) &&
+                     aligned_ok && scales_ok;
+  if (c.kernel == 1 || (c.kernel == 0 && tc_ok)) {
+    PKV_CHECK(tc_ok, PKV_ERR_UNSUPPORTED,
+              "tensor-core kernel on a one-byte pool needs bf16 queries, head_dim 128, G <= 8, "
+              "block_size %% 16 == 0 and 16-byte aligned pools and scales");
+    c.kernel = 1;
+    return plan_attention(S, H_q, H_kv, D, K, max_len, num_blocks, PKV_BF16, &c, true, plan);
+  }
   c.kernel = 2;
   return plan_attention(S, H_q, H_kv, D, K, max_len, 1, q_dt, &c, false, plan);
 }
@@ -230,47 +246,54 @@ pkv::Workspace carve_workspace(void* ws, const AttnPlan& p, int H_q, int D) {
 }
 
 // ---- tensor-core kernel dispatch ------------------------------------------------
-template <int D, int HPC>
+template <int D, int HPC, int CT>
 struct TcInst {
-  // as many stages as fit in ~192 KiB of shared memory, between 2 and 8
-  static constexpr int STAGE_BYTES = 2 * HPC * (D / 64) * pkv::kBoxBytes;
-  static constexpr int NS_FIT = 196608 / STAGE_BYTES;
+  // stages: as many as fit in ~192 KiB (bf16) / ~203 KiB (one-byte pools)
+  // of shared memory, between 2 and 8
+  static constexpr int STAGE_BYTES = pkv::TcCfg<D, HPC, 2, CT>::STAGE;
+  static constexpr int BUDGET = CT ? 217088 - 9216 : 196608;
+  static constexpr int NS_FIT = BUDGET / STAGE_BYTES;
   static constexpr int NS = NS_FIT < 2 ? 2 : (NS_FIT > 8 ? 8 : NS_FIT);
-  using C = pkv::TcCfg<D, HPC, NS>;
+  using C = pkv::TcCfg<D, HPC, NS, CT>;
   static std::once_flag flags[kMaxDevices];
   static cudaError_t errs[kMaxDevices];
   static pkv_status launch(const pkv::TcParams& prm, int n, int groups, cudaStream_t st, int dev) {
-    auto k = pkv::attn_tc_kernel<D, HPC, NS>;
+    auto k = pkv::attn_tc_kernel<D, HPC, NS, CT>;
     pkv_status s = set_smem_once(k, C::SMEM, flags, errs, dev);
     if (s != PKV_OK) return s;
     PKV_CUDA(launch_pdl(k, dim3(n, groups), dim3(C::THREADS), (size_t)C::SMEM, st, prm));
     return PKV_OK;
   }
 };
-template <int D, int HPC> std::once_flag TcInst<D, HPC>::flags[kMaxDevices];
-template <int D, int HPC> cudaError_t TcInst<D, HPC>::errs[kMaxDevices];
+template <int D, int HPC, int CT> std::once_flag TcInst<D, HPC, CT>::flags[kMaxDevices];
+template <int D, int HPC, int CT> cudaError_t TcInst<D, HPC, CT>::errs[kMaxDevices];
 
-template <int D>
+template <int D, int CT>
 pkv_status launch_tc_d(int hpc, const pkv::TcParams& prm, int n, int groups, cudaStream_t st,
                        int dev) {
   switch (hpc) {
-    case 8: return TcInst<D, 8>::launch(prm, n, groups, st, dev);
-    case 4: return TcInst<D, 4>::launch(prm, n, groups, st, dev);
-    case 2: return TcInst<D, 2>::launch(prm, n, groups, st, dev);
-    default: return TcInst<D, 1>::launch(prm, n, groups, st, dev);
+    case 8: return TcInst<D, 8, CT>::launch(prm, n, groups, st, dev);
+    case 4: return TcInst<D, 4, CT>::launch(prm, n, groups, st, dev);
+    case 2: return TcInst<D, 2, CT>::launch(prm, n, groups, st, dev);
+    default: return TcInst<D, 1, CT>::launch(prm, n, groups, st, dev);
   }
 }
 
+// Tensor map over a pool seen as [rows = num_blocks * K][H_kv][D]: boxes of
+// 128 bytes x 1 head x 16 rows (64 bf16 columns, or a full 128-column row of
+// one-byte codes), 128-byte swizzle.
 pkv_status encode_pool_map(CUtensorMap* map, const void* pool, int64_t num_blocks, int K, int H_kv,
-                           int D) {
+                           int D, bool one_byte = false) {
   PFN_cuTensorMapEncodeTiled_v12000 enc;
   pkv_status st = get_encode(&enc);
   if (st != PKV_OK) return st;
+  const cuuint64_t eb = one_byte ? 1 : 2;
   cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H_kv, (cuuint64_t)(num_blocks * K)};
-  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H_kv * D * 2};
-  cuuint32_t box[3] = {64, 1, (cuuint32_t)pkv::kTcChunk};
+  cuuint64_t strides[2] = {(cuuint64_t)D * eb, (cuuint64_t)H_kv * D * eb};
+  cuuint32_t box[3] = {one_byte ? 128u : 64u, 1, (cuuint32_t)pkv::kTcChunk};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pool), dims, strides,
+  CUresult r = enc(map, one_byte ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                   3, const_cast<void*>(pool), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   PKV_CHECK(r == CUDA_SUCCESS, PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
@@ -692,8 +715,8 @@ pkv_status attention_impl(const void* q, const void* k_cache, const void* v_cach
   const bool tma_aligned = aligned(k_cache, 16) && aligned(v_cache, 16);
   AttnPlan plan;
   pkv_status st = quant ? plan_attention_quant(num_seqs, num_q_heads, num_kv_heads, head_dim,
-                                               block_size, max_context_len, dtype, quant, config,
-                                               &plan)
+                                               block_size, max_context_len, num_blocks, dtype,
+                                               quant, config, tma_aligned, &plan)
                         : plan_attention(num_seqs, num_q_heads, num_kv_heads, head_dim,
                                          block_size, max_context_len, num_blocks, dtype, config,
                                          tma_aligned, &plan);
@@ -724,10 +747,15 @@ pkv_status attention_impl(const void* q, const void* k_cache, const void* v_cach
     st = device_facts(&dev, &sms);
     if (st != PKV_OK) return st;
     memset(&prm, 0, sizeof(prm));
-    st = encode_pool_map(&prm.tmap_k, k_cache, num_blocks, block_size, H_kv, D);
+    st = encode_pool_map(&prm.tmap_k, k_cache, num_blocks, block_size, H_kv, D, quant != nullptr);
     if (st != PKV_OK) return st;
-    st = encode_pool_map(&prm.tmap_v, v_cache, num_blocks, block_size, H_kv, D);
+    st = encode_pool_map(&prm.tmap_v, v_cache, num_blocks, block_size, H_kv, D, quant != nullptr);
     if (st != PKV_OK) return st;
+    if (quant) {
+      prm.v_scale = quant->format == PKV_KV_FP8_E4M3 ? quant->v_scale : 1.f;
+      prm.k_ts = quant->k_token_scales;
+      prm.v_ts = quant->v_token_scales;
+    }
   }
   for (int s0 = 0; s0 < num_seqs; s0 += plan.seq_batch) {
     const int S = std::min(plan.seq_batch, num_seqs - s0);
@@ -749,8 +777,15 @@ pkv_status attention_impl(const void* q, const void* k_cache, const void* v_cach
       prm.G = H_q / H_kv;
       prm.block_size = block_size;
       prm.scale_log2 = sl;
-      st = D == 64 ? launch_tc_d<64>(plan.hpc, prm, plan.n_per_group, plan.groups, strm, dev)
-                   : launch_tc_d<128>(plan.hpc, prm, plan.n_per_group, plan.groups, strm, dev);
+      if (quant == nullptr) {
+        st = D == 64 ? launch_tc_d<64, 0>(plan.hpc, prm, plan.n_per_group, plan.groups, strm, dev)
+                     : launch_tc_d<128, 0>(plan.hpc, prm, plan.n_per_group, plan.groups, strm, dev);
+      } else if (quant->format == PKV_KV_FP8_E4M3) {
+        prm.scale_log2 = (float)((double)scale * log2e * (double)quant->k_scale);
+        st = launch_tc_d<128, 1>(plan.hpc, prm, plan.n_per_group, plan.groups, strm, dev);
+      } else {
+        st = launch_tc_d<128, 2>(plan.hpc, prm, plan.n_per_group, plan.groups, strm, dev);
+      }
     } else {
       const SimtArgs a{btb, max_blocks_per_seq, lb, max_context_len, S, H_q, H_kv,
                        block_size, num_blocks, sl, ws, plan.ps, plan.pmax};
@@ -811,11 +846,24 @@ pkv_status pkv_attention_quant_workspace_bytes(int32_t num_seqs, int32_t num_q_h
   PKV_CHECK(bytes != nullptr, PKV_ERR_INVALID_ARGUMENT, "null bytes pointer");
   pkv_status st = check_quant(quant, false);
   if (st != PKV_OK) return st;
+  // aligned pools are assumed; a misaligned pool takes the CUDA-core plan,
+  // so report the larger of the two workspaces
   AttnPlan plan;
   st = plan_attention_quant(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                            max_context_len, q_dtype, quant, config, &plan);
+                            max_context_len, 1, q_dtype, quant, config, true, &plan);
   if (st != PKV_OK) return st;
-  *bytes = plan.ws_bytes;
+  size_t need = plan.ws_bytes;
+  pkv_attention_config c2 = {};
+  if (config) c2 = *config;
+  if (plan.kind == KIND_TC && c2.kernel == 0) {
+    c2.kernel = 2;
+    c2.num_splits = 0;
+    AttnPlan alt;
+    if (plan_attention_quant(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                             max_context_len, 1, q_dtype, quant, &c2, true, &alt) == PKV_OK)
+      need = std::max(need, alt.ws_bytes);
+  }
+  *bytes = need;
   return PKV_OK;
 }
 

@@ -48,20 +48,33 @@ struct TcParams {
   int H_q;
   int G;
   int block_size;
-  float scale_log2;
+  float scale_log2;   // scale * log2(e) (FP8 pools: times the K scale)
+  // one-byte pools only
+  float v_scale;            // FP8: scale of the V pool
+  const float* k_ts;        // INT8: per-slot scales
+  const float* v_ts;
 };
 
-template <int D, int HPC, int NS>
+// Pool formats of the kernel: CT 0 = bf16, 1 = FP8 e4m3 (per-tensor scale),
+// 2 = INT8 (per-slot scale).  A one-byte pool row of D = 128 is one 128-byte
+// box per head; a bf16 row is D / 64 boxes.  One-byte tiles are read straight
+// into f16 mma fragments (e4m3 and int8 codes are exact in f16); bf16 tiles
+// go through ldmatrix into bf16 mma fragments.
+template <int D, int HPC, int NS, int CT = 0>
 struct TcCfg {
-  static constexpr int NH = D / 64;
+  static constexpr int NH = CT ? 1 : D / 64;              // boxes per head row
   static constexpr int NBOX = 2 * HPC * NH;
   static constexpr int KPART = HPC * NH * kBoxBytes;
-  static constexpr int STAGE = 2 * KPART;
+  static constexpr int SCALE_OFF = 2 * KPART;             // INT8: 16 K + 16 V scales
+  static constexpr int SCALE_BYTES = CT == 2 ? 128 : 0;
+  static constexpr int STAGE = ((2 * KPART + SCALE_BYTES + 1023) / 1024) * 1024;
   static constexpr int THREADS = (HPC + 1) * 32;
   static constexpr int BAR_OFF = NS * STAGE;
   static constexpr int CSTART_OFF = BAR_OFF + 2 * NS * 8 + 16;
   static constexpr int SMEM = CSTART_OFF + (kTcMaxSeqs + 1) * 4 + 1024;  // + alignment slack
-  static_assert(NBOX <= 32, "one TMA box per producer lane");
+  static constexpr uint32_t TX = 2 * KPART + SCALE_BYTES;  // bytes landing per stage
+  static_assert(NBOX + (CT == 2 ? 2 : 0) <= 32, "one copy per producer lane");
+  static_assert(CT == 0 || D == 128, "one-byte pools need head_dim 128");
 };
 
 // Largest CTA index i whose range starts at or before chunk c.
@@ -79,10 +92,10 @@ __device__ __forceinline__ int seq_of_chunk(const int* cstart, int S, int c) {
   return lo;
 }
 
-template <int D, int HPC, int NS>
-__global__ void __launch_bounds__(TcCfg<D, HPC, NS>::THREADS, 1)
+template <int D, int HPC, int NS, int CT = 0>
+__global__ void __launch_bounds__(TcCfg<D, HPC, NS, CT>::THREADS, 1)
 attn_tc_kernel(const __grid_constant__ TcParams p) {
-  using C = TcCfg<D, HPC, NS>;
+  using C = TcCfg<D, HPC, NS, CT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -203,7 +216,7 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
           ok = false;
           break;
         }
-        if (lane == 0) mbar_arrive_expect_tx(bar_full + 8 * stage, C::STAGE);
+        if (lane == 0) mbar_arrive_expect_tx(bar_full + 8 * stage, C::TX);
         __syncwarp();
         if (lane < C::NBOX) {
           const int kv = lane / (HPC * C::NH);
@@ -213,6 +226,16 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
                                         (h * C::NH + half) * kBoxBytes);
           tma_load_3d(dst, kv ? &p.tmap_v : &p.tmap_k, bar_full + 8 * stage, half * 64,
                       head0 + h, r, policy);
+        }
+        if constexpr (CT == 2) {
+          // the chunk's 16 per-slot scales of K and of V (64 bytes each); an
+          // out-of-range block reads slot 0's scales, which meet zero codes
+          if (lane == C::NBOX || lane == C::NBOX + 1) {
+            const int kv = lane - C::NBOX;
+            const float* src = (kv ? p.v_ts : p.k_ts) + (r >= 0 ? r : 0);
+            bulk_load(smem_u32(smem + stage * C::STAGE + C::SCALE_OFF + kv * 64), src, 64,
+                      bar_full + 8 * stage);
+          }
         }
         __syncwarp();
       }
@@ -233,6 +256,7 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
 
   uint32_t qf[D / 16][2];
   float o[D / 16][4];
+  float slc0 = sl, slc1 = sl;   // per score column (one-byte pools: q's 2^e folded in)
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
   int s = seq_of_chunk(cstart, S, cb);
   int len_s = 0;
@@ -244,14 +268,52 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
       // ---- new partition: load the q-group as the B fragments of Q^T
       len_s = effective_len(p.context_lens[s], p.max_len, row_tokens);
       const __nv_bfloat16* qrow = p.q + ((int64_t)s * H_q + j * G + g) * D;
+      if constexpr (CT == 0) {
 #pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks) {
-        if (g < G) {
-          qf[ks][0] = __ldg(reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 2 * tq));
-          qf[ks][1] = __ldg(reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 8 + 2 * tq));
-        } else {
-          qf[ks][0] = qf[ks][1] = 0u;
+        for (int ks = 0; ks < D / 16; ++ks) {
+          if (g < G) {
+            qf[ks][0] = __ldg(reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 2 * tq));
+            qf[ks][1] = __ldg(reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 8 + 2 * tq));
+          } else {
+            qf[ks][0] = qf[ks][1] = 0u;
+          }
         }
+      } else {
+        // f16 fragments.  The mma k order inside each 16-column step is
+        // permuted (k 2tq, 2tq+1 -> d 4tq, 4tq+1; k 2tq+8, 2tq+9 -> d 4tq+2,
+        // 4tq+3) to match the K fragments read straight from the byte tile.
+        // Each head is scaled by a power of two 2^-e that puts its largest
+        // |q| in [2^14, 2^15): exact, and far inside the f16 range; the
+        // scores are multiplied back by 2^e.
+        float qv[D / 16][4];
+        float amax = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          if (g < G) {
+            const uint2 raw = __ldg(reinterpret_cast<const uint2*>(qrow + ks * 16 + 4 * tq));
+            const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
+            const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
+            qv[ks][0] = lo.x; qv[ks][1] = lo.y; qv[ks][2] = hi.x; qv[ks][3] = hi.y;
+          } else {
+            qv[ks][0] = qv[ks][1] = qv[ks][2] = qv[ks][3] = 0.f;
+          }
+#pragma unroll
+          for (int e = 0; e < 4; ++e) amax = fmaxf(amax, fabsf(qv[ks][e]));
+        }
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));   // head g's max
+        const int eg = amax > 0.f ? ilogbf(amax) - 14 : 0;
+        const float down = ldexpf(1.f, -eg);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          qf[ks][0] = pack_f16x2(qv[ks][0] * down, qv[ks][1] * down);
+          qf[ks][1] = pack_f16x2(qv[ks][2] * down, qv[ks][3] * down);
+        }
+        // score columns of this thread are heads 2tq, 2tq+1 (held by lanes 8tq, 8tq+4)
+        const int e0 = __shfl_sync(0xffffffffu, eg, 8 * tq);
+        const int e1 = __shfl_sync(0xffffffffu, eg, 8 * tq + 4);
+        slc0 = ldexpf(sl, e0);
+        slc1 = ldexpf(sl, e1);
       }
 #pragma unroll
       for (int mt = 0; mt < D / 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
@@ -264,9 +326,33 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
       record_error(PKV_DEVERR_TIMEOUT);
       return;
     }
-    uint8_t* kt = smem + stage * C::STAGE + w * C::NH * kBoxBytes;
-    uint8_t* vt = kt + C::KPART;
-    if (valid < kTcChunk) {
+    uint8_t* kt;
+    uint8_t* vt;
+    // per-token-row K scales (rows g, g+8) and V scales folded into P
+    float ksg = 1.f, ksg8 = 1.f, vsg = 1.f, vsg8 = 1.f;
+    if constexpr (CT != 0) {
+      // this head's byte tiles (16 rows x 128 codes, 128-byte swizzle)
+      kt = smem + stage * C::STAGE + w * kBoxBytes;
+      vt = kt + C::KPART;
+      if constexpr (CT == 2) {
+        const float* sc = reinterpret_cast<const float*>(smem + stage * C::STAGE + C::SCALE_OFF);
+        ksg = sc[g];
+        ksg8 = sc[g + 8];
+        vsg = sc[16 + g];
+        vsg8 = sc[16 + g + 8];
+        // slots past the sequence end may hold anything; their weight is 0
+        ksg = isfinite(ksg) ? ksg : 0.f;
+        ksg8 = isfinite(ksg8) ? ksg8 : 0.f;
+        vsg = isfinite(vsg) ? vsg : 0.f;
+        vsg8 = isfinite(vsg8) ? vsg8 : 0.f;
+      } else {
+        vsg = vsg8 = p.v_scale;
+      }
+    } else {
+      kt = smem + stage * C::STAGE + w * C::NH * kBoxBytes;
+      vt = kt + C::KPART;
+    }
+    if (CT == 0 && valid < kTcChunk) {
       // rows past the sequence end may hold anything (stale slots, NaN):
       // give them zero V so that 0-weight x V stays 0 in the tensor core
       const int nvec = (kTcChunk - valid) * C::NH * 8;
@@ -282,7 +368,7 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
     }
     // ---- S^T[16 tok x 8 heads] = K_tile[16 x D] . Q^T[D x 8]
     float sacc[4] = {0.f, 0.f, 0.f, 0.f};
-    {
+    if constexpr (CT == 0) {
       const int r = (lane & 7) + ((lane >> 3) & 1) * 8;
       const int chs = lane >> 4;
 #pragma unroll
@@ -294,9 +380,38 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
         ldmatrix_x4(addr, a0, a1, a2, a3);
         mma_bf16_16816(sacc, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
       }
+    } else {
+      // byte tile: rows g and g+8 share a swizzle phase; the 16-code chunk ks
+      // holds d = 16 ks .. 16 ks + 15, this thread's 4 codes at byte 4 tq
+      const uint8_t* rg = kt + g * 128 + 4 * tq;
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        const int off = (ks ^ (g & 7)) << 4;
+        const uint32_t w0 = *reinterpret_cast<const uint32_t*>(rg + off);
+        const uint32_t w1 = *reinterpret_cast<const uint32_t*>(rg + 8 * 128 + off);
+        uint32_t a0, a1, a2, a3;
+        if constexpr (CT == 1) {
+          a0 = e4m3x2_to_f16x2(w0);
+          a2 = e4m3x2_to_f16x2(w0 >> 16);
+          a1 = e4m3x2_to_f16x2(w1);
+          a3 = e4m3x2_to_f16x2(w1 >> 16);
+        } else {
+          a0 = s8x2_to_f16x2(w0);
+          a2 = s8x2_to_f16x2(w0 >> 16);
+          a1 = s8x2_to_f16x2(w1);
+          a3 = s8x2_to_f16x2(w1 >> 16);
+        }
+        mma_f16_16816(sacc, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+      }
     }
     // ---- online softmax on (tok g / g+8) x (head 2tq / 2tq+1)
-    float x0 = sacc[0] * sl, x1 = sacc[1] * sl, x2 = sacc[2] * sl, x3 = sacc[3] * sl;
+    float x0 = sacc[0] * slc0, x1 = sacc[1] * slc1, x2 = sacc[2] * slc0, x3 = sacc[3] * slc1;
+    if constexpr (CT == 2) {
+      x0 *= ksg;
+      x1 *= ksg;
+      x2 *= ksg8;
+      x3 *= ksg8;
+    }
     if (g >= valid) x0 = x1 = -INFINITY;
     if (g + 8 >= valid) x2 = x3 = -INFINITY;
     float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
@@ -323,13 +438,53 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
     // P enters the tensor core as bf16: split it into hi + lo bf16 terms so
     // that the product carries ~16 significant bits of each weight (a single
     // bf16 rounding of P costs up to 2^-9 relative per weight)
+    // (one-byte pools: f16 hi + lo of P times the V scale of its token)
     uint32_t ph01, pl01, ph23, pl23;
-    split_bf16x2(p0, p1, ph01, pl01);
-    split_bf16x2(p2, p3, ph23, pl23);
+    if constexpr (CT == 0) {
+      split_bf16x2(p0, p1, ph01, pl01);
+      split_bf16x2(p2, p3, ph23, pl23);
+    } else {
+      split_f16x2(p0 * vsg, p1 * vsg, ph01, pl01);
+      split_f16x2(p2 * vsg8, p3 * vsg8, ph23, pl23);
+    }
     const uint32_t pb0 = movmatrix_trans(ph01), pb1 = movmatrix_trans(ph23);
     const uint32_t pc0 = movmatrix_trans(pl01), pc1 = movmatrix_trans(pl23);
     // ---- O^T[D x 8] += V^T[D x 16 tok] . P^T[16 tok x 8]
-    {
+    if constexpr (CT != 0) {
+      // byte tile; the rows of each 16-row m tile are permuted: row g -> d =
+      // 16 mt + 2g, row g + 8 -> d = 16 mt + 2g + 1, so one 16-bit load per
+      // token gives both rows.  Tokens past the end read as 0 (their codes
+      // may be NaN and 0 * NaN must not reach the accumulator).
+      const int t0 = 2 * tq, t1 = 2 * tq + 1, t2 = 2 * tq + 8, t3 = 2 * tq + 9;
+      const bool v0 = t0 < valid, v1 = t1 < valid, v2 = t2 < valid, v3 = t3 < valid;
+#pragma unroll
+      for (int mt = 0; mt < D / 16; ++mt) {
+        const uint32_t l0 = v0 ? *reinterpret_cast<const uint16_t*>(
+                                     vt + t0 * 128 + ((mt ^ (t0 & 7)) << 4) + 2 * g) : 0u;
+        const uint32_t l1 = v1 ? *reinterpret_cast<const uint16_t*>(
+                                     vt + t1 * 128 + ((mt ^ (t1 & 7)) << 4) + 2 * g) : 0u;
+        const uint32_t l2 = v2 ? *reinterpret_cast<const uint16_t*>(
+                                     vt + t2 * 128 + ((mt ^ (t2 & 7)) << 4) + 2 * g) : 0u;
+        const uint32_t l3 = v3 ? *reinterpret_cast<const uint16_t*>(
+                                     vt + t3 * 128 + ((mt ^ (t3 & 7)) << 4) + 2 * g) : 0u;
+        const uint32_t q01lo = __byte_perm(l0, l1, 0x0040), q01hi = __byte_perm(l0, l1, 0x0051);
+        const uint32_t q23lo = __byte_perm(l2, l3, 0x0040), q23hi = __byte_perm(l2, l3, 0x0051);
+        uint32_t a0, a1, a2, a3;
+        if constexpr (CT == 1) {
+          a0 = e4m3x2_to_f16x2(q01lo);
+          a1 = e4m3x2_to_f16x2(q01hi);
+          a2 = e4m3x2_to_f16x2(q23lo);
+          a3 = e4m3x2_to_f16x2(q23hi);
+        } else {
+          a0 = s8x2_to_f16x2(q01lo);
+          a1 = s8x2_to_f16x2(q01hi);
+          a2 = s8x2_to_f16x2(q23lo);
+          a3 = s8x2_to_f16x2(q23hi);
+        }
+        mma_f16_16816(o[mt], a0, a1, a2, a3, pb0, pb1);
+        mma_f16_16816(o[mt], a0, a1, a2, a3, pc0, pc1);
+      }
+    } else {
       const int r = (lane & 7) + (lane >> 4) * 8;
       const int chs = (lane >> 3) & 1;
 #pragma unroll
@@ -363,14 +518,16 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
         __nv_bfloat16* orow = p.out + ((int64_t)s * H_q + j * G) * D;
 #pragma unroll
         for (int mt = 0; mt < D / 16; ++mt) {
-          const int d0 = mt * 16 + g;
+          // O^T rows g and g+8 of tile mt are d0 and d1 (see the PV product)
+          const int d0 = CT == 0 ? mt * 16 + g : mt * 16 + 2 * g;
+          const int d1 = CT == 0 ? d0 + 8 : d0 + 1;
           if (n0 < G) {
             orow[n0 * D + d0] = __float2bfloat16_rn(o[mt][0] * i0);
-            orow[n0 * D + d0 + 8] = __float2bfloat16_rn(o[mt][2] * i0);
+            orow[n0 * D + d1] = __float2bfloat16_rn(o[mt][2] * i0);
           }
           if (n1 < G) {
             orow[n1 * D + d0] = __float2bfloat16_rn(o[mt][1] * i1);
-            orow[n1 * D + d0 + 8] = __float2bfloat16_rn(o[mt][3] * i1);
+            orow[n1 * D + d1] = __float2bfloat16_rn(o[mt][3] * i1);
           }
         }
       } else if (part < p.ws.pmax) {
@@ -378,14 +535,15 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
         float* ob = p.ws.o + base * D;
 #pragma unroll
         for (int mt = 0; mt < D / 16; ++mt) {
-          const int d0 = mt * 16 + g;
+          const int d0 = CT == 0 ? mt * 16 + g : mt * 16 + 2 * g;
+          const int d1 = CT == 0 ? d0 + 8 : d0 + 1;
           if (n0 < G) {
             ob[n0 * D + d0] = o[mt][0];
-            ob[n0 * D + d0 + 8] = o[mt][2];
+            ob[n0 * D + d1] = o[mt][2];
           }
           if (n1 < G) {
             ob[n1 * D + d0] = o[mt][1];
-            ob[n1 * D + d0 + 8] = o[mt][3];
+            ob[n1 * D + d1] = o[mt][3];
           }
         }
         if (g == 0) {

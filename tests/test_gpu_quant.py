@@ -155,10 +155,28 @@ SHAPES = [(128, 4, 16), (64, 2, 4), (128, 8, 32)]
 @pytest.mark.parametrize("D,G,K", SHAPES)
 @pytest.mark.parametrize("num_splits", [0, 64])
 def test_quant_step_matches_oracle(ops, fmt, q_dtype, D, G, K, num_splits):
-    H_kv = 2
-    lens = [1, 17, 0, 300, 64, 601]
+    run_quant_step(ops, fmt, q_dtype, D, G, K, [1, 17, 0, 300, 64, 601], H_kv=2,
+                   num_splits=num_splits)
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "int8"])
+@pytest.mark.parametrize("kernel", [1, 2])
+@pytest.mark.parametrize("num_splits", [0, 3, 40])
+def test_quant_tensor_core_and_cuda_core(ops, fmt, kernel, num_splits):
+    lens = [0, 1, 15, 16, 17, 700, 33, 2048]
+    run_quant_step(ops, fmt, "bf16", 128, 4, 16, lens, H_kv=8, kernel=kernel,
+                   num_splits=num_splits)
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "int8"])
+@pytest.mark.parametrize("G,K,H_kv", [(8, 32, 8), (2, 64, 4), (1, 16, 1)])
+def test_quant_tensor_core_shapes(ops, fmt, G, K, H_kv):
+    run_quant_step(ops, fmt, "bf16", 128, G, K, [5, 130, 1000, 64], H_kv=H_kv, kernel=1)
+
+
+def run_quant_step(ops, fmt, q_dtype, D, G, K, lens, H_kv=2, **attn_kw):
     w, c, kc, vc, kts, vts = quant_problem(fmt, lens, G * H_kv, H_kv, D, K, q_dtype,
-                                           seed=D + G + K)
+                                           seed=D + G + K + len(lens))
     dkc, dvc = torch.from_numpy(kc).to(DEV), torch.from_numpy(vc).to(DEV)
     if fmt == "fp8":
         qd = ops.kv_quant("fp8", 0.5, 1.5)
@@ -171,8 +189,7 @@ def test_quant_step_matches_oracle(ops, fmt, q_dtype, D, G, K, num_splits):
                               dvc, qd)
     out = ops.paged_attention_decode_quant(d["q"], dkc, dvc, d["block_tables"],
                                            d["context_lens"], w.scale, qd,
-                                           max_context_len=w.max_context_len,
-                                           num_splits=num_splits)
+                                           max_context_len=w.max_context_len, **attn_kw)
     torch.cuda.synchronize()
     assert ops.get_device_error() == 0
     slots = oracle.slot_mapping(w.block_tables, w.positions, w.block_size)
@@ -189,7 +206,7 @@ def test_quant_step_matches_oracle(ops, fmt, q_dtype, D, G, K, num_splits):
     assert np.array_equal(dkc.cpu().numpy(), okc) and np.array_equal(dvc.cpu().numpy(), ovc)
     ref = Q.paged_attention_decode_quant(storage(c["q"]), okc, ovc, w.block_tables,
                                          w.context_lens, w.scale, q_dtype, fmt, **scales, **tok)
-    check_attention(as_f64(out), ref, q_dtype, f"{fmt} {q_dtype} D{D} G{G} K{K}")
+    check_attention(as_f64(out), ref, q_dtype, f"{fmt} {q_dtype} D{D} G{G} K{K} {attn_kw}")
 
 
 def test_quant_rejects_bad_descriptions(ops):
