@@ -1,4 +1,5 @@
-// TMA + tensor-core decode-attention partition kernel (bf16).
+// TMA + tensor-core decode-attention partition kernel (bf16 queries; bf16,
+// FP8 e4m3 or INT8 pools).
 #pragma once
 
 #include "pkv_attention_common.cuh"
@@ -6,32 +7,39 @@
 namespace pkv {
 
 // ===========================================================================
-// TMA + tensor-core partition kernel (bf16, K % 16 == 0, D in {64, 128},
-// G <= 8).
+// TMA + tensor-core partition kernel (bf16 queries, block_size % 16 == 0,
+// G <= 8; bf16 pools with D in {64, 128}, one-byte pools with D = 128).
 //
-// Work decomposition: the token range of the batch is cut into chunks of 16
-// tokens (one tensor-core M tile).  Chunks are numbered sequence-major; with
-// T chunks and n CTAs per KV-head group, CTA i owns chunks
+// Work decomposition: the token range of the batch is cut into chunks (16
+// tokens for bf16 pools, 32 for one-byte pools), numbered sequence-major;
+// with T chunks and n CTAs per KV-head group, CTA i owns chunks
 // [floor(i T / n), floor((i+1) T / n)) — equal work per CTA whatever the
 // length mix.  A run of chunks of one sequence inside a CTA is a split-K
 // partition; its (m, l, o) goes to the workspace unless the CTA holds the
 // whole sequence, in which case it writes the final output.
 //
-// Roles: warp HPC is the producer; one elected pass of its lanes issues the
-// TMA loads of a stage (16 tokens x HPC heads, K and V, one box per head and
-// 64-column half) completing on the stage's "full" mbarrier.  Warps
-// 0..HPC-1 are consumers, warp w owning KV head (group * HPC + w): it waits
-// on "full", computes S^T = K_tile Q^T and O^T += V^T P^T with
-// mma.m16n8k16 (tokens x heads, the q-group padded to 8 columns), does the
-// online softmax on the 16 x 8 score tile with warp shuffles, and arrives
-// on the stage's "empty" mbarrier.
+// Roles: warp HPC is the producer; its lanes issue the TMA loads of a stage
+// (one chunk x HPC heads, K and V: one box of 16 token rows x 128 bytes per
+// head, 16-row tile and 128-byte column group) completing on the stage's
+// "full" mbarrier.  Warps 0..HPC-1 are consumers, warp w owning KV head
+// (group * HPC + w): it waits on "full", computes S^T = K_tile Q^T and
+// O^T += V^T P^T with mma.m16n8k16 for each 16-row tile (tokens x heads, the
+// q-group padded to 8 columns; P as a hi + lo pair), does the online softmax
+// over the chunk with warp shuffles, and arrives on the stage's "empty"
+// mbarrier.  A 32-token chunk gives each consumer two independent tile
+// products per softmax step, halving the per-token cost of the softmax,
+// rescaling and barrier handshakes that bound the one-byte pools.
 //
-// Shared-memory tiles use the 128-byte swizzle, so the 8 rows an ldmatrix
-// phase reads (8 tokens, same 16-byte column) land in 8 distinct bank groups.
+// Shared-memory tiles use the 128-byte swizzle, so the 8 rows a warp phase
+// reads (8 tokens, same 16-byte column) land in 8 distinct bank groups.
 // ===========================================================================
-constexpr int kTcChunk = 16;
+constexpr int kTile = 16;          // token rows per TMA box and per mma tile
+constexpr int kTcChunk = kTile;    // chunk of the bf16 kernel
 constexpr int kTcMaxSeqs = 2048;
-constexpr int kBoxBytes = kTcChunk * 128;
+constexpr int kBoxBytes = kTile * 128;
+
+// tokens per stream-K chunk for a pool format (0 bf16, 1 FP8, 2 INT8)
+constexpr int tc_chunk_tokens(int ct) { return ct ? 2 * kTile : kTile; }
 
 struct TcParams {
   CUtensorMap tmap_k;
@@ -60,21 +68,32 @@ struct TcParams {
 // box per head; a bf16 row is D / 64 boxes.  One-byte tiles are read straight
 // into f16 mma fragments (e4m3 and int8 codes are exact in f16); bf16 tiles
 // go through ldmatrix into bf16 mma fragments.
+//
+// Stage layout: K boxes [head][tile][column group], then V boxes, then (INT8)
+// the 16 per-slot scales of each tile: K tiles, then V tiles.
 template <int D, int HPC, int NS, int CT = 0>
 struct TcCfg {
+  static constexpr int TL = CT ? 2 : 1;                   // 16-row tiles per chunk
+  static constexpr int CH = kTile * TL;                   // tokens per chunk
   static constexpr int NH = CT ? 1 : D / 64;              // boxes per head row
-  static constexpr int NBOX = 2 * HPC * NH;
-  static constexpr int KPART = HPC * NH * kBoxBytes;
-  static constexpr int SCALE_OFF = 2 * KPART;             // INT8: 16 K + 16 V scales
-  static constexpr int SCALE_BYTES = CT == 2 ? 128 : 0;
+  static constexpr int NBOX = 2 * HPC * TL * NH;
+  static constexpr int KPART = HPC * TL * NH * kBoxBytes;
+  static constexpr int SCALE_OFF = 2 * KPART;
+  static constexpr int SCALE_BYTES = CT == 2 ? 2 * TL * kTile * 4 : 0;
+  static constexpr int NCOPY = NBOX + (CT == 2 ? 2 * TL : 0);
   static constexpr int STAGE = ((2 * KPART + SCALE_BYTES + 1023) / 1024) * 1024;
   static constexpr int THREADS = (HPC + 1) * 32;
   static constexpr int BAR_OFF = NS * STAGE;
   static constexpr int CSTART_OFF = BAR_OFF + 2 * NS * 8 + 16;
   static constexpr int SMEM = CSTART_OFF + (kTcMaxSeqs + 1) * 4 + 1024;  // + alignment slack
   static constexpr uint32_t TX = 2 * KPART + SCALE_BYTES;  // bytes landing per stage
-  static_assert(NBOX + (CT == 2 ? 2 : 0) <= 32, "one copy per producer lane");
+  static_assert(NBOX <= 32, "one box per producer lane");
   static_assert(CT == 0 || D == 128, "one-byte pools need head_dim 128");
+  static_assert(tc_chunk_tokens(CT) == CH, "chunk size");
+  // smem offset of head h's box (tile t, column group half) of K (kv 0) or V
+  __host__ __device__ static constexpr int box_off(int kv, int h, int t, int half) {
+    return kv * KPART + ((h * TL + t) * NH + half) * kBoxBytes;
+  }
 };
 
 // Largest CTA index i whose range starts at or before chunk c.
@@ -96,6 +115,7 @@ template <int D, int HPC, int NS, int CT = 0>
 __global__ void __launch_bounds__(TcCfg<D, HPC, NS, CT>::THREADS, 1)
 attn_tc_kernel(const __grid_constant__ TcParams p) {
   using C = TcCfg<D, HPC, NS, CT>;
+  constexpr int TL = C::TL, CH = C::CH;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -118,13 +138,13 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
   }
   pdl_wait_primary();
 
-  // ---- chunk prefix sums over the batch: cstart[s] = sum_{s'<s} ceil(L/16)
+  // ---- chunk prefix sums over the batch: cstart[s] = sum_{s'<s} ceil(L/CH)
   {
     const int per = (S + C::THREADS - 1) / C::THREADS;
     const int a = min(S, tid * per), b = min(S, a + per);
     int local = 0;
     for (int s = a; s < b; ++s)
-      local += (effective_len(p.context_lens[s], p.max_len, row_tokens) + kTcChunk - 1) / kTcChunk;
+      local += (effective_len(p.context_lens[s], p.max_len, row_tokens) + CH - 1) / CH;
     int incl = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -146,7 +166,7 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
     int run = (warp ? s_wsum[warp - 1] : 0) + incl - local;
     for (int s = a; s < b; ++s) {
       cstart[s] = run;
-      run += (effective_len(p.context_lens[s], p.max_len, row_tokens) + kTcChunk - 1) / kTcChunk;
+      run += (effective_len(p.context_lens[s], p.max_len, row_tokens) + CH - 1) / CH;
     }
     if (tid == C::THREADS - 1) cstart[S] = run;
     __syncthreads();
@@ -191,24 +211,35 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
     int k = 0;
     bool ok = true;
     for (int c0 = cb; c0 < ce && ok; c0 += 32) {
-      // block-table entries of the next 32 chunks, one per lane
-      int row = 0;
+      // pool rows of the tiles of the next 32 chunks, one chunk per lane; a
+      // tile past the sequence end (or of an out-of-range block) gets a row
+      // that is wholly out of bounds, which TMA fills with zeros
+      int row[TL];
+#pragma unroll
+      for (int t = 0; t < TL; ++t) row[t] = -2 * kTile;
       const int c = c0 + lane;
       if (c < ce) {
         const int s = seq_of_chunk(cstart, S, c);
-        const int tok = (c - cstart[s]) * kTcChunk;
-        const int lb = tok / K;
-        const long long phys = p.block_tables[(int64_t)s * p.max_blocks_per_seq + lb];
-        if (phys < 0 || phys >= p.num_blocks) {
-          record_error(PKV_DEVERR_BLOCK_ID);
-          row = -2 * kTcChunk;          // whole box out of bounds: zero fill
-        } else {
-          row = (int)(phys * K + (tok - lb * K));
+        const int L = TL > 1 ? effective_len(p.context_lens[s], p.max_len, row_tokens) : 1 << 30;
+#pragma unroll
+        for (int t = 0; t < TL; ++t) {
+          const int tok = (c - cstart[s]) * CH + t * kTile;
+          if (tok < L) {
+            const int lb = tok / K;
+            const long long phys = p.block_tables[(int64_t)s * p.max_blocks_per_seq + lb];
+            if (phys < 0 || phys >= p.num_blocks) {
+              record_error(PKV_DEVERR_BLOCK_ID);
+            } else {
+              row[t] = (int)(phys * K + (tok - lb * K));
+            }
+          }
         }
       }
       const int cnt = min(32, ce - c0);
       for (int b = 0; b < cnt; ++b, ++k) {
-        const int r = __shfl_sync(0xffffffffu, row, b);
+        int r[TL];
+#pragma unroll
+        for (int t = 0; t < TL; ++t) r[t] = __shfl_sync(0xffffffffu, row[t], b);
         const int stage = k % NS;
         const uint32_t parity = ((k / NS) & 1) ^ 1;
         if (!mbar_wait_bounded(bar_empty + 8 * stage, parity)) {
@@ -218,22 +249,24 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
         }
         if (lane == 0) mbar_arrive_expect_tx(bar_full + 8 * stage, C::TX);
         __syncwarp();
-        if (lane < C::NBOX) {
-          const int kv = lane / (HPC * C::NH);
-          const int rem = lane - kv * (HPC * C::NH);
-          const int h = rem / C::NH, half = rem - h * C::NH;
-          const uint32_t dst = smem_u32(smem + stage * C::STAGE + kv * C::KPART +
-                                        (h * C::NH + half) * kBoxBytes);
-          tma_load_3d(dst, kv ? &p.tmap_v : &p.tmap_k, bar_full + 8 * stage, half * 64,
-                      head0 + h, r, policy);
-        }
-        if constexpr (CT == 2) {
-          // the chunk's 16 per-slot scales of K and of V (64 bytes each); an
-          // out-of-range block reads slot 0's scales, which meet zero codes
-          if (lane == C::NBOX || lane == C::NBOX + 1) {
-            const int kv = lane - C::NBOX;
-            const float* src = (kv ? p.v_ts : p.k_ts) + (r >= 0 ? r : 0);
-            bulk_load(smem_u32(smem + stage * C::STAGE + C::SCALE_OFF + kv * 64), src, 64,
+        uint8_t* sb = smem + stage * C::STAGE;
+        for (int i = lane; i < C::NCOPY; i += 32) {
+          if (i < C::NBOX) {
+            const int kv = i / (HPC * TL * C::NH);
+            const int rem = i - kv * (HPC * TL * C::NH);
+            const int h = rem / (TL * C::NH);
+            const int rem2 = rem - h * (TL * C::NH);
+            const int t = rem2 / C::NH, half = rem2 - t * C::NH;
+            tma_load_3d(smem_u32(sb + C::box_off(kv, h, t, half)), kv ? &p.tmap_v : &p.tmap_k,
+                        bar_full + 8 * stage, half * 64, head0 + h, t ? r[TL - 1] : r[0], policy);
+          } else if constexpr (CT == 2) {
+            // a tile's 16 per-slot scales (64 bytes); a tile with no rows
+            // reads slot 0's scales, which meet zero codes
+            const int idx = i - C::NBOX;
+            const int kv = idx / TL, t = idx - kv * TL;
+            const int rt = t ? r[TL - 1] : r[0];
+            const float* src = (kv ? p.v_ts : p.k_ts) + (rt >= 0 ? rt : 0);
+            bulk_load(smem_u32(sb + C::SCALE_OFF + (kv * TL + t) * 64), src, 64,
                       bar_full + 8 * stage);
           }
         }
@@ -320,42 +353,37 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
       m0 = m1 = -INFINITY;
       l0 = l1 = 0.f;
     }
-    const int valid = min(kTcChunk, len_s - (c - a) * kTcChunk);
+    const int valid = min(CH, len_s - (c - a) * CH);   // tokens of this chunk
     const int stage = k % NS;
     if (!mbar_wait_bounded(bar_full + 8 * stage, (k / NS) & 1)) {
       record_error(PKV_DEVERR_TIMEOUT);
       return;
     }
-    uint8_t* kt;
-    uint8_t* vt;
-    // per-token-row K scales (rows g, g+8) and V scales folded into P
-    float ksg = 1.f, ksg8 = 1.f, vsg = 1.f, vsg8 = 1.f;
-    if constexpr (CT != 0) {
-      // this head's byte tiles (16 rows x 128 codes, 128-byte swizzle)
-      kt = smem + stage * C::STAGE + w * kBoxBytes;
-      vt = kt + C::KPART;
+    uint8_t* sb = smem + stage * C::STAGE;
+    // per-token-row K scales and V scales (folded into P) of rows g, g+8 of
+    // each tile: INT8 per slot, FP8 per tensor (K's folded into sl)
+    float ksr[TL][2], vsr[TL][2];
+#pragma unroll
+    for (int t = 0; t < TL; ++t) {
       if constexpr (CT == 2) {
-        const float* sc = reinterpret_cast<const float*>(smem + stage * C::STAGE + C::SCALE_OFF);
-        ksg = sc[g];
-        ksg8 = sc[g + 8];
-        vsg = sc[16 + g];
-        vsg8 = sc[16 + g + 8];
+        const float* kscl = reinterpret_cast<const float*>(sb + C::SCALE_OFF + t * 64);
+        const float* vscl = reinterpret_cast<const float*>(sb + C::SCALE_OFF + (TL + t) * 64);
         // slots past the sequence end may hold anything; their weight is 0
-        ksg = isfinite(ksg) ? ksg : 0.f;
-        ksg8 = isfinite(ksg8) ? ksg8 : 0.f;
-        vsg = isfinite(vsg) ? vsg : 0.f;
-        vsg8 = isfinite(vsg8) ? vsg8 : 0.f;
+        const float k0 = kscl[g], k8 = kscl[g + 8], v0 = vscl[g], v8 = vscl[g + 8];
+        ksr[t][0] = isfinite(k0) ? k0 : 0.f;
+        ksr[t][1] = isfinite(k8) ? k8 : 0.f;
+        vsr[t][0] = isfinite(v0) ? v0 : 0.f;
+        vsr[t][1] = isfinite(v8) ? v8 : 0.f;
       } else {
-        vsg = vsg8 = p.v_scale;
+        ksr[t][0] = ksr[t][1] = 1.f;
+        vsr[t][0] = vsr[t][1] = CT == 1 ? p.v_scale : 1.f;
       }
-    } else {
-      kt = smem + stage * C::STAGE + w * C::NH * kBoxBytes;
-      vt = kt + C::KPART;
     }
-    if (CT == 0 && valid < kTcChunk) {
+    if (CT == 0 && valid < kTile) {
       // rows past the sequence end may hold anything (stale slots, NaN):
       // give them zero V so that 0-weight x V stays 0 in the tensor core
-      const int nvec = (kTcChunk - valid) * C::NH * 8;
+      uint8_t* vt = sb + C::box_off(1, w, 0, 0);
+      const int nvec = (kTile - valid) * C::NH * 8;
       for (int i = lane; i < nvec; i += 32) {
         const int r = valid + i / (C::NH * 8);
         const int rem = i % (C::NH * 8);
@@ -366,11 +394,14 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
       fence_proxy_async_smem();
       __syncwarp();
     }
-    // ---- S^T[16 tok x 8 heads] = K_tile[16 x D] . Q^T[D x 8]
-    float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+    // ---- S^T[16 tok x 8 heads] = K_tile[16 x D] . Q^T[D x 8], per tile
+    float sacc[TL][4];
+#pragma unroll
+    for (int t = 0; t < TL; ++t) sacc[t][0] = sacc[t][1] = sacc[t][2] = sacc[t][3] = 0.f;
     if constexpr (CT == 0) {
       const int r = (lane & 7) + ((lane >> 3) & 1) * 8;
       const int chs = lane >> 4;
+      const uint8_t* kt = sb + C::box_off(0, w, 0, 0);
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) {
         const int half = ks >> 2;
@@ -378,43 +409,49 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
         const uint32_t addr = smem_u32(kt + half * kBoxBytes) + r * 128 + ((ch ^ (r & 7)) << 4);
         uint32_t a0, a1, a2, a3;
         ldmatrix_x4(addr, a0, a1, a2, a3);
-        mma_bf16_16816(sacc, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+        mma_bf16_16816(sacc[0], a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
       }
     } else {
-      // byte tile: rows g and g+8 share a swizzle phase; the 16-code chunk ks
-      // holds d = 16 ks .. 16 ks + 15, this thread's 4 codes at byte 4 tq
-      const uint8_t* rg = kt + g * 128 + 4 * tq;
+      // byte tiles: rows g and g+8 share a swizzle phase; the 16-code chunk
+      // ks holds d = 16 ks .. 16 ks + 15, this thread's 4 codes at byte 4 tq
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) {
-        const int off = (ks ^ (g & 7)) << 4;
-        const uint32_t w0 = *reinterpret_cast<const uint32_t*>(rg + off);
-        const uint32_t w1 = *reinterpret_cast<const uint32_t*>(rg + 8 * 128 + off);
-        uint32_t a0, a1, a2, a3;
-        if constexpr (CT == 1) {
-          a0 = e4m3x2_to_f16x2(w0);
-          a2 = e4m3x2_to_f16x2(w0 >> 16);
-          a1 = e4m3x2_to_f16x2(w1);
-          a3 = e4m3x2_to_f16x2(w1 >> 16);
-        } else {
-          a0 = s8x2_to_f16x2(w0);
-          a2 = s8x2_to_f16x2(w0 >> 16);
-          a1 = s8x2_to_f16x2(w1);
-          a3 = s8x2_to_f16x2(w1 >> 16);
+        const int off = g * 128 + ((ks ^ (g & 7)) << 4) + 4 * tq;
+#pragma unroll
+        for (int t = 0; t < TL; ++t) {
+          const uint8_t* kt = sb + C::box_off(0, w, t, 0);
+          const uint32_t w0 = *reinterpret_cast<const uint32_t*>(kt + off);
+          const uint32_t w1 = *reinterpret_cast<const uint32_t*>(kt + off + 8 * 128);
+          uint32_t a0, a1, a2, a3;
+          if constexpr (CT == 1) {
+            a0 = e4m3x2_to_f16x2(w0);
+            a2 = e4m3x2_to_f16x2(w0 >> 16);
+            a1 = e4m3x2_to_f16x2(w1);
+            a3 = e4m3x2_to_f16x2(w1 >> 16);
+          } else {
+            a0 = s8x2_to_f16x2(w0);
+            a2 = s8x2_to_f16x2(w0 >> 16);
+            a1 = s8x2_to_f16x2(w1);
+            a3 = s8x2_to_f16x2(w1 >> 16);
+          }
+          mma_f16_16816(sacc[t], a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
         }
-        mma_f16_16816(sacc, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
       }
     }
-    // ---- online softmax on (tok g / g+8) x (head 2tq / 2tq+1)
-    float x0 = sacc[0] * slc0, x1 = sacc[1] * slc1, x2 = sacc[2] * slc0, x3 = sacc[3] * slc1;
-    if constexpr (CT == 2) {
-      x0 *= ksg;
-      x1 *= ksg;
-      x2 *= ksg8;
-      x3 *= ksg8;
+    // ---- online softmax on (tok 16t+g / 16t+g+8) x (head 2tq / 2tq+1)
+    float x[TL][4];
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int t = 0; t < TL; ++t) {
+      x[t][0] = sacc[t][0] * slc0 * ksr[t][0];
+      x[t][1] = sacc[t][1] * slc1 * ksr[t][0];
+      x[t][2] = sacc[t][2] * slc0 * ksr[t][1];
+      x[t][3] = sacc[t][3] * slc1 * ksr[t][1];
+      if (t * kTile + g >= valid) x[t][0] = x[t][1] = -INFINITY;
+      if (t * kTile + g + 8 >= valid) x[t][2] = x[t][3] = -INFINITY;
+      mx0 = fmaxf(mx0, fmaxf(x[t][0], x[t][2]));
+      mx1 = fmaxf(mx1, fmaxf(x[t][1], x[t][3]));
     }
-    if (g >= valid) x0 = x1 = -INFINITY;
-    if (g + 8 >= valid) x2 = x3 = -INFINITY;
-    float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
       mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
@@ -422,10 +459,19 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
     }
     const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
     const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
-    const float p0 = exp2f(x0 - mn0), p1 = exp2f(x1 - mn1);
-    const float p2 = exp2f(x2 - mn0), p3 = exp2f(x3 - mn1);
-    l0 = l0 * al0 + (p0 + p2);
-    l1 = l1 * al1 + (p1 + p3);
+    float pr[TL][4];
+    float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+    for (int t = 0; t < TL; ++t) {
+      pr[t][0] = exp2f(x[t][0] - mn0);
+      pr[t][1] = exp2f(x[t][1] - mn1);
+      pr[t][2] = exp2f(x[t][2] - mn0);
+      pr[t][3] = exp2f(x[t][3] - mn1);
+      ps0 += pr[t][0] + pr[t][2];
+      ps1 += pr[t][1] + pr[t][3];
+    }
+    l0 = l0 * al0 + ps0;
+    l1 = l1 * al1 + ps1;
     m0 = mn0;
     m1 = mn1;
 #pragma unroll
@@ -435,58 +481,76 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
       o[mt][2] *= al0;
       o[mt][3] *= al1;
     }
-    // P enters the tensor core as bf16: split it into hi + lo bf16 terms so
-    // that the product carries ~16 significant bits of each weight (a single
-    // bf16 rounding of P costs up to 2^-9 relative per weight)
-    // (one-byte pools: f16 hi + lo of P times the V scale of its token)
-    uint32_t ph01, pl01, ph23, pl23;
-    if constexpr (CT == 0) {
-      split_bf16x2(p0, p1, ph01, pl01);
-      split_bf16x2(p2, p3, ph23, pl23);
-    } else {
-      split_f16x2(p0 * vsg, p1 * vsg, ph01, pl01);
-      split_f16x2(p2 * vsg8, p3 * vsg8, ph23, pl23);
+    // P enters the tensor core as a hi + lo pair of 16-bit terms so that the
+    // product carries ~16 significant bits of each weight (one bf16 rounding
+    // of P costs up to 2^-9 relative per weight); one-byte pools: f16 terms
+    // of P times the V scale of its token
+    uint32_t pb[TL][2], pc[TL][2];
+#pragma unroll
+    for (int t = 0; t < TL; ++t) {
+      uint32_t ph01, pl01, ph23, pl23;
+      if constexpr (CT == 0) {
+        split_bf16x2(pr[t][0], pr[t][1], ph01, pl01);
+        split_bf16x2(pr[t][2], pr[t][3], ph23, pl23);
+      } else {
+        split_f16x2(pr[t][0] * vsr[t][0], pr[t][1] * vsr[t][0], ph01, pl01);
+        split_f16x2(pr[t][2] * vsr[t][1], pr[t][3] * vsr[t][1], ph23, pl23);
+      }
+      pb[t][0] = movmatrix_trans(ph01);
+      pb[t][1] = movmatrix_trans(ph23);
+      pc[t][0] = movmatrix_trans(pl01);
+      pc[t][1] = movmatrix_trans(pl23);
     }
-    const uint32_t pb0 = movmatrix_trans(ph01), pb1 = movmatrix_trans(ph23);
-    const uint32_t pc0 = movmatrix_trans(pl01), pc1 = movmatrix_trans(pl23);
-    // ---- O^T[D x 8] += V^T[D x 16 tok] . P^T[16 tok x 8]
+    // ---- O^T[D x 8] += V^T[D x 16 tok] . P^T[16 tok x 8], per tile
     if constexpr (CT != 0) {
-      // byte tile; the rows of each 16-row m tile are permuted: row g -> d =
+      // byte tiles; the rows of each 16-row m tile are permuted: row g -> d =
       // 16 mt + 2g, row g + 8 -> d = 16 mt + 2g + 1, so one 16-bit load per
       // token gives both rows.  Tokens past the end read as 0 (their codes
       // may be NaN and 0 * NaN must not reach the accumulator).
       const int t0 = 2 * tq, t1 = 2 * tq + 1, t2 = 2 * tq + 8, t3 = 2 * tq + 9;
-      const bool v0 = t0 < valid, v1 = t1 < valid, v2 = t2 < valid, v3 = t3 < valid;
+      bool vv[TL][4];
+#pragma unroll
+      for (int t = 0; t < TL; ++t) {
+        vv[t][0] = t * kTile + t0 < valid;
+        vv[t][1] = t * kTile + t1 < valid;
+        vv[t][2] = t * kTile + t2 < valid;
+        vv[t][3] = t * kTile + t3 < valid;
+      }
 #pragma unroll
       for (int mt = 0; mt < D / 16; ++mt) {
-        const uint32_t l0 = v0 ? *reinterpret_cast<const uint16_t*>(
-                                     vt + t0 * 128 + ((mt ^ (t0 & 7)) << 4) + 2 * g) : 0u;
-        const uint32_t l1 = v1 ? *reinterpret_cast<const uint16_t*>(
-                                     vt + t1 * 128 + ((mt ^ (t1 & 7)) << 4) + 2 * g) : 0u;
-        const uint32_t l2 = v2 ? *reinterpret_cast<const uint16_t*>(
-                                     vt + t2 * 128 + ((mt ^ (t2 & 7)) << 4) + 2 * g) : 0u;
-        const uint32_t l3 = v3 ? *reinterpret_cast<const uint16_t*>(
-                                     vt + t3 * 128 + ((mt ^ (t3 & 7)) << 4) + 2 * g) : 0u;
-        const uint32_t q01lo = __byte_perm(l0, l1, 0x0040), q01hi = __byte_perm(l0, l1, 0x0051);
-        const uint32_t q23lo = __byte_perm(l2, l3, 0x0040), q23hi = __byte_perm(l2, l3, 0x0051);
-        uint32_t a0, a1, a2, a3;
-        if constexpr (CT == 1) {
-          a0 = e4m3x2_to_f16x2(q01lo);
-          a1 = e4m3x2_to_f16x2(q01hi);
-          a2 = e4m3x2_to_f16x2(q23lo);
-          a3 = e4m3x2_to_f16x2(q23hi);
-        } else {
-          a0 = s8x2_to_f16x2(q01lo);
-          a1 = s8x2_to_f16x2(q01hi);
-          a2 = s8x2_to_f16x2(q23lo);
-          a3 = s8x2_to_f16x2(q23hi);
+#pragma unroll
+        for (int t = 0; t < TL; ++t) {
+          const uint8_t* vt = sb + C::box_off(1, w, t, 0) + 2 * g;
+          const uint32_t l0 = vv[t][0] ? *reinterpret_cast<const uint16_t*>(
+                                             vt + t0 * 128 + ((mt ^ (t0 & 7)) << 4)) : 0u;
+          const uint32_t l1 = vv[t][1] ? *reinterpret_cast<const uint16_t*>(
+                                             vt + t1 * 128 + ((mt ^ (t1 & 7)) << 4)) : 0u;
+          const uint32_t l2 = vv[t][2] ? *reinterpret_cast<const uint16_t*>(
+                                             vt + t2 * 128 + ((mt ^ (t2 & 7)) << 4)) : 0u;
+          const uint32_t l3 = vv[t][3] ? *reinterpret_cast<const uint16_t*>(
+                                             vt + t3 * 128 + ((mt ^ (t3 & 7)) << 4)) : 0u;
+          const uint32_t q01lo = __byte_perm(l0, l1, 0x0040), q01hi = __byte_perm(l0, l1, 0x0051);
+          const uint32_t q23lo = __byte_perm(l2, l3, 0x0040), q23hi = __byte_perm(l2, l3, 0x0051);
+          uint32_t a0, a1, a2, a3;
+          if constexpr (CT == 1) {
+            a0 = e4m3x2_to_f16x2(q01lo);
+            a1 = e4m3x2_to_f16x2(q01hi);
+            a2 = e4m3x2_to_f16x2(q23lo);
+            a3 = e4m3x2_to_f16x2(q23hi);
+          } else {
+            a0 = s8x2_to_f16x2(q01lo);
+            a1 = s8x2_to_f16x2(q01hi);
+            a2 = s8x2_to_f16x2(q23lo);
+            a3 = s8x2_to_f16x2(q23hi);
+          }
+          mma_f16_16816(o[mt], a0, a1, a2, a3, pb[t][0], pb[t][1]);
+          mma_f16_16816(o[mt], a0, a1, a2, a3, pc[t][0], pc[t][1]);
         }
-        mma_f16_16816(o[mt], a0, a1, a2, a3, pb0, pb1);
-        mma_f16_16816(o[mt], a0, a1, a2, a3, pc0, pc1);
       }
     } else {
       const int r = (lane & 7) + (lane >> 4) * 8;
       const int chs = (lane >> 3) & 1;
+      const uint8_t* vt = sb + C::box_off(1, w, 0, 0);
 #pragma unroll
       for (int mt = 0; mt < D / 16; ++mt) {
         const int half = mt >> 2;
@@ -494,8 +558,8 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
         const uint32_t addr = smem_u32(vt + half * kBoxBytes) + r * 128 + ((ch ^ (r & 7)) << 4);
         uint32_t a0, a1, a2, a3;
         ldmatrix_x4_trans(addr, a0, a1, a2, a3);
-        mma_bf16_16816(o[mt], a0, a1, a2, a3, pb0, pb1);
-        mma_bf16_16816(o[mt], a0, a1, a2, a3, pc0, pc1);
+        mma_bf16_16816(o[mt], a0, a1, a2, a3, pb[0][0], pb[0][1]);
+        mma_bf16_16816(o[mt], a0, a1, a2, a3, pc[0][0], pc[0][1]);
       }
     }
     __syncwarp();
