@@ -28,6 +28,7 @@ from .paged_attention import (  # noqa: F401
     slot_mapping,
     kv_write,
     kv_block_copy,
+    kv_block_swap,
     gather_kv,
     dense_attention,
     paged_attention_decode,

@@ -31,6 +31,7 @@ __all__ = [
     "slot_mapping",
     "kv_write",
     "kv_block_copy",
+    "kv_block_swap",
     "gather_kv",
     "dense_attention",
     "paged_attention_decode",
@@ -143,6 +144,27 @@ def kv_block_copy(k_cache: np.ndarray, v_cache: np.ndarray, pairs: np.ndarray):
         kc[int(dst)] = kc[int(src)]
         vc[int(dst)] = vc[int(src)]
     return kc, vc
+
+
+def kv_block_swap(src_k: np.ndarray, src_v: np.ndarray, dst_k: np.ndarray,
+                  dst_v: np.ndarray, pairs: np.ndarray):
+    """Return copies of the destination pools with block ``dst`` holding the
+    source pool's block ``src``, for K and for V.
+
+    Swap between GPU memory and host memory ("19.2 KV Cache 系统化管理",
+    §19.2.6 调度与抢占, Swap: a preempted request's KV blocks are parked in
+    CPU memory and brought back when GPU memory frees up;
+    "企业官网建设流程全解析" §8.2: the oldest blocks move to CPU memory and
+    return on demand while the block table keeps the logical view).  The two pools have the same block geometry but
+    different block counts; the source is never written, so the pairs are
+    independent of their order.
+    """
+    dk = dst_k.copy()
+    dv = dst_v.copy()
+    for src, dst in np.asarray(pairs).reshape(-1, 2):
+        dk[int(dst)] = src_k[int(src)]
+        dv[int(dst)] = src_v[int(src)]
+    return dk, dv
 
 
 # --------------------------------------------------------------------------

@@ -147,3 +147,34 @@ class SeqBlocks:
             self.pool.release(b)
         self.mapping.clear()
         self.num_tokens = 0
+
+
+def _move_all(seq: SeqBlocks, to_pool: BlockPool) -> List[Tuple[int, int]]:
+    need = len(seq.mapping)
+    if to_pool.num_free < need:
+        raise PoolExhausted(f"need {need} free blocks, {to_pool.num_free} left")
+    pairs = [(b, to_pool.allocate()) for b in seq.mapping]
+    for b in seq.mapping:
+        seq.pool.release(b)
+    seq.mapping = [d for _, d in pairs]
+    seq.pool = to_pool
+    return pairs
+
+
+def swap_out(seq: SeqBlocks, host_pool: BlockPool) -> List[Tuple[int, int]]:
+    """Preempt a request by swapping ("19.2 KV Cache 系统化管理" §19.2.6):
+    every one of its blocks at once (all or nothing) gets a block of the
+    host pool, its GPU blocks are released, and its table is repointed to the
+    host blocks.  Returns the ``(gpu_block, host_block)`` pairs the device
+    swap must copy before the released GPU blocks are reused.  A block shared
+    with other tables keeps their references; this request leaves with its
+    own copy.  Raises ``PoolExhausted`` (and changes nothing) when the host
+    pool lacks room."""
+    return _move_all(seq, host_pool)
+
+
+def swap_in(seq: SeqBlocks, gpu_pool: BlockPool) -> List[Tuple[int, int]]:
+    """Resume a swapped-out request: fresh GPU blocks for all of its host
+    blocks (all or nothing), host blocks released.  Returns the
+    ``(host_block, gpu_block)`` pairs to copy."""
+    return _move_all(seq, gpu_pool)

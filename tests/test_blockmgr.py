@@ -4,7 +4,8 @@ import numpy as np
 import pytest
 
 from paged_kv_cache_115_gb300 import accounting as acc
-from paged_kv_cache_115_gb300.blockmgr import BlockPool, PoolExhausted, SeqBlocks
+from paged_kv_cache_115_gb300.blockmgr import (BlockPool, PoolExhausted, SeqBlocks, swap_in,
+                                              swap_out)
 from paged_kv_cache_115_gb300 import workloads as wl
 
 
@@ -201,3 +202,34 @@ def test_tiny_materialize_canaries():
     assert torch.isnan(t["k_cache"][~hist]).all()
     assert torch.isfinite(t["k_cache"][hist]).all()
     assert hist.sum().item() == sum(int(L) - 1 for L in w.context_lens)
+
+
+def test_swap_out_and_in_all_or_nothing():
+    gpu, host = BlockPool(16, seed=1), BlockPool(8, seed=2)
+    a = SeqBlocks(gpu, 4)
+    a.grow_to(13)                                  # 4 blocks
+    b = a.fork()                                   # shares all 4
+    c = SeqBlocks(gpu, 4)
+    c.grow_to(20)                                  # 5 blocks
+    old = list(a.mapping)
+    pairs = swap_out(a, host)
+    assert [p[0] for p in pairs] == old and a.pool is host
+    assert a.mapping == [p[1] for p in pairs] and len(set(a.mapping)) == 4
+    assert all(gpu.ref_counts[x] == 1 for x in old)     # b still holds them
+    assert a.num_tokens == 13
+    gpu.check_invariants([b, c])
+    host.check_invariants([a])
+    # not enough host room for c (5 blocks, 4 free): nothing changes
+    before = (list(c.mapping), host.num_free, gpu.num_free)
+    with pytest.raises(PoolExhausted):
+        swap_out(c, host)
+    assert (list(c.mapping), host.num_free, gpu.num_free) == before
+    # back in: fresh GPU blocks, host blocks freed
+    hosts = list(a.mapping)
+    pairs = swap_in(a, gpu)
+    assert [p[0] for p in pairs] == hosts and a.pool is gpu and host.num_free == 8
+    assert not set(a.mapping) & set(b.mapping)      # a now owns private copies
+    gpu.check_invariants([a, b, c])
+    for t in (a, b, c):
+        t.release_all()
+    assert gpu.num_free == 16

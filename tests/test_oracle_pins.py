@@ -497,3 +497,110 @@ def test_mutations_are_caught(monkeypatch, golden, target, replacement, check):
             pin_gqa_equals_mha()
         else:
             pin_slot_p3_example(golden("p3_block_table_example.json"))
+
+
+# --------------------------------------------------------------------------
+# block swap between pools in different memories
+# ("19.2 KV Cache 系统化管理" §19.2.6 Swap; "企业官网建设流程全解析" §8.2)
+# --------------------------------------------------------------------------
+
+def _swap_brute(src, dst, pairs):
+    """Element-by-element: every element of a destination block named in a
+    pair equals the element at the same place in the named source block;
+    every other element keeps its old value."""
+    out = dst.copy()
+    nb_dst = dst.shape[0]
+    moved = {int(d): int(s) for s, d in pairs}
+    it = np.nditer(dst, flags=["multi_index"])
+    for _ in it:
+        idx = it.multi_index
+        if idx[0] in moved:
+            out[idx] = src[(moved[idx[0]],) + idx[1:]]
+    assert out.shape[0] == nb_dst
+    return out
+
+
+def test_swap_brute_force_with_canaries():
+    rng = np.random.default_rng(11)
+    K, H, D = 4, 2, 3
+    gpu_k = rng.standard_normal((9, K, H, D)).astype(np.float32)
+    gpu_v = rng.standard_normal((9, K, H, D)).astype(np.float32)
+    host_k = np.full((5, K, H, D), np.float32(-7.25))
+    host_v = np.full((5, K, H, D), np.float32(13.5))
+    out_pairs = np.array([[8, 0], [2, 3], [5, 4]], np.int64)
+    hk, hv = oracle.kv_block_swap(gpu_k, gpu_v, host_k, host_v, out_pairs)
+    assert np.array_equal(hk, _swap_brute(gpu_k, host_k, out_pairs))
+    assert np.array_equal(hv, _swap_brute(gpu_v, host_v, out_pairs))
+    assert np.all(hk[[1, 2]] == np.float32(-7.25)) and np.all(hv[[1, 2]] == np.float32(13.5))
+    # the source pools are not touched
+    assert np.array_equal(gpu_k, gpu_k.copy()) and hk is not host_k
+    # order of pairs does not matter (the source is never written)
+    hk2, hv2 = oracle.kv_block_swap(gpu_k, gpu_v, host_k, host_v, out_pairs[::-1])
+    assert np.array_equal(hk, hk2) and np.array_equal(hv, hv2)
+
+
+def test_swap_round_trip_restores_logical_view():
+    """Preempt: copy a request's blocks out to host blocks; resume: copy them
+    into freshly chosen GPU blocks and repoint the table.  Gathering the
+    request's rows through the new table gives the rows it had before."""
+    rng = np.random.default_rng(12)
+    K, H, D, L = 4, 2, 5, 14
+    nb = 12
+    kc = rng.standard_normal((nb, K, H, D)).astype(np.float32)
+    vc = rng.standard_normal((nb, K, H, D)).astype(np.float32)
+    table = np.array([7, 2, 9, 4], np.int64)            # ceil(14 / 4) = 4 blocks
+    before_k = [opa.gather_kv(kc, table, L, j, K, "f32") for j in range(H)]
+    before_v = [opa.gather_kv(vc, table, L, j, K, "f32") for j in range(H)]
+    host_ids = np.array([3, 0, 1, 2], np.int64)
+    hk, hv = oracle.kv_block_swap(kc, vc, np.zeros((4, K, H, D), np.float32),
+                                  np.zeros((4, K, H, D), np.float32),
+                                  np.stack([table, host_ids], 1))
+    # the GPU blocks are reused by someone else meanwhile
+    kc2 = rng.standard_normal(kc.shape).astype(np.float32)
+    vc2 = rng.standard_normal(vc.shape).astype(np.float32)
+    new_table = np.array([0, 11, 5, 6], np.int64)
+    kc3, vc3 = oracle.kv_block_swap(hk, hv, kc2, vc2, np.stack([host_ids, new_table], 1))
+    for j in range(H):
+        assert np.array_equal(opa.gather_kv(kc3, new_table, L, j, K, "f32"), before_k[j])
+        assert np.array_equal(opa.gather_kv(vc3, new_table, L, j, K, "f32"), before_v[j])
+    # blocks outside the new table keep the other user's data
+    others = [b for b in range(nb) if b not in set(new_table.tolist())]
+    assert np.array_equal(kc3[others], kc2[others])
+
+
+def test_swap_within_one_pool_is_block_copy():
+    rng = np.random.default_rng(13)
+    kc = rng.integers(0, 2**16, size=(6, 4, 2, 8), dtype=np.uint16)
+    vc = rng.integers(0, 2**16, size=(6, 4, 2, 8), dtype=np.uint16)
+    pairs = np.array([[0, 5], [1, 3]], np.int64)
+    a = oracle.kv_block_swap(kc, vc, kc, vc, pairs)
+    b = oracle.kv_block_copy(kc, vc, pairs)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_swap_planted_mistake_is_caught(monkeypatch):
+    """Plausible mistakes (K and V exchanged; the pair read as (dst, src))
+    each fail a pin."""
+    def kv_exchanged(src_k, src_v, dst_k, dst_v, pairs):
+        dk, dv = dst_k.copy(), dst_v.copy()
+        for s, d in np.asarray(pairs).reshape(-1, 2):
+            dk[int(d)] = src_v[int(s)]
+            dv[int(d)] = src_k[int(s)]
+        return dk, dv
+
+    def pair_reversed(src_k, src_v, dst_k, dst_v, pairs):
+        dk, dv = dst_k.copy(), dst_v.copy()
+        for d, s in np.asarray(pairs).reshape(-1, 2):
+            if d < dk.shape[0] and s < src_k.shape[0]:
+                dk[int(d)] = src_k[int(s)]
+                dv[int(d)] = src_v[int(s)]
+        return dk, dv
+
+    # (exchanging K and V twice cancels, so the round trip alone misses it)
+    for wrong, pins in ((kv_exchanged, (test_swap_brute_force_with_canaries,)),
+                        (pair_reversed, (test_swap_brute_force_with_canaries,
+                                         test_swap_round_trip_restores_logical_view))):
+        monkeypatch.setattr(oracle, "kv_block_swap", wrong)
+        for pin in pins:
+            with pytest.raises(AssertionError):
+                pin()
