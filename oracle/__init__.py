@@ -19,6 +19,11 @@ section:
 * "推理与 KV Cache 02:分页、共享与回收如何协作", section "从一个位置找到缓存块"
   (logical block, offset and token-slot formulas and the worked K=4 example).
 
+Submodules: ``oracle.quant`` (FP8 e4m3 / INT8 per-token KV formats, pinned in
+``tests/test_oracle_quant_pins.py``) and ``oracle.prefill`` (multi-query
+attention of several new tokens per sequence, pinned in
+``tests/test_oracle_prefill_pins.py``).
+
 Pins (checks against things other than the oracle itself) live in
 ``tests/test_oracle_pins.py``.  No function here is "parity unpinned".
 """
