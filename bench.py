@@ -248,7 +248,8 @@ def run_gpu(args):
         dist.barrier()
     from paged_kv_cache_115_gb300 import ops
 
-    w = wl.build(args.workload, seed=rank_seed(args.seed, rank))
+    w = wl.build(args.workload, seed=rank_seed(args.seed, rank),
+                 block_size=args.block_size or None)
     t = wl.materialize(w, device=dev, seed=rank_seed(args.seed, rank), canary=False,
                        values_device="cuda")
     fmt = args.kv_format
@@ -332,6 +333,23 @@ def run_gpu(args):
     assert ops.get_device_error(dev) == 0
 
     K = args.steps
+    if args.graph:
+        # the whole step as one graph; the attention call alone as another
+        # (for the per-launch roofline timing)
+        # (capture needs a side stream; replays run on the timing stream)
+        g_step, g_attn = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        with torch.cuda.graph(g_step, stream=cap):
+            prologue()
+            attention()
+        with torch.cuda.graph(g_attn, stream=cap):
+            attention()
+        stream.wait_stream(cap)
+        torch.cuda.synchronize(dev)
+        for _ in range(3):
+            g_step.replay()
+        torch.cuda.synchronize(dev)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(K)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -342,12 +360,21 @@ def run_gpu(args):
     torch.cuda.synchronize(dev)
     start.record(stream)
     for i in range(K):
-        prologue()
-        ev[i][0].record(stream)
-        attention()
-        ev[i][1].record(stream)
+        if args.graph:
+            g_step.replay()
+        else:
+            prologue()
+            ev[i][0].record(stream)
+            attention()
+            ev[i][1].record(stream)
     stop.record(stream)
     torch.cuda.synchronize(dev)
+    if args.graph:
+        for i in range(K):
+            ev[i][0].record(stream)
+            g_attn.replay()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
     clock_info = clocks.stop() if clocks else None
     if world > 1:
         dist.barrier()
@@ -439,6 +466,12 @@ def run_gpu(args):
     cfg["l2"] = (f"inputs larger than L2: {kv_bytes / 1e6:.0f} MB of KV read per step "
                  f"vs 129 MB L2; no flush between steps")
     cfg["parallelism"] = f"replicas x{world}" if world > 1 else "single GPU"
+    cfg["launch"] = "CUDA graph replay (one graph per step)" if args.graph else "eager launches"
+    blocks_used = int(sum(-(-int(L) // w.block_size) for L in w.context_lens))
+    cfg["kv_reserved_bytes"] = blocks_used * w.block_size * w.num_kv_heads * w.head_dim * 2 * \
+        (w.elem_bytes if fmt == "bf16" else 1)
+    cfg["tail_waste_tokens"] = blocks_used * w.block_size - int(w.context_lens.sum())
+    cfg["block_table_bytes"] = int(w.block_tables.nbytes)
     line = {
         "metric": METRIC,
         "value": value,
@@ -486,6 +519,212 @@ def run_gpu(args):
 
 
 # ---------------------------------------------------------------------------
+# block swap (GPU <-> pinned host): preempt half the batch and bring it back
+# ---------------------------------------------------------------------------
+SWAP_METRIC = "KV block swap GB/s (GPU pool <-> pinned host pool, out + in)"
+
+
+def swap_plan(w, seed: int):
+    """Every other sequence of the workload is preempted by swap: its blocks
+    (K and V) go to a host pool in a seeded shuffled order, and come back into
+    a seeded permutation of the same GPU blocks (scattered placement)."""
+    import numpy as np
+    rng = np.random.default_rng(seed + 101)
+    blocks = []
+    for s in range(1, w.num_seqs, 2):
+        n = -(-int(w.context_lens[s]) // w.block_size)
+        blocks.extend(int(b) for b in w.block_tables[s, :n])
+    blocks = np.array(blocks, np.int64)
+    host = rng.permutation(len(blocks)).astype(np.int64)
+    out_pairs = np.stack([blocks, host], 1)
+    in_pairs = np.stack([host, rng.permutation(blocks)], 1)
+    return out_pairs, in_pairs
+
+
+def _swap_cpu_sample(budget_s: float) -> dict:
+    """The oracle's swap on 512 pairs between two 512-block pools of the
+    Qwen-shaped geometry, repeated for about budget_s seconds."""
+    import numpy as np
+    import oracle
+    rng = np.random.default_rng(0)
+    shape = (512, 16, 8, 128)
+    a = rng.integers(0, 2**16, size=shape, dtype=np.uint16)
+    b = rng.integers(0, 2**16, size=shape, dtype=np.uint16)
+    pairs = np.stack([rng.permutation(512), rng.permutation(512)], 1)
+    moved, t0 = 0, time.perf_counter()
+    while time.perf_counter() - t0 < budget_s:
+        oracle.kv_block_swap(a, a, b, b, pairs)
+        moved += 2 * a.nbytes
+    sec = time.perf_counter() - t0
+    return {"bytes": moved, "seconds": sec}
+
+
+def run_swap(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
+    torch.cuda.set_device(dev)
+    from paged_kv_cache_115_gb300 import build, workloads as wl
+    if rank == 0 or world == 1:
+        build.build()
+    if world > 1:
+        dist.barrier()
+    from paged_kv_cache_115_gb300 import ops
+
+    w = wl.build(args.workload, seed=rank_seed(args.seed, rank))
+    out_np, in_np = swap_plan(w, rank_seed(args.seed, rank))
+    n = len(out_np)
+    shape = (w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim)
+    td = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    g = torch.Generator(device=dev)
+    g.manual_seed(rank_seed(args.seed, rank))
+    kc = torch.empty(shape, dtype=td, device=dev).normal_(generator=g)
+    vc = torch.empty(shape, dtype=td, device=dev).normal_(generator=g)
+    hk = torch.empty((n,) + shape[1:], dtype=td).pin_memory()
+    hv = torch.empty((n,) + shape[1:], dtype=td).pin_memory()
+    out_pairs = torch.from_numpy(out_np).to(dev)
+    in_pairs = torch.from_numpy(in_np).to(dev)
+    blk = w.block_size * w.num_kv_heads * w.head_dim * kc.element_size()
+    dir_bytes = 2 * n * blk                       # K and V, one direction
+    step_bytes = 2 * dir_bytes
+    stream = torch.cuda.current_stream(dev)
+
+    def swap_out():
+        ops.kv_block_swap(kc, vc, hk, hv, out_pairs)
+
+    def swap_in():
+        ops.kv_block_swap(hk, hv, kc, vc, in_pairs)
+
+    for _ in range(max(args.warmup, 3)):
+        swap_out()
+        swap_in()
+    torch.cuda.synchronize(dev)
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    for a, b, c in ev:
+        a.record(stream)
+        swap_out()
+        b.record(stream)
+        swap_in()
+        c.record(stream)
+    torch.cuda.synchronize(dev)
+    clock_info = clocks.stop()
+    out_ms = statistics.median(a.elapsed_time(b) for a, b, _ in ev)
+    in_ms = statistics.median(b.elapsed_time(c) for _, b, c in ev)
+    total_ms = ev[0][0].elapsed_time(ev[-1][2])
+
+    # the link's own rate for the same bytes: one contiguous copy each way
+    dflat = torch.empty(dir_bytes, dtype=torch.uint8, device=dev)
+    hflat = torch.empty(dir_bytes, dtype=torch.uint8).pin_memory()
+
+    def best(fn, reps=5):
+        ts = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            ts.append(e0.elapsed_time(e1))
+        return min(ts)
+
+    d2h_ms = best(lambda: hflat.copy_(dflat, non_blocking=True))
+    h2d_ms = best(lambda: dflat.copy_(hflat, non_blocking=True))
+    # one copy call per block and tensor, the way a loop of memcpys would do it
+    blocks_np = out_np[: min(n, 1024)]
+    pb_bytes = 2 * len(blocks_np) * blk
+
+    def per_block():
+        for s_, d_ in blocks_np:
+            hk[int(d_)].copy_(kc[int(s_)], non_blocking=True)
+            hv[int(d_)].copy_(vc[int(s_)], non_blocking=True)
+    per_block()
+    pb_ms = best(per_block, reps=2)
+    del dflat, hflat
+
+    # e2e: the public call with the pairs read straight from pinned host memory
+    out_pin, in_pin = torch.from_numpy(out_np).pin_memory(), torch.from_numpy(in_np).pin_memory()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(3, min(K, 20))
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        ops.kv_block_swap(kc, vc, hk, hv, out_pin)
+        ops.kv_block_swap(hk, hv, kc, vc, in_pin)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+
+    total_ms, e2e_ms = max_over_ranks([total_ms, e2e_ms], dev)
+    ms_step = total_ms / K
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return None
+    link_ms = d2h_ms + h2d_ms
+    achieved = step_bytes / ((out_ms + in_ms) * 1e-3) / 1e9
+    peak = step_bytes / (link_ms * 1e-3) / 1e9
+    cfg = {"workload": f"{w.name}: swap out and back in every other sequence",
+           "sequences_swapped": len(range(1, w.num_seqs, 2)), "blocks_swapped": n,
+           "block_bytes_per_tensor": blk, "num_kv_heads": w.num_kv_heads,
+           "head_dim": w.head_dim, "block_size": w.block_size,
+           "step": "kv_block_swap GPU->pinned host (K+V), then pinned host->GPU into a "
+                   "permutation of the same blocks",
+           "l2": f"{dir_bytes / 1e6:.0f} MB per direction vs 129 MB L2; no flush",
+           "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+    line = {
+        "metric": SWAP_METRIC, "value": world * step_bytes / (ms_step * 1e-3) / 1e9,
+        "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic: seeded N(0,1) pool values",
+        "config": cfg,
+        "roofline": {"bound": "link", "kernel": "block_move_kernel (swap out + swap in)",
+                     "achieved": achieved, "peak": peak,
+                     "peak_source": "measured in this run: one contiguous pinned-host copy of "
+                                    "the same bytes each way (cudaMemcpyAsync via torch)",
+                     "unit": "GB/s", "frac": achieved / peak,
+                     "algorithmic_bytes_per_launch": dir_bytes,
+                     "avg_launch_ms": (out_ms + in_ms) / 2, "traffic": None},
+        "rows": {"swap_out": {"median_us": out_ms * 1e3,
+                              "GBps": dir_bytes / (out_ms * 1e-3) / 1e9,
+                              "contiguous_copy_GBps": dir_bytes / (d2h_ms * 1e-3) / 1e9},
+                 "swap_in": {"median_us": in_ms * 1e3,
+                             "GBps": dir_bytes / (in_ms * 1e-3) / 1e9,
+                             "contiguous_copy_GBps": dir_bytes / (h2d_ms * 1e-3) / 1e9},
+                 "per_block_copy_calls": {"blocks": len(blocks_np), "ms": pb_ms,
+                                          "GBps": pb_bytes / (pb_ms * 1e-3) / 1e9}},
+        "e2e": {"value": world * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": dir_bytes + 2 * out_pin.nbytes,
+                "d2h_bytes_per_step": dir_bytes},
+        "gpu_launches": 2 * K,
+        "clocks": clock_info,
+    }
+    if not args.no_cpu_baseline:
+        r = _swap_cpu_sample(min(args.cpu_budget, 10.0))
+        line["cpu_baseline"] = {"value": r["bytes"] / r["seconds"] / 1e9, "unit": "GB/s",
+                                "cores": 1, "kind": "oracle",
+                                "sample": "oracle kv_block_swap, 512 pairs between two "
+                                          "512-block bf16 pools, single-threaded, repeated "
+                                          f"for {r['seconds']:.1f} s"}
+    if world > 1:
+        dist.destroy_process_group()
+    return line
+
+
+# ---------------------------------------------------------------------------
 # reference arm: the CPU oracle as it stands
 # ---------------------------------------------------------------------------
 def run_reference(args):
@@ -495,6 +734,28 @@ def run_reference(args):
     from paged_kv_cache_115_gb300 import workloads as wl
     w = wl.build(args.workload, seed=args.seed)
     per_step = max(1.0, args.cpu_budget / max(1, args.steps))
+    if args.op == "swap":
+        _swap_cpu_sample(min(per_step, 1.0))
+        moved, sec = 0, 0.0
+        for _ in range(args.steps):
+            r = _swap_cpu_sample(per_step)
+            moved += r["bytes"]
+            sec += r["seconds"]
+        value = moved / sec / 1e9
+        return {
+            "impl": "reference", "metric": SWAP_METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": sec / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bytes",
+            "data": "synthetic", "config": {"workload": f"{args.workload} geometry, 512-pair "
+                                                        "sample"},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": "oracle kv_block_swap, 512 pairs between two 512-block "
+                                       "bf16 pools"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0,
+        }
     for _ in range(args.warmup):
         _cpu_sample(args.workload, args.seed, min(per_step, 1.0))
     tot_bytes, tot_s, seqs = 0, 0.0, 0
@@ -529,6 +790,12 @@ def main(argv=None):
     ap.add_argument("--kv-format", choices=["bf16", "fp8", "int8"], default="bf16",
                     help="KV pool storage: bf16, FP8 e4m3 (per-tensor scale) or INT8 "
                          "(per-token scale)")
+    ap.add_argument("--block-size", type=int, default=0,
+                    help="override the workload's block size (block-size sweep); 0 keeps it")
+    ap.add_argument("--graph", action="store_true",
+                    help="capture the step in CUDA graphs and time graph replays")
+    ap.add_argument("--op", choices=["decode", "swap"], default="decode",
+                    help="decode: the decode step (default); swap: block swap GPU <-> host")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of CPU work for the oracle baseline sample")
@@ -540,7 +807,10 @@ def main(argv=None):
             os.environ[k] = "1"
     if args.warmup < 3 and args.impl == "gpu":
         args.warmup = 3
-    line = run_reference(args) if args.impl == "reference" else run_gpu(args)
+    if args.impl == "reference":
+        line = run_reference(args)
+    else:
+        line = run_swap(args) if args.op == "swap" else run_gpu(args)
     if line is not None:
         print(json.dumps(line), flush=True)
 

@@ -141,8 +141,9 @@ PKV_API pkv_status pkv_kv_block_copy(void* k_cache, void* v_cache, const int64_t
 /* Optional tuning of pkv_attention_decode (pass NULL for the defaults). */
 typedef struct {
   int32_t kernel;        /* 0 = automatic, 1 = TMA + tensor-core kernel
-                            (bf16, block_size % 16 == 0, head_dim 64 or 128,
-                            G <= 8), 2 = CUDA-core kernel (any supported shape) */
+                            (bf16, block_size 8 or a multiple of 16, head_dim
+                            64 or 128, G <= 8), 2 = CUDA-core kernel (any
+                            supported shape) */
   int32_t num_splits;    /* kernel 1: CTAs sharing the token range of one KV-head
                             group (0 = SM count x CTAs per SM).  kernel 2:
                             tokens per partition (0 = automatic).              */
@@ -293,6 +294,39 @@ PKV_API pkv_status pkv_kv_block_copy_quant(void* k_cache, void* v_cache,
                                            int64_t num_blocks, int32_t block_size,
                                            int32_t num_kv_heads, int32_t head_dim,
                                            const pkv_kv_quant* quant, void* stream);
+
+/*
+ * Block swap between two pools that may live in different memories
+ * ("19.2 KV Cache 系统化管理" §19.2.6 调度与抢占, Swap: a preempted
+ * request's KV blocks are parked in CPU memory and brought back when GPU
+ * memory frees up; "企业官网建设流程全解析" §8.2: CPU memory as a second tier
+ * of the block pool, oldest blocks out first, the block table hiding where
+ * a block lives).
+ *   for each i: dst_k[pairs[i][1]] = src_k[pairs[i][0]]; same for v.
+ * One kernel moves every pair; the GPU reads and writes host memory directly
+ * (NVLink-C2C / PCIe), so many small blocks cost one launch instead of one
+ * copy call each.
+ *   src_k, src_v: source pools, src_num_blocks blocks of block_bytes bytes.
+ *   dst_k, dst_v: destination pools, dst_num_blocks blocks of block_bytes.
+ *   block_bytes:  bytes of one block of one tensor: block_size * H_kv * D *
+ *                 element bytes for a KV pool (any format), block_size * 4
+ *                 for the float32 slot-scale arrays of an INT8 pool.
+ *   pairs:        int64 [num_pairs, 2] (src block, dst block), in device
+ *                 memory or in page-locked host memory.
+ * src_v and dst_v may both be NULL (a single array per side).  Every pool
+ * pointer must be device memory of the current device, or page-locked host
+ * memory mapped into its address space (cudaHostAlloc, cudaHostRegister);
+ * pageable host memory is refused with PKV_ERR_INVALID_ARGUMENT.  The source
+ * is never written, so source and destination may be the same pool when no
+ * destination block is also a source.  Ids outside their pool skip the pair
+ * and record PKV_DEVERR_COPY_PAIR.  Bit-exact.  Asynchronous on `stream`:
+ * the caller keeps host memory alive and unchanged until the stream reaches
+ * the copy.
+ */
+PKV_API pkv_status pkv_kv_block_swap(const void* src_k, const void* src_v,
+                                     int64_t src_num_blocks, void* dst_k, void* dst_v,
+                                     int64_t dst_num_blocks, int64_t block_bytes,
+                                     const int64_t* pairs, int64_t num_pairs, void* stream);
 
 /* Workspace bytes of pkv_attention_decode_quant for these sizes. */
 PKV_API pkv_status pkv_attention_quant_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,

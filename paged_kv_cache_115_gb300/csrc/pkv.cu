@@ -140,7 +140,7 @@ struct AttnPlan {
 };
 
 bool tc_shape_ok(int G, int D, int K, int64_t num_blocks, pkv_dtype dt) {
-  return dt == PKV_BF16 && (D == 64 || D == 128) && G >= 1 && G <= 8 && K % 16 == 0 &&
+  return dt == PKV_BF16 && (D == 64 || D == 128) && G >= 1 && G <= 8 && (K % 16 == 0 || K == 8) &&
          num_blocks * K < (int64_t(1) << 31) - 64;
 }
 
@@ -171,7 +171,7 @@ pkv_status plan_attention(int S, int H_q, int H_kv, int D, int K, int max_len, i
   AttnPlan p;
   if (c.kernel == 1 || (c.kernel == 0 && tc_ok)) {
     PKV_CHECK(tc_ok, PKV_ERR_UNSUPPORTED,
-              "tensor-core kernel needs bf16, head_dim 64/128, G <= 8, block_size %% 16 == 0 "
+              "tensor-core kernel needs bf16, head_dim 64/128, G <= 8, block_size 8 or a multiple of 16 "
               "and a 16-byte aligned pool");
     int dev, sms;
     pkv_status st = device_facts(&dev, &sms);
@@ -203,7 +203,7 @@ pkv_status plan_attention(int S, int H_q, int H_kv, int D, int K, int max_len, i
 }
 
 // Plan for a quantized pool: the tensor-core kernel when the shape allows it
-// (bf16 queries, head_dim 128, G <= 8, block_size % 16 == 0, 16-byte aligned
+// (bf16 queries, head_dim 128, G <= 8, block_size 8 or a multiple of 16, 16-byte aligned
 // pools and scales), else the CUDA-core kernel (head_dim 64 / 128, G <= 16).
 pkv_status plan_attention_quant(int S, int H_q, int H_kv, int D, int K, int max_len,
                                 int64_t num_blocks, pkv_dtype q_dt, const pkv_kv_quant* quant,
@@ -224,7 +224,7 @@ pkv_status plan_attention_quant(int S, int H_q, int H_kv, int D, int K, int max_
   if (c.kernel == 1 || (c.kernel == 0 && tc_ok)) {
     PKV_CHECK(tc_ok, PKV_ERR_UNSUPPORTED,
               "tensor-core kernel on a one-byte pool needs bf16 queries, head_dim 128, G <= 8, "
-              "block_size %% 16 == 0 and 16-byte aligned pools and scales");
+              "block_size 8 or a multiple of 16 and 16-byte aligned pools and scales");
     c.kernel = 1;
     return plan_attention(S, H_q, H_kv, D, K, max_len, num_blocks, PKV_BF16, &c, true, plan);
   }
@@ -290,7 +290,9 @@ pkv_status encode_pool_map(CUtensorMap* map, const void* pool, int64_t num_block
   const cuuint64_t eb = one_byte ? 1 : 2;
   cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H_kv, (cuuint64_t)(num_blocks * K)};
   cuuint64_t strides[2] = {(cuuint64_t)D * eb, (cuuint64_t)H_kv * D * eb};
-  cuuint32_t box[3] = {one_byte ? 128u : 64u, 1, (cuuint32_t)pkv::kTcChunk};
+  // one tile of 16 rows, or (8-token blocks) half a tile: a box never
+  // crosses a block boundary
+  cuuint32_t box[3] = {one_byte ? 128u : 64u, 1, (cuuint32_t)std::min(K, pkv::kTile)};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(map, one_byte ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                    3, const_cast<void*>(pool), dims, strides,
@@ -400,26 +402,71 @@ int vec_width(int64_t row_bytes, std::initializer_list<const void*> ptrs) {
   return 0;
 }
 
-// Copy whole blocks of `blk` bytes in both pools for every (src, dst) pair.
-pkv_status copy_blocks(void* k_cache, void* v_cache, const int64_t* pairs, int64_t num_pairs,
-                       int64_t num_blocks, int64_t blk, cudaStream_t st) {
+// Moves whole blocks of `blk` bytes from the source pools to the destination
+// pools for every (src, dst) pair; src_v / dst_v null means one tensor.
+pkv_status move_blocks(const void* src_k, const void* src_v, int64_t src_nb, void* dst_k,
+                       void* dst_v, int64_t dst_nb, const int64_t* pairs, int64_t num_pairs,
+                       int64_t blk, cudaStream_t st) {
   PKV_CHECK(num_pairs <= 2147483647, PKV_ERR_UNSUPPORTED, "too many pairs");
-  const int vw = vec_width(blk, {k_cache, v_cache});
+  const bool two = src_v != nullptr;
+  const int vw = two ? vec_width(blk, {src_k, src_v, dst_k, dst_v}) : vec_width(blk, {src_k, dst_k});
   PKV_CHECK(vw > 0, PKV_ERR_INVALID_ARGUMENT, "misaligned pools");
   constexpr int threads = 256, unroll = 4;
   const int64_t chunks = ceil_div(blk / vw, threads * unroll);
   PKV_CHECK(chunks <= 65535, PKV_ERR_UNSUPPORTED, "block too large");
-  dim3 grid((unsigned)num_pairs, (unsigned)chunks, 2);
-  auto* kc = static_cast<uint8_t*>(k_cache);
-  auto* vc = static_cast<uint8_t*>(v_cache);
+  dim3 grid((unsigned)num_pairs, (unsigned)chunks, two ? 2 : 1);
+  auto* sk = static_cast<const uint8_t*>(src_k);
+  auto* sv = static_cast<const uint8_t*>(src_v);
+  auto* dk = static_cast<uint8_t*>(dst_k);
+  auto* dv = static_cast<uint8_t*>(dst_v);
+#define PKV_MOVE(W)                                                                           \
+  PKV_CUDA(launch_pdl(pkv::block_move_kernel<W, unroll>, grid, dim3(threads), 0, st, sk, sv, \
+                      dk, dv, pairs, src_nb, dst_nb, blk))
   switch (vw) {
-    case 16: PKV_CUDA(launch_pdl(pkv::block_copy_kernel<16, unroll>, grid, dim3(threads), 0, st, kc, vc, pairs, num_blocks, blk)); break;
-    case 8: PKV_CUDA(launch_pdl(pkv::block_copy_kernel<8, unroll>, grid, dim3(threads), 0, st, kc, vc, pairs, num_blocks, blk)); break;
-    case 4: PKV_CUDA(launch_pdl(pkv::block_copy_kernel<4, unroll>, grid, dim3(threads), 0, st, kc, vc, pairs, num_blocks, blk)); break;
-    case 2: PKV_CUDA(launch_pdl(pkv::block_copy_kernel<2, unroll>, grid, dim3(threads), 0, st, kc, vc, pairs, num_blocks, blk)); break;
-    default: PKV_CUDA(launch_pdl(pkv::block_copy_kernel<1, unroll>, grid, dim3(threads), 0, st, kc, vc, pairs, num_blocks, blk)); break;
+    case 16: PKV_MOVE(16); break;
+    case 8: PKV_MOVE(8); break;
+    case 4: PKV_MOVE(4); break;
+    case 2: PKV_MOVE(2); break;
+    default: PKV_MOVE(1); break;
   }
+#undef PKV_MOVE
   return PKV_OK;
+}
+
+// Copy-on-write: blocks move within one pool.
+pkv_status copy_blocks(void* k_cache, void* v_cache, const int64_t* pairs, int64_t num_pairs,
+                       int64_t num_blocks, int64_t blk, cudaStream_t st) {
+  return move_blocks(k_cache, v_cache, num_blocks, k_cache, v_cache, num_blocks, pairs, num_pairs,
+                     blk, st);
+}
+
+// The address kernels use for a caller's buffer: device memory of the current
+// device as it is, page-locked host memory through its device mapping.
+// Pageable host memory and other devices' memory are refused.
+pkv_status device_view(const void* p, const char* what, const void** out) {
+  cudaPointerAttributes a{};
+  const cudaError_t e = cudaPointerGetAttributes(&a, p);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return fail(PKV_ERR_INVALID_ARGUMENT, "%s: not a CUDA-visible pointer", what);
+  }
+  int dev = -1;
+  PKV_CUDA(cudaGetDevice(&dev));
+  switch (a.type) {
+    case cudaMemoryTypeDevice:
+    case cudaMemoryTypeManaged:
+      PKV_CHECK(a.device == dev, PKV_ERR_INVALID_ARGUMENT, "%s: memory of another device", what);
+      *out = a.devicePointer;
+      return PKV_OK;
+    case cudaMemoryTypeHost:
+      PKV_CHECK(a.devicePointer != nullptr, PKV_ERR_INVALID_ARGUMENT,
+                "%s: page-locked host memory not mapped for this device", what);
+      *out = a.devicePointer;
+      return PKV_OK;
+    default:
+      return fail(PKV_ERR_INVALID_ARGUMENT,
+                  "%s: pageable host memory (pin it: cudaHostAlloc / cudaHostRegister)", what);
+  }
 }
 
 // Validates a quantized-pool description (token scales required for INT8).
@@ -591,6 +638,30 @@ pkv_status pkv_kv_block_copy(void* k_cache, void* v_cache, const int64_t* src_ds
   PKV_CHECK(k_cache && v_cache && src_dst_pairs, PKV_ERR_INVALID_ARGUMENT, "null pointer");
   const int64_t blk = (int64_t)block_size * num_kv_heads * head_dim * elem_bytes(dtype);
   return copy_blocks(k_cache, v_cache, src_dst_pairs, num_pairs, num_blocks, blk,
+                     as_stream(stream));
+}
+
+pkv_status pkv_kv_block_swap(const void* src_k, const void* src_v, int64_t src_num_blocks,
+                             void* dst_k, void* dst_v, int64_t dst_num_blocks, int64_t block_bytes,
+                             const int64_t* pairs, int64_t num_pairs, void* stream) {
+  PKV_CHECK(num_pairs >= 0 && src_num_blocks >= 1 && dst_num_blocks >= 1 && block_bytes >= 1,
+            PKV_ERR_INVALID_ARGUMENT, "bad block-swap sizes");
+  PKV_CHECK((src_v == nullptr) == (dst_v == nullptr), PKV_ERR_INVALID_ARGUMENT,
+            "src_v and dst_v must both be given or both be NULL");
+  PKV_CHECK(src_num_blocks <= INT64_MAX / block_bytes && dst_num_blocks <= INT64_MAX / block_bytes,
+            PKV_ERR_INVALID_ARGUMENT, "pool too large");
+  if (num_pairs == 0) return PKV_OK;
+  PKV_CHECK(src_k && dst_k && pairs, PKV_ERR_INVALID_ARGUMENT, "null pointer");
+  PKV_CHECK(aligned(pairs, 8), PKV_ERR_INVALID_ARGUMENT, "misaligned pairs");
+  const void *sk = nullptr, *sv = nullptr, *dk = nullptr, *dv = nullptr, *pr = nullptr;
+  pkv_status st = device_view(src_k, "src_k", &sk);
+  if (st == PKV_OK) st = device_view(dst_k, "dst_k", &dk);
+  if (st == PKV_OK && src_v) st = device_view(src_v, "src_v", &sv);
+  if (st == PKV_OK && dst_v) st = device_view(dst_v, "dst_v", &dv);
+  if (st == PKV_OK) st = device_view(pairs, "pairs", &pr);
+  if (st != PKV_OK) return st;
+  return move_blocks(sk, sv, src_num_blocks, const_cast<void*>(dk), const_cast<void*>(dv),
+                     dst_num_blocks, static_cast<const int64_t*>(pr), num_pairs, block_bytes,
                      as_stream(stream));
 }
 

@@ -208,38 +208,48 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
       prefetch_tensormap(&p.tmap_v);
     }
     const uint64_t policy = l2_policy_evict_first();
+    const int sbl = K < kTile ? 1 : 0;       // log2 of the boxes per tile row
     int k = 0;
     bool ok = true;
     for (int c0 = cb; c0 < ce && ok; c0 += 32) {
       // pool rows of the tiles of the next 32 chunks, one chunk per lane; a
       // tile past the sequence end (or of an out-of-range block) gets a row
-      // that is wholly out of bounds, which TMA fills with zeros
-      int row[TL];
+      // that is wholly out of bounds, which TMA fills with zeros.  With
+      // 8-token blocks a tile spans two blocks: two 8-row boxes (u = 0, 1),
+      // each a whole 1024-byte swizzle atom, land where one 16-row box would.
+      int row[TL][2];
 #pragma unroll
-      for (int t = 0; t < TL; ++t) row[t] = -2 * kTile;
+      for (int t = 0; t < TL; ++t) row[t][0] = row[t][1] = -2 * kTile;
       const int c = c0 + lane;
       if (c < ce) {
         const int s = seq_of_chunk(cstart, S, c);
-        const int L = TL > 1 ? effective_len(p.context_lens[s], p.max_len, row_tokens) : 1 << 30;
+        const int L = (TL > 1 || sbl) ? effective_len(p.context_lens[s], p.max_len, row_tokens)
+                                      : 1 << 30;
 #pragma unroll
         for (int t = 0; t < TL; ++t) {
-          const int tok = (c - cstart[s]) * CH + t * kTile;
-          if (tok < L) {
-            const int lb = tok / K;
-            const long long phys = p.block_tables[(int64_t)s * p.max_blocks_per_seq + lb];
-            if (phys < 0 || phys >= p.num_blocks) {
-              record_error(PKV_DEVERR_BLOCK_ID);
-            } else {
-              row[t] = (int)(phys * K + (tok - lb * K));
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int tok = (c - cstart[s]) * CH + t * kTile + u * K;
+            if (u <= sbl && tok < L) {
+              const int lb = tok / K;
+              const long long phys = p.block_tables[(int64_t)s * p.max_blocks_per_seq + lb];
+              if (phys < 0 || phys >= p.num_blocks) {
+                record_error(PKV_DEVERR_BLOCK_ID);
+              } else {
+                row[t][u] = (int)(phys * K + (tok - lb * K));
+              }
             }
           }
         }
       }
       const int cnt = min(32, ce - c0);
       for (int b = 0; b < cnt; ++b, ++k) {
-        int r[TL];
+        int r[TL][2];
 #pragma unroll
-        for (int t = 0; t < TL; ++t) r[t] = __shfl_sync(0xffffffffu, row[t], b);
+        for (int t = 0; t < TL; ++t) {
+          r[t][0] = __shfl_sync(0xffffffffu, row[t][0], b);
+          r[t][1] = __shfl_sync(0xffffffffu, row[t][1], b);
+        }
         const int stage = k % NS;
         const uint32_t parity = ((k / NS) & 1) ^ 1;
         if (!mbar_wait_bounded(bar_empty + 8 * stage, parity)) {
@@ -250,23 +260,31 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
         if (lane == 0) mbar_arrive_expect_tx(bar_full + 8 * stage, C::TX);
         __syncwarp();
         uint8_t* sb = smem + stage * C::STAGE;
-        for (int i = lane; i < C::NCOPY; i += 32) {
-          if (i < C::NBOX) {
-            const int kv = i / (HPC * TL * C::NH);
-            const int rem = i - kv * (HPC * TL * C::NH);
+        for (int i = lane; i < (C::NCOPY << sbl); i += 32) {
+          const int ci = i >> sbl, u = i & sbl;
+          if (ci < C::NBOX) {
+            const int kv = ci / (HPC * TL * C::NH);
+            const int rem = ci - kv * (HPC * TL * C::NH);
             const int h = rem / (TL * C::NH);
             const int rem2 = rem - h * (TL * C::NH);
             const int t = rem2 / C::NH, half = rem2 - t * C::NH;
-            tma_load_3d(smem_u32(sb + C::box_off(kv, h, t, half)), kv ? &p.tmap_v : &p.tmap_k,
-                        bar_full + 8 * stage, half * 64, head0 + h, t ? r[TL - 1] : r[0], policy);
+            const int r0 = t ? r[TL - 1][0] : r[0][0];
+            const int r1 = t ? r[TL - 1][1] : r[0][1];
+            tma_load_3d(smem_u32(sb + C::box_off(kv, h, t, half) + u * (kBoxBytes / 2)),
+                        kv ? &p.tmap_v : &p.tmap_k, bar_full + 8 * stage, half * 64, head0 + h,
+                        u ? r1 : r0, policy);
           } else if constexpr (CT == 2) {
-            // a tile's 16 per-slot scales (64 bytes); a tile with no rows
-            // reads slot 0's scales, which meet zero codes
-            const int idx = i - C::NBOX;
+            // a tile's 16 per-slot scales (64 bytes, or two 32-byte halves
+            // with 8-token blocks); a tile with no rows reads slot 0's
+            // scales, which meet zero codes
+            const int idx = ci - C::NBOX;
             const int kv = idx / TL, t = idx - kv * TL;
-            const int rt = t ? r[TL - 1] : r[0];
-            const float* src = (kv ? p.v_ts : p.k_ts) + (rt >= 0 ? rt : 0);
-            bulk_load(smem_u32(sb + C::SCALE_OFF + (kv * TL + t) * 64), src, 64,
+            const int r0 = t ? r[TL - 1][0] : r[0][0];
+            const int r1 = t ? r[TL - 1][1] : r[0][1];
+            const int rr = u ? r1 : r0;
+            const int nbytes = 64 >> sbl;
+            const float* src = (kv ? p.v_ts : p.k_ts) + (rr >= 0 ? rr : 0);
+            bulk_load(smem_u32(sb + C::SCALE_OFF + (kv * TL + t) * 64 + u * nbytes), src, nbytes,
                       bar_full + 8 * stage);
           }
         }

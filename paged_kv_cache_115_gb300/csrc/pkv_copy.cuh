@@ -209,24 +209,31 @@ __global__ void selftest_wait_timeout_kernel(long long limit) {
   if (!ok && threadIdx.x == 0) record_error(PKV_DEVERR_TIMEOUT);
 }
 
-// a5: copy whole blocks, K and V.  grid = (pairs, chunks of a block, 2);
-// each thread moves UNROLL vectors, all loads before all stores.
+// a5 and block swap: move whole blocks from a source pool to a destination
+// pool (the same pool for copy-on-write, a device pool and a mapped host pool
+// for swap).  grid = (pairs, slices of a block, tensors); each thread moves
+// UNROLL vectors, all loads before all stores, so a CTA keeps
+// blockDim.x * UNROLL * VW bytes in flight (what hides the latency of host
+// memory across the chip-to-chip link).  A destination block is never also
+// a source block in the same launch (caller contract), so the restrict
+// qualifiers hold even when the two pools are one.
 template <int VW, int UNROLL>
-__global__ void block_copy_kernel(uint8_t* __restrict__ k_cache, uint8_t* __restrict__ v_cache,
-                                  const int64_t* __restrict__ pairs, int64_t num_blocks,
+__global__ void block_move_kernel(const uint8_t* __restrict__ src_k,
+                                  const uint8_t* __restrict__ src_v, uint8_t* __restrict__ dst_k,
+                                  uint8_t* __restrict__ dst_v, const int64_t* __restrict__ pairs,
+                                  int64_t src_num_blocks, int64_t dst_num_blocks,
                                   int64_t block_bytes) {
   using V = typename VecT<VW>::T;
   pdl_wait_primary();
   pdl_launch_dependents();
   const int64_t p = blockIdx.x;
   const int64_t src = pairs[2 * p], dst = pairs[2 * p + 1];
-  if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+  if (src < 0 || src >= src_num_blocks || dst < 0 || dst >= dst_num_blocks) {
     if (threadIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) record_error(PKV_DEVERR_COPY_PAIR);
     return;
   }
-  uint8_t* base = blockIdx.z ? v_cache : k_cache;
-  const V* s = reinterpret_cast<const V*>(base + src * block_bytes);
-  V* d = reinterpret_cast<V*>(base + dst * block_bytes);
+  const V* s = reinterpret_cast<const V*>((blockIdx.z ? src_v : src_k) + src * block_bytes);
+  V* d = reinterpret_cast<V*>((blockIdx.z ? dst_v : dst_k) + dst * block_bytes);
   const int64_t nvec = block_bytes / VW;
   const int64_t first = (int64_t)blockIdx.y * blockDim.x * UNROLL + threadIdx.x;
   V buf[UNROLL];

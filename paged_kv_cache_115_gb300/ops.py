@@ -27,6 +27,7 @@ if not os.path.exists(_LIB_PATH):
 _lib = ctypes.CDLL(_LIB_PATH)
 
 PKV_OK = 0
+PKV_ERR_INVALID_ARGUMENT = 1
 PKV_ERR_DEVICE_CHECK = 5
 PKV_F32, PKV_BF16 = 0, 1
 
@@ -69,6 +70,8 @@ _kv_append = _sig("pkv_kv_append", c_i32, c_vp, c_vp, c_vp, c_i32, c_vp, c_i32, 
 _selftest_timeout = _sig("pkv_selftest_wait_timeout", c_i32, c_i64, c_vp)
 _block_copy = _sig("pkv_kv_block_copy", c_i32, c_vp, c_vp, c_vp, c_i64, c_i64, c_i32, c_i32, c_i32,
                    c_i32, c_vp)
+_block_swap = _sig("pkv_kv_block_swap", c_i32, c_vp, c_vp, c_i64, c_vp, c_vp, c_i64, c_i64, c_vp,
+                   c_i64, c_vp)
 _ws_bytes = _sig("pkv_attention_workspace_bytes", c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, c_i32,
                  c_i32, ctypes.POINTER(AttentionConfig), ctypes.POINTER(c_sz))
 _launch_count = _sig("pkv_attention_launch_count", c_i32, c_i32, c_i32, c_i32, c_i32, c_i32,
@@ -96,7 +99,8 @@ _dev_error = _sig("pkv_get_device_error", c_i32, ctypes.POINTER(c_i32), c_vp)
 NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 EXPORTED = ("pkv_status_string", "pkv_last_error_message", "pkv_version", "pkv_slot_mapping",
-            "pkv_kv_write", "pkv_kv_append", "pkv_kv_block_copy", "pkv_selftest_wait_timeout", "pkv_attention_workspace_bytes",
+            "pkv_kv_write", "pkv_kv_append", "pkv_kv_block_copy", "pkv_kv_block_swap",
+            "pkv_selftest_wait_timeout", "pkv_attention_workspace_bytes",
             "pkv_attention_launch_count", "pkv_attention_decode",
             "pkv_attention_decode_noalloc", "pkv_kv_append_quant", "pkv_kv_block_copy_quant",
             "pkv_attention_quant_workspace_bytes", "pkv_attention_decode_quant",
@@ -220,6 +224,51 @@ def kv_block_copy(k_cache: torch.Tensor, v_cache: torch.Tensor,
     _check(_block_copy(_ptr(k_cache), _ptr(v_cache), _ptr(src_dst_pairs), src_dst_pairs.shape[0],
                        nb, K, H, D, _dtype_code(k_cache), _stream(k_cache.device)),
            "pkv_kv_block_copy")
+
+
+def _need_swap_side(t: torch.Tensor, name: str) -> None:
+    if t.is_cuda:
+        _need(t, name)
+    elif t.device.type == "cpu" and t.is_pinned():
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    else:
+        raise ValueError(f"{name} must be a CUDA tensor or a pinned CPU tensor")
+
+
+def kv_block_swap(src_k: torch.Tensor, src_v: Optional[torch.Tensor], dst_k: torch.Tensor,
+                  dst_v: Optional[torch.Tensor], src_dst_pairs: torch.Tensor) -> None:
+    """Block swap between pools that may live in different memories:
+    ``dst[pairs[i][1]] = src[pairs[i][0]]`` for K and V (V may be None on
+    both sides).  Each pool is a CUDA tensor or a pinned CPU tensor whose
+    first axis counts blocks (a KV pool ``[nb, K, H_kv, D]`` in any format, or
+    an INT8 pool's slot scales viewed as ``[nb, K]``); the pairs are int64
+    ``[n, 2]`` on the GPU or pinned.  One launch on the current stream; the
+    caller keeps pinned buffers alive until the stream passes the copy."""
+    if (src_v is None) != (dst_v is None):
+        raise ValueError("src_v and dst_v must both be given or both be None")
+    sides = [(src_k, "src_k"), (dst_k, "dst_k")]
+    if src_v is not None:
+        sides += [(src_v, "src_v"), (dst_v, "dst_v")]
+    for t, name in sides:
+        _need_swap_side(t, name)
+        if t.dtype != src_k.dtype or tuple(t.shape[1:]) != tuple(src_k.shape[1:]):
+            raise ValueError(f"{name}: every pool needs src_k's dtype and block shape")
+    if src_v is not None and (src_v.shape[0] != src_k.shape[0] or dst_v.shape[0] != dst_k.shape[0]):
+        raise ValueError("K and V pools of one side must have the same number of blocks")
+    _need_swap_side(src_dst_pairs, "src_dst_pairs")
+    if src_dst_pairs.dtype != torch.int64 or src_dst_pairs.dim() != 2 or \
+            src_dst_pairs.shape[1] != 2:
+        raise ValueError("src_dst_pairs must be int64 [n, 2]")
+    block_bytes = src_k[0].numel() * src_k.element_size() if src_k.shape[0] else 0
+    cuda = [t.device for t, _ in sides if t.is_cuda]
+    dev = cuda[0] if cuda else torch.device("cuda", torch.cuda.current_device())
+    with torch.cuda.device(dev):
+        _check(_block_swap(_ptr(src_k), _ptr(src_v) if src_v is not None else None,
+                           src_k.shape[0], _ptr(dst_k),
+                           _ptr(dst_v) if dst_v is not None else None, dst_k.shape[0],
+                           block_bytes, _ptr(src_dst_pairs), src_dst_pairs.shape[0],
+                           _stream(dev)), "pkv_kv_block_swap")
 
 
 def _cfg(kernel: int, num_splits: int) -> AttentionConfig:

@@ -190,22 +190,29 @@ def build_prefix_cow(num_parents: int = 256, prefix_len: int = 2048,
         scale=1.0 / math.sqrt(head_dim))
 
 
-def build(name: str, seed: int = 0, pad="garbage") -> Workload:
+def build(name: str, seed: int = 0, pad="garbage", block_size: Optional[int] = None) -> Workload:
+    """The named workload; ``block_size`` replaces its block size (the same
+    lengths and shapes, a pool re-cut into blocks of that many tokens), for
+    block-size sweeps."""
     rng = np.random.default_rng(10_000 + seed)
+
+    def K(default):
+        return int(block_size) if block_size else default
+
     if name == "tiny":
-        return build_decode("tiny", [10, 7, 16, 3], 4, 2, 64, 4, "f32",
-                            num_blocks=32, seed=seed, pad=pad)
+        return build_decode("tiny", [10, 7, 16, 3], 4, 2, 64, K(4), "f32",
+                            num_blocks=32 if not block_size else None, seed=seed, pad=pad)
     if name == "qwen3_0_6b":
         lens = rng.integers(512, 4096 + 1, size=64)
-        return build_decode(name, lens, 16, 8, 128, 16, "bf16", seed=seed, pad=pad)
+        return build_decode(name, lens, 16, 8, 128, K(16), "bf16", seed=seed, pad=pad)
     if name == "mistral_7b":
         lens = np.concatenate([np.full(64, 8192), rng.integers(1024, 8192 + 1, size=64)])
         lens = rng.permutation(lens)
-        return build_decode(name, lens, 32, 8, 128, 16, "bf16", seed=seed, pad=pad)
+        return build_decode(name, lens, 32, 8, 128, K(16), "bf16", seed=seed, pad=pad)
     if name == "llama31_70b":
-        return build_decode(name, [131072] * 4, 64, 8, 128, 32, "bf16", seed=seed, pad=pad)
+        return build_decode(name, [131072] * 4, 64, 8, 128, K(32), "bf16", seed=seed, pad=pad)
     if name == "prefix_cow":
-        return build_prefix_cow(seed=seed, pad=pad)
+        return build_prefix_cow(seed=seed, pad=pad, block_size=K(16))
     raise KeyError(name)
 
 

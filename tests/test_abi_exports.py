@@ -69,6 +69,16 @@ def test_host_validation_without_launch(lib):
     g.argtypes = [vp, vp, vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
                   ctypes.c_int32, ctypes.c_int32, vp]
     assert g(None, None, None, -1, 8, 16, 8, 128, 1, None) == 1
+    sw = lib.pkv_kv_block_swap
+    sw.argtypes = [vp, vp, ctypes.c_int64, vp, vp, ctypes.c_int64, ctypes.c_int64, vp,
+                   ctypes.c_int64, vp]
+    assert sw(None, None, 8, None, None, 4, 32768, None, 0, None) == 0      # nothing to move
+    assert sw(None, None, 8, None, None, 4, 32768, None, -1, None) == 1     # negative count
+    assert sw(None, None, 8, None, None, 4, 0, None, 1, None) == 1          # empty blocks
+    assert sw(None, vp(64), 8, None, None, 4, 32768, None, 1, None) == 1    # V on one side only
+    assert b"both" in lib.pkv_last_error_message()
+    assert sw(None, None, 8, None, None, 4, 32768, None, 1, None) == 1      # null pools
+    assert sw(vp(64), None, 2**62, vp(64), None, 4, 32768, vp(64), 1, None) == 1  # overflow
     h = lib.pkv_slot_mapping
     h.argtypes = [vp, ctypes.c_int32, vp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, vp, vp]
     assert h(None, 4, None, 0, 16, 10, None, None) == 0

@@ -175,7 +175,7 @@ def test_tiny_step(ops, num_splits):
 LENS_RAGGED = [1, 15, 16, 17, 31, 33, 100, 257, 600]
 
 
-@pytest.mark.parametrize("K", [16, 32, 64])
+@pytest.mark.parametrize("K", [8, 16, 32, 64])
 @pytest.mark.parametrize("G", [1, 2, 4, 8])
 @pytest.mark.parametrize("D", [64, 128])
 def test_tc_kernel_shapes(ops, K, G, D):

@@ -169,7 +169,7 @@ def test_quant_tensor_core_and_cuda_core(ops, fmt, kernel, num_splits):
 
 
 @pytest.mark.parametrize("fmt", ["fp8", "int8"])
-@pytest.mark.parametrize("G,K,H_kv", [(8, 32, 8), (2, 64, 4), (1, 16, 1)])
+@pytest.mark.parametrize("G,K,H_kv", [(8, 32, 8), (2, 64, 4), (1, 16, 1), (4, 8, 8), (2, 8, 2)])
 def test_quant_tensor_core_shapes(ops, fmt, G, K, H_kv):
     run_quant_step(ops, fmt, "bf16", 128, G, K, [5, 130, 1000, 64], H_kv=H_kv, kernel=1)
 
