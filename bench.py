@@ -725,6 +725,223 @@ def run_swap(args):
 
 
 # ---------------------------------------------------------------------------
+# multi-query (prefill) attention: packed new tokens per sequence
+# ---------------------------------------------------------------------------
+PREFILL_METRIC = "paged multi-query attention (prefill) TFLOP/s and KV GB/s"
+
+
+def prefill_flops(w) -> int:
+    """Dense causal attention FLOPs: 4 * D per (query head, key) pair, each new
+    token at position p seeing p + 1 keys."""
+    tot = 0
+    for P_, n in zip(w.prefix, w.news):
+        # sum over i < n of (P_ + i + 1)
+        tot += int(n) * int(P_) + int(n) * (int(n) + 1) // 2
+    return 4 * w.head_dim * w.num_q_heads * tot
+
+
+def _prefill_cpu_sample(name: str, seed: int, budget_s: float) -> dict:
+    """The oracle on the first new tokens of the workload until budget_s."""
+    import numpy as np
+    import oracle
+    from oracle import prefill as OP
+    from paged_kv_cache_115_gb300 import workloads as wl
+    w = wl.build_prefill(name, seed=seed)
+    rng = np.random.default_rng(seed)
+    D, H_q, H_kv, K = w.head_dim, w.num_q_heads, w.num_kv_heads, w.block_size
+    flops, t0, done = 0, time.perf_counter(), 0
+    s = 0
+    L = int(w.context_lens[s])
+    nb = -(-L // K)
+    # a private pool with just this sequence's blocks, renumbered 0 .. nb-1
+    kc = rng.standard_normal((nb, K, H_kv, D)).astype(np.float32)
+    vc = rng.standard_normal((nb, K, H_kv, D)).astype(np.float32)
+    bt = np.arange(nb, dtype=np.int64)[None, :]
+    n_all = int(w.news[s])
+    while time.perf_counter() - t0 < budget_s and done < n_all:
+        # one new token at a time (its own causal row), the last ones first
+        i = n_all - 1 - done
+        q = rng.standard_normal((1, H_q, D)).astype(np.float32)
+        pos = L - n_all + i
+        OP.paged_attention_prefill(q, kc, vc, bt, [0, 1], [pos + 1], w.scale, "f32")
+        flops += 4 * D * H_q * (pos + 1)
+        done += 1
+    sec = time.perf_counter() - t0
+    return {"flops": flops, "seconds": sec, "tokens": done}
+
+
+def run_prefill(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
+    torch.cuda.set_device(dev)
+    from paged_kv_cache_115_gb300 import build, workloads as wl
+    if rank == 0 or world == 1:
+        build.build()
+    if world > 1:
+        dist.barrier()
+    from paged_kv_cache_115_gb300 import ops
+
+    w = wl.build_prefill(args.workload, seed=rank_seed(args.seed, rank))
+    g = torch.Generator(device=dev)
+    g.manual_seed(rank_seed(args.seed, rank))
+    shape = (w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim)
+    T = w.num_tokens
+    kc = torch.empty(shape, dtype=torch.bfloat16, device=dev).normal_(generator=g)
+    vc = torch.empty(shape, dtype=torch.bfloat16, device=dev).normal_(generator=g)
+    q = torch.empty((T, w.num_q_heads, w.head_dim), dtype=torch.bfloat16,
+                    device=dev).normal_(generator=g)
+    k_new = torch.empty((T, w.num_kv_heads, w.head_dim), dtype=torch.bfloat16,
+                        device=dev).normal_(generator=g)
+    v_new = torch.empty_like(k_new).normal_(generator=g)
+    bt = torch.from_numpy(w.block_tables).to(dev)
+    cu = torch.from_numpy(w.cu_seqlens).to(dev)
+    lens = torch.from_numpy(w.context_lens).to(dev)
+    out = torch.empty_like(q)
+    max_q, max_len = int(w.news.max()), int(w.context_lens.max())
+    stream = torch.cuda.current_stream(dev)
+
+    def append():
+        ops.paged_kv_append_varlen(k_new, v_new, cu, lens, bt, kc, vc)
+
+    def attention():
+        ops.paged_attention_prefill(q, kc, vc, bt, cu, lens, w.scale, max_q, max_len, out=out)
+
+    for _ in range(max(args.warmup, 3)):
+        append()
+        attention()
+    torch.cuda.synchronize(dev)
+    assert ops.get_device_error(dev) == 0
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(dev.index) if rank == 0 else None
+    time.sleep(0.2 if clocks else 0)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    start.record(stream)
+    for i in range(K):
+        append()
+        ev[i][0].record(stream)
+        attention()
+        ev[i][1].record(stream)
+    stop.record(stream)
+    torch.cuda.synchronize(dev)
+    clock_info = clocks.stop() if clocks else None
+    total_ms = start.elapsed_time(stop)
+    attn_ms = sum(a.elapsed_time(b) for a, b in ev) / K
+    assert ops.get_device_error(dev) == 0
+
+    # end to end: host buffers in, output back, through the public calls
+    pin = {"q": q.cpu().pin_memory(), "k": k_new.cpu().pin_memory(),
+           "v": v_new.cpu().pin_memory(), "bt": bt.cpu().pin_memory(),
+           "cu": cu.cpu().pin_memory(), "lens": lens.cpu().pin_memory()}
+    dst = {"q": q, "k": k_new, "v": v_new, "bt": bt, "cu": cu, "lens": lens}
+    host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    h2d = sum(v.numel() * v.element_size() for v in pin.values())
+    d2h = host_out.numel() * host_out.element_size()
+    e2e_steps = max(3, min(K, 50))
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        for k_, v_ in pin.items():
+            dst[k_].copy_(v_, non_blocking=True)
+        append()
+        attention()
+        host_out.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+
+    total_ms, attn_ms, e2e_ms = max_over_ranks([total_ms, attn_ms, e2e_ms], dev)
+    ms_step = total_ms / K
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return None
+    flops = prefill_flops(w)
+    kv_bytes = int(w.context_lens.sum()) * w.num_kv_heads * w.head_dim * 2 * 2
+    peaks, peak_src = read_peaks()
+    tflops = flops / (attn_ms * 1e-3) / 1e12
+    gbs = kv_bytes / (attn_ms * 1e-3) / 1e9
+    tensor_bound = flops / kv_bytes > 400            # FLOP per byte vs ridge of ~280
+    if tensor_bound:
+        peak = float(peaks.get("bf16_tflops", 1900.0))
+        roof = {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
+                "frac": tflops / peak,
+                "peak_source": f"{peak_src} bf16_tflops (cuBLAS dense bf16, burst)"}
+    else:
+        peak = float(peaks["hbm_gbs"])
+        roof = {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                "frac": gbs / peak, "peak_source": f"{peak_src} hbm_gbs (copy, read+write)"}
+    roof.update({"kernel": "attn_prefill_kernel (pkv_attention_prefill)",
+                 "algorithmic_flops_per_launch": flops,
+                 "algorithmic_bytes_per_launch": kv_bytes, "avg_launch_ms": attn_ms,
+                 "traffic": None})
+    value = world * (tflops if tensor_bound else gbs)
+    cfg = {"workload": w.name, "num_seqs": w.num_seqs, "new_tokens": T,
+           "new_tokens_per_seq": {"min": int(w.news.min()), "max": max_q},
+           "cached_prefix": {"min": int(w.prefix.min()), "max": int(w.prefix.max()),
+                             "mean": float(w.prefix.mean())},
+           "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
+           "head_dim": w.head_dim, "block_size": w.block_size, "num_blocks": w.num_blocks,
+           "step": "paged_kv_append_varlen (slot mapping + KV write of the new tokens) + "
+                   "paged_attention_prefill",
+           "l2": f"{kv_bytes / 1e6:.0f} MB of KV per step vs 129 MB L2; no flush",
+           "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+    line = {
+        "metric": PREFILL_METRIC, "value": value,
+        "unit": "TFLOP/s" if tensor_bound else "GB/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic: seeded N(0,1) q / new K,V / pool values; block tables from a "
+                "seeded shuffled free list",
+        "config": cfg, "attention_tflops": tflops, "attention_kv_GBps": gbs,
+        "new_tokens_per_s": world * T / (ms_step * 1e-3),
+        "roofline": roof,
+        "e2e": {"value": world * (flops if tensor_bound else kv_bytes) / (e2e_ms * 1e-3) /
+                (1e12 if tensor_bound else 1e9),
+                "unit": "TFLOP/s" if tensor_bound else "GB/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 2 * K,
+        "clocks": clock_info,
+    }
+    if not args.no_cpu_baseline:
+        env = dict(os.environ)
+        for k_ in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+            env[k_] = "1"
+        env["CUDA_VISIBLE_DEVICES"] = ""
+        code = ("import json,sys; sys.path.insert(0, %r); import bench; "
+                "print(json.dumps(bench._prefill_cpu_sample(%r, %d, %f)))"
+                % (ROOT, args.workload, args.seed, min(args.cpu_budget, 10.0)))
+        r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
+                           cwd=ROOT, timeout=600)
+        if r.returncode == 0:
+            res = json.loads(r.stdout.strip().splitlines()[-1])
+            line["cpu_baseline"] = {
+                "value": res["flops"] / res["seconds"] / 1e12, "unit": "TFLOP/s", "cores": 1,
+                "kind": "oracle",
+                "sample": f"fp64 numpy oracle, single-threaded, {res['tokens']} of the first "
+                          f"sequence's new tokens ({res['seconds']:.1f} s)"}
+        else:
+            line["cpu_baseline"] = {"value": None, "kind": "oracle", "error": r.stderr[-300:]}
+    if world > 1:
+        dist.destroy_process_group()
+    return line
+
+
+# ---------------------------------------------------------------------------
 # reference arm: the CPU oracle as it stands
 # ---------------------------------------------------------------------------
 def run_reference(args):
@@ -732,8 +949,28 @@ def run_reference(args):
     if rank != 0:
         return None
     from paged_kv_cache_115_gb300 import workloads as wl
-    w = wl.build(args.workload, seed=args.seed)
     per_step = max(1.0, args.cpu_budget / max(1, args.steps))
+    w = wl.build(args.workload, seed=args.seed) if args.op == "decode" else None
+    if args.op == "prefill":
+        fl, sec = 0, 0.0
+        for _ in range(args.steps):
+            r = _prefill_cpu_sample(args.workload, args.seed, per_step)
+            fl += r["flops"]
+            sec += r["seconds"]
+        value = fl / sec / 1e12
+        return {
+            "impl": "reference", "metric": PREFILL_METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": sec / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": args.workload},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                             "sample": "fp64 numpy oracle on the first sequence's last new "
+                                       "tokens"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0,
+        }
     if args.op == "swap":
         _swap_cpu_sample(min(per_step, 1.0))
         moved, sec = 0, 0.0
@@ -794,8 +1031,10 @@ def main(argv=None):
                     help="override the workload's block size (block-size sweep); 0 keeps it")
     ap.add_argument("--graph", action="store_true",
                     help="capture the step in CUDA graphs and time graph replays")
-    ap.add_argument("--op", choices=["decode", "swap"], default="decode",
-                    help="decode: the decode step (default); swap: block swap GPU <-> host")
+    ap.add_argument("--op", choices=["decode", "swap", "prefill"], default="decode",
+                    help="decode: the decode step (default); swap: block swap GPU <-> host; "
+                         "prefill: multi-query attention (workloads suffix_prefill, "
+                         "speculative_decode)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of CPU work for the oracle baseline sample")
@@ -810,7 +1049,7 @@ def main(argv=None):
     if args.impl == "reference":
         line = run_reference(args)
     else:
-        line = run_swap(args) if args.op == "swap" else run_gpu(args)
+        line = {"swap": run_swap, "prefill": run_prefill}.get(args.op, run_gpu)(args)
     if line is not None:
         print(json.dumps(line), flush=True)
 

@@ -353,6 +353,58 @@ PKV_API pkv_status pkv_attention_decode_quant(
     const pkv_attention_config* config, void* stream);
 
 /*
+ * Multi-query paged attention: several new tokens per sequence attend at
+ * once over the paged cache — the chunks of a long prompt ("KV Cache：长上下文
+ * 为什么吃显存，PagedAttention 怎么救" §06, Chunked Prefill), the suffix after a
+ * prefix-cache hit ("推理与 KV Cache 02:分页、共享与回收如何协作", 前缀索引与
+ * Block Table: the suffix still reads the prefix's KV), or speculative
+ * candidate tokens ("企业官网建设流程全解析" §8.2).  Each new token is a query
+ * of the new-token attention of "KV Cache：长上下文为什么吃显存" §01 at its own
+ * position, causal among the new tokens:
+ *   for sequence s with n = cu_seqlens[s+1] - cu_seqlens[s] new tokens and
+ *   L = context_lens[s] (all tokens, the new ones included, already stored),
+ *   new token i (packed row t = cu_seqlens[s] + i) at position p = L - n + i:
+ *   out[t][h] = softmax_x(scale * q[t][h] . K[x][h/G]) V[x][h/G], x = 0 .. p.
+ *   q, out:        [num_tokens, num_q_heads, head_dim] (dtype), packed by sequence.
+ *   cu_seqlens:    int32 [num_seqs + 1], cu_seqlens[0] = 0, non-decreasing,
+ *                  cu_seqlens[num_seqs] = num_tokens.
+ *   context_lens:  int32 [num_seqs], each >= its new-token count.
+ *   max_query_len: host bound on the new tokens of any sequence (sizes the
+ *                  grid); max_context_len: host bound on context_lens.
+ *   k_cache, v_cache, block_tables: as pkv_attention_decode.
+ * Supported: PKV_BF16, head_dim 64 or 128, block_size 8 or a multiple of 16
+ * (else PKV_ERR_UNSUPPORTED).  n = 1 for every sequence is the decode step.
+ * Inconsistent counts (n < 0, n > L, cu_seqlens past num_tokens) skip the
+ * sequence and record PKV_DEVERR_CONTEXT_LEN.  Needs no workspace.
+ */
+PKV_API pkv_status pkv_attention_prefill(const void* q, const void* k_cache, const void* v_cache,
+                                         const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                         const int32_t* cu_seqlens, const int32_t* context_lens,
+                                         int32_t num_seqs, int32_t num_tokens,
+                                         int32_t max_query_len, int32_t max_context_len,
+                                         int32_t num_q_heads, int32_t num_kv_heads,
+                                         int32_t head_dim, int32_t block_size,
+                                         int64_t num_blocks, float scale, void* out,
+                                         pkv_dtype dtype, void* stream);
+
+/*
+ * a1 + a2 for the packed new tokens of pkv_attention_prefill: token t of
+ * sequence s (cu_seqlens[s] <= t < cu_seqlens[s+1]) is stored at the slot of
+ * position context_lens[s] - n_s + (t - cu_seqlens[s]) in s's block-table
+ * row: k_cache.view(-1, H_kv, D)[slot] = k[t], same for v.  k, v:
+ * [num_tokens, H_kv, D] (dtype).  slot_mapping_out (int64 [num_tokens]) may
+ * be NULL; it receives the slots (-1 for skipped tokens).  Out-of-range
+ * positions or block ids skip the token and record a device error.
+ */
+PKV_API pkv_status pkv_kv_append_varlen(const void* k, const void* v, const int32_t* cu_seqlens,
+                                        const int32_t* context_lens, const int32_t* block_tables,
+                                        int32_t max_blocks_per_seq, int32_t num_seqs,
+                                        int32_t num_tokens, void* k_cache, void* v_cache,
+                                        int64_t num_blocks, int32_t block_size,
+                                        int32_t num_kv_heads, int32_t head_dim, pkv_dtype dtype,
+                                        int64_t* slot_mapping_out, void* stream);
+
+/*
  * Synchronises `stream`, copies the current device's error word into *code
  * (a PKV_DEVERR_* value) and clears it.  Returns PKV_ERR_DEVICE_CHECK when
  * the word was non-zero, PKV_OK when it was zero.

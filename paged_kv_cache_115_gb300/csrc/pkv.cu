@@ -13,6 +13,7 @@
 
 #include "pkv_attention_simt.cuh"
 #include "pkv_attention_tc.cuh"
+#include "pkv_prefill.cuh"
 #include "pkv_reduce.cuh"
 #include "pkv_copy.cuh"
 #include "pkv_device.cuh"
@@ -267,6 +268,27 @@ struct TcInst {
 };
 template <int D, int HPC, int CT> std::once_flag TcInst<D, HPC, CT>::flags[kMaxDevices];
 template <int D, int HPC, int CT> cudaError_t TcInst<D, HPC, CT>::errs[kMaxDevices];
+
+// ---- multi-query (prefill) kernel dispatch -----------------------------------------
+template <int D, int NW>
+struct PfInst {
+  using C = pkv::PfCfg<D, NW>;
+  static std::once_flag flags[kMaxDevices];
+  static cudaError_t errs[kMaxDevices];
+  static pkv_status launch(const pkv::PfParams& prm, int tiles, int H_kv, int S, cudaStream_t st,
+                           int dev) {
+    auto k = pkv::attn_prefill_kernel<D, NW>;
+    pkv_status s = set_smem_once(k, C::SMEM, flags, errs, dev);
+    if (s != PKV_OK) return s;
+    PKV_CUDA(launch_pdl(k, dim3(tiles, H_kv, S), dim3(C::THREADS), (size_t)C::SMEM, st, prm));
+    return PKV_OK;
+  }
+};
+template <int D, int NW> std::once_flag PfInst<D, NW>::flags[kMaxDevices];
+template <int D, int NW> cudaError_t PfInst<D, NW>::errs[kMaxDevices];
+
+// Query rows per KV head and tile: 16 per consumer warp, 1, 2 or 4 warps.
+int prefill_warps(int64_t rows) { return rows <= 16 ? 1 : (rows <= 32 ? 2 : 4); }
 
 template <int D, int CT>
 pkv_status launch_tc_d(int hpc, const pkv::TcParams& prm, int n, int groups, cudaStream_t st,
@@ -961,6 +983,117 @@ pkv_status pkv_attention_decode_noalloc(const void* q, const void* k_cache, cons
                               max_context_len, num_seqs, num_q_heads, num_kv_heads, head_dim,
                               block_size, num_blocks, scale, out, scratch,
                               PKV_NOALLOC_SCRATCH_BYTES, dtype, config, stream);
+}
+
+pkv_status pkv_attention_prefill(const void* q, const void* k_cache, const void* v_cache,
+                                 const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                 const int32_t* cu_seqlens, const int32_t* context_lens,
+                                 int32_t num_seqs, int32_t num_tokens, int32_t max_query_len,
+                                 int32_t max_context_len, int32_t num_q_heads,
+                                 int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                 int64_t num_blocks, float scale, void* out, pkv_dtype dtype,
+                                 void* stream) {
+  PKV_CHECK(num_seqs >= 0 && num_tokens >= 0 && max_query_len >= 0 && max_context_len >= 0 &&
+                max_blocks_per_seq >= 1 && num_blocks >= 1 && block_size >= 1 &&
+                num_q_heads >= 1 && num_kv_heads >= 1 && head_dim >= 1 && dtype_ok(dtype),
+            PKV_ERR_INVALID_ARGUMENT, "bad prefill sizes");
+  PKV_CHECK(num_q_heads % num_kv_heads == 0, PKV_ERR_INVALID_ARGUMENT,
+            "num_q_heads must be a multiple of num_kv_heads");
+  PKV_CHECK(max_query_len <= max_context_len, PKV_ERR_INVALID_ARGUMENT,
+            "max_query_len above max_context_len");
+  PKV_CHECK(std::isfinite(scale), PKV_ERR_INVALID_ARGUMENT, "scale must be finite");
+  PKV_CHECK(dtype == PKV_BF16 && (head_dim == 64 || head_dim == 128) &&
+                (block_size % 16 == 0 || block_size == 8),
+            PKV_ERR_UNSUPPORTED,
+            "prefill kernel needs bf16, head_dim 64 or 128, block_size 8 or a multiple of 16");
+  PKV_CHECK(num_blocks <= ((int64_t(1) << 31) - 64) / block_size, PKV_ERR_UNSUPPORTED,
+            "pool too large for 32-bit tile rows");
+  PKV_CHECK(num_seqs <= 65535 && num_kv_heads <= 65535, PKV_ERR_UNSUPPORTED,
+            "at most 65535 sequences and KV heads per call");
+  PKV_CHECK((int64_t)max_blocks_per_seq * block_size <= 2147483647, PKV_ERR_UNSUPPORTED,
+            "table row too long");
+  if (num_seqs == 0 || num_tokens == 0 || max_query_len == 0) return PKV_OK;
+  PKV_CHECK(q && k_cache && v_cache && block_tables && cu_seqlens && context_lens && out,
+            PKV_ERR_INVALID_ARGUMENT, "null pointer");
+  PKV_CHECK(aligned(k_cache, 16) && aligned(v_cache, 16) && aligned(q, 4) && aligned(out, 4),
+            PKV_ERR_INVALID_ARGUMENT, "pools must be 16-byte aligned, q and out 4-byte aligned");
+  const int G = num_q_heads / num_kv_heads;
+  const int64_t rows = (int64_t)max_query_len * G;
+  const int nw = prefill_warps(rows);
+  const int64_t tiles = ceil_div(rows, 16 * nw);
+  PKV_CHECK(tiles <= 2147483647, PKV_ERR_UNSUPPORTED, "too many query rows");
+  int dev = 0, sms = 0;
+  pkv_status st = device_facts(&dev, &sms);
+  if (st != PKV_OK) return st;
+  pkv::PfParams prm{};
+  st = encode_pool_map(&prm.tmap_k, k_cache, num_blocks, block_size, num_kv_heads, head_dim);
+  if (st != PKV_OK) return st;
+  st = encode_pool_map(&prm.tmap_v, v_cache, num_blocks, block_size, num_kv_heads, head_dim);
+  if (st != PKV_OK) return st;
+  prm.q = static_cast<const __nv_bfloat16*>(q);
+  prm.out = static_cast<__nv_bfloat16*>(out);
+  prm.block_tables = block_tables;
+  prm.cu_seqlens = cu_seqlens;
+  prm.context_lens = context_lens;
+  prm.num_blocks = num_blocks;
+  prm.max_blocks_per_seq = max_blocks_per_seq;
+  prm.num_seqs = num_seqs;
+  prm.num_tokens = num_tokens;
+  prm.max_len = max_context_len;
+  prm.H_q = num_q_heads;
+  prm.G = G;
+  prm.block_size = block_size;
+  prm.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  cudaStream_t strm = as_stream(stream);
+  const int T = (int)tiles;
+  if (head_dim == 128) {
+    if (nw == 1) return PfInst<128, 1>::launch(prm, T, num_kv_heads, num_seqs, strm, dev);
+    if (nw == 2) return PfInst<128, 2>::launch(prm, T, num_kv_heads, num_seqs, strm, dev);
+    return PfInst<128, 4>::launch(prm, T, num_kv_heads, num_seqs, strm, dev);
+  }
+  if (nw == 1) return PfInst<64, 1>::launch(prm, T, num_kv_heads, num_seqs, strm, dev);
+  if (nw == 2) return PfInst<64, 2>::launch(prm, T, num_kv_heads, num_seqs, strm, dev);
+  return PfInst<64, 4>::launch(prm, T, num_kv_heads, num_seqs, strm, dev);
+}
+
+pkv_status pkv_kv_append_varlen(const void* k, const void* v, const int32_t* cu_seqlens,
+                                const int32_t* context_lens, const int32_t* block_tables,
+                                int32_t max_blocks_per_seq, int32_t num_seqs, int32_t num_tokens,
+                                void* k_cache, void* v_cache, int64_t num_blocks,
+                                int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                                pkv_dtype dtype, int64_t* slot_mapping_out, void* stream) {
+  PKV_CHECK(num_seqs >= 0 && num_tokens >= 0 && max_blocks_per_seq >= 1 && num_blocks >= 1 &&
+                block_size >= 1 && num_kv_heads >= 1 && head_dim >= 1 && dtype_ok(dtype),
+            PKV_ERR_INVALID_ARGUMENT, "bad kv_append_varlen sizes");
+  if (num_tokens == 0) return PKV_OK;
+  PKV_CHECK(num_seqs >= 1, PKV_ERR_INVALID_ARGUMENT, "tokens without sequences");
+  PKV_CHECK(k && v && cu_seqlens && context_lens && block_tables && k_cache && v_cache,
+            PKV_ERR_INVALID_ARGUMENT, "null pointer");
+  PKV_CHECK(num_blocks <= INT64_MAX / block_size, PKV_ERR_INVALID_ARGUMENT, "pool too large");
+  const int64_t row = (int64_t)num_kv_heads * head_dim * elem_bytes(dtype);
+  const int vw = vec_width(row, {k, v, k_cache, v_cache});
+  PKV_CHECK(vw >= 2, PKV_ERR_INVALID_ARGUMENT, "misaligned rows");
+  constexpr int threads = 128;
+  const int64_t chunks = ceil_div(row / vw, threads);
+  PKV_CHECK(chunks <= 65535, PKV_ERR_UNSUPPORTED, "rows too long");
+  dim3 grid((unsigned)num_tokens, (unsigned)chunks, 2);
+  cudaStream_t st = as_stream(stream);
+  auto* kb = static_cast<const uint8_t*>(k);
+  auto* vb = static_cast<const uint8_t*>(v);
+  auto* kc = static_cast<uint8_t*>(k_cache);
+  auto* vc = static_cast<uint8_t*>(v_cache);
+#define PKV_APPEND_VARLEN(W)                                                                      \
+  PKV_CUDA(launch_pdl(pkv::kv_append_varlen_kernel<W>, grid, dim3(threads), 0, st, kb, vb,       \
+                      cu_seqlens, context_lens, num_seqs, block_tables, max_blocks_per_seq,     \
+                      block_size, num_blocks, kc, vc, row, slot_mapping_out))
+  switch (vw) {
+    case 16: PKV_APPEND_VARLEN(16); break;
+    case 8: PKV_APPEND_VARLEN(8); break;
+    case 4: PKV_APPEND_VARLEN(4); break;
+    default: PKV_APPEND_VARLEN(2); break;
+  }
+#undef PKV_APPEND_VARLEN
+  return PKV_OK;
 }
 
 pkv_status pkv_get_device_error(int32_t* code, void* stream) {

@@ -110,6 +110,57 @@ __global__ void kv_append_kernel(const uint8_t* __restrict__ k, const uint8_t* _
   *reinterpret_cast<V*>(dst) = __ldg(reinterpret_cast<const V*>(src));
 }
 
+// a1 + a2 for packed new tokens of several sequences (prefill): token i
+// belongs to the sequence s with cu_seqlens[s] <= i < cu_seqlens[s + 1] and
+// sits at position context_lens[s] - n_s + (i - cu_seqlens[s]); its slot
+// comes from that sequence's block-table row.  grid = (tokens, vector chunks,
+// 2).  Tokens whose position is out of range are skipped and reported.
+template <int VW>
+__global__ void kv_append_varlen_kernel(const uint8_t* __restrict__ k,
+                                        const uint8_t* __restrict__ v,
+                                        const int32_t* __restrict__ cu_seqlens,
+                                        const int32_t* __restrict__ context_lens, int32_t num_seqs,
+                                        const int32_t* __restrict__ block_tables,
+                                        int32_t max_blocks_per_seq, int32_t block_size,
+                                        int64_t num_blocks, uint8_t* __restrict__ k_cache,
+                                        uint8_t* __restrict__ v_cache, int64_t row_bytes,
+                                        int64_t* __restrict__ slots) {
+  using V = typename VecT<VW>::T;
+  pdl_wait_primary();
+  pdl_launch_dependents();
+  const int i = blockIdx.x;
+  const int64_t e = (int64_t)blockIdx.y * blockDim.x + threadIdx.x;
+  const bool leader = e == 0 && blockIdx.z == 0;
+  int lo = 0, hi = num_seqs;            // largest s with cu_seqlens[s] <= i
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (cu_seqlens[mid] <= i) lo = mid; else hi = mid;
+  }
+  const int c0 = cu_seqlens[lo], c1 = cu_seqlens[lo + 1];
+  const int pos = context_lens[lo] - (c1 - c0) + (i - c0);
+  int64_t slot = -1;
+  if (i < c0 || i >= c1 || pos < 0) {
+    if (leader) record_error(PKV_DEVERR_POSITION);
+  } else {
+    const int lb = pos / block_size;
+    if (lb >= max_blocks_per_seq) {
+      if (leader) record_error(PKV_DEVERR_POSITION);
+    } else {
+      const int64_t phys = block_tables[(int64_t)lo * max_blocks_per_seq + lb];
+      if (phys < 0 || phys >= num_blocks) {
+        if (leader) record_error(PKV_DEVERR_BLOCK_ID);
+      } else {
+        slot = phys * block_size + (pos - lb * block_size);
+      }
+    }
+  }
+  if (leader && slots != nullptr) slots[i] = slot;
+  if (slot < 0 || e * VW >= row_bytes) return;
+  const uint8_t* src = (blockIdx.z ? v : k) + (int64_t)i * row_bytes + e * VW;
+  uint8_t* dst = (blockIdx.z ? v_cache : k_cache) + slot * row_bytes + e * VW;
+  *reinterpret_cast<V*>(dst) = __ldg(reinterpret_cast<const V*>(src));
+}
+
 // a1 + a2 into a quantized pool.  grid = (tokens, 2 for K/V), 128 threads.
 // FMT 1: e4m3(x / scale) per element (per-tensor scale).  FMT 2: the token's
 // row (all heads) gets scale = max|x| / 127 and codes rint(x / scale), the

@@ -72,6 +72,10 @@ _block_copy = _sig("pkv_kv_block_copy", c_i32, c_vp, c_vp, c_vp, c_i64, c_i64, c
                    c_i32, c_vp)
 _block_swap = _sig("pkv_kv_block_swap", c_i32, c_vp, c_vp, c_i64, c_vp, c_vp, c_i64, c_i64, c_vp,
                    c_i64, c_vp)
+_prefill = _sig("pkv_attention_prefill", c_i32, c_vp, c_vp, c_vp, c_vp, c_i32, c_vp, c_vp, c_i32,
+                c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, c_i64, c_f, c_vp, c_i32, c_vp)
+_append_varlen = _sig("pkv_kv_append_varlen", c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, c_i32,
+                      c_i32, c_vp, c_vp, c_i64, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp)
 _ws_bytes = _sig("pkv_attention_workspace_bytes", c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, c_i32,
                  c_i32, ctypes.POINTER(AttentionConfig), ctypes.POINTER(c_sz))
 _launch_count = _sig("pkv_attention_launch_count", c_i32, c_i32, c_i32, c_i32, c_i32, c_i32,
@@ -104,7 +108,7 @@ EXPORTED = ("pkv_status_string", "pkv_last_error_message", "pkv_version", "pkv_s
             "pkv_attention_launch_count", "pkv_attention_decode",
             "pkv_attention_decode_noalloc", "pkv_kv_append_quant", "pkv_kv_block_copy_quant",
             "pkv_attention_quant_workspace_bytes", "pkv_attention_decode_quant",
-            "pkv_get_device_error")
+            "pkv_attention_prefill", "pkv_kv_append_varlen", "pkv_get_device_error")
 
 
 class PagedKVError(RuntimeError):
@@ -503,4 +507,71 @@ def paged_attention_decode_quant(q: torch.Tensor, k_cache: torch.Tensor, v_cache
                             workspace.numel(), _dtype_code(q), ctypes.byref(quant),
                             ctypes.byref(cfg), _stream(q.device)),
            "pkv_attention_decode_quant")
+    return out
+
+
+# ---------------------------------------------------------------------------
+# multi-query (prefill) attention over the paged cache
+# ---------------------------------------------------------------------------
+
+def paged_kv_append_varlen(k: torch.Tensor, v: torch.Tensor, cu_seqlens: torch.Tensor,
+                           context_lens: torch.Tensor, block_tables: torch.Tensor,
+                           k_cache: torch.Tensor, v_cache: torch.Tensor,
+                           slot_mapping_out: Optional[torch.Tensor] = None) -> None:
+    """Store the packed new tokens (k, v: [T, H_kv, D]) of every sequence at
+    their positions context_lens[s] - n_s + i (slot mapping + write, one
+    launch)."""
+    _need(k_cache, "k_cache", None, 4)
+    _need(v_cache, "v_cache", k_cache.dtype, 4)
+    nb, K, H, D = k_cache.shape
+    _need(k, "k", k_cache.dtype, 3)
+    _need(v, "v", k_cache.dtype, 3)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    _need(context_lens, "context_lens", torch.int32, 1)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    T, S = k.shape[0], context_lens.shape[0]
+    if tuple(k.shape) != (T, H, D) or tuple(v.shape) != (T, H, D) or \
+            cu_seqlens.shape[0] != S + 1 or block_tables.shape[0] != S or \
+            v_cache.shape != k_cache.shape:
+        raise ValueError("inconsistent shapes")
+    sm = None
+    if slot_mapping_out is not None:
+        _need(slot_mapping_out, "slot_mapping_out", torch.int64, 1)
+        sm = _ptr(slot_mapping_out)
+    _check(_append_varlen(_ptr(k), _ptr(v), _ptr(cu_seqlens), _ptr(context_lens),
+                          _ptr(block_tables), block_tables.shape[1], S, T, _ptr(k_cache),
+                          _ptr(v_cache), nb, K, H, D, _dtype_code(k_cache), sm,
+                          _stream(k.device)), "pkv_kv_append_varlen")
+
+
+def paged_attention_prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                            block_tables: torch.Tensor, cu_seqlens: torch.Tensor,
+                            context_lens: torch.Tensor, scale: float, max_query_len: int,
+                            max_context_len: int, out: Optional[torch.Tensor] = None
+                            ) -> torch.Tensor:
+    """Multi-query paged attention: packed queries q [T, H_q, D] of several new
+    tokens per sequence (cu_seqlens int32 [S+1]); token i of n at position
+    context_lens[s] - n + i attends to positions 0 .. itself.  The host bounds
+    max_query_len / max_context_len size the launch."""
+    _need(q, "q", None, 3)
+    _need(k_cache, "k_cache", q.dtype, 4)
+    _need(v_cache, "v_cache", q.dtype, 4)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    _need(context_lens, "context_lens", torch.int32, 1)
+    T, H_q, D = q.shape
+    nb, K, H_kv, D2 = k_cache.shape
+    S = context_lens.shape[0]
+    if D2 != D or v_cache.shape != k_cache.shape or cu_seqlens.shape[0] != S + 1 or \
+            block_tables.shape[0] != S:
+        raise ValueError("inconsistent shapes")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", q.dtype, 3)
+    if tuple(out.shape) != tuple(q.shape):
+        raise ValueError("out must have q's shape")
+    _check(_prefill(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                    block_tables.shape[1], _ptr(cu_seqlens), _ptr(context_lens), S, T,
+                    int(max_query_len), int(max_context_len), H_q, H_kv, D, K, nb, float(scale),
+                    _ptr(out), _dtype_code(q), _stream(q.device)), "pkv_attention_prefill")
     return out

@@ -274,3 +274,75 @@ def materialize(w: Workload, device="cpu", seed: int = 0, canary: bool = True,
         copy_pairs=torch.from_numpy(w.copy_pairs.copy()),
     )
     return {k: v.to(device) for k, v in out.items()}
+
+
+# --------------------------------------------------------------------------
+# multi-query (prefill) workloads
+# --------------------------------------------------------------------------
+
+@dataclass
+class PrefillWorkload:
+    """Sequences with ``prefix[s]`` cached tokens and ``news[s]`` new tokens
+    (queries packed by ``cu_seqlens``); ``context_lens = prefix + news``."""
+    name: str
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    block_size: int
+    num_blocks: int
+    prefix: np.ndarray
+    news: np.ndarray
+    block_tables: np.ndarray
+    scale: float
+
+    @property
+    def context_lens(self) -> np.ndarray:
+        return (self.prefix + self.news).astype(np.int32)
+
+    @property
+    def cu_seqlens(self) -> np.ndarray:
+        return np.concatenate([[0], np.cumsum(self.news)]).astype(np.int32)
+
+    @property
+    def num_seqs(self) -> int:
+        return len(self.news)
+
+    @property
+    def num_tokens(self) -> int:
+        return int(self.news.sum())
+
+
+def build_prefill(name: str, seed: int = 0) -> PrefillWorkload:
+    """``suffix_prefill``: 32 requests that hit a cached prefix of U[1024, 4096]
+    tokens and prefill a 512-token suffix ("推理与 KV Cache 02", 前缀索引与
+    Block Table), Mistral-7B attention shape.  ``speculative_decode``: the
+    Qwen3-0.6B decode batch (64 sequences, U[512, 4096] cached tokens) with 4
+    candidate tokens each ("企业官网建设流程全解析" §8.2)."""
+    rng = np.random.default_rng(20_000 + seed)
+    if name == "suffix_prefill":
+        prefix = rng.integers(1024, 4096 + 1, size=32)
+        news = np.full(32, 512)
+        H_q, H_kv, D, K = 32, 8, 128, 16
+    elif name == "speculative_decode":
+        prefix = rng.integers(512, 4096 + 1, size=64)
+        news = np.full(64, 4)
+        H_q, H_kv, D, K = 16, 8, 128, 16
+    else:
+        raise KeyError(name)
+    lens = prefix + news
+    need = int(sum(-(-int(L) // K) for L in lens))
+    nb = math.ceil(need * 1.25)
+    pool = BlockPool(nb, seed=int(rng.integers(2**31)))
+    rows = []
+    for L in lens:
+        sb = SeqBlocks(pool, K)
+        sb.grow_to(int(L))
+        rows.append(list(sb.mapping))
+    return PrefillWorkload(name=name, num_q_heads=H_q, num_kv_heads=H_kv, head_dim=D,
+                           block_size=K, num_blocks=nb, prefix=prefix.astype(np.int64),
+                           news=news.astype(np.int64),
+                           block_tables=_pad_tables(rows, "garbage", rng),
+                           scale=1.0 / math.sqrt(D))
+
+
+PREFILL_NAMES = ("suffix_prefill", "speculative_decode")
