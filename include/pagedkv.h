@@ -372,6 +372,11 @@ PKV_API pkv_status pkv_attention_decode_quant(
  *   max_query_len: host bound on the new tokens of any sequence (sizes the
  *                  grid); max_context_len: host bound on context_lens.
  *   k_cache, v_cache, block_tables: as pkv_attention_decode.
+ *   config:        NULL or kernel 0 = automatic (tcgen05 tiles of 128 query
+ *                  rows when a KV head has more than 64 rows: max_query_len x
+ *                  num_q_heads / num_kv_heads; mma.sync tiles of 16 / 32 / 64
+ *                  rows otherwise), 1 = tcgen05, 2 = mma.sync; num_splits and
+ *                  reserved fields must be 0.
  * Supported: PKV_BF16, head_dim 64 or 128, block_size 8 or a multiple of 16
  * (else PKV_ERR_UNSUPPORTED).  n = 1 for every sequence is the decode step.
  * Inconsistent counts (n < 0, n > L, cu_seqlens past num_tokens) skip the
@@ -385,7 +390,8 @@ PKV_API pkv_status pkv_attention_prefill(const void* q, const void* k_cache, con
                                          int32_t num_q_heads, int32_t num_kv_heads,
                                          int32_t head_dim, int32_t block_size,
                                          int64_t num_blocks, float scale, void* out,
-                                         pkv_dtype dtype, void* stream);
+                                         pkv_dtype dtype, const pkv_attention_config* config,
+                                         void* stream);
 
 /*
  * a1 + a2 for the packed new tokens of pkv_attention_prefill: token t of

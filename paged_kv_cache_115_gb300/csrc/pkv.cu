@@ -14,6 +14,7 @@
 #include "pkv_attention_simt.cuh"
 #include "pkv_attention_tc.cuh"
 #include "pkv_prefill.cuh"
+#include "pkv_prefill_tc05.cuh"
 #include "pkv_reduce.cuh"
 #include "pkv_copy.cuh"
 #include "pkv_device.cuh"
@@ -286,6 +287,23 @@ struct PfInst {
 };
 template <int D, int NW> std::once_flag PfInst<D, NW>::flags[kMaxDevices];
 template <int D, int NW> cudaError_t PfInst<D, NW>::errs[kMaxDevices];
+
+template <int D>
+struct T5Inst {
+  using C = pkv::T5Cfg<D>;
+  static std::once_flag flags[kMaxDevices];
+  static cudaError_t errs[kMaxDevices];
+  static pkv_status launch(const pkv::PfParams& prm, int tiles, int H_kv, int S, cudaStream_t st,
+                           int dev) {
+    auto k = pkv::attn_prefill_tc05_kernel<D>;
+    pkv_status s = set_smem_once(k, C::SMEM, flags, errs, dev);
+    if (s != PKV_OK) return s;
+    PKV_CUDA(launch_pdl(k, dim3(tiles, H_kv, S), dim3(C::THREADS), (size_t)C::SMEM, st, prm));
+    return PKV_OK;
+  }
+};
+template <int D> std::once_flag T5Inst<D>::flags[kMaxDevices];
+template <int D> cudaError_t T5Inst<D>::errs[kMaxDevices];
 
 // Query rows per KV head and tile: 16 per consumer warp, 1, 2 or 4 warps.
 int prefill_warps(int64_t rows) { return rows <= 16 ? 1 : (rows <= 32 ? 2 : 4); }
@@ -992,7 +1010,13 @@ pkv_status pkv_attention_prefill(const void* q, const void* k_cache, const void*
                                  int32_t max_context_len, int32_t num_q_heads,
                                  int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                                  int64_t num_blocks, float scale, void* out, pkv_dtype dtype,
-                                 void* stream) {
+                                 const pkv_attention_config* config, void* stream) {
+  pkv_attention_config cfg = {};
+  if (config) cfg = *config;
+  bool reserved_zero = cfg.num_splits == 0;
+  for (int r : cfg.reserved) reserved_zero = reserved_zero && r == 0;
+  PKV_CHECK(reserved_zero && cfg.kernel >= 0 && cfg.kernel <= 2, PKV_ERR_INVALID_ARGUMENT,
+            "prefill config: kernel 0, 1 or 2; num_splits and reserved fields 0");
   PKV_CHECK(num_seqs >= 0 && num_tokens >= 0 && max_query_len >= 0 && max_context_len >= 0 &&
                 max_blocks_per_seq >= 1 && num_blocks >= 1 && block_size >= 1 &&
                 num_q_heads >= 1 && num_kv_heads >= 1 && head_dim >= 1 && dtype_ok(dtype),
@@ -1019,8 +1043,11 @@ pkv_status pkv_attention_prefill(const void* q, const void* k_cache, const void*
             PKV_ERR_INVALID_ARGUMENT, "pools must be 16-byte aligned, q and out 4-byte aligned");
   const int G = num_q_heads / num_kv_heads;
   const int64_t rows = (int64_t)max_query_len * G;
+  // tcgen05 tiles of 128 rows once a KV head has more than 64 query rows;
+  // mma.sync tiles of 16 / 32 / 64 rows below that
+  const bool tc05 = cfg.kernel == 1 || (cfg.kernel == 0 && rows > 64);
   const int nw = prefill_warps(rows);
-  const int64_t tiles = ceil_div(rows, 16 * nw);
+  const int64_t tiles = ceil_div(rows, tc05 ? pkv::kT5Rows : 16 * nw);
   PKV_CHECK(tiles <= 2147483647, PKV_ERR_UNSUPPORTED, "too many query rows");
   int dev = 0, sms = 0;
   pkv_status st = device_facts(&dev, &sms);
@@ -1046,6 +1073,10 @@ pkv_status pkv_attention_prefill(const void* q, const void* k_cache, const void*
   prm.scale_log2 = (float)((double)scale * 1.4426950408889634);
   cudaStream_t strm = as_stream(stream);
   const int T = (int)tiles;
+  if (tc05) {
+    if (head_dim == 128) return T5Inst<128>::launch(prm, T, num_kv_heads, num_seqs, strm, dev);
+    return T5Inst<64>::launch(prm, T, num_kv_heads, num_seqs, strm, dev);
+  }
   if (head_dim == 128) {
     if (nw == 1) return PfInst<128, 1>::launch(prm, T, num_kv_heads, num_seqs, strm, dev);
     if (nw == 2) return PfInst<128, 2>::launch(prm, T, num_kv_heads, num_seqs, strm, dev);

@@ -73,7 +73,8 @@ _block_copy = _sig("pkv_kv_block_copy", c_i32, c_vp, c_vp, c_vp, c_i64, c_i64, c
 _block_swap = _sig("pkv_kv_block_swap", c_i32, c_vp, c_vp, c_i64, c_vp, c_vp, c_i64, c_i64, c_vp,
                    c_i64, c_vp)
 _prefill = _sig("pkv_attention_prefill", c_i32, c_vp, c_vp, c_vp, c_vp, c_i32, c_vp, c_vp, c_i32,
-                c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, c_i64, c_f, c_vp, c_i32, c_vp)
+                c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, c_i64, c_f, c_vp, c_i32,
+                ctypes.POINTER(AttentionConfig), c_vp)
 _append_varlen = _sig("pkv_kv_append_varlen", c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, c_i32,
                       c_i32, c_vp, c_vp, c_i64, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp)
 _ws_bytes = _sig("pkv_attention_workspace_bytes", c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, c_i32,
@@ -547,12 +548,13 @@ def paged_kv_append_varlen(k: torch.Tensor, v: torch.Tensor, cu_seqlens: torch.T
 def paged_attention_prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                             block_tables: torch.Tensor, cu_seqlens: torch.Tensor,
                             context_lens: torch.Tensor, scale: float, max_query_len: int,
-                            max_context_len: int, out: Optional[torch.Tensor] = None
-                            ) -> torch.Tensor:
+                            max_context_len: int, out: Optional[torch.Tensor] = None,
+                            kernel: int = 0) -> torch.Tensor:
     """Multi-query paged attention: packed queries q [T, H_q, D] of several new
     tokens per sequence (cu_seqlens int32 [S+1]); token i of n at position
     context_lens[s] - n + i attends to positions 0 .. itself.  The host bounds
-    max_query_len / max_context_len size the launch."""
+    max_query_len / max_context_len size the launch.  ``kernel``: 0 automatic,
+    1 tcgen05 tiles of 128 query rows, 2 mma.sync tiles."""
     _need(q, "q", None, 3)
     _need(k_cache, "k_cache", q.dtype, 4)
     _need(v_cache, "v_cache", q.dtype, 4)
@@ -573,5 +575,6 @@ def paged_attention_prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: tor
     _check(_prefill(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                     block_tables.shape[1], _ptr(cu_seqlens), _ptr(context_lens), S, T,
                     int(max_query_len), int(max_context_len), H_q, H_kv, D, K, nb, float(scale),
-                    _ptr(out), _dtype_code(q), _stream(q.device)), "pkv_attention_prefill")
+                    _ptr(out), _dtype_code(q), ctypes.byref(_cfg(kernel, 0)), _stream(q.device)),
+           "pkv_attention_prefill")
     return out

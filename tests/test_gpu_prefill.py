@@ -75,7 +75,7 @@ def oracle_pools(pb):
     return slots, kc, vc
 
 
-def run_gpu(ops, pb):
+def run_gpu(ops, pb, kernel=0):
     d = {k: pb[k].to(DEV) for k in ("kc", "vc", "q", "k_new", "v_new")}
     bt = torch.from_numpy(pb["bt"]).to(DEV)
     cu = torch.from_numpy(pb["cu"]).to(DEV)
@@ -84,13 +84,13 @@ def run_gpu(ops, pb):
     ops.paged_kv_append_varlen(d["k_new"], d["v_new"], cu, lens, bt, d["kc"], d["vc"], slots)
     out = ops.paged_attention_prefill(d["q"], d["kc"], d["vc"], bt, cu, lens, pb["scale"],
                                       max_query_len=max(pb["max_q"], 1),
-                                      max_context_len=max(max(pb["lens"]), 1))
+                                      max_context_len=max(max(pb["lens"]), 1), kernel=kernel)
     torch.cuda.synchronize()
     return slots, d, out
 
 
-def full_check(ops, pb, what=""):
-    slots, d, out = run_gpu(ops, pb)
+def full_check(ops, pb, what="", kernel=0):
+    slots, d, out = run_gpu(ops, pb, kernel)
     assert ops.get_device_error() == 0
     eslots, ekc, evc = oracle_pools(pb)
     assert np.array_equal(slots.cpu().numpy(), eslots), what
@@ -100,35 +100,40 @@ def full_check(ops, pb, what=""):
     return check_attention(as_f64(out), ref, "bf16", what)
 
 
+@pytest.mark.parametrize("kernel", [1, 2])
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("G", [1, 2, 4, 8])
 @pytest.mark.parametrize("K", [8, 16, 32])
-def test_prefill_shapes(ops, D, G, K):
+def test_prefill_shapes(ops, kernel, D, G, K):
     H_kv = 2
     prefix = [0, 5, 100, 0, 33, 600, 17]
     news = [1, 3, 16, 70, 0, 9, 129]
     pb = prefill_problem(prefix, news, G * H_kv, H_kv, D, K, seed=D + G + K)
-    full_check(ops, pb, f"D={D} G={G} K={K}")
+    full_check(ops, pb, f"kernel={kernel} D={D} G={G} K={K}", kernel)
 
 
-def test_fresh_prompts_and_long_chunks(ops):
+@pytest.mark.parametrize("kernel", [1, 2])
+def test_fresh_prompts_and_long_chunks(ops, kernel):
     # whole prompts (no prefix), one long enough for several query tiles and key tiles
     pb = prefill_problem([0, 0, 0, 0], [1, 15, 300, 513], 32, 8, 128, 16, seed=3)
-    full_check(ops, pb, "fresh prompts")
+    full_check(ops, pb, "fresh prompts", kernel)
 
 
-def test_prefix_hit_suffix(ops):
+@pytest.mark.parametrize("kernel", [1, 2])
+def test_prefix_hit_suffix(ops, kernel):
     # a long cached prefix and a suffix of new tokens (prefix-cache hit)
     pb = prefill_problem([2048, 1000, 4096], [256, 64, 100], 32, 8, 128, 16, seed=4)
-    full_check(ops, pb, "suffix prefill")
+    full_check(ops, pb, "suffix prefill", kernel)
 
 
+@pytest.mark.parametrize("kernel", [0, 1])
 @pytest.mark.parametrize("n", [2, 4, 8])
-def test_speculative_tokens_long_context(ops, n):
-    # a few candidate tokens per sequence over long contexts (one consumer warp)
+def test_speculative_tokens_long_context(ops, n, kernel):
+    # a few candidate tokens per sequence over long contexts (automatic: one
+    # consumer warp; tcgen05: a 128-row tile mostly of padding rows)
     prefix = [3000, 1, 777, 5000, 64]
     pb = prefill_problem(prefix, [n] * len(prefix), 16, 4, 128, 16, seed=n)
-    full_check(ops, pb, f"speculative n={n}")
+    full_check(ops, pb, f"speculative n={n}", kernel)
 
 
 def test_one_new_token_matches_decode(ops):
@@ -178,15 +183,17 @@ def test_chunked_prefill_matches_one_shot(ops):
 def test_empty_sequences_and_bad_counts(ops):
     # sequences with no new tokens produce no rows; the others are unaffected
     pb = prefill_problem([40, 0, 300, 7], [0, 0, 33, 5], 8, 2, 64, 16, seed=9)
-    full_check(ops, pb, "empty members")
+    for kernel in (1, 2):
+        full_check(ops, pb, "empty members", kernel)
     # more new tokens than the context holds: skipped and reported
     d = {k: pb[k].to(DEV) for k in ("kc", "vc", "q")}
     bt = torch.from_numpy(pb["bt"]).to(DEV)
     cu = torch.from_numpy(pb["cu"]).to(DEV)
     bad = torch.tensor([40, 0, 20, 12], dtype=torch.int32, device=DEV)     # 33 new > 20
-    ops.paged_attention_prefill(d["q"], d["kc"], d["vc"], bt, cu, bad, pb["scale"],
-                                max_query_len=33, max_context_len=333)
-    assert ops.get_device_error() == 4
+    for kernel in (1, 2):
+        ops.paged_attention_prefill(d["q"], d["kc"], d["vc"], bt, cu, bad, pb["scale"],
+                                    max_query_len=33, max_context_len=333, kernel=kernel)
+        assert ops.get_device_error() == 4
 
 
 def test_unsupported_shapes_refused(ops):
