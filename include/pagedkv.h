@@ -375,8 +375,9 @@ PKV_API pkv_status pkv_attention_decode_quant(
  *   config:        NULL or kernel 0 = automatic (tcgen05 tiles of 128 query
  *                  rows when a KV head has more than 64 rows: max_query_len x
  *                  num_q_heads / num_kv_heads; mma.sync tiles of 16 / 32 / 64
- *                  rows otherwise), 1 = tcgen05, 2 = mma.sync; num_splits and
- *                  reserved fields must be 0.
+ *                  rows otherwise, or when scale <= 0), 1 = tcgen05 (scale
+ *                  > 0), 2 = mma.sync; num_splits and reserved fields must
+ *                  be 0.
  * Supported: PKV_BF16, head_dim 64 or 128, block_size 8 or a multiple of 16
  * (else PKV_ERR_UNSUPPORTED).  n = 1 for every sequence is the decode step.
  * Inconsistent counts (n < 0, n > L, cu_seqlens past num_tokens) skip the

@@ -1045,7 +1045,10 @@ pkv_status pkv_attention_prefill(const void* q, const void* k_cache, const void*
   const int64_t rows = (int64_t)max_query_len * G;
   // tcgen05 tiles of 128 rows once a KV head has more than 64 query rows;
   // mma.sync tiles of 16 / 32 / 64 rows below that
-  const bool tc05 = cfg.kernel == 1 || (cfg.kernel == 0 && rows > 64);
+  // (the tcgen05 kernel folds a positive scale into its exponent)
+  PKV_CHECK(cfg.kernel != 1 || scale > 0.f, PKV_ERR_UNSUPPORTED,
+            "the tcgen05 prefill kernel needs scale > 0");
+  const bool tc05 = cfg.kernel == 1 || (cfg.kernel == 0 && rows > 64 && scale > 0.f);
   const int nw = prefill_warps(rows);
   const int64_t tiles = ceil_div(rows, tc05 ? pkv::kT5Rows : 16 * nw);
   PKV_CHECK(tiles <= 2147483647, PKV_ERR_UNSUPPORTED, "too many query rows");
