@@ -16,6 +16,7 @@ namespace pkv {
 // Sequences with P <= 1 were finished by the partition kernel.
 // ===========================================================================
 constexpr int kReduceWarps = 8;
+constexpr int kReduceFast = 8;   // partial counts merged with all loads issued at once
 
 template <int V>
 __device__ __forceinline__ void load_f(const float* p, float (&v)[V]) {
@@ -52,6 +53,34 @@ attn_reduce_kernel(Workspace ws, int S, int H_q, T* __restrict__ out) {
     np = ws.pmax;
   }
   const int64_t base = (int64_t)s * ws.pmax * H_q + h;   // partial p at base + p * H_q
+  if (np <= kReduceFast) {
+    // few partials (the common case): the (m, l) pairs and the partial
+    // outputs are all loaded at once, so the merge costs one round trip
+    const float2 ml = lane < np ? ws.ml[base + (int64_t)lane * H_q] : make_float2(-INFINITY, 0.f);
+    float v[kReduceFast][V];
+    const float* o0 = ws.o + base * D + lane * V;
+#pragma unroll
+    for (int u = 0; u < kReduceFast; ++u)
+      if (u < np) load_f<V>(o0 + (int64_t)u * H_q * D, v[u]);
+    const float M = warp_max(ml.x);
+    const float w = lane < np ? exp2f(ml.x - M) : 0.f;
+    const float inv = 1.f / warp_sum(ml.y * w);
+    float acc[V];
+#pragma unroll
+    for (int e = 0; e < V; ++e) acc[e] = 0.f;
+#pragma unroll
+    for (int u = 0; u < kReduceFast; ++u) {
+      const float wu = __shfl_sync(0xffffffffu, w, u) * inv;
+      if (u < np) {
+#pragma unroll
+        for (int e = 0; e < V; ++e) acc[e] = fmaf(wu, v[u][e], acc[e]);
+      }
+    }
+    T* dst = out + ((int64_t)s * H_q + h) * D + lane * V;
+#pragma unroll
+    for (int e = 0; e < V; ++e) dst[e] = from_f32<T>(acc[e]);
+    return;
+  }
   float M = -INFINITY;
   for (int p = lane; p < np; p += 32) M = fmaxf(M, ws.ml[base + (int64_t)p * H_q].x);
   M = warp_max(M);
