@@ -812,8 +812,16 @@ def run_prefill(args):
     def append():
         ops.paged_kv_append_varlen(k_new, v_new, cu, lens, bt, kc, vc)
 
+    ws_bytes = ops.prefill_workspace_bytes(w.num_seqs, T, max_q, max_len, w.num_q_heads,
+                                           w.num_kv_heads, w.head_dim, w.block_size, w.scale,
+                                           torch.bfloat16)
+    workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    # append + attention (+ the merge of key-range partials when the kernel splits keys)
+    launches_per_step = 2 + (1 if ws_bytes > 0 else 0)
+
     def attention():
-        ops.paged_attention_prefill(q, kc, vc, bt, cu, lens, w.scale, max_q, max_len, out=out)
+        ops.paged_attention_prefill(q, kc, vc, bt, cu, lens, w.scale, max_q, max_len, out=out,
+                                    workspace=workspace)
 
     for _ in range(max(args.warmup, 3)):
         append()
@@ -914,7 +922,7 @@ def run_prefill(args):
                 (1e12 if tensor_bound else 1e9),
                 "unit": "TFLOP/s" if tensor_bound else "GB/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": 2 * K,
+        "gpu_launches": launches_per_step * K,
         "clocks": clock_info,
     }
     if not args.no_cpu_baseline:

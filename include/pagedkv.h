@@ -376,12 +376,17 @@ PKV_API pkv_status pkv_attention_decode_quant(
  *                  rows when a KV head has more than 64 rows: max_query_len x
  *                  num_q_heads / num_kv_heads; mma.sync tiles of 16 / 32 / 64
  *                  rows otherwise, or when scale <= 0), 1 = tcgen05 (scale
- *                  > 0), 2 = mma.sync; num_splits and reserved fields must
- *                  be 0.
+ *                  > 0, no split), 2 = mma.sync.  num_splits (mma.sync
+ *                  kernel): 0 = automatic (key ranges of 512 tokens per CTA
+ *                  when the grid would be small), n >= 1 = that many key
+ *                  ranges.  Reserved fields must be 0.
+ *   workspace:     device scratch of pkv_attention_prefill_workspace_bytes
+ *                  bytes (256-byte aligned; may be NULL when that is 0),
+ *                  holding the key-range partials merged by a second launch.
  * Supported: PKV_BF16, head_dim 64 or 128, block_size 8 or a multiple of 16
  * (else PKV_ERR_UNSUPPORTED).  n = 1 for every sequence is the decode step.
  * Inconsistent counts (n < 0, n > L, cu_seqlens past num_tokens) skip the
- * sequence and record PKV_DEVERR_CONTEXT_LEN.  Needs no workspace.
+ * sequence and record PKV_DEVERR_CONTEXT_LEN.
  */
 PKV_API pkv_status pkv_attention_prefill(const void* q, const void* k_cache, const void* v_cache,
                                          const int32_t* block_tables, int32_t max_blocks_per_seq,
@@ -391,8 +396,21 @@ PKV_API pkv_status pkv_attention_prefill(const void* q, const void* k_cache, con
                                          int32_t num_q_heads, int32_t num_kv_heads,
                                          int32_t head_dim, int32_t block_size,
                                          int64_t num_blocks, float scale, void* out,
+                                         void* workspace, size_t workspace_bytes,
                                          pkv_dtype dtype, const pkv_attention_config* config,
                                          void* stream);
+
+/* Workspace bytes of pkv_attention_prefill for these sizes (0 when no key-
+ * range split is used). */
+PKV_API pkv_status pkv_attention_prefill_workspace_bytes(int32_t num_seqs, int32_t num_tokens,
+                                                         int32_t max_query_len,
+                                                         int32_t max_context_len,
+                                                         int32_t num_q_heads,
+                                                         int32_t num_kv_heads, int32_t head_dim,
+                                                         int32_t block_size, float scale,
+                                                         pkv_dtype dtype,
+                                                         const pkv_attention_config* config,
+                                                         size_t* bytes);
 
 /*
  * a1 + a2 for the packed new tokens of pkv_attention_prefill: token t of

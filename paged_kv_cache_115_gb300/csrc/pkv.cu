@@ -308,6 +308,81 @@ template <int D> cudaError_t T5Inst<D>::errs[kMaxDevices];
 // Query rows per KV head and tile: 16 per consumer warp, 1, 2 or 4 warps.
 int prefill_warps(int64_t rows) { return rows <= 16 ? 1 : (rows <= 32 ? 2 : 4); }
 
+struct PrefillPlan {
+  bool tc05 = false;
+  int nw = 1;              // mma.sync kernel: consumer warps (16 rows each)
+  int64_t tiles = 0;       // row tiles per (KV head, sequence)
+  int nsp = 1;             // key-range splits (mma.sync kernel)
+  int split_tiles = 0;     // 64-key tiles per split
+  size_t ws_bytes = 0;
+};
+
+// Validates a multi-query attention call and picks the kernel, the row tiles
+// and, for the mma.sync kernel, the key-range split: when the grid would be
+// under four CTAs per SM and contexts span more than 8 key tiles, every CTA
+// takes 8 tiles (512 keys) and the partials are merged by the split-K reduce.
+pkv_status plan_prefill(int num_seqs, int num_tokens, int max_query_len, int max_context_len,
+                        int H_q, int H_kv, int D, int K, int64_t num_blocks, float scale,
+                        pkv_dtype dtype, const pkv_attention_config* config, PrefillPlan* out) {
+  pkv_attention_config cfg = {};
+  if (config) cfg = *config;
+  bool reserved_zero = true;
+  for (int r : cfg.reserved) reserved_zero = reserved_zero && r == 0;
+  PKV_CHECK(reserved_zero && cfg.kernel >= 0 && cfg.kernel <= 2 && cfg.num_splits >= 0,
+            PKV_ERR_INVALID_ARGUMENT,
+            "prefill config: kernel 0, 1 or 2; num_splits >= 0; reserved fields 0");
+  PKV_CHECK(num_seqs >= 0 && num_tokens >= 0 && max_query_len >= 0 && max_context_len >= 0 &&
+                num_blocks >= 1 && K >= 1 && H_q >= 1 && H_kv >= 1 && D >= 1 && dtype_ok(dtype),
+            PKV_ERR_INVALID_ARGUMENT, "bad prefill sizes");
+  PKV_CHECK(H_q % H_kv == 0, PKV_ERR_INVALID_ARGUMENT,
+            "num_q_heads must be a multiple of num_kv_heads");
+  PKV_CHECK(max_query_len <= max_context_len, PKV_ERR_INVALID_ARGUMENT,
+            "max_query_len above max_context_len");
+  PKV_CHECK(std::isfinite(scale), PKV_ERR_INVALID_ARGUMENT, "scale must be finite");
+  PKV_CHECK(dtype == PKV_BF16 && (D == 64 || D == 128) && (K % 16 == 0 || K == 8),
+            PKV_ERR_UNSUPPORTED,
+            "prefill kernel needs bf16, head_dim 64 or 128, block_size 8 or a multiple of 16");
+  PKV_CHECK(num_blocks <= ((int64_t(1) << 31) - 64) / K, PKV_ERR_UNSUPPORTED,
+            "pool too large for 32-bit tile rows");
+  PKV_CHECK(num_seqs <= 65535 && H_kv <= 65535, PKV_ERR_UNSUPPORTED,
+            "at most 65535 sequences and KV heads per call");
+  // (the tcgen05 kernel folds a positive scale into its exponent and takes
+  // no key-range split)
+  PKV_CHECK(cfg.kernel != 1 || (scale > 0.f && cfg.num_splits <= 1), PKV_ERR_UNSUPPORTED,
+            "the tcgen05 prefill kernel needs scale > 0 and no key-range split");
+  PrefillPlan p;
+  const int64_t rows = (int64_t)max_query_len * (H_q / H_kv);
+  // tcgen05 tiles of 128 rows once a KV head has more than 64 query rows;
+  // mma.sync tiles of 16 / 32 / 64 rows below that
+  p.tc05 = cfg.kernel == 1 || (cfg.kernel == 0 && cfg.num_splits <= 1 && rows > 64 && scale > 0.f);
+  p.nw = prefill_warps(rows);
+  p.tiles = std::max<int64_t>(1, ceil_div(rows, p.tc05 ? pkv::kT5Rows : 16 * p.nw));
+  const int64_t max_tiles = std::max<int64_t>(1, ceil_div(max_context_len, pkv::kPfBN));
+  if (!p.tc05) {
+    if (cfg.num_splits > 0) {
+      const int64_t want = std::min<int64_t>(cfg.num_splits, max_tiles);
+      p.split_tiles = (int)ceil_div(max_tiles, want);
+      p.nsp = (int)ceil_div(max_tiles, p.split_tiles);
+    } else if (max_tiles > 8) {
+      int dev = 0, sms = 0;
+      pkv_status st = device_facts(&dev, &sms);
+      if (st != PKV_OK) return st;
+      if (p.tiles * H_kv * std::max(num_seqs, 1) < 4LL * sms) {
+        p.split_tiles = 8;
+        p.nsp = (int)ceil_div(max_tiles, 8);
+      }
+    }
+  }
+  PKV_CHECK(p.tiles * p.nsp <= 2147483647, PKV_ERR_UNSUPPORTED, "too many query rows");
+  if (p.nsp > 1) {
+    const size_t T = (size_t)num_tokens;
+    p.ws_bytes = align256(T * 4) + align256(T * p.nsp * H_q * sizeof(float2)) +
+                 align256(T * p.nsp * H_q * (size_t)D * sizeof(float));
+  }
+  *out = p;
+  return PKV_OK;
+}
+
 template <int D, int CT>
 pkv_status launch_tc_d(int hpc, const pkv::TcParams& prm, int n, int groups, cudaStream_t st,
                        int dev) {
@@ -1003,37 +1078,38 @@ pkv_status pkv_attention_decode_noalloc(const void* q, const void* k_cache, cons
                               PKV_NOALLOC_SCRATCH_BYTES, dtype, config, stream);
 }
 
+pkv_status pkv_attention_prefill_workspace_bytes(int32_t num_seqs, int32_t num_tokens,
+                                                 int32_t max_query_len, int32_t max_context_len,
+                                                 int32_t num_q_heads, int32_t num_kv_heads,
+                                                 int32_t head_dim, int32_t block_size,
+                                                 float scale, pkv_dtype dtype,
+                                                 const pkv_attention_config* config,
+                                                 size_t* bytes) {
+  PKV_CHECK(bytes != nullptr, PKV_ERR_INVALID_ARGUMENT, "null bytes pointer");
+  PrefillPlan plan;
+  pkv_status st = plan_prefill(num_seqs, num_tokens, max_query_len, max_context_len, num_q_heads,
+                               num_kv_heads, head_dim, block_size, 1, scale, dtype, config,
+                               &plan);
+  if (st != PKV_OK) return st;
+  *bytes = plan.ws_bytes;
+  return PKV_OK;
+}
+
 pkv_status pkv_attention_prefill(const void* q, const void* k_cache, const void* v_cache,
                                  const int32_t* block_tables, int32_t max_blocks_per_seq,
                                  const int32_t* cu_seqlens, const int32_t* context_lens,
                                  int32_t num_seqs, int32_t num_tokens, int32_t max_query_len,
                                  int32_t max_context_len, int32_t num_q_heads,
                                  int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
-                                 int64_t num_blocks, float scale, void* out, pkv_dtype dtype,
+                                 int64_t num_blocks, float scale, void* out, void* workspace,
+                                 size_t workspace_bytes, pkv_dtype dtype,
                                  const pkv_attention_config* config, void* stream) {
-  pkv_attention_config cfg = {};
-  if (config) cfg = *config;
-  bool reserved_zero = cfg.num_splits == 0;
-  for (int r : cfg.reserved) reserved_zero = reserved_zero && r == 0;
-  PKV_CHECK(reserved_zero && cfg.kernel >= 0 && cfg.kernel <= 2, PKV_ERR_INVALID_ARGUMENT,
-            "prefill config: kernel 0, 1 or 2; num_splits and reserved fields 0");
-  PKV_CHECK(num_seqs >= 0 && num_tokens >= 0 && max_query_len >= 0 && max_context_len >= 0 &&
-                max_blocks_per_seq >= 1 && num_blocks >= 1 && block_size >= 1 &&
-                num_q_heads >= 1 && num_kv_heads >= 1 && head_dim >= 1 && dtype_ok(dtype),
-            PKV_ERR_INVALID_ARGUMENT, "bad prefill sizes");
-  PKV_CHECK(num_q_heads % num_kv_heads == 0, PKV_ERR_INVALID_ARGUMENT,
-            "num_q_heads must be a multiple of num_kv_heads");
-  PKV_CHECK(max_query_len <= max_context_len, PKV_ERR_INVALID_ARGUMENT,
-            "max_query_len above max_context_len");
-  PKV_CHECK(std::isfinite(scale), PKV_ERR_INVALID_ARGUMENT, "scale must be finite");
-  PKV_CHECK(dtype == PKV_BF16 && (head_dim == 64 || head_dim == 128) &&
-                (block_size % 16 == 0 || block_size == 8),
-            PKV_ERR_UNSUPPORTED,
-            "prefill kernel needs bf16, head_dim 64 or 128, block_size 8 or a multiple of 16");
-  PKV_CHECK(num_blocks <= ((int64_t(1) << 31) - 64) / block_size, PKV_ERR_UNSUPPORTED,
-            "pool too large for 32-bit tile rows");
-  PKV_CHECK(num_seqs <= 65535 && num_kv_heads <= 65535, PKV_ERR_UNSUPPORTED,
-            "at most 65535 sequences and KV heads per call");
+  PKV_CHECK(max_blocks_per_seq >= 1, PKV_ERR_INVALID_ARGUMENT, "bad prefill sizes");
+  PrefillPlan plan;
+  pkv_status st = plan_prefill(num_seqs, num_tokens, max_query_len, max_context_len, num_q_heads,
+                               num_kv_heads, head_dim, block_size, num_blocks, scale, dtype,
+                               config, &plan);
+  if (st != PKV_OK) return st;
   PKV_CHECK((int64_t)max_blocks_per_seq * block_size <= 2147483647, PKV_ERR_UNSUPPORTED,
             "table row too long");
   if (num_seqs == 0 || num_tokens == 0 || max_query_len == 0) return PKV_OK;
@@ -1041,19 +1117,12 @@ pkv_status pkv_attention_prefill(const void* q, const void* k_cache, const void*
             PKV_ERR_INVALID_ARGUMENT, "null pointer");
   PKV_CHECK(aligned(k_cache, 16) && aligned(v_cache, 16) && aligned(q, 4) && aligned(out, 4),
             PKV_ERR_INVALID_ARGUMENT, "pools must be 16-byte aligned, q and out 4-byte aligned");
-  const int G = num_q_heads / num_kv_heads;
-  const int64_t rows = (int64_t)max_query_len * G;
-  // tcgen05 tiles of 128 rows once a KV head has more than 64 query rows;
-  // mma.sync tiles of 16 / 32 / 64 rows below that
-  // (the tcgen05 kernel folds a positive scale into its exponent)
-  PKV_CHECK(cfg.kernel != 1 || scale > 0.f, PKV_ERR_UNSUPPORTED,
-            "the tcgen05 prefill kernel needs scale > 0");
-  const bool tc05 = cfg.kernel == 1 || (cfg.kernel == 0 && rows > 64 && scale > 0.f);
-  const int nw = prefill_warps(rows);
-  const int64_t tiles = ceil_div(rows, tc05 ? pkv::kT5Rows : 16 * nw);
-  PKV_CHECK(tiles <= 2147483647, PKV_ERR_UNSUPPORTED, "too many query rows");
+  PKV_CHECK(workspace_bytes >= plan.ws_bytes && (plan.ws_bytes == 0 || workspace != nullptr),
+            PKV_ERR_WORKSPACE_TOO_SMALL, "prefill workspace: need %zu bytes", plan.ws_bytes);
+  PKV_CHECK(plan.ws_bytes == 0 || aligned(workspace, 256), PKV_ERR_INVALID_ARGUMENT,
+            "workspace must be 256-byte aligned");
   int dev = 0, sms = 0;
-  pkv_status st = device_facts(&dev, &sms);
+  st = device_facts(&dev, &sms);
   if (st != PKV_OK) return st;
   pkv::PfParams prm{};
   st = encode_pool_map(&prm.tmap_k, k_cache, num_blocks, block_size, num_kv_heads, head_dim);
@@ -1071,23 +1140,40 @@ pkv_status pkv_attention_prefill(const void* q, const void* k_cache, const void*
   prm.num_tokens = num_tokens;
   prm.max_len = max_context_len;
   prm.H_q = num_q_heads;
-  prm.G = G;
+  prm.G = num_q_heads / num_kv_heads;
   prm.block_size = block_size;
   prm.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  prm.num_splits = plan.nsp;
+  prm.split_tiles = plan.split_tiles;
+  if (plan.nsp > 1) {
+    uint8_t* b = static_cast<uint8_t*>(workspace);
+    const size_t T = (size_t)num_tokens;
+    prm.ws.nparts = reinterpret_cast<int*>(b);
+    b += align256(T * 4);
+    prm.ws.ml = reinterpret_cast<float2*>(b);
+    b += align256(T * plan.nsp * num_q_heads * sizeof(float2));
+    prm.ws.o = reinterpret_cast<float*>(b);
+    prm.ws.pmax = plan.nsp;
+  }
   cudaStream_t strm = as_stream(stream);
-  const int T = (int)tiles;
-  if (tc05) {
-    if (head_dim == 128) return T5Inst<128>::launch(prm, T, num_kv_heads, num_seqs, strm, dev);
-    return T5Inst<64>::launch(prm, T, num_kv_heads, num_seqs, strm, dev);
+  const int grid_x = (int)(plan.tiles * plan.nsp);
+  if (plan.tc05) {
+    if (head_dim == 128) return T5Inst<128>::launch(prm, grid_x, num_kv_heads, num_seqs, strm, dev);
+    return T5Inst<64>::launch(prm, grid_x, num_kv_heads, num_seqs, strm, dev);
   }
+  const int nw = plan.nw;
   if (head_dim == 128) {
-    if (nw == 1) return PfInst<128, 1>::launch(prm, T, num_kv_heads, num_seqs, strm, dev);
-    if (nw == 2) return PfInst<128, 2>::launch(prm, T, num_kv_heads, num_seqs, strm, dev);
-    return PfInst<128, 4>::launch(prm, T, num_kv_heads, num_seqs, strm, dev);
+    st = nw == 1 ? PfInst<128, 1>::launch(prm, grid_x, num_kv_heads, num_seqs, strm, dev)
+       : nw == 2 ? PfInst<128, 2>::launch(prm, grid_x, num_kv_heads, num_seqs, strm, dev)
+                 : PfInst<128, 4>::launch(prm, grid_x, num_kv_heads, num_seqs, strm, dev);
+  } else {
+    st = nw == 1 ? PfInst<64, 1>::launch(prm, grid_x, num_kv_heads, num_seqs, strm, dev)
+       : nw == 2 ? PfInst<64, 2>::launch(prm, grid_x, num_kv_heads, num_seqs, strm, dev)
+                 : PfInst<64, 4>::launch(prm, grid_x, num_kv_heads, num_seqs, strm, dev);
   }
-  if (nw == 1) return PfInst<64, 1>::launch(prm, T, num_kv_heads, num_seqs, strm, dev);
-  if (nw == 2) return PfInst<64, 2>::launch(prm, T, num_kv_heads, num_seqs, strm, dev);
-  return PfInst<64, 4>::launch(prm, T, num_kv_heads, num_seqs, strm, dev);
+  if (st != PKV_OK || plan.nsp == 1) return st;
+  // merge the key-range partials of every (token, head)
+  return launch_reduce<__nv_bfloat16>(head_dim, prm.ws, num_tokens, num_q_heads, out, strm);
 }
 
 pkv_status pkv_kv_append_varlen(const void* k, const void* v, const int32_t* cu_seqlens,

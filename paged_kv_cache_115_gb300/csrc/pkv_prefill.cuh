@@ -25,6 +25,7 @@
 // PKV_DEVERR_TIMEOUT when it gives up.
 #pragma once
 
+#include "pkv_attention_common.cuh"
 #include "pkv_device.cuh"
 
 namespace pkv {
@@ -49,6 +50,14 @@ struct PfParams {
   int G;
   int block_size;
   float scale_log2;               // scale * log2(e)
+  // key-range split (mma.sync kernel): num_splits CTAs per row tile, CTA sp
+  // taking key tiles [sp * split_tiles, (sp + 1) * split_tiles); with
+  // num_splits > 1 every CTA writes an (m, l, o) partial per row into ws
+  // (rows indexed by packed token, like sequences in the decode workspace)
+  // and the split-K reduce merges them
+  int num_splits;
+  int split_tiles;
+  Workspace ws;
 };
 
 template <int D, int NW>
@@ -81,7 +90,9 @@ attn_prefill_kernel(const __grid_constant__ PfParams p) {
   const uint32_t bar_empty = bar_full + 8 * kPfStages;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int s = blockIdx.z, j = blockIdx.y;
-  const int tile = gridDim.x - 1 - blockIdx.x;             // heaviest tiles first
+  const int nsp = p.num_splits;
+  const int tix = blockIdx.x / nsp, sp = blockIdx.x - tix * nsp;
+  const int tile = gridDim.x / nsp - 1 - tix;              // heaviest tiles first
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kPfStages; ++i) {
@@ -109,6 +120,9 @@ attn_prefill_kernel(const __grid_constant__ PfParams p) {
   const int i_last = min(R - 1, r0 + C::BM - 1) / G;
   const int pmax = L - n + i_last;              // last key any row of the tile sees
   const int nkt = pmax / kPfBN + 1;
+  // this CTA's key tiles
+  const int kt0 = nsp > 1 ? min(nkt, sp * p.split_tiles) : 0;
+  const int kt1 = nsp > 1 ? min(nkt, kt0 + p.split_tiles) : nkt;
 
   if (warp == NW) {
     // =================== producer ===================
@@ -121,11 +135,11 @@ attn_prefill_kernel(const __grid_constant__ PfParams p) {
     const uint64_t policy = l2_policy_evict_normal();
     const int sbl = K < 16 ? 1 : 0;           // 8-token blocks: two 8-row boxes per 16 rows
     const int ncopy = C::NBOX << sbl;
-    int kt = 0;
+    int k = 0;                                 // ring position: kt - kt0
     bool ok = true;
-    for (; kt < nkt; ++kt) {
-      const int stage = kt % kPfStages;
-      const uint32_t parity = ((kt / kPfStages) & 1) ^ 1;
+    for (int kt = kt0; kt < kt1; ++kt, ++k) {
+      const int stage = k % kPfStages;
+      const uint32_t parity = ((k / kPfStages) & 1) ^ 1;
       if (!mbar_wait_bounded(bar_empty + 8 * stage, parity)) {
         record_error(PKV_DEVERR_TIMEOUT);
         ok = false;
@@ -158,7 +172,7 @@ attn_prefill_kernel(const __grid_constant__ PfParams p) {
     }
     if (!ok) {
       // do not leave the CTA while our own copies may still land in smem
-      for (int kk = max(0, kt - kPfStages); kk < kt; ++kk)
+      for (int kk = max(0, k - kPfStages); kk < k; ++kk)
         mbar_wait_bounded(bar_full + 8 * (kk % kPfStages), (kk / kPfStages) & 1);
     }
     return;
@@ -197,9 +211,9 @@ attn_prefill_kernel(const __grid_constant__ PfParams p) {
   const float sl = p.scale_log2;
   const int mi = lane >> 3, rr = lane & 7;     // ldmatrix: matrix and row of this lane
 
-  for (int kt = 0; kt < nkt; ++kt) {
-    const int stage = kt % kPfStages;
-    if (!mbar_wait_bounded(bar_full + 8 * stage, (kt / kPfStages) & 1)) {
+  for (int kt = kt0; kt < kt1; ++kt) {
+    const int stage = (kt - kt0) % kPfStages;
+    if (!mbar_wait_bounded(bar_full + 8 * stage, ((kt - kt0) / kPfStages) & 1)) {
       record_error(PKV_DEVERR_TIMEOUT);
       return;
     }
@@ -306,6 +320,29 @@ attn_prefill_kernel(const __grid_constant__ PfParams p) {
   la += __shfl_xor_sync(0xffffffffu, la, 2);
   lb += __shfl_xor_sync(0xffffffffu, lb, 1);
   lb += __shfl_xor_sync(0xffffffffu, lb, 2);
+  if (nsp > 1) {
+    // partial state of this key range: unnormalised o, running max m (base
+    // 2), row sum l; an empty range leaves (-inf, 0, 0), which merges as 0
+    if (sp == 0 && t4 == 0) {
+      if (va) p.ws.nparts[q0 + ia] = nsp;
+      if (vb) p.ws.nparts[q0 + ib] = nsp;
+    }
+    if (va) {
+      const int64_t base = ((int64_t)(q0 + ia) * p.ws.pmax + sp) * p.H_q + ha;
+      float2* ob = reinterpret_cast<float2*>(p.ws.o + base * D);
+#pragma unroll
+      for (int dt = 0; dt < D / 8; ++dt) ob[dt * 4 + t4] = make_float2(o[dt][0], o[dt][1]);
+      if (t4 == 0) p.ws.ml[base] = make_float2(ma, la);
+    }
+    if (vb) {
+      const int64_t base = ((int64_t)(q0 + ib) * p.ws.pmax + sp) * p.H_q + hb;
+      float2* ob = reinterpret_cast<float2*>(p.ws.o + base * D);
+#pragma unroll
+      for (int dt = 0; dt < D / 8; ++dt) ob[dt * 4 + t4] = make_float2(o[dt][2], o[dt][3]);
+      if (t4 == 0) p.ws.ml[base] = make_float2(mb, lb);
+    }
+    return;
+  }
   if (va) {
     const float inv = 1.f / la;
     uint32_t* orow = reinterpret_cast<uint32_t*>(p.out + ((int64_t)(q0 + ia) * p.H_q + ha) * D);

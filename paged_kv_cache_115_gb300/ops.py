@@ -73,8 +73,11 @@ _block_copy = _sig("pkv_kv_block_copy", c_i32, c_vp, c_vp, c_vp, c_i64, c_i64, c
 _block_swap = _sig("pkv_kv_block_swap", c_i32, c_vp, c_vp, c_i64, c_vp, c_vp, c_i64, c_i64, c_vp,
                    c_i64, c_vp)
 _prefill = _sig("pkv_attention_prefill", c_i32, c_vp, c_vp, c_vp, c_vp, c_i32, c_vp, c_vp, c_i32,
-                c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, c_i64, c_f, c_vp, c_i32,
-                ctypes.POINTER(AttentionConfig), c_vp)
+                c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, c_i64, c_f, c_vp, c_vp, c_sz,
+                c_i32, ctypes.POINTER(AttentionConfig), c_vp)
+_prefill_ws = _sig("pkv_attention_prefill_workspace_bytes", c_i32, c_i32, c_i32, c_i32, c_i32,
+                   c_i32, c_i32, c_i32, c_i32, c_f, c_i32, ctypes.POINTER(AttentionConfig),
+                   ctypes.POINTER(c_sz))
 _append_varlen = _sig("pkv_kv_append_varlen", c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, c_i32,
                       c_i32, c_vp, c_vp, c_i64, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp)
 _ws_bytes = _sig("pkv_attention_workspace_bytes", c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, c_i32,
@@ -109,7 +112,8 @@ EXPORTED = ("pkv_status_string", "pkv_last_error_message", "pkv_version", "pkv_s
             "pkv_attention_launch_count", "pkv_attention_decode",
             "pkv_attention_decode_noalloc", "pkv_kv_append_quant", "pkv_kv_block_copy_quant",
             "pkv_attention_quant_workspace_bytes", "pkv_attention_decode_quant",
-            "pkv_attention_prefill", "pkv_kv_append_varlen", "pkv_get_device_error")
+            "pkv_attention_prefill", "pkv_attention_prefill_workspace_bytes",
+            "pkv_kv_append_varlen", "pkv_get_device_error")
 
 
 class PagedKVError(RuntimeError):
@@ -549,12 +553,15 @@ def paged_attention_prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: tor
                             block_tables: torch.Tensor, cu_seqlens: torch.Tensor,
                             context_lens: torch.Tensor, scale: float, max_query_len: int,
                             max_context_len: int, out: Optional[torch.Tensor] = None,
-                            kernel: int = 0) -> torch.Tensor:
+                            kernel: int = 0, num_splits: int = 0,
+                            workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
     """Multi-query paged attention: packed queries q [T, H_q, D] of several new
     tokens per sequence (cu_seqlens int32 [S+1]); token i of n at position
     context_lens[s] - n + i attends to positions 0 .. itself.  The host bounds
     max_query_len / max_context_len size the launch.  ``kernel``: 0 automatic,
-    1 tcgen05 tiles of 128 query rows, 2 mma.sync tiles."""
+    1 tcgen05 tiles of 128 query rows, 2 mma.sync tiles; ``num_splits``: key
+    ranges per row tile (mma.sync), 0 automatic.  ``workspace``: uint8 CUDA
+    tensor of :func:`prefill_workspace_bytes` bytes (allocated when None)."""
     _need(q, "q", None, 3)
     _need(k_cache, "k_cache", q.dtype, 4)
     _need(v_cache, "v_cache", q.dtype, 4)
@@ -572,9 +579,27 @@ def paged_attention_prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: tor
     _need(out, "out", q.dtype, 3)
     if tuple(out.shape) != tuple(q.shape):
         raise ValueError("out must have q's shape")
+    cfg = _cfg(kernel, num_splits)
+    need = prefill_workspace_bytes(S, T, max_query_len, max_context_len, H_q, H_kv, D, K,
+                                   scale, q.dtype, kernel, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _need(workspace, "workspace", torch.uint8, 1)
     _check(_prefill(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                     block_tables.shape[1], _ptr(cu_seqlens), _ptr(context_lens), S, T,
                     int(max_query_len), int(max_context_len), H_q, H_kv, D, K, nb, float(scale),
-                    _ptr(out), _dtype_code(q), ctypes.byref(_cfg(kernel, 0)), _stream(q.device)),
-           "pkv_attention_prefill")
+                    _ptr(out), _ptr(workspace), workspace.numel(), _dtype_code(q),
+                    ctypes.byref(cfg), _stream(q.device)), "pkv_attention_prefill")
     return out
+
+
+def prefill_workspace_bytes(num_seqs, num_tokens, max_query_len, max_context_len, num_q_heads,
+                            num_kv_heads, head_dim, block_size, scale, dtype: torch.dtype,
+                            kernel: int = 0, num_splits: int = 0) -> int:
+    out = c_sz(0)
+    code = PKV_BF16 if dtype == torch.bfloat16 else PKV_F32
+    _check(_prefill_ws(num_seqs, num_tokens, int(max_query_len), int(max_context_len),
+                       num_q_heads, num_kv_heads, head_dim, block_size, float(scale), code,
+                       ctypes.byref(_cfg(kernel, num_splits)), ctypes.byref(out)),
+           "pkv_attention_prefill_workspace_bytes")
+    return int(out.value)

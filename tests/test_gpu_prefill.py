@@ -75,7 +75,7 @@ def oracle_pools(pb):
     return slots, kc, vc
 
 
-def run_gpu(ops, pb, kernel=0):
+def run_gpu(ops, pb, kernel=0, num_splits=0):
     d = {k: pb[k].to(DEV) for k in ("kc", "vc", "q", "k_new", "v_new")}
     bt = torch.from_numpy(pb["bt"]).to(DEV)
     cu = torch.from_numpy(pb["cu"]).to(DEV)
@@ -84,13 +84,14 @@ def run_gpu(ops, pb, kernel=0):
     ops.paged_kv_append_varlen(d["k_new"], d["v_new"], cu, lens, bt, d["kc"], d["vc"], slots)
     out = ops.paged_attention_prefill(d["q"], d["kc"], d["vc"], bt, cu, lens, pb["scale"],
                                       max_query_len=max(pb["max_q"], 1),
-                                      max_context_len=max(max(pb["lens"]), 1), kernel=kernel)
+                                      max_context_len=max(max(pb["lens"]), 1), kernel=kernel,
+                                      num_splits=num_splits)
     torch.cuda.synchronize()
     return slots, d, out
 
 
-def full_check(ops, pb, what="", kernel=0):
-    slots, d, out = run_gpu(ops, pb, kernel)
+def full_check(ops, pb, what="", kernel=0, num_splits=0):
+    slots, d, out = run_gpu(ops, pb, kernel, num_splits)
     assert ops.get_device_error() == 0
     eslots, ekc, evc = oracle_pools(pb)
     assert np.array_equal(slots.cpu().numpy(), eslots), what
@@ -204,3 +205,35 @@ def test_unsupported_shapes_refused(ops):
     bt = torch.zeros((1, 2), dtype=torch.int32, device=DEV)
     with pytest.raises(ops.PagedKVError):
         ops.paged_attention_prefill(q, kc, kc, bt, cu, lens, 0.1, 4, 4)
+
+
+@pytest.mark.parametrize("num_splits", [1, 2, 3, 7, 100])
+def test_key_range_splits(ops, num_splits):
+    """The mma.sync kernel with its keys cut into ranges merged by the split-K
+    reduce: any number of ranges gives the oracle's rows (ranges past a tile's
+    last key are empty and merge as zero weight)."""
+    prefix = [3000, 1, 777, 5000, 64, 0]
+    news = [4, 4, 4, 4, 4, 37]
+    pb = prefill_problem(prefix, news, 16, 4, 128, 16, seed=31 + num_splits)
+    full_check(ops, pb, f"splits={num_splits}", kernel=2, num_splits=num_splits)
+
+
+def test_split_workspace_refusals(ops):
+    pb = prefill_problem([3000, 10], [4, 4], 16, 4, 128, 16, seed=5)
+    d = {k: pb[k].to(DEV) for k in ("kc", "vc", "q")}
+    bt = torch.from_numpy(pb["bt"]).to(DEV)
+    cu = torch.from_numpy(pb["cu"]).to(DEV)
+    lens = torch.tensor(pb["lens"], dtype=torch.int32, device=DEV)
+    need = ops.prefill_workspace_bytes(2, 8, 4, 3004, 16, 4, 128, 16, pb["scale"],
+                                       torch.bfloat16, kernel=2, num_splits=6)
+    assert need > 0
+    small = torch.empty(need - 256, dtype=torch.uint8, device=DEV)
+    with pytest.raises(ops.PagedKVError):
+        ops.paged_attention_prefill(d["q"], d["kc"], d["vc"], bt, cu, lens, pb["scale"], 4, 3004,
+                                    kernel=2, num_splits=6, workspace=small)
+    # the tcgen05 kernel takes no split
+    with pytest.raises(ops.PagedKVError):
+        ops.paged_attention_prefill(d["q"], d["kc"], d["vc"], bt, cu, lens, pb["scale"], 4, 3004,
+                                    kernel=1, num_splits=3)
+    assert ops.prefill_workspace_bytes(2, 8, 4, 3004, 16, 4, 128, 16, pb["scale"],
+                                       torch.bfloat16, kernel=1) == 0
