@@ -310,6 +310,8 @@ int prefill_warps(int64_t rows) { return rows <= 16 ? 1 : (rows <= 32 ? 2 : 4); 
 
 struct PrefillPlan {
   bool tc05 = false;
+  bool dec = false;        // stream-K decode kernel with several query rows per sequence
+  AttnPlan ap;             // its plan
   int nw = 1;              // mma.sync kernel: consumer warps (16 rows each)
   int64_t tiles = 0;       // row tiles per (KV head, sequence)
   int nsp = 1;             // key-range splits (mma.sync kernel)
@@ -328,9 +330,9 @@ pkv_status plan_prefill(int num_seqs, int num_tokens, int max_query_len, int max
   if (config) cfg = *config;
   bool reserved_zero = true;
   for (int r : cfg.reserved) reserved_zero = reserved_zero && r == 0;
-  PKV_CHECK(reserved_zero && cfg.kernel >= 0 && cfg.kernel <= 2 && cfg.num_splits >= 0,
+  PKV_CHECK(reserved_zero && cfg.kernel >= 0 && cfg.kernel <= 3 && cfg.num_splits >= 0,
             PKV_ERR_INVALID_ARGUMENT,
-            "prefill config: kernel 0, 1 or 2; num_splits >= 0; reserved fields 0");
+            "prefill config: kernel 0 .. 3; num_splits >= 0; reserved fields 0");
   PKV_CHECK(num_seqs >= 0 && num_tokens >= 0 && max_query_len >= 0 && max_context_len >= 0 &&
                 num_blocks >= 1 && K >= 1 && H_q >= 1 && H_kv >= 1 && D >= 1 && dtype_ok(dtype),
             PKV_ERR_INVALID_ARGUMENT, "bad prefill sizes");
@@ -352,6 +354,26 @@ pkv_status plan_prefill(int num_seqs, int num_tokens, int max_query_len, int max
             "the tcgen05 prefill kernel needs scale > 0 and no key-range split");
   PrefillPlan p;
   const int64_t rows = (int64_t)max_query_len * (H_q / H_kv);
+  // up to 8 query rows per KV head: the stream-K decode kernel, queries as the
+  // 8 score columns of its tensor-core tiles
+  const bool dec_ok = rows <= 8 && num_seqs <= pkv::kTcMaxSeqs &&
+                      tc_shape_ok((int)std::max<int64_t>(rows, 1), D, K, num_blocks, dtype);
+  PKV_CHECK(cfg.kernel != 3 || (dec_ok && cfg.num_splits == 0), PKV_ERR_UNSUPPORTED,
+            "kernel 3 needs at most 8 query rows per KV head (max_query_len x G), at most "
+            "2048 sequences, a tensor-core decode shape, and no key-range split");
+  if (cfg.kernel == 3 || (cfg.kernel == 0 && cfg.num_splits == 0 && dec_ok)) {
+    pkv_attention_config dc = {};
+    dc.kernel = 1;
+    pkv_status st = plan_attention(std::max(num_seqs, 1), H_q, H_kv, D, K, max_context_len,
+                                   num_blocks, dtype, &dc, true, &p.ap);
+    if (st != PKV_OK) return st;
+    p.dec = true;
+    const size_t T = (size_t)num_tokens;
+    p.ws_bytes = align256(T * 4) + align256(T * p.ap.pmax * H_q * sizeof(float2)) +
+                 align256(T * p.ap.pmax * H_q * (size_t)D * sizeof(float));
+    *out = p;
+    return PKV_OK;
+  }
   // tcgen05 tiles of 128 rows once a KV head has more than 64 query rows;
   // mma.sync tiles of 16 / 32 / 64 rows below that
   p.tc05 = cfg.kernel == 1 || (cfg.kernel == 0 && cfg.num_splits <= 1 && rows > 64 && scale > 0.f);
@@ -1143,6 +1165,41 @@ pkv_status pkv_attention_prefill(const void* q, const void* k_cache, const void*
   prm.G = num_q_heads / num_kv_heads;
   prm.block_size = block_size;
   prm.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  if (plan.dec) {
+    // several query rows per sequence through the stream-K decode kernel
+    pkv::TcParams tp;
+    memset(&tp, 0, sizeof(tp));
+    tp.tmap_k = prm.tmap_k;
+    tp.tmap_v = prm.tmap_v;
+    tp.q = prm.q;
+    tp.out = prm.out;
+    tp.block_tables = block_tables;
+    tp.context_lens = context_lens;
+    tp.cu_seqlens = cu_seqlens;
+    uint8_t* b = static_cast<uint8_t*>(workspace);
+    const size_t T = (size_t)num_tokens;
+    tp.ws.nparts = reinterpret_cast<int*>(b);
+    b += align256(T * 4);
+    tp.ws.ml = reinterpret_cast<float2*>(b);
+    b += align256(T * plan.ap.pmax * num_q_heads * sizeof(float2));
+    tp.ws.o = reinterpret_cast<float*>(b);
+    tp.ws.pmax = plan.ap.pmax;
+    tp.num_blocks = num_blocks;
+    tp.max_blocks_per_seq = max_blocks_per_seq;
+    tp.num_seqs = num_seqs;
+    tp.max_len = max_context_len;
+    tp.H_q = num_q_heads;
+    tp.G = num_q_heads / num_kv_heads;
+    tp.block_size = block_size;
+    tp.scale_log2 = prm.scale_log2;
+    cudaStream_t strm = as_stream(stream);
+    st = head_dim == 64
+             ? launch_tc_d<64, 0>(plan.ap.hpc, tp, plan.ap.n_per_group, plan.ap.groups, strm, dev)
+             : launch_tc_d<128, 0>(plan.ap.hpc, tp, plan.ap.n_per_group, plan.ap.groups, strm,
+                                   dev);
+    if (st != PKV_OK || plan.ap.pmax <= 1) return st;
+    return launch_reduce<__nv_bfloat16>(head_dim, tp.ws, num_tokens, num_q_heads, out, strm);
+  }
   prm.num_splits = plan.nsp;
   prm.split_tiles = plan.split_tiles;
   if (plan.nsp > 1) {

@@ -61,6 +61,12 @@ struct TcParams {
   float v_scale;            // FP8: scale of the V pool
   const float* k_ts;        // INT8: per-slot scales
   const float* v_ts;
+  // several query tokens per sequence (bf16 pools): sequence s owns query
+  // rows cu_seqlens[s] .. cu_seqlens[s+1]-1; its new token i of n sits at
+  // position len - n + i and is score column i * G + (head in group), so
+  // n * G <= 8.  Outputs and partials are indexed by query row.  nullptr:
+  // one query per sequence, row s (decode).
+  const int32_t* cu_seqlens;
 };
 
 // Pool formats of the kernel: CT 0 = bf16, 1 = FP8 e4m3 (per-tensor scale),
@@ -128,6 +134,19 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
   const int S = p.num_seqs;
   const int K = p.block_size;
   const int row_tokens = p.max_blocks_per_seq * K;
+  // chunks of sequence s (none for a sequence without query rows)
+  auto nchunks = [&](int s) -> int {
+    const int L = effective_len(p.context_lens[s], p.max_len, row_tokens);
+    if (p.cu_seqlens != nullptr) {
+      const int nq = p.cu_seqlens[s + 1] - p.cu_seqlens[s];
+      if (nq < 0 || nq > L) {
+        record_error(PKV_DEVERR_CONTEXT_LEN);
+        return 0;
+      }
+      if (nq == 0) return 0;
+    }
+    return (L + CH - 1) / CH;
+  };
 
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
@@ -143,8 +162,7 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
     const int per = (S + C::THREADS - 1) / C::THREADS;
     const int a = min(S, tid * per), b = min(S, a + per);
     int local = 0;
-    for (int s = a; s < b; ++s)
-      local += (effective_len(p.context_lens[s], p.max_len, row_tokens) + CH - 1) / CH;
+    for (int s = a; s < b; ++s) local += nchunks(s);
     int incl = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -166,7 +184,7 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
     int run = (warp ? s_wsum[warp - 1] : 0) + incl - local;
     for (int s = a; s < b; ++s) {
       cstart[s] = run;
-      run += (effective_len(p.context_lens[s], p.max_len, row_tokens) + CH - 1) / CH;
+      run += nchunks(s);
     }
     if (tid == C::THREADS - 1) cstart[S] = run;
     __syncthreads();
@@ -188,15 +206,24 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
   for (int s = tid; s < S; s += C::THREADS) {
     const int a = cstart[s], b = cstart[s + 1];
     if (a == b) {
+      // empty context: zero output (decode); a sequence without query rows
+      // has no output
       const int owner = a < T ? cta_of_chunk(a, T, n) : n - 1;
-      if (owner == cta) {
+      if (owner == cta && p.cu_seqlens == nullptr) {
         if (group == 0) p.ws.nparts[s] = 0;
         __nv_bfloat16* o = p.out + ((int64_t)s * H_q + head0 * G) * D;
         for (int i = 0; i < HPC * G * D; ++i) o[i] = __float2bfloat16_rn(0.f);
       }
     } else if (group == 0) {
       const int first = cta_of_chunk(a, T, n);
-      if (first == cta) p.ws.nparts[s] = cta_of_chunk(b - 1, T, n) - first + 1;
+      if (first == cta) {
+        const int np = cta_of_chunk(b - 1, T, n) - first + 1;
+        if (p.cu_seqlens == nullptr) {
+          p.ws.nparts[s] = np;
+        } else {
+          for (int r = p.cu_seqlens[s]; r < p.cu_seqlens[s + 1]; ++r) p.ws.nparts[r] = np;
+        }
+      }
     }
   }
   if (cb >= ce) return;
@@ -311,6 +338,10 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
   int s = seq_of_chunk(cstart, S, cb);
   int len_s = 0;
+  // this thread's score columns 2tq and 2tq+1: their query rows (-1: padding
+  // column) and last visible key positions
+  int64_t rowA = -1, rowB = -1;
+  int limA = 0, limB = 0;
   int k = 0;
   for (int c = cb; c < ce; ++c, ++k) {
     while (c >= cstart[s + 1]) ++s;
@@ -318,11 +349,21 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
     if (c == cb || c == a) {
       // ---- new partition: load the q-group as the B fragments of Q^T
       len_s = effective_len(p.context_lens[s], p.max_len, row_tokens);
-      const __nv_bfloat16* qrow = p.q + ((int64_t)s * H_q + j * G + g) * D;
+      const int qr0 = p.cu_seqlens ? p.cu_seqlens[s] : s;           // first query row
+      const int nq = p.cu_seqlens ? p.cu_seqlens[s + 1] - qr0 : 1;  // query rows
+      const int ncol = nq * G;                                     // valid score columns
+      const int cA = 2 * tq, cB = 2 * tq + 1;
+      rowA = cA < ncol ? (int64_t)(qr0 + cA / G) * H_q + j * G + cA % G : -1;
+      rowB = cB < ncol ? (int64_t)(qr0 + cB / G) * H_q + j * G + cB % G : -1;
+      limA = cA < ncol ? len_s - nq + cA / G : len_s - 1;
+      limB = cB < ncol ? len_s - nq + cB / G : len_s - 1;
+      // this lane's B-fragment column g
+      const __nv_bfloat16* qrow =
+          p.q + ((int64_t)(qr0 + (g < ncol ? g / G : 0)) * H_q + j * G + g % G) * D;
       if constexpr (CT == 0) {
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          if (g < G) {
+          if (g < ncol) {
             qf[ks][0] = __ldg(reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 2 * tq));
             qf[ks][1] = __ldg(reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 8 + 2 * tq));
           } else {
@@ -465,8 +506,12 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
       x[t][1] = sacc[t][1] * slc1 * ksr[t][0];
       x[t][2] = sacc[t][2] * slc0 * ksr[t][1];
       x[t][3] = sacc[t][3] * slc1 * ksr[t][1];
-      if (t * kTile + g >= valid) x[t][0] = x[t][1] = -INFINITY;
-      if (t * kTile + g + 8 >= valid) x[t][2] = x[t][3] = -INFINITY;
+      // causal limit of each score column (decode: the sequence end)
+      const int kp = (c - a) * CH + t * kTile + g;     // key position of row g
+      if (kp > limA) x[t][0] = -INFINITY;
+      if (kp > limB) x[t][1] = -INFINITY;
+      if (kp + 8 > limA) x[t][2] = -INFINITY;
+      if (kp + 8 > limB) x[t][3] = -INFINITY;
       mx0 = fmaxf(mx0, fmaxf(x[t][0], x[t][2]));
       mx1 = fmaxf(mx1, fmaxf(x[t][1], x[t][3]));
     }
@@ -476,15 +521,18 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
       mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
     }
     const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
+    // a column may have seen no visible key yet (several query rows): keep
+    // its state (-inf, 0, 0) instead of forming -inf - -inf
+    const float mu0 = mn0 == -INFINITY ? 0.f : mn0, mu1 = mn1 == -INFINITY ? 0.f : mn1;
+    const float al0 = exp2f(m0 - mu0), al1 = exp2f(m1 - mu1);
     float pr[TL][4];
     float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
     for (int t = 0; t < TL; ++t) {
-      pr[t][0] = exp2f(x[t][0] - mn0);
-      pr[t][1] = exp2f(x[t][1] - mn1);
-      pr[t][2] = exp2f(x[t][2] - mn0);
-      pr[t][3] = exp2f(x[t][3] - mn1);
+      pr[t][0] = exp2f(x[t][0] - mu0);
+      pr[t][1] = exp2f(x[t][1] - mu1);
+      pr[t][2] = exp2f(x[t][2] - mu0);
+      pr[t][3] = exp2f(x[t][3] - mu1);
       ps0 += pr[t][0] + pr[t][2];
       ps1 += pr[t][1] + pr[t][3];
     }
@@ -594,43 +642,46 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
       const int first = cta_of_chunk(a, T, n);
       const int np = cta_of_chunk(b - 1, T, n) - first + 1;
       const int part = cta - first;
-      const int n0 = 2 * tq, n1 = 2 * tq + 1;
       if (np == 1) {
         const float i0 = 1.f / lt0, i1 = 1.f / lt1;
-        __nv_bfloat16* orow = p.out + ((int64_t)s * H_q + j * G) * D;
+        __nv_bfloat16* oa = p.out + (rowA >= 0 ? rowA : 0) * D;
+        __nv_bfloat16* obb = p.out + (rowB >= 0 ? rowB : 0) * D;
 #pragma unroll
         for (int mt = 0; mt < D / 16; ++mt) {
           // O^T rows g and g+8 of tile mt are d0 and d1 (see the PV product)
           const int d0 = CT == 0 ? mt * 16 + g : mt * 16 + 2 * g;
           const int d1 = CT == 0 ? d0 + 8 : d0 + 1;
-          if (n0 < G) {
-            orow[n0 * D + d0] = __float2bfloat16_rn(o[mt][0] * i0);
-            orow[n0 * D + d1] = __float2bfloat16_rn(o[mt][2] * i0);
+          if (rowA >= 0) {
+            oa[d0] = __float2bfloat16_rn(o[mt][0] * i0);
+            oa[d1] = __float2bfloat16_rn(o[mt][2] * i0);
           }
-          if (n1 < G) {
-            orow[n1 * D + d0] = __float2bfloat16_rn(o[mt][1] * i1);
-            orow[n1 * D + d1] = __float2bfloat16_rn(o[mt][3] * i1);
+          if (rowB >= 0) {
+            obb[d0] = __float2bfloat16_rn(o[mt][1] * i1);
+            obb[d1] = __float2bfloat16_rn(o[mt][3] * i1);
           }
         }
       } else if (part < p.ws.pmax) {
-        const int64_t base = ((int64_t)s * p.ws.pmax + part) * H_q + j * G;
-        float* ob = p.ws.o + base * D;
+        // partial of (query row, head) at ((row * Pmax + part) * H_q + head)
+        const int64_t pa = rowA >= 0 ? (rowA / H_q * p.ws.pmax + part) * H_q + rowA % H_q : 0;
+        const int64_t pb = rowB >= 0 ? (rowB / H_q * p.ws.pmax + part) * H_q + rowB % H_q : 0;
+        float* oa = p.ws.o + pa * D;
+        float* obb = p.ws.o + pb * D;
 #pragma unroll
         for (int mt = 0; mt < D / 16; ++mt) {
           const int d0 = CT == 0 ? mt * 16 + g : mt * 16 + 2 * g;
           const int d1 = CT == 0 ? d0 + 8 : d0 + 1;
-          if (n0 < G) {
-            ob[n0 * D + d0] = o[mt][0];
-            ob[n0 * D + d1] = o[mt][2];
+          if (rowA >= 0) {
+            oa[d0] = o[mt][0];
+            oa[d1] = o[mt][2];
           }
-          if (n1 < G) {
-            ob[n1 * D + d0] = o[mt][1];
-            ob[n1 * D + d1] = o[mt][3];
+          if (rowB >= 0) {
+            obb[d0] = o[mt][1];
+            obb[d1] = o[mt][3];
           }
         }
         if (g == 0) {
-          if (n0 < G) p.ws.ml[base + n0] = make_float2(m0, lt0);
-          if (n1 < G) p.ws.ml[base + n1] = make_float2(m1, lt1);
+          if (rowA >= 0) p.ws.ml[pa] = make_float2(m0, lt0);
+          if (rowB >= 0) p.ws.ml[pb] = make_float2(m1, lt1);
         }
       }
     }

@@ -559,7 +559,8 @@ def paged_attention_prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: tor
     tokens per sequence (cu_seqlens int32 [S+1]); token i of n at position
     context_lens[s] - n + i attends to positions 0 .. itself.  The host bounds
     max_query_len / max_context_len size the launch.  ``kernel``: 0 automatic,
-    1 tcgen05 tiles of 128 query rows, 2 mma.sync tiles; ``num_splits``: key
+    1 tcgen05 tiles of 128 query rows, 2 mma.sync tiles, 3 the stream-K decode
+    kernel (at most 8 query rows per KV head); ``num_splits``: key
     ranges per row tile (mma.sync), 0 automatic.  ``workspace``: uint8 CUDA
     tensor of :func:`prefill_workspace_bytes` bytes (allocated when None)."""
     _need(q, "q", None, 3)

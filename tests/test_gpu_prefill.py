@@ -237,3 +237,34 @@ def test_split_workspace_refusals(ops):
                                     kernel=1, num_splits=3)
     assert ops.prefill_workspace_bytes(2, 8, 4, 3004, 16, 4, 128, 16, pb["scale"],
                                        torch.bfloat16, kernel=1) == 0
+
+
+@pytest.mark.parametrize("K", [8, 16, 32])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("G,n", [(1, 8), (2, 4), (4, 2), (8, 1), (2, 3), (1, 5)])
+def test_multi_token_decode_kernel(ops, K, D, G, n):
+    """Several query tokens per sequence through the stream-K decode kernel
+    (queries as the score columns of its tiles, a causal limit per column):
+    short and long contexts, sequences with fewer or no new tokens."""
+    H_kv = 2
+    prefix = [0, 3, 40, 700, 16, 1500, 9, 250]
+    news = [n, n, max(n - 1, 0), n, 0, n, 1, n]
+    news[0] = n                         # a fresh prompt of n tokens
+    pb = prefill_problem(prefix, news, G * H_kv, H_kv, D, K, seed=K + D + 3 * G + n)
+    full_check(ops, pb, f"decode kernel K={K} D={D} G={G} n={n}", kernel=3)
+
+
+def test_multi_token_decode_kernel_counts(ops):
+    # more new tokens than the context holds: skipped and reported
+    pb = prefill_problem([40, 10], [2, 2], 8, 2, 128, 16, seed=2)
+    d = {k: pb[k].to(DEV) for k in ("kc", "vc", "q")}
+    bt = torch.from_numpy(pb["bt"]).to(DEV)
+    cu = torch.from_numpy(pb["cu"]).to(DEV)
+    bad = torch.tensor([42, 1], dtype=torch.int32, device=DEV)
+    ops.paged_attention_prefill(d["q"], d["kc"], d["vc"], bt, cu, bad, pb["scale"], 2, 42,
+                                kernel=3)
+    assert ops.get_device_error() == 4
+    # more than 8 rows per KV head is refused for this kernel
+    with pytest.raises(ops.PagedKVError):
+        ops.paged_attention_prefill(d["q"], d["kc"], d["vc"], bt, cu, bad, pb["scale"], 5, 42,
+                                    kernel=3)
