@@ -498,6 +498,7 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
       }
     }
     // ---- online softmax on (tok 16t+g / 16t+g+8) x (head 2tq / 2tq+1)
+    const bool cmask = (c - a) * CH + CH - 1 > min(limA, limB);
     float x[TL][4];
     float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
@@ -506,12 +507,15 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
       x[t][1] = sacc[t][1] * slc1 * ksr[t][0];
       x[t][2] = sacc[t][2] * slc0 * ksr[t][1];
       x[t][3] = sacc[t][3] * slc1 * ksr[t][1];
-      // causal limit of each score column (decode: the sequence end)
-      const int kp = (c - a) * CH + t * kTile + g;     // key position of row g
-      if (kp > limA) x[t][0] = -INFINITY;
-      if (kp > limB) x[t][1] = -INFINITY;
-      if (kp + 8 > limA) x[t][2] = -INFINITY;
-      if (kp + 8 > limB) x[t][3] = -INFINITY;
+      // causal limit of each score column (decode: the sequence end); a
+      // chunk wholly below both limits needs no mask
+      if (cmask) {
+        const int kp = (c - a) * CH + t * kTile + g;   // key position of row g
+        if (kp > limA) x[t][0] = -INFINITY;
+        if (kp > limB) x[t][1] = -INFINITY;
+        if (kp + 8 > limA) x[t][2] = -INFINITY;
+        if (kp + 8 > limB) x[t][3] = -INFINITY;
+      }
       mx0 = fmaxf(mx0, fmaxf(x[t][0], x[t][2]));
       mx1 = fmaxf(mx1, fmaxf(x[t][1], x[t][3]));
     }
