@@ -152,3 +152,69 @@ def test_block_sizes_give_the_same_attention(ops):
         outs[K] = as_f64(out)
     for K in (16, 32, 64):
         check_attention(outs[K], outs[8], "bf16", f"K={K} vs K=8")
+
+
+@pytest.mark.parametrize("news", [[3, 3, 2, 3], [40, 200, 7, 130]])
+def test_graph_replay_multi_query(ops, news):
+    """A packed multi-query step (KV append of the new tokens + attention)
+    captured once and replayed: speculative tokens take the stream-K decode
+    kernel, longer chunks the tcgen05 kernel; replay equals eager launches."""
+    import math
+    from paged_kv_cache_115_gb300.blockmgr import BlockPool, SeqBlocks
+    H_q, H_kv, D, K = 16, 8, 128, 16
+    prefix = [500, 33, 1200, 64]
+    lens = [a + b for a, b in zip(prefix, news)]
+    pool = BlockPool(sum(-(-L // K) for L in lens) + 4, seed=7)
+    rows = []
+    for L in lens:
+        sb = SeqBlocks(pool, K)
+        sb.grow_to(L)
+        rows.append(sb.mapping)
+    bt = np.zeros((4, max(len(r) for r in rows)), np.int32)
+    for i, r in enumerate(rows):
+        bt[i, :len(r)] = r
+    g = torch.Generator().manual_seed(1)
+    nb = pool.num_blocks
+    T = sum(news)
+    t = dict(kc=torch.randn((nb, K, H_kv, D), generator=g).to(torch.bfloat16),
+             vc=torch.randn((nb, K, H_kv, D), generator=g).to(torch.bfloat16),
+             q=torch.randn((T, H_q, D), generator=g).to(torch.bfloat16),
+             k=torch.randn((T, H_kv, D), generator=g).to(torch.bfloat16),
+             v=torch.randn((T, H_kv, D), generator=g).to(torch.bfloat16))
+    d = {k_: v_.to(DEV) for k_, v_ in t.items()}
+    bt_d = torch.from_numpy(bt).to(DEV)
+    cu = torch.tensor([0] + list(np.cumsum(news)), dtype=torch.int32, device=DEV)
+    cl = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    scale = 1.0 / math.sqrt(D)
+    need = ops.prefill_workspace_bytes(4, T, max(news), max(lens), H_q, H_kv, D, K, scale,
+                                       torch.bfloat16)
+    ws = torch.empty(max(need, 256), dtype=torch.uint8, device=DEV)
+    out = torch.empty_like(d["q"])
+
+    def step(x, o):
+        ops.paged_kv_append_varlen(x["k"], x["v"], cu, cl, bt_d, x["kc"], x["vc"])
+        ops.paged_attention_prefill(x["q"], x["kc"], x["vc"], bt_d, cu, cl, scale, max(news),
+                                    max(lens), out=o, workspace=ws)
+
+    scratch = {k_: v_.clone() for k_, v_ in d.items()}
+    step(scratch, torch.empty_like(out))
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            step(d, out)
+    torch.cuda.current_stream().wait_stream(side)
+    gen = torch.Generator().manual_seed(2)
+    for it in range(2):
+        for name in ("q", "k", "v"):
+            d[name].copy_(torch.randn(d[name].shape, generator=gen).to(torch.bfloat16))
+        eager = {k_: v_.clone() for k_, v_ in d.items()}
+        eager_out = torch.empty_like(out)
+        step(eager, eager_out)
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), eager_out.view(torch.int16)), it
+        assert torch.equal(d["kc"].view(torch.int16), eager["kc"].view(torch.int16))
+    assert ops.get_device_error() == 0
