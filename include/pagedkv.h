@@ -372,14 +372,15 @@ PKV_API pkv_status pkv_attention_decode_quant(
  *   max_query_len: host bound on the new tokens of any sequence (sizes the
  *                  grid); max_context_len: host bound on context_lens.
  *   k_cache, v_cache, block_tables: as pkv_attention_decode.
- *   config:        NULL or kernel 0 = automatic (tcgen05 tiles of 128 query
- *                  rows when a KV head has more than 64 rows: max_query_len x
- *                  num_q_heads / num_kv_heads; mma.sync tiles of 16 / 32 / 64
- *                  rows otherwise, or when scale <= 0; the stream-K decode
- *                  kernel when a KV head has at most 8 rows), 1 = tcgen05
- *                  (scale > 0, no split), 2 = mma.sync, 3 = stream-K decode
- *                  kernel (at most 8 rows per KV head, at most 2048
- *                  sequences, no split).  num_splits (mma.sync
+ *   config:        NULL or kernel 0 = automatic, by the query rows of one
+ *                  KV head (max_query_len x num_q_heads / num_kv_heads): up
+ *                  to 8 -> the stream-K decode kernel; 9 .. 64, or scale <= 0
+ *                  -> mma.sync tiles of 16 / 32 / 64 rows; more -> tcgen05
+ *                  tiles of 128 rows (two per CTA, sharing every K/V tile,
+ *                  above 128 rows).  1 = tcgen05 (scale > 0, no split),
+ *                  2 = mma.sync, 3 = stream-K decode kernel (at most 8 rows
+ *                  per KV head, at most 2048 sequences, no split).
+ *                  num_splits (mma.sync
  *                  kernel): 0 = automatic (key ranges of 512 tokens per CTA
  *                  when the grid would be small), n >= 1 = that many key
  *                  ranges.  Reserved fields must be 0.

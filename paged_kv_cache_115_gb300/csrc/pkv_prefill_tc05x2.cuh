@@ -1,0 +1,402 @@
+// Multi-query paged attention on tcgen05 with two 128-row query tiles per CTA.
+// Same function as attn_prefill_kernel / attn_prefill_tc05_kernel (new token
+// i of n at position len - n + i attends to positions 0 .. itself).
+//
+// The two query tiles (A: rows r0 .. r0+127, B: the next 128 rows of the same
+// KV head and sequence) share every K and V tile: one TMA load feeds
+// S_A = Q_A K^T and S_B = Q_B K^T, and O_A += P_A V, O_B += P_B V.  Each tile
+// has its own softmax warpgroup, its own two S buffers and its own O in TMEM
+// (4 x 128 = 512 columns), so the softmax of one tile runs while the tensor
+// cores work on the other.
+//
+// Warps 0-3: softmax / epilogue of tile A, warps 4-7: of tile B (one thread
+// per query row = TMEM lane, a full 64-key tile per thread).  Warp 8: TMA
+// producer of K tiles (3-deep ring); warp 10: of V tiles (3-deep ring).
+// Warp 9: TMEM allocation and, on one lane, the S = Q K^T issue for both
+// tiles (up to two tiles ahead per query tile); warp 11, one lane: the
+// O += P V issue.  P (split hi + lo bf16) has one shared-memory buffer per
+// query tile.  The exponent base of a row is raised only when its maximum
+// grows by more than 2^8 (O rescaled in TMEM rarely).  Every wait is bounded
+// and records PKV_DEVERR_TIMEOUT; TMEM is freed on every path after both
+// issuing threads have seen their MMAs complete.
+#pragma once
+
+#include "pkv_prefill_tc05.cuh"
+
+namespace pkv {
+
+constexpr int kX2KStages = 3;
+constexpr int kX2VStages = 3;
+
+template <int D>
+struct X2Cfg {
+  static constexpr int NH = D / 64;
+  static constexpr int QHALF = kT5Rows * 128;             // 16 KiB
+  static constexpr int QBYTES = NH * QHALF;               // one query tile
+  static constexpr int KVHALF = kPfBN * 128;              // 8 KiB
+  static constexpr int KBYTES = NH * KVHALF;              // one K (or V) tile
+  static constexpr int NBOX = NH * (kPfBN / 16);
+  static constexpr int PBUF = kT5Rows * 128;              // 128 rows x 64 keys bf16
+  static constexpr int Q_OFF = 0;                         // [tile][half]
+  static constexpr int K_OFF = 2 * QBYTES;
+  static constexpr int V_OFF = K_OFF + kX2KStages * KBYTES;
+  static constexpr int P_OFF = V_OFF + kX2VStages * KBYTES;   // [tile][hi, lo]
+  static constexpr int BAR_OFF = P_OFF + 4 * PBUF;
+  // k_full/k_empty[KS], v_full/v_empty[VS], per tile: s_full[2], s_free[2],
+  // p_full, o_done, q_full; mma_idle
+  static constexpr int NBAR = 2 * (kX2KStages + kX2VStages) + 2 * 7 + 1;
+  static constexpr int SLOT_OFF = BAR_OFF + 8 * NBAR;
+  static constexpr int SMEM = SLOT_OFF + 16 + 1024;
+  static constexpr int THREADS = 384;
+  static constexpr uint32_t TMEM_COLS = 512;              // per tile: S0 S1 (128), O (128)
+  static constexpr uint32_t IDESC_QK = umma_idesc_bf16(kT5Rows, kPfBN, 0, 0);
+  static constexpr uint32_t IDESC_PV = umma_idesc_bf16(kT5Rows, D, 0, 1);
+};
+
+template <int D>
+__global__ void __launch_bounds__(X2Cfg<D>::THREADS, 1)
+attn_prefill_tc05x2_kernel(const __grid_constant__ PfParams p) {
+  using C = X2Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bars = sbase + C::BAR_OFF;
+  const uint32_t k_full = bars, k_empty = k_full + 8 * kX2KStages;
+  const uint32_t v_full = k_empty + 8 * kX2KStages, v_empty = v_full + 8 * kX2VStages;
+  const uint32_t tb0 = v_empty + 8 * kX2VStages;          // per-tile barriers, 7 each
+  auto s_full = [&](int x, int b) { return tb0 + 56 * x + 8 * b; };
+  auto s_free = [&](int x, int b) { return tb0 + 56 * x + 16 + 8 * b; };
+  auto p_full = [&](int x) { return tb0 + 56 * x + 32; };
+  auto o_done = [&](int x) { return tb0 + 56 * x + 40; };
+  auto q_full = [&](int x) { return tb0 + 56 * x + 48; };
+  const uint32_t mma_idle = tb0 + 112;
+  uint32_t* slot = reinterpret_cast<uint32_t*>(smem + C::SLOT_OFF);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int s = blockIdx.z, j = blockIdx.y;
+  const int pair = gridDim.x - 1 - blockIdx.x;             // heaviest tile pairs first
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kX2KStages; ++i) {
+      mbar_init(k_full + 8 * i, 1);
+      mbar_init(k_empty + 8 * i, 2);                      // S_A and S_B both read K
+    }
+    for (int i = 0; i < kX2VStages; ++i) {
+      mbar_init(v_full + 8 * i, 1);
+      mbar_init(v_empty + 8 * i, 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(s_full(x, b), 1);
+        mbar_init(s_free(x, b), kT5Rows);
+      }
+      mbar_init(p_full(x), kT5Rows);
+      mbar_init(o_done(x), 1);
+      mbar_init(q_full(x), kT5Rows);
+    }
+    mbar_init(mma_idle, 2);
+    fence_barrier_init();
+  }
+  if (warp == 9) tmem_alloc(smem_u32(slot), C::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *slot;
+  pdl_wait_primary();
+  pdl_launch_dependents();
+
+  const int K = p.block_size;
+  const int G = p.G;
+  const int q0 = p.cu_seqlens[s], q1 = p.cu_seqlens[s + 1];
+  const int L = effective_len(p.context_lens[s], p.max_len, p.max_blocks_per_seq * K);
+  const int n = q1 - q0;
+  bool active = true;
+  if (q0 < 0 || n < 0 || q1 > p.num_tokens || n > L) {
+    if (threadIdx.x == 0 && pair == 0) record_error(PKV_DEVERR_CONTEXT_LEN);
+    active = false;
+  }
+  const int R = active ? n * G : 0;
+  const int r0 = pair * 2 * kT5Rows;                      // tile A; tile B at r0 + 128
+  if (r0 >= R) active = false;
+  int pmax = -1, nkt = 0;
+  if (active) {
+    pmax = L - n + min(R - 1, r0 + 2 * kT5Rows - 1) / G;  // last key any row of the pair sees
+    nkt = pmax / kPfBN + 1;
+  }
+  // tile B has rows only when R > r0 + 128; without rows it still runs its
+  // (masked) softmax so that every barrier count stays the same
+
+  if (warp == 8 || warp == 10) {
+    // =================== TMA producers: warp 8 K tiles, warp 10 V tiles ===================
+    if (active) {
+      const int kv = warp == 10;
+      const CUtensorMap* map = kv ? &p.tmap_v : &p.tmap_k;
+      const int NS = kv ? kX2VStages : kX2KStages;
+      const uint32_t full = kv ? v_full : k_full, empty = kv ? v_empty : k_empty;
+      uint8_t* ring = smem + (kv ? C::V_OFF : C::K_OFF);
+      if (lane == 0) prefetch_tensormap(map);
+      const uint64_t policy = l2_policy_evict_normal();
+      const int sbl = K < 16 ? 1 : 0;
+      const int ncopy = C::NBOX << sbl;
+      int kt = 0;
+      bool ok = true;
+      for (; kt < nkt; ++kt) {
+        const int stage = kt % NS;
+        if (!mbar_wait_bounded(empty + 8 * stage, ((kt / NS) & 1) ^ 1)) {
+          record_error(PKV_DEVERR_TIMEOUT);
+          ok = false;
+          break;
+        }
+        if (lane == 0) mbar_arrive_expect_tx(full + 8 * stage, C::KBYTES);
+        __syncwarp();
+        uint8_t* sb = ring + stage * C::KBYTES;
+        for (int i = lane; i < ncopy; i += 32) {
+          const int bi = i >> sbl, u = i & sbl;
+          const int half = bi >> 2, rb = bi & 3;
+          const int tr = rb * 16 + (u << 3);
+          const int tok = kt * kPfBN + tr;
+          int row = -32;
+          if (tok <= pmax) {
+            const int lb = tok / K;
+            const long long phys = p.block_tables[(int64_t)s * p.max_blocks_per_seq + lb];
+            if (phys < 0 || phys >= p.num_blocks) {
+              record_error(PKV_DEVERR_BLOCK_ID);
+            } else {
+              row = (int)(phys * K + (tok - lb * K));
+            }
+          }
+          tma_load_3d(smem_u32(sb + half * C::KVHALF + tr * 128), map, full + 8 * stage,
+                      half * 64, j, row, policy);
+        }
+        __syncwarp();
+      }
+      if (!ok) {
+        for (int kk = max(0, kt - NS); kk < kt; ++kk)
+          mbar_wait_bounded(full + 8 * (kk % NS), (kk / NS) & 1);
+      }
+    }
+  } else if (warp == 9 || warp == 11) {
+    // =================== MMA issue: warp 9 S = Q K^T, warp 11 O += P V ===================
+    if (active && lane == 0) {
+      bool ok = true;
+      if (warp == 9) {
+        ok = mbar_wait_bounded(q_full(0), 0) && mbar_wait_bounded(q_full(1), 0);
+        for (int kt = 0; kt < nkt && ok; ++kt) {
+          const int stage = kt % kX2KStages, b = kt & 1;
+          if (!mbar_wait_bounded(k_full + 8 * stage, (kt / kX2KStages) & 1)) {
+            ok = false;
+            break;
+          }
+          const uint32_t kb = sbase + C::K_OFF + stage * C::KBYTES;
+          for (int x = 0; x < 2 && ok; ++x) {
+            // S buffer b of tile x is free once its softmax has read S(kt - 2)
+            if (kt >= 2 && !mbar_wait_bounded(s_free(x, b), ((kt >> 1) - 1) & 1)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t qb = sbase + C::Q_OFF + x * C::QBYTES;
+            const uint32_t sd = tmem + x * 256 + b * kPfBN;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint64_t ad = umma_desc_sw128(qb + (kk >> 2) * C::QHALF + (kk & 3) * 32, 16, 1024);
+              const uint64_t bd = umma_desc_sw128(kb + (kk >> 2) * C::KVHALF + (kk & 3) * 32, 16, 1024);
+              umma_ss(sd, ad, bd, C::IDESC_QK, kk > 0 ? 1u : 0u);
+            }
+            umma_commit(s_full(x, b));
+            umma_commit(k_empty + 8 * stage);
+          }
+        }
+      } else {
+        for (int t = 0; t < nkt && ok; ++t) {
+          const int stage = t % kX2VStages;
+          if (!mbar_wait_bounded(v_full + 8 * stage, (t / kX2VStages) & 1)) {
+            ok = false;
+            break;
+          }
+          const uint32_t vb = sbase + C::V_OFF + stage * C::KBYTES;
+          for (int x = 0; x < 2 && ok; ++x) {
+            if (!mbar_wait_bounded(p_full(x), t & 1)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t ph = sbase + C::P_OFF + (2 * x) * C::PBUF;
+            const uint32_t od = tmem + x * 256 + 128;
+#pragma unroll
+            for (int k16 = 0; k16 < kPfBN / 16; ++k16) {
+              const uint64_t bd = umma_desc_sw128(vb + k16 * 2048, C::KVHALF, 1024);
+              umma_ss(od, umma_desc_sw128(ph + k16 * 32, 16, 1024), bd, C::IDESC_PV,
+                      (t > 0 || k16 > 0) ? 1u : 0u);
+              umma_ss(od, umma_desc_sw128(ph + C::PBUF + k16 * 32, 16, 1024), bd, C::IDESC_PV, 1u);
+            }
+            umma_commit(o_done(x));
+          }
+          if (ok) umma_commit(v_empty + 8 * stage);
+        }
+      }
+      if (!ok) record_error(PKV_DEVERR_TIMEOUT);
+      umma_commit(mma_idle);
+      mbar_wait_bounded(mma_idle, 0);
+    }
+  } else {
+    // =================== softmax warps: warps 0-3 tile A, 4-7 tile B ===================
+    const int x = warp >> 2;
+    const int row = (warp & 3) * 32 + lane;      // TMEM lane = query row of tile x
+    const int r = r0 + x * kT5Rows + row;
+    const bool valid = active && r < R;
+    const int i = valid ? r / G : 0;
+    const int h = j * G + (valid ? r - i * G : 0);
+    const int prow = valid ? L - n + i : -1;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t scol = x * 256, ocol = x * 256 + 128;
+    int pw_min = valid ? prow : 0x7fffffff;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) pw_min = min(pw_min, __shfl_xor_sync(0xffffffffu, pw_min, o));
+    bool ok = true;
+    if (active) {
+      const uint4* qrow = reinterpret_cast<const uint4*>(p.q + ((int64_t)(q0 + i) * p.H_q + h) * D);
+      uint8_t* qt = smem + C::Q_OFF + x * C::QBYTES;
+#pragma unroll
+      for (int c = 0; c < D / 8; ++c) {
+        const uint4 v = valid ? __ldg(qrow + c) : make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(qt + (c >> 3) * C::QHALF + row * 128 +
+                                  (((c & 7) ^ (row & 7)) << 4)) = v;
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(q_full(x));
+    }
+    const float sl = p.scale_log2;
+    float m_used = 0.f, l = 0.f;
+    for (int kt = 0; kt < nkt && ok; ++kt) {
+      const int b = kt & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait_bounded(s_full(x, b), (kt >> 1) & 1));
+      if (!ok) break;
+      tc_fence_after();
+      float xs[kPfBN];
+      {
+        uint32_t sr[32];
+        tmem_ld32(tmem + lane_base + scol + b * kPfBN, sr);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) xs[e] = __uint_as_float(sr[e]);
+        tmem_ld32(tmem + lane_base + scol + b * kPfBN + 32, sr);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) xs[32 + e] = __uint_as_float(sr[e]);
+      }
+      tc_fence_before();
+      mbar_arrive(s_free(x, b));                  // S buffer may be overwritten
+      const int kbase = kt * kPfBN;
+      if (kbase + kPfBN - 1 > pw_min) {
+        const int lim = prow - kbase;
+#pragma unroll
+        for (int e = 0; e < kPfBN; ++e) xs[e] = e <= lim ? xs[e] : -INFINITY;
+      }
+      float m4[4] = {xs[0], xs[1], xs[2], xs[3]};
+#pragma unroll
+      for (int e = 4; e < kPfBN; ++e) m4[e & 3] = fmaxf(m4[e & 3], xs[e]);
+      const float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl;
+      if (kt == 0) {
+        m_used = mt == -INFINITY ? 0.f : mt;
+      } else {
+        const bool need = mt > m_used + kT5Slack;
+        if (__any_sync(0xffffffffu, need)) {
+          // O in TMEM is rescaled; O += P(kt-1) V must have landed first
+          ok = __all_sync(0xffffffffu, mbar_wait_bounded(o_done(x), (kt - 1) & 1));
+          if (!ok) break;
+          tc_fence_after();
+          const float mn = need ? mt : m_used;
+          const float alpha = exp2f(m_used - mn);
+          l *= alpha;
+          m_used = mn;
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tmem + lane_base + ocol + c * 32, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32(tmem + lane_base + ocol + c * 32, o);
+          }
+          tmem_wait_st();
+        }
+      }
+      float s4[4] = {0.f, 0.f, 0.f, 0.f};
+      const float nm = -m_used;
+#pragma unroll
+      for (int e = 0; e < kPfBN; ++e) {
+        xs[e] = ex2_approx(fmaf(xs[e], sl, nm));
+        s4[e & 3] += xs[e];
+      }
+      l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
+      // this tile's P buffer is free once O += P(kt-1) V has completed
+      if (kt >= 1) ok = __all_sync(0xffffffffu, mbar_wait_bounded(o_done(x), (kt - 1) & 1));
+      if (!ok) break;
+      uint8_t* phi = smem + C::P_OFF + (2 * x) * C::PBUF + row * 128;
+#pragma unroll
+      for (int cc = 0; cc < kPfBN / 8; ++cc) {
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          split_bf16x2(xs[cc * 8 + 2 * e], xs[cc * 8 + 2 * e + 1], hi[e], lo[e]);
+        const int off = ((cc ^ (row & 7)) << 4);
+        *reinterpret_cast<uint4*>(phi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(phi + C::PBUF + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      }
+      if (x == 0 && kt == nkt - 1 && L - kbase < kPfBN) {
+        // V rows at or past the context end inside fetched boxes may hold
+        // anything (NaN included): tile A zeroes them before its O += P V
+        // (tile B's product is issued after tile A's)
+        const int stage = kt % kX2VStages;
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(v_full + 8 * stage, (kt / kX2VStages) & 1));
+        if (!ok) break;
+        const int z0 = L - kbase, z1 = min(kPfBN, ((pmax - kbase) / 16 + 1) * 16);
+        uint8_t* vs = smem + C::V_OFF + stage * C::KBYTES;
+        for (int x2 = z0 * 8 + row; x2 < z1 * 8; x2 += kT5Rows) {
+#pragma unroll
+          for (int hh = 0; hh < C::NH; ++hh)
+            *reinterpret_cast<uint4*>(vs + hh * C::KVHALF + x2 * 16) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(p_full(x));
+    }
+    // ---- epilogue: O / l from TMEM to the output rows
+    if (active && ok) {
+      ok = __all_sync(0xffffffffu, mbar_wait_bounded(o_done(x), (nkt - 1) & 1));
+      if (ok) {
+        tc_fence_after();
+        const float inv = valid ? 1.f / l : 0.f;
+        uint4* orow = reinterpret_cast<uint4*>(p.out + ((int64_t)(q0 + i) * p.H_q + h) * D);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tmem + lane_base + ocol + c * 32, o);
+          tmem_wait_ld();
+          if (valid) {
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              uint32_t w[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                w[e] = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2 * e]) * inv,
+                                   __uint_as_float(o[q4 * 8 + 2 * e + 1]) * inv);
+              orow[c * 4 + q4] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+        }
+      }
+    }
+    if (active && !ok) record_error(PKV_DEVERR_TIMEOUT);
+  }
+
+  // ---- teardown: every warp, every path
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 9) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+}  // namespace pkv
