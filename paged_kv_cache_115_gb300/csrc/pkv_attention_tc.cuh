@@ -438,17 +438,16 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
         vsr[t][0] = vsr[t][1] = CT == 1 ? p.v_scale : 1.f;
       }
     }
-    if (CT == 0 && valid < kTile) {
-      // rows past the sequence end may hold anything (stale slots, NaN):
-      // give them zero V so that 0-weight x V stays 0 in the tensor core
-      uint8_t* vt = sb + C::box_off(1, w, 0, 0);
-      const int nvec = (kTile - valid) * C::NH * 8;
+    if (valid < CH) {
+      // rows past the sequence end may hold anything (stale slots, NaN
+      // codes): give them zero V so that 0-weight x V stays 0 in the tensor core
+      const int nvec = (CH - valid) * C::NH * 8;
       for (int i = lane; i < nvec; i += 32) {
-        const int r = valid + i / (C::NH * 8);
+        const int r = valid + i / (C::NH * 8);          // chunk row: tile r / 16
         const int rem = i % (C::NH * 8);
         const int half = rem >> 3, ch = rem & 7;
-        *reinterpret_cast<uint4*>(vt + half * kBoxBytes + r * 128 + ch * 16) =
-            make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(sb + C::box_off(1, w, r / kTile, half) + (r % kTile) * 128 +
+                                  ch * 16) = make_uint4(0u, 0u, 0u, 0u);
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -574,47 +573,37 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
     // ---- O^T[D x 8] += V^T[D x 16 tok] . P^T[16 tok x 8], per tile
     if constexpr (CT != 0) {
       // byte tiles; the rows of each 16-row m tile are permuted: row g -> d =
-      // 16 mt + 2g, row g + 8 -> d = 16 mt + 2g + 1, so one 16-bit load per
-      // token gives both rows.  Tokens past the end read as 0 (their codes
-      // may be NaN and 0 * NaN must not reach the accumulator).
-      const int t0 = 2 * tq, t1 = 2 * tq + 1, t2 = 2 * tq + 8, t3 = 2 * tq + 9;
-      bool vv[TL][4];
+      // 16 mt + 2g, row g + 8 -> d = 16 mt + 2g + 1.  ldmatrix.trans over 8
+      // token rows x 16 bytes (byte pairs as 16-bit elements) hands this
+      // thread bytes 2g, 2g+1 of tokens 2tq and 2tq+1; one byte permute pairs
+      // the two tokens of each d.  Rows past the end were zeroed above.
+      const int lm = lane >> 3, lr = lane & 7;       // matrix and row this lane addresses
+      const int tok = (lm & 1) * 8 + lr;
 #pragma unroll
       for (int t = 0; t < TL; ++t) {
-        vv[t][0] = t * kTile + t0 < valid;
-        vv[t][1] = t * kTile + t1 < valid;
-        vv[t][2] = t * kTile + t2 < valid;
-        vv[t][3] = t * kTile + t3 < valid;
-      }
+        const uint32_t vt = smem_u32(sb + C::box_off(1, w, t, 0)) + tok * 128;
 #pragma unroll
-      for (int mt = 0; mt < D / 16; ++mt) {
+        for (int mt = 0; mt < D / 16; mt += 2) {
+          uint32_t r[4];
+          ldmatrix_x4_trans(vt + (((mt + (lm >> 1)) ^ (tok & 7)) << 4), r[0], r[1], r[2], r[3]);
 #pragma unroll
-        for (int t = 0; t < TL; ++t) {
-          const uint8_t* vt = sb + C::box_off(1, w, t, 0) + 2 * g;
-          const uint32_t l0 = vv[t][0] ? *reinterpret_cast<const uint16_t*>(
-                                             vt + t0 * 128 + ((mt ^ (t0 & 7)) << 4)) : 0u;
-          const uint32_t l1 = vv[t][1] ? *reinterpret_cast<const uint16_t*>(
-                                             vt + t1 * 128 + ((mt ^ (t1 & 7)) << 4)) : 0u;
-          const uint32_t l2 = vv[t][2] ? *reinterpret_cast<const uint16_t*>(
-                                             vt + t2 * 128 + ((mt ^ (t2 & 7)) << 4)) : 0u;
-          const uint32_t l3 = vv[t][3] ? *reinterpret_cast<const uint16_t*>(
-                                             vt + t3 * 128 + ((mt ^ (t3 & 7)) << 4)) : 0u;
-          const uint32_t q01lo = __byte_perm(l0, l1, 0x0040), q01hi = __byte_perm(l0, l1, 0x0051);
-          const uint32_t q23lo = __byte_perm(l2, l3, 0x0040), q23hi = __byte_perm(l2, l3, 0x0051);
-          uint32_t a0, a1, a2, a3;
-          if constexpr (CT == 1) {
-            a0 = e4m3x2_to_f16x2(q01lo);
-            a1 = e4m3x2_to_f16x2(q01hi);
-            a2 = e4m3x2_to_f16x2(q23lo);
-            a3 = e4m3x2_to_f16x2(q23hi);
-          } else {
-            a0 = s8x2_to_f16x2(q01lo);
-            a1 = s8x2_to_f16x2(q01hi);
-            a2 = s8x2_to_f16x2(q23lo);
-            a3 = s8x2_to_f16x2(q23hi);
+          for (int u = 0; u < 2; ++u) {
+            // r[2u]: tokens 2tq, 2tq+1 of m tile mt + u; r[2u+1]: tokens + 8
+            uint32_t a0, a1, a2, a3;
+            if constexpr (CT == 1) {
+              a0 = e4m3x2_to_f16x2(__byte_perm(r[2 * u], 0u, 0x0020));
+              a1 = e4m3x2_to_f16x2(__byte_perm(r[2 * u], 0u, 0x0031));
+              a2 = e4m3x2_to_f16x2(__byte_perm(r[2 * u + 1], 0u, 0x0020));
+              a3 = e4m3x2_to_f16x2(__byte_perm(r[2 * u + 1], 0u, 0x0031));
+            } else {
+              a0 = s8x2_to_f16x2(__byte_perm(r[2 * u], 0u, 0x0020));
+              a1 = s8x2_to_f16x2(__byte_perm(r[2 * u], 0u, 0x0031));
+              a2 = s8x2_to_f16x2(__byte_perm(r[2 * u + 1], 0u, 0x0020));
+              a3 = s8x2_to_f16x2(__byte_perm(r[2 * u + 1], 0u, 0x0031));
+            }
+            mma_f16_16816(o[mt + u], a0, a1, a2, a3, pb[t][0], pb[t][1]);
+            mma_f16_16816(o[mt + u], a0, a1, a2, a3, pc[t][0], pc[t][1]);
           }
-          mma_f16_16816(o[mt], a0, a1, a2, a3, pb[t][0], pb[t][1]);
-          mma_f16_16816(o[mt], a0, a1, a2, a3, pc[t][0], pc[t][1]);
         }
       }
     } else {
