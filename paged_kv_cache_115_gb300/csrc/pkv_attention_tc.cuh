@@ -77,6 +77,18 @@ struct TcParams {
 //
 // Stage layout: K boxes [head][tile][column group], then V boxes, then (INT8)
 // the 16 per-slot scales of each tile: K tiles, then V tiles.
+// Two int8 codes of a word whose bytes were already XORed with 0x80, chosen
+// by a byte-permute selector that puts them in the low bytes of two f16
+// halves with exponent bits 0x64 (selector nibbles: code byte, 4 = 0x64,
+// code byte, 5 = 0x64): each half is 1024 + (code + 128), and subtracting
+// 1152 leaves the code exactly.
+__device__ __forceinline__ uint32_t s8_pair_to_f16x2(uint32_t xored, uint32_t sel) {
+  const uint32_t biased = __byte_perm(xored, 0x6464u, sel);
+  __half2 h = *reinterpret_cast<const __half2*>(&biased);
+  h = __hsub2(h, __floats2half2_rn(1152.f, 1152.f));
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
 template <int D, int HPC, int NS, int CT = 0>
 struct TcCfg {
   static constexpr int TL = CT ? 2 : 1;                   // 16-row tiles per chunk
@@ -487,10 +499,11 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
             a1 = e4m3x2_to_f16x2(w1);
             a3 = e4m3x2_to_f16x2(w1 >> 16);
           } else {
-            a0 = s8x2_to_f16x2(w0);
-            a2 = s8x2_to_f16x2(w0 >> 16);
-            a1 = s8x2_to_f16x2(w1);
-            a3 = s8x2_to_f16x2(w1 >> 16);
+            const uint32_t x0 = w0 ^ 0x80808080u, x1 = w1 ^ 0x80808080u;
+            a0 = s8_pair_to_f16x2(x0, 0x5140);
+            a2 = s8_pair_to_f16x2(x0, 0x5342);
+            a1 = s8_pair_to_f16x2(x1, 0x5140);
+            a3 = s8_pair_to_f16x2(x1, 0x5342);
           }
           mma_f16_16816(sacc[t], a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
         }
@@ -596,10 +609,11 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
               a2 = e4m3x2_to_f16x2(__byte_perm(r[2 * u + 1], 0u, 0x0020));
               a3 = e4m3x2_to_f16x2(__byte_perm(r[2 * u + 1], 0u, 0x0031));
             } else {
-              a0 = s8x2_to_f16x2(__byte_perm(r[2 * u], 0u, 0x0020));
-              a1 = s8x2_to_f16x2(__byte_perm(r[2 * u], 0u, 0x0031));
-              a2 = s8x2_to_f16x2(__byte_perm(r[2 * u + 1], 0u, 0x0020));
-              a3 = s8x2_to_f16x2(__byte_perm(r[2 * u + 1], 0u, 0x0031));
+              const uint32_t x0 = r[2 * u] ^ 0x80808080u, x1 = r[2 * u + 1] ^ 0x80808080u;
+              a0 = s8_pair_to_f16x2(x0, 0x5240);
+              a1 = s8_pair_to_f16x2(x0, 0x5341);
+              a2 = s8_pair_to_f16x2(x1, 0x5240);
+              a3 = s8_pair_to_f16x2(x1, 0x5341);
             }
             mma_f16_16816(o[mt + u], a0, a1, a2, a3, pb[t][0], pb[t][1]);
             mma_f16_16816(o[mt + u], a0, a1, a2, a3, pc[t][0], pc[t][1]);
