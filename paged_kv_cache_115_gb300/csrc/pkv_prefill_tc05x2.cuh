@@ -11,11 +11,13 @@
 //
 // Warps 0-3: softmax / epilogue of tile A, warps 4-7: of tile B (one thread
 // per query row = TMEM lane, a full 64-key tile per thread).  Warp 8: TMA
-// producer of K tiles (3-deep ring); warp 10: of V tiles (3-deep ring).
+// producer of K tiles (5-deep ring); warp 10: of V tiles (5-deep ring).
 // Warp 9: TMEM allocation and, on one lane, the S = Q K^T issue for both
 // tiles (up to two tiles ahead per query tile); warp 11, one lane: the
-// O += P V issue.  P (split hi + lo bf16) has one shared-memory buffer per
-// query tile.  The exponent base of a row is raised only when its maximum
+// O += P V issue.  P (split hi + lo bf16) is written by the softmax over the
+// S buffer it came from and read from TMEM by the O += P V product (A operand
+// in tensor memory); the S buffer is free again when that product is done.
+// K and V rings are 5 deep.  The exponent base of a row is raised only when its maximum
 // grows by more than 2^8 (O rescaled in TMEM rarely).  Every wait is bounded
 // and records PKV_DEVERR_TIMEOUT; TMEM is freed on every path after both
 // issuing threads have seen their MMAs complete.
@@ -25,8 +27,8 @@
 
 namespace pkv {
 
-constexpr int kX2KStages = 3;
-constexpr int kX2VStages = 3;
+constexpr int kX2KStages = 5;
+constexpr int kX2VStages = 5;
 
 template <int D>
 struct X2Cfg {
@@ -36,19 +38,19 @@ struct X2Cfg {
   static constexpr int KVHALF = kPfBN * 128;              // 8 KiB
   static constexpr int KBYTES = NH * KVHALF;              // one K (or V) tile
   static constexpr int NBOX = NH * (kPfBN / 16);
-  static constexpr int PBUF = kT5Rows * 128;              // 128 rows x 64 keys bf16
   static constexpr int Q_OFF = 0;                         // [tile][half]
   static constexpr int K_OFF = 2 * QBYTES;
   static constexpr int V_OFF = K_OFF + kX2KStages * KBYTES;
-  static constexpr int P_OFF = V_OFF + kX2VStages * KBYTES;   // [tile][hi, lo]
-  static constexpr int BAR_OFF = P_OFF + 4 * PBUF;
-  // k_full/k_empty[KS], v_full/v_empty[VS], per tile: s_full[2], s_free[2],
-  // p_full, o_done, q_full; mma_idle
-  static constexpr int NBAR = 2 * (kX2KStages + kX2VStages) + 2 * 7 + 1;
+  static constexpr int BAR_OFF = V_OFF + kX2VStages * KBYTES;
+  // k_full/k_empty[KS], v_full/v_empty[VS], per tile: s_full[2], p_free[2],
+  // p_full[2], o_done, q_full; mma_idle
+  static constexpr int NBAR = 2 * (kX2KStages + kX2VStages) + 2 * 8 + 1;
   static constexpr int SLOT_OFF = BAR_OFF + 8 * NBAR;
   static constexpr int SMEM = SLOT_OFF + 16 + 1024;
   static constexpr int THREADS = 384;
-  static constexpr uint32_t TMEM_COLS = 512;              // per tile: S0 S1 (128), O (128)
+  // per tile: S buffers 0, 1 (64 columns each, fp32 S, then P hi | lo as
+  // bf16 pairs in the same columns), O (128)
+  static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t IDESC_QK = umma_idesc_bf16(kT5Rows, kPfBN, 0, 0);
   static constexpr uint32_t IDESC_PV = umma_idesc_bf16(kT5Rows, D, 0, 1);
 };
@@ -64,13 +66,16 @@ attn_prefill_tc05x2_kernel(const __grid_constant__ PfParams p) {
   const uint32_t bars = sbase + C::BAR_OFF;
   const uint32_t k_full = bars, k_empty = k_full + 8 * kX2KStages;
   const uint32_t v_full = k_empty + 8 * kX2KStages, v_empty = v_full + 8 * kX2VStages;
-  const uint32_t tb0 = v_empty + 8 * kX2VStages;          // per-tile barriers, 7 each
-  auto s_full = [&](int x, int b) { return tb0 + 56 * x + 8 * b; };
-  auto s_free = [&](int x, int b) { return tb0 + 56 * x + 16 + 8 * b; };
-  auto p_full = [&](int x) { return tb0 + 56 * x + 32; };
-  auto o_done = [&](int x) { return tb0 + 56 * x + 40; };
-  auto q_full = [&](int x) { return tb0 + 56 * x + 48; };
-  const uint32_t mma_idle = tb0 + 112;
+  const uint32_t tb0 = v_empty + 8 * kX2VStages;          // per-tile barriers, 8 each
+  // Every barrier of S buffer b (s_full, p_full, p_free) completes once per
+  // key tile kt with kt & 1 == b, at phase kt >> 1; a buffer cannot run two
+  // phases ahead of its waiter, since S(kt + 2) needs O += P(kt) V done.
+  auto s_full = [&](int x, int b) { return tb0 + 64 * x + 8 * b; };
+  auto p_free = [&](int x, int b) { return tb0 + 64 * x + 16 + 8 * b; };
+  auto p_full = [&](int x, int b) { return tb0 + 64 * x + 32 + 8 * b; };
+  auto o_done = [&](int x) { return tb0 + 64 * x + 48; };
+  auto q_full = [&](int x) { return tb0 + 64 * x + 56; };
+  const uint32_t mma_idle = tb0 + 128;
   uint32_t* slot = reinterpret_cast<uint32_t*>(smem + C::SLOT_OFF);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int s = blockIdx.z, j = blockIdx.y;
@@ -88,9 +93,9 @@ attn_prefill_tc05x2_kernel(const __grid_constant__ PfParams p) {
     for (int x = 0; x < 2; ++x) {
       for (int b = 0; b < 2; ++b) {
         mbar_init(s_full(x, b), 1);
-        mbar_init(s_free(x, b), kT5Rows);
+        mbar_init(p_free(x, b), 1);
+        mbar_init(p_full(x, b), kT5Rows);
       }
-      mbar_init(p_full(x), kT5Rows);
       mbar_init(o_done(x), 1);
       mbar_init(q_full(x), kT5Rows);
     }
@@ -189,8 +194,8 @@ attn_prefill_tc05x2_kernel(const __grid_constant__ PfParams p) {
           }
           const uint32_t kb = sbase + C::K_OFF + stage * C::KBYTES;
           for (int x = 0; x < 2 && ok; ++x) {
-            // S buffer b of tile x is free once its softmax has read S(kt - 2)
-            if (kt >= 2 && !mbar_wait_bounded(s_free(x, b), ((kt >> 1) - 1) & 1)) {
+            // S buffer b of tile x holds P(kt - 2) until O += P(kt - 2) V is done
+            if (kt >= 2 && !mbar_wait_bounded(p_free(x, b), ((kt >> 1) - 1) & 1)) {
               ok = false;
               break;
             }
@@ -216,21 +221,22 @@ attn_prefill_tc05x2_kernel(const __grid_constant__ PfParams p) {
           }
           const uint32_t vb = sbase + C::V_OFF + stage * C::KBYTES;
           for (int x = 0; x < 2 && ok; ++x) {
-            if (!mbar_wait_bounded(p_full(x), t & 1)) {
+            if (!mbar_wait_bounded(p_full(x, t & 1), (t >> 1) & 1)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint32_t ph = sbase + C::P_OFF + (2 * x) * C::PBUF;
+            // P hi in columns 0..31 of the S buffer, P lo in 32..63 (8 per 16 keys)
+            const uint32_t pt = tmem + x * 256 + (t & 1) * kPfBN;
             const uint32_t od = tmem + x * 256 + 128;
 #pragma unroll
             for (int k16 = 0; k16 < kPfBN / 16; ++k16) {
               const uint64_t bd = umma_desc_sw128(vb + k16 * 2048, C::KVHALF, 1024);
-              umma_ss(od, umma_desc_sw128(ph + k16 * 32, 16, 1024), bd, C::IDESC_PV,
-                      (t > 0 || k16 > 0) ? 1u : 0u);
-              umma_ss(od, umma_desc_sw128(ph + C::PBUF + k16 * 32, 16, 1024), bd, C::IDESC_PV, 1u);
+              umma_ts(od, pt + k16 * 8, bd, C::IDESC_PV, (t > 0 || k16 > 0) ? 1u : 0u);
+              umma_ts(od, pt + 32 + k16 * 8, bd, C::IDESC_PV, 1u);
             }
             umma_commit(o_done(x));
+            umma_commit(p_free(x, t & 1));
           }
           if (ok) umma_commit(v_empty + 8 * stage);
         }
@@ -285,24 +291,26 @@ attn_prefill_tc05x2_kernel(const __grid_constant__ PfParams p) {
 #pragma unroll
         for (int e = 0; e < 32; ++e) xs[32 + e] = __uint_as_float(sr[e]);
       }
-      tc_fence_before();
-      mbar_arrive(s_free(x, b));                  // S buffer may be overwritten
       const int kbase = kt * kPfBN;
       if (kbase + kPfBN - 1 > pw_min) {
         const int lim = prow - kbase;
 #pragma unroll
         for (int e = 0; e < kPfBN; ++e) xs[e] = e <= lim ? xs[e] : -INFINITY;
       }
-      float m4[4] = {xs[0], xs[1], xs[2], xs[3]};
+      // row maximum: four chains of three-input max over the 64 scores
+      float m4[4] = {fmax3(xs[0], xs[1], xs[2]), fmax3(xs[3], xs[4], xs[5]),
+                     fmax3(xs[6], xs[7], xs[8]), fmax3(xs[9], xs[10], xs[11])};
 #pragma unroll
-      for (int e = 4; e < kPfBN; ++e) m4[e & 3] = fmaxf(m4[e & 3], xs[e]);
-      const float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl;
+      for (int e = 12; e + 1 < kPfBN; e += 2) m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], xs[e], xs[e + 1]);
+      const float mt = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3])) * sl;
       if (kt == 0) {
         m_used = mt == -INFINITY ? 0.f : mt;
       } else {
         const bool need = mt > m_used + kT5Slack;
         if (__any_sync(0xffffffffu, need)) {
-          // O in TMEM is rescaled; O += P(kt-1) V must have landed first
+          // O in TMEM is rescaled; O += P(kt-1) V must have landed first.  S(kt)
+          // full implies O += P(kt-2) V done, so o_done is at most one phase behind
+          // and its parity names the phase unambiguously
           ok = __all_sync(0xffffffffu, mbar_wait_bounded(o_done(x), (kt - 1) & 1));
           if (!ok) break;
           tc_fence_after();
@@ -322,27 +330,26 @@ attn_prefill_tc05x2_kernel(const __grid_constant__ PfParams p) {
           tmem_wait_st();
         }
       }
-      float s4[4] = {0.f, 0.f, 0.f, 0.f};
-      const float nm = -m_used;
+      // p = 2^(s * scale * log2 e - m): the scale and shift as packed fp32x2 FMAs,
+      // the row sum as packed adds
+      float2 s2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      const float2 sl2 = make_float2(sl, sl), nm2 = make_float2(-m_used, -m_used);
 #pragma unroll
-      for (int e = 0; e < kPfBN; ++e) {
-        xs[e] = ex2_approx(fmaf(xs[e], sl, nm));
-        s4[e & 3] += xs[e];
+      for (int c = 0; c < kPfBN / 2; ++c) {
+        const float2 y = __ffma2_rn(make_float2(xs[2 * c], xs[2 * c + 1]), sl2, nm2);
+        xs[2 * c] = ex2_approx(y.x);
+        xs[2 * c + 1] = ex2_approx(y.y);
+        s2[c & 1] = __fadd2_rn(s2[c & 1], make_float2(xs[2 * c], xs[2 * c + 1]));
       }
-      l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
-      // this tile's P buffer is free once O += P(kt-1) V has completed
-      if (kt >= 1) ok = __all_sync(0xffffffffu, mbar_wait_bounded(o_done(x), (kt - 1) & 1));
-      if (!ok) break;
-      uint8_t* phi = smem + C::P_OFF + (2 * x) * C::PBUF + row * 128;
+      l += (s2[0].x + s2[0].y) + (s2[1].x + s2[1].y);
+      // P hi | lo over the S just read (this thread's row = its TMEM lane)
+      {
+        uint32_t hi[32], lo[32];
 #pragma unroll
-      for (int cc = 0; cc < kPfBN / 8; ++cc) {
-        uint32_t hi[4], lo[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          split_bf16x2(xs[cc * 8 + 2 * e], xs[cc * 8 + 2 * e + 1], hi[e], lo[e]);
-        const int off = ((cc ^ (row & 7)) << 4);
-        *reinterpret_cast<uint4*>(phi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(phi + C::PBUF + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        for (int c = 0; c < 32; ++c) split_bf16x2_trunc(xs[2 * c], xs[2 * c + 1], hi[c], lo[c]);
+        tmem_st32(tmem + lane_base + scol + b * kPfBN, hi);
+        tmem_st32(tmem + lane_base + scol + b * kPfBN + 32, lo);
+        tmem_wait_st();
       }
       if (x == 0 && kt == nkt - 1 && L - kbase < kPfBN) {
         // V rows at or past the context end inside fetched boxes may hold
@@ -361,11 +368,14 @@ attn_prefill_tc05x2_kernel(const __grid_constant__ PfParams p) {
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(p_full(x));
+      mbar_arrive(p_full(x, b));
     }
     // ---- epilogue: O / l from TMEM to the output rows
     if (active && ok) {
-      ok = __all_sync(0xffffffffu, mbar_wait_bounded(o_done(x), (nkt - 1) & 1));
+      // o_done may still be two phases behind here; the last buffer's P-free
+      // commit follows every O += P V of this tile
+      ok = __all_sync(0xffffffffu,
+                      mbar_wait_bounded(p_free(x, (nkt - 1) & 1), ((nkt - 1) >> 1) & 1));
       if (ok) {
         tc_fence_after();
         const float inv = valid ? 1.f / l : 0.f;
