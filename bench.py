@@ -36,14 +36,23 @@ DEFAULT_WORKLOAD = "qwen3_0_6b"
 KERNEL_SRC = ["paged_kv_cache_115_gb300/csrc/pkv_attention_tc.cuh",
               "paged_kv_cache_115_gb300/csrc/pkv_attention_common.cuh",
               "paged_kv_cache_115_gb300/csrc/pkv_device.cuh"]
+# sources of the two-tile tcgen05 prefill kernel
+PREFILL_SRC = ["paged_kv_cache_115_gb300/csrc/pkv_prefill_tc05x2.cuh",
+               "paged_kv_cache_115_gb300/csrc/pkv_prefill_tc05.cuh",
+               "paged_kv_cache_115_gb300/csrc/pkv_umma.cuh",
+               "paged_kv_cache_115_gb300/csrc/pkv_device.cuh"]
 
 
-def kernel_src_sha() -> str:
+def src_sha(paths) -> str:
     h = hashlib.sha256()
-    for p in KERNEL_SRC:
+    for p in paths:
         with open(os.path.join(ROOT, p), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
+
+
+def kernel_src_sha() -> str:
+    return src_sha(KERNEL_SRC)
 
 
 def read_peaks():
@@ -54,15 +63,20 @@ def read_peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
 
 
-def read_traffic():
-    """DRAM bytes per attention launch from the committed ncu summary, valid
-    only while the kernel source is unchanged since the capture."""
+def read_traffic(name="attention_traffic.json", workload=None):
+    """DRAM bytes per launch of a kernel from a committed ncu summary, valid
+    only while the kernel's sources are unchanged since the capture.  Files
+    with several records are keyed by workload name."""
     try:
-        with open(os.path.join(ROOT, "profiles", "attention_traffic.json")) as f:
+        with open(os.path.join(ROOT, "profiles", name)) as f:
             t = json.load(f)
     except OSError:
         return None
-    if t.get("kernel_src_sha") != kernel_src_sha():
+    if workload is not None:
+        t = t.get(workload)
+        if t is None:
+            return None
+    if t.get("kernel_src_sha") != src_sha(t.get("sources", KERNEL_SRC)):
         return None
     return t
 
@@ -730,6 +744,18 @@ def run_swap(args):
 PREFILL_METRIC = "paged multi-query attention (prefill) TFLOP/s and KV GB/s"
 
 
+def prefill_kernel(w) -> str:
+    """The kernel the automatic prefill plan picks for workload w (mirrors
+    the library's plan: up to 8 query rows per KV head -> the stream-K decode
+    kernel; more than 64 -> tcgen05, two query tiles per CTA above 128)."""
+    rows = int(w.news.max()) * (w.num_q_heads // w.num_kv_heads)
+    if rows <= 8 and w.num_seqs <= 2048:
+        return "attn_tc_kernel (stream-K decode kernel, query rows as score columns)"
+    if rows > 64 and w.scale > 0:
+        return "attn_prefill_tc05x2_kernel" if rows > 128 else "attn_prefill_tc05_kernel"
+    return "attn_prefill_kernel (mma.sync)"
+
+
 def prefill_flops(w) -> int:
     """Dense causal attention FLOPs: 4 * D per (query head, key) pair, each new
     token at position p seeing p + 1 keys."""
@@ -893,10 +919,11 @@ def run_prefill(args):
         peak = float(peaks["hbm_gbs"])
         roof = {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
                 "frac": gbs / peak, "peak_source": f"{peak_src} hbm_gbs (copy, read+write)"}
-    roof.update({"kernel": "attn_prefill_kernel (pkv_attention_prefill)",
+    traffic = read_traffic("prefill_traffic.json", w.name)
+    roof.update({"kernel": prefill_kernel(w),
                  "algorithmic_flops_per_launch": flops,
                  "algorithmic_bytes_per_launch": kv_bytes, "avg_launch_ms": attn_ms,
-                 "traffic": None})
+                 "traffic": traffic["bytes_per_launch"] if traffic else None})
     value = world * (tflops if tensor_bound else gbs)
     cfg = {"workload": w.name, "num_seqs": w.num_seqs, "new_tokens": T,
            "new_tokens_per_seq": {"min": int(w.news.min()), "max": max_q},

@@ -141,12 +141,25 @@ attn_prefill_tc05x2_kernel(const __grid_constant__ PfParams p) {
       uint8_t* ring = smem + (kv ? C::V_OFF : C::K_OFF);
       if (lane == 0) prefetch_tensormap(map);
       const uint64_t policy = l2_policy_evict_normal();
-      const int sbl = K < 16 ? 1 : 0;
-      const int ncopy = C::NBOX << sbl;
+      const int sbl = K < 16 ? 1 : 0;                     // 8-token blocks: 8-row boxes
+      const int ncopy = C::NBOX << sbl;                   // <= 16: one box per lane
+      const int bi = lane >> sbl, u = lane & sbl;
+      const int half = bi >> 2, rb = bi & 3;
+      const int tr = rb * 16 + (u << 3);
+      // the block-table entry of this lane's box, loaded one key tile ahead so
+      // that its latency hides behind the wait for a free stage
+      auto table_entry = [&](int kt) -> long long {
+        const int tok = kt * kPfBN + tr;
+        if (lane >= ncopy || kt >= nkt || tok > pmax) return -1;
+        return p.block_tables[(int64_t)s * p.max_blocks_per_seq + tok / K];
+      };
+      long long phys_next = table_entry(0);
       int kt = 0;
       bool ok = true;
       for (; kt < nkt; ++kt) {
         const int stage = kt % NS;
+        const long long phys = phys_next;
+        phys_next = table_entry(kt + 1);
         if (!mbar_wait_bounded(empty + 8 * stage, ((kt / NS) & 1) ^ 1)) {
           record_error(PKV_DEVERR_TIMEOUT);
           ok = false;
@@ -154,22 +167,17 @@ attn_prefill_tc05x2_kernel(const __grid_constant__ PfParams p) {
         }
         if (lane == 0) mbar_arrive_expect_tx(full + 8 * stage, C::KBYTES);
         __syncwarp();
-        uint8_t* sb = ring + stage * C::KBYTES;
-        for (int i = lane; i < ncopy; i += 32) {
-          const int bi = i >> sbl, u = i & sbl;
-          const int half = bi >> 2, rb = bi & 3;
-          const int tr = rb * 16 + (u << 3);
+        if (lane < ncopy) {
           const int tok = kt * kPfBN + tr;
-          int row = -32;
+          int row = -32;                                  // past the last key: zero fill
           if (tok <= pmax) {
-            const int lb = tok / K;
-            const long long phys = p.block_tables[(int64_t)s * p.max_blocks_per_seq + lb];
             if (phys < 0 || phys >= p.num_blocks) {
               record_error(PKV_DEVERR_BLOCK_ID);
             } else {
-              row = (int)(phys * K + (tok - lb * K));
+              row = (int)(phys * K + (tok - (tok / K) * K));
             }
           }
+          uint8_t* sb = ring + stage * C::KBYTES;
           tma_load_3d(smem_u32(sb + half * C::KVHALF + tr * 128), map, full + 8 * stage,
                       half * 64, j, row, policy);
         }
