@@ -4,7 +4,8 @@
 A step is the whole hot path for one attention layer of a decode batch:
 copy-on-write block copies (when the workload has any), slot mapping of the
 new tokens, the slot-mapped KV write, and paged decode attention (partition
-kernel + split-K reduce).  Prints ONE JSON line (rank 0).
+kernel + split-K reduce).  The step is captured once as a CUDA graph and
+replayed (`--eager`: plain launches).  Prints ONE JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the CPU oracle, timed on host cores
@@ -324,6 +325,13 @@ def run_gpu(args):
                                                        w.num_kv_heads, w.head_dim, w.block_size,
                                                        max_len, t["q"].dtype, qd)
     workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    use_graph = not args.eager
+    # the step's inputs live back to back in one device buffer with a pinned
+    # host twin, so that the end-to-end leg moves them in one copy
+    names = ["q", "k_new", "v_new", "block_tables", "context_lens", "positions"]
+    if has_copy:
+        names.append("copy_pairs")
+    dev_stage, host_stage = staged_inputs(t, names, dev)
 
     def attention():
         if fmt == "bf16":
@@ -369,7 +377,7 @@ def run_gpu(args):
     assert ops.get_device_error(dev) == 0
 
     K = args.steps
-    if args.graph:
+    if use_graph:
         # the whole step as one graph; the attention call alone as another
         # (for the per-launch roofline timing)
         # (capture needs a side stream; replays run on the timing stream)
@@ -396,7 +404,7 @@ def run_gpu(args):
     torch.cuda.synchronize(dev)
     start.record(stream)
     for i in range(K):
-        if args.graph:
+        if use_graph:
             g_step.replay()
         else:
             prologue()
@@ -405,7 +413,7 @@ def run_gpu(args):
             ev[i][1].record(stream)
     stop.record(stream)
     torch.cuda.synchronize(dev)
-    if args.graph:
+    if use_graph:
         for i in range(K):
             ev[i][0].record(stream)
             g_attn.replay()
@@ -452,12 +460,8 @@ def run_gpu(args):
     assert ops.get_device_error(dev) == 0
 
     # ---- end to end through the public API with host buffers: the step's
-    # inputs sit back to back in one pinned host buffer and come over in one
-    # copy; the output goes back in one copy
-    names = ["q", "k_new", "v_new", "block_tables", "context_lens", "positions"]
-    if has_copy:
-        names.append("copy_pairs")
-    dev_stage, host_stage = staged_inputs(t, names, dev)
+    # inputs come over from the pinned host buffer in one copy, the step runs
+    # as timed above, the output goes back in one copy
     host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
     h2d = host_stage.numel()
     d2h = host_out.numel() * host_out.element_size()
@@ -465,8 +469,11 @@ def run_gpu(args):
 
     def e2e_step():
         dev_stage.copy_(host_stage, non_blocking=True)
-        prologue()
-        attention()
+        if use_graph:
+            g_step.replay()
+        else:
+            prologue()
+            attention()
         host_out.copy_(out, non_blocking=True)
 
     for _ in range(3):
@@ -506,7 +513,7 @@ def run_gpu(args):
     cfg["l2"] = (f"inputs larger than L2: {kv_bytes / 1e6:.0f} MB of KV read per step "
                  f"vs 129 MB L2; no flush between steps")
     cfg["parallelism"] = f"replicas x{world}" if world > 1 else "single GPU"
-    cfg["launch"] = "CUDA graph replay (one graph per step)" if args.graph else "eager launches"
+    cfg["launch"] = "CUDA graph replay (one graph per step)" if use_graph else "eager launches"
     blocks_used = int(sum(-(-int(L) // w.block_size) for L in w.context_lens))
     cfg["kv_reserved_bytes"] = blocks_used * w.block_size * w.num_kv_heads * w.head_dim * 2 * \
         (w.elem_bytes if fmt == "bf16" else 1)
@@ -1090,8 +1097,10 @@ def main(argv=None):
                          "(per-token scale)")
     ap.add_argument("--block-size", type=int, default=0,
                     help="override the workload's block size (block-size sweep); 0 keeps it")
+    ap.add_argument("--eager", action="store_true",
+                    help="decode: time eager launches instead of CUDA-graph replays of the step")
     ap.add_argument("--graph", action="store_true",
-                    help="capture the step in CUDA graphs and time graph replays")
+                    help="decode: time CUDA-graph replays of the step (the default)")
     ap.add_argument("--op", choices=["decode", "swap", "prefill"], default="decode",
                     help="decode: the decode step (default); swap: block swap GPU <-> host; "
                          "prefill: multi-query attention (workloads suffix_prefill, "
