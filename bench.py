@@ -102,7 +102,7 @@ def workload_desc(w) -> dict:
     }
 
 
-def staged_inputs(t: dict, names, dev):
+def staged_inputs(t: dict, names, dev, pin: bool = True):
     """One device buffer and one pinned host buffer holding the tensors
     t[name] back to back (256-byte aligned), so that a step's host-to-device
     transfer is a single copy; t[name] is rebound to its view of the device
@@ -113,7 +113,7 @@ def staged_inputs(t: dict, names, dev):
         offs[k] = total
         total += -(-(t[k].numel() * t[k].element_size()) // 256) * 256
     dev_buf = torch.empty(total, dtype=torch.uint8, device=dev)
-    host_buf = torch.empty(total, dtype=torch.uint8, pin_memory=True)
+    host_buf = torch.empty(total, dtype=torch.uint8, pin_memory=pin)
     for k in names:
         src = t[k].contiguous()
         n = src.numel() * src.element_size()

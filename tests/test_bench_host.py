@@ -1,0 +1,83 @@
+"""Host-side pieces of bench.py (no GPU): the staged input buffer of the
+end-to-end leg, the DRAM-traffic records and their source hashes, and the
+kernel name reported for the multi-query workloads."""
+
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import bench
+from paged_kv_cache_115_gb300 import workloads as wl
+
+
+def test_staged_inputs_views_hold_the_values():
+    g = torch.Generator().manual_seed(0)
+    t = {"q": torch.randn((5, 3, 8), generator=g).to(torch.bfloat16),
+         "tables": torch.arange(21, dtype=torch.int32).view(3, 7),
+         "pos": torch.arange(5, dtype=torch.int64),
+         "odd": torch.arange(3, dtype=torch.uint8)}
+    ref = {k: v.clone() for k, v in t.items()}
+    dev_buf, host_buf = bench.staged_inputs(t, list(t), torch.device("cpu"), pin=False)
+    assert dev_buf.numel() == host_buf.numel() and dev_buf.numel() % 256 == 0
+    for k in ref:
+        assert t[k].dtype == ref[k].dtype and t[k].shape == ref[k].shape
+        assert torch.equal(t[k], ref[k])
+        # every view starts on a 256-byte boundary of the device buffer
+        off = t[k].untyped_storage().data_ptr() - dev_buf.untyped_storage().data_ptr()
+        assert t[k].storage_offset() * t[k].element_size() % 256 == 0 and off == 0
+    # one copy of the host twin refills every view
+    dev_buf.zero_()
+    assert not torch.equal(t["tables"], ref["tables"])
+    dev_buf.copy_(host_buf)
+    for k in ref:
+        assert torch.equal(t[k], ref[k])
+
+
+def _write(root, rel, text):
+    p = os.path.join(root, rel)
+    os.makedirs(os.path.dirname(p), exist_ok=True)
+    with open(p, "w") as f:
+        f.write(text)
+
+
+def test_traffic_record_follows_its_sources(tmp_path, monkeypatch):
+    root = str(tmp_path)
+    _write(root, "src/a.cuh", "kernel a")
+    _write(root, "src/b.cuh", "kernel b")
+    monkeypatch.setattr(bench, "ROOT", root)
+    sha = bench.src_sha(["src/a.cuh", "src/b.cuh"])
+    rec = {"w1": {"sources": ["src/a.cuh", "src/b.cuh"], "kernel_src_sha": sha,
+                  "bytes_per_launch": 123.0}}
+    _write(root, "profiles/t.json", json.dumps(rec))
+    assert bench.read_traffic("t.json", "w1")["bytes_per_launch"] == 123.0
+    assert bench.read_traffic("t.json", "w2") is None          # another workload
+    assert bench.read_traffic("missing.json", "w1") is None
+    _write(root, "src/b.cuh", "kernel b, changed")
+    assert bench.read_traffic("t.json", "w1") is None          # stale after a change
+
+
+def test_committed_traffic_records_name_their_workload():
+    t = bench.read_traffic()
+    if t is not None:
+        assert t["workload"] in wl.CONFIG_NAMES and t["kv_format"] == "bf16"
+    with open(os.path.join(bench.ROOT, "profiles", "prefill_traffic.json")) as f:
+        recs = json.load(f)
+    for name, r in recs.items():
+        assert name in wl.PREFILL_NAMES and r["workload"] == name
+        assert r["bytes_per_launch"] >= r["algorithmic_bytes_per_launch"] * 0.9
+
+
+@pytest.mark.parametrize("name,kernel", [("suffix_prefill", "attn_prefill_tc05x2_kernel"),
+                                         ("speculative_decode", "attn_tc_kernel")])
+def test_prefill_kernel_name(name, kernel):
+    assert bench.prefill_kernel(wl.build_prefill(name)).startswith(kernel)
+
+
+def test_prefill_flops_closed_form():
+    # one sequence of P cached + n new tokens: sum over i < n of (P + i + 1) keys
+    class W:
+        prefix = np.array([10]); news = np.array([4]); head_dim = 2; num_q_heads = 3
+    assert bench.prefill_flops(W) == 4 * 2 * 3 * (11 + 12 + 13 + 14)
