@@ -261,6 +261,9 @@ PKV_API pkv_status pkv_selftest_wait_timeout(int64_t limit_cycles, void* stream)
  *   num_blocks * block_size floats) computed over the token's whole row (all
  *   KV heads x head_dim): scale = max|x| / 127 (float32), code =
  *   round_half_even(x / scale); an all-zero row gets scale 0 and codes 0.
+ *   The tensor-core attention kernel forms each softmax weight times its
+ *   token's V scale in f16: V scales must stay below 2048 (|v| below about
+ *   260,000); larger ones may overflow to inf in the output.
  */
 typedef enum { PKV_KV_PLAIN = 0, PKV_KV_FP8_E4M3 = 1, PKV_KV_INT8_TOKEN = 2 } pkv_kv_format;
 

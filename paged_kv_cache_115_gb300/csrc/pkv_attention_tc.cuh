@@ -89,6 +89,18 @@ __device__ __forceinline__ uint32_t s8_pair_to_f16x2(uint32_t xored, uint32_t se
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// One-byte pools: slack of the lazily raised exponent base.  Weights stay
+// below 2^4, so an INT8 weight times its token's V scale stays inside f16
+// while that scale is below 2^11 (|v| below ~260,000); the FP8 V scale
+// multiplies o once per partition instead.
+constexpr float kQuantSlack = 4.f;
+
+__device__ __forceinline__ float ex2_approx_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 template <int D, int HPC, int NS, int CT = 0>
 struct TcCfg {
   static constexpr int TL = CT ? 2 : 1;                   // 16-row tiles per chunk
@@ -447,7 +459,7 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
         vsr[t][1] = isfinite(v8) ? v8 : 0.f;
       } else {
         ksr[t][0] = ksr[t][1] = 1.f;
-        vsr[t][0] = vsr[t][1] = CT == 1 ? p.v_scale : 1.f;
+        vsr[t][0] = vsr[t][1] = 1.f;      // FP8: the V scale multiplies o at the end
       }
     }
     if (valid < CH) {
@@ -536,32 +548,69 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
       mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
       mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
     }
-    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    // a column may have seen no visible key yet (several query rows): keep
-    // its state (-inf, 0, 0) instead of forming -inf - -inf
-    const float mu0 = mn0 == -INFINITY ? 0.f : mn0, mu1 = mn1 == -INFINITY ? 0.f : mn1;
-    const float al0 = exp2f(m0 - mu0), al1 = exp2f(m1 - mu1);
     float pr[TL][4];
     float ps0 = 0.f, ps1 = 0.f;
+    if constexpr (CT == 0) {
+      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+      // a column may have seen no visible key yet (several query rows): keep
+      // its state (-inf, 0, 0) instead of forming -inf - -inf
+      const float mu0 = mn0 == -INFINITY ? 0.f : mn0, mu1 = mn1 == -INFINITY ? 0.f : mn1;
+      const float al0 = exp2f(m0 - mu0), al1 = exp2f(m1 - mu1);
 #pragma unroll
-    for (int t = 0; t < TL; ++t) {
-      pr[t][0] = exp2f(x[t][0] - mu0);
-      pr[t][1] = exp2f(x[t][1] - mu1);
-      pr[t][2] = exp2f(x[t][2] - mu0);
-      pr[t][3] = exp2f(x[t][3] - mu1);
-      ps0 += pr[t][0] + pr[t][2];
-      ps1 += pr[t][1] + pr[t][3];
-    }
-    l0 = l0 * al0 + ps0;
-    l1 = l1 * al1 + ps1;
-    m0 = mn0;
-    m1 = mn1;
+      for (int t = 0; t < TL; ++t) {
+        pr[t][0] = exp2f(x[t][0] - mu0);
+        pr[t][1] = exp2f(x[t][1] - mu1);
+        pr[t][2] = exp2f(x[t][2] - mu0);
+        pr[t][3] = exp2f(x[t][3] - mu1);
+        ps0 += pr[t][0] + pr[t][2];
+        ps1 += pr[t][1] + pr[t][3];
+      }
+      l0 = l0 * al0 + ps0;
+      l1 = l1 * al1 + ps1;
+      m0 = mn0;
+      m1 = mn1;
 #pragma unroll
-    for (int mt = 0; mt < D / 16; ++mt) {
-      o[mt][0] *= al0;
-      o[mt][1] *= al1;
-      o[mt][2] *= al0;
-      o[mt][3] *= al1;
+      for (int mt = 0; mt < D / 16; ++mt) {
+        o[mt][0] *= al0;
+        o[mt][1] *= al1;
+        o[mt][2] *= al0;
+        o[mt][3] *= al1;
+      }
+    } else {
+      // one-byte pools (consumer-bound): the exponent base m of a column is
+      // raised only when a score exceeds it by more than 2^kQuantSlack, so
+      // o and l are rescaled rarely; the weights stay below 2^kQuantSlack and
+      // the final o / l is the same softmax.  A column that has seen no
+      // visible key keeps (-inf, 0, 0).
+      const bool need = mx0 > m0 + kQuantSlack || mx1 > m1 + kQuantSlack;
+      if (__any_sync(0xffffffffu, need)) {
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const float mu0 = mn0 == -INFINITY ? 0.f : mn0, mu1 = mn1 == -INFINITY ? 0.f : mn1;
+        const float al0 = exp2f(m0 - mu0), al1 = exp2f(m1 - mu1);
+        l0 *= al0;
+        l1 *= al1;
+        m0 = mn0;
+        m1 = mn1;
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+          o[mt][0] *= al0;
+          o[mt][1] *= al1;
+          o[mt][2] *= al0;
+          o[mt][3] *= al1;
+        }
+      }
+      const float mu0 = m0 == -INFINITY ? 0.f : m0, mu1 = m1 == -INFINITY ? 0.f : m1;
+#pragma unroll
+      for (int t = 0; t < TL; ++t) {
+        pr[t][0] = ex2_approx_ftz(x[t][0] - mu0);
+        pr[t][1] = ex2_approx_ftz(x[t][1] - mu1);
+        pr[t][2] = ex2_approx_ftz(x[t][2] - mu0);
+        pr[t][3] = ex2_approx_ftz(x[t][3] - mu1);
+        ps0 += pr[t][0] + pr[t][2];
+        ps1 += pr[t][1] + pr[t][3];
+      }
+      l0 += ps0;
+      l1 += ps1;
     }
     // P enters the tensor core as a hi + lo pair of 16-bit terms so that the
     // product carries ~16 significant bits of each weight (one bf16 rounding
@@ -640,6 +689,12 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
 
     if (c == ce - 1 || c == b - 1) {
       // ---- end of partition: write the final output or a partial state
+      if constexpr (CT == 1) {
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) o[mt][e] *= p.v_scale;
+      }
       float lt0 = l0, lt1 = l1;
 #pragma unroll
       for (int off = 4; off < 32; off <<= 1) {

@@ -404,7 +404,9 @@ def kv_quant(fmt: str, k_scale: float = 1.0, v_scale: float = 1.0,
              k_token_scales: Optional[torch.Tensor] = None,
              v_token_scales: Optional[torch.Tensor] = None) -> KvQuant:
     """Describe a quantized pool: ``fmt`` "fp8" (scales per tensor) or "int8"
-    (float32 CUDA tensors of one scale per token slot)."""
+    (float32 CUDA tensors of one scale per token slot).  The description
+    holds references to the scale tensors, so that their memory lives as
+    long as it does."""
     qd = KvQuant()
     if fmt == "fp8":
         qd.format, qd.k_scale, qd.v_scale = KV_FP8_E4M3, float(k_scale), float(v_scale)
@@ -416,6 +418,7 @@ def kv_quant(fmt: str, k_scale: float = 1.0, v_scale: float = 1.0,
         qd.format = KV_INT8_TOKEN
         qd.k_token_scales = k_token_scales.data_ptr()
         qd.v_token_scales = v_token_scales.data_ptr()
+        qd._scale_tensors = (k_token_scales, v_token_scales)
     else:
         raise ValueError(f"unknown quantized format {fmt!r}")
     return qd

@@ -220,3 +220,54 @@ def test_quant_rejects_bad_descriptions(ops):
     bad.format = 2                              # int8 without scale arrays
     with pytest.raises(ops.PagedKVError, match="scale"):
         ops.paged_attention_decode_quant(q, kc, kc, bt, lens, 0.1, bad)
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "int8"])
+@pytest.mark.parametrize("kernel", [0, 1, 2])
+def test_quant_rising_scores_rescale(ops, fmt, kernel):
+    """Scores that rise along every sequence (and jump at its last token), so
+    that the running exponent base of the one-byte tensor-core path is raised
+    many times; the output must still be the oracle's softmax."""
+    lens = [40, 700, 2048, 17]
+    H_kv, G, D, K = 2, 4, 128, 16
+    w = wl.build_decode("rising", lens, G * H_kv, H_kv, D, K, "bf16", seed=3)
+    rng = np.random.default_rng(3)
+    nb = w.num_blocks
+    shape = (nb, K, H_kv, D)
+    q = torch.ones((len(lens), G * H_kv, D), dtype=torch.bfloat16)
+    # key value of position t of sequence s: 6 t / len, the last token 12
+    kval = np.zeros((nb, K), np.float32)
+    for s, L in enumerate(lens):
+        t = np.arange(L)
+        v = 6.0 * t / L
+        v[-1] = 12.0
+        kval[w.block_tables[s][t // K], t % K] = v
+    if fmt == "fp8":
+        vals = Q.e4m3_values()
+        finite = np.array([i for i in range(256) if np.isfinite(vals[i])], np.uint8)
+        fv = vals[finite]
+        near = finite[np.abs(fv[None, :] - kval.reshape(-1, 1)).argmin(axis=1)].reshape(nb, K)
+        kc = np.repeat(near[:, :, None, None], H_kv, 2).repeat(D, 3).astype(np.uint8)
+        ok = np.array([i for i in range(256) if np.isfinite(vals[i]) and abs(vals[i]) <= 8],
+                      np.uint8)
+        vc = rng.choice(ok, size=shape).astype(np.uint8)
+        qd = ops.kv_quant("fp8", 1.0, 0.75)
+        extra = dict(k_scale=1.0, v_scale=0.75)
+    else:
+        kc = np.full(shape, 100, np.int8)
+        kts = (kval.reshape(-1) / 100.0).astype(np.float32)
+        vc = rng.integers(-127, 128, size=shape).astype(np.int8)
+        vts = rng.uniform(0.002, 0.03, size=nb * K).astype(np.float32)
+        qd = ops.kv_quant("int8", k_token_scales=torch.from_numpy(kts).to(DEV),
+                          v_token_scales=torch.from_numpy(vts).to(DEV))
+        extra = dict(k_tok_scales=kts, v_tok_scales=vts)
+    out = ops.paged_attention_decode_quant(q.to(DEV), torch.from_numpy(kc).to(DEV),
+                                           torch.from_numpy(vc).to(DEV),
+                                           torch.from_numpy(w.block_tables).to(DEV),
+                                           torch.tensor(lens, dtype=torch.int32, device=DEV),
+                                           w.scale, qd, max_context_len=max(lens), kernel=kernel)
+    torch.cuda.synchronize()
+    assert ops.get_device_error() == 0
+    ref = Q.paged_attention_decode_quant(storage(q), kc, vc, w.block_tables, np.array(lens),
+                                         w.scale, "bf16", fmt, **extra)
+    check_attention(as_f64(out), ref, "bf16", f"rising {fmt} kernel={kernel}")
