@@ -653,10 +653,13 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
             // r[2u]: tokens 2tq, 2tq+1 of m tile mt + u; r[2u+1]: tokens + 8
             uint32_t a0, a1, a2, a3;
             if constexpr (CT == 1) {
-              a0 = e4m3x2_to_f16x2(__byte_perm(r[2 * u], 0u, 0x0020));
-              a1 = e4m3x2_to_f16x2(__byte_perm(r[2 * u], 0u, 0x0031));
-              a2 = e4m3x2_to_f16x2(__byte_perm(r[2 * u + 1], 0u, 0x0020));
-              a3 = e4m3x2_to_f16x2(__byte_perm(r[2 * u + 1], 0u, 0x0031));
+              // one permute makes both pairs: bytes (0, 2) low, (1, 3) high
+              const uint32_t p0 = __byte_perm(r[2 * u], 0u, 0x3120);
+              const uint32_t p1 = __byte_perm(r[2 * u + 1], 0u, 0x3120);
+              a0 = e4m3x2_to_f16x2(p0);
+              a1 = e4m3x2_to_f16x2(p0 >> 16);
+              a2 = e4m3x2_to_f16x2(p1);
+              a3 = e4m3x2_to_f16x2(p1 >> 16);
             } else {
               const uint32_t x0 = r[2 * u] ^ 0x80808080u, x1 = r[2 * u + 1] ^ 0x80808080u;
               a0 = s8_pair_to_f16x2(x0, 0x5240);
