@@ -89,6 +89,14 @@ __device__ __forceinline__ uint32_t s8_pair_to_f16x2(uint32_t xored, uint32_t se
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// Four e4m3 codes of a word -> two f16 pairs (codes 0, 1 and codes 2, 3),
+// the word's 16-bit halves handed to the conversion directly.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi) : "r"(w));
+}
+
 // One-byte pools: slack of the lazily raised exponent base.  Weights stay
 // below 2^4, so an INT8 weight times its token's V scale stays inside f16
 // while that scale is below 2^11 (|v| below ~260,000); the FP8 V scale
@@ -506,10 +514,8 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
           const uint32_t w1 = *reinterpret_cast<const uint32_t*>(kt + off + 8 * 128);
           uint32_t a0, a1, a2, a3;
           if constexpr (CT == 1) {
-            a0 = e4m3x2_to_f16x2(w0);
-            a2 = e4m3x2_to_f16x2(w0 >> 16);
-            a1 = e4m3x2_to_f16x2(w1);
-            a3 = e4m3x2_to_f16x2(w1 >> 16);
+            e4m3x4_to_f16x2x2(w0, a0, a2);
+            e4m3x4_to_f16x2x2(w1, a1, a3);
           } else {
             const uint32_t x0 = w0 ^ 0x80808080u, x1 = w1 ^ 0x80808080u;
             a0 = s8_pair_to_f16x2(x0, 0x5140);
@@ -654,12 +660,8 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
             uint32_t a0, a1, a2, a3;
             if constexpr (CT == 1) {
               // one permute makes both pairs: bytes (0, 2) low, (1, 3) high
-              const uint32_t p0 = __byte_perm(r[2 * u], 0u, 0x3120);
-              const uint32_t p1 = __byte_perm(r[2 * u + 1], 0u, 0x3120);
-              a0 = e4m3x2_to_f16x2(p0);
-              a1 = e4m3x2_to_f16x2(p0 >> 16);
-              a2 = e4m3x2_to_f16x2(p1);
-              a3 = e4m3x2_to_f16x2(p1 >> 16);
+              e4m3x4_to_f16x2x2(__byte_perm(r[2 * u], 0u, 0x3120), a0, a1);
+              e4m3x4_to_f16x2x2(__byte_perm(r[2 * u + 1], 0u, 0x3120), a2, a3);
             } else {
               const uint32_t x0 = r[2 * u] ^ 0x80808080u, x1 = r[2 * u + 1] ^ 0x80808080u;
               a0 = s8_pair_to_f16x2(x0, 0x5240);
