@@ -368,6 +368,10 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
   float o[D / 16][4];
   float slc0 = sl, slc1 = sl;   // per score column (one-byte pools: q's 2^e folded in)
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  // INT8 pools: V enters the tensor core as 1152 + code (the exact f16 the
+  // byte permute makes, without the subtraction); vw = sum of weight x V
+  // scale per column, so that 1152 vw is taken off o at the partition end
+  float vw0 = 0.f, vw1 = 0.f;
   int s = seq_of_chunk(cstart, S, cb);
   int len_s = 0;
   // this thread's score columns 2tq and 2tq+1: their query rows (-1: padding
@@ -443,6 +447,7 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
       for (int mt = 0; mt < D / 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
       m0 = m1 = -INFINITY;
       l0 = l1 = 0.f;
+      vw0 = vw1 = 0.f;
     }
     const int valid = min(CH, len_s - (c - a) * CH);   // tokens of this chunk
     const int stage = k % NS;
@@ -595,6 +600,8 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
         const float al0 = exp2f(m0 - mu0), al1 = exp2f(m1 - mu1);
         l0 *= al0;
         l1 *= al1;
+        vw0 *= al0;
+        vw1 *= al1;
         m0 = mn0;
         m1 = mn1;
 #pragma unroll
@@ -630,8 +637,14 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
         split_bf16x2(pr[t][0], pr[t][1], ph01, pl01);
         split_bf16x2(pr[t][2], pr[t][3], ph23, pl23);
       } else {
-        split_f16x2(pr[t][0] * vsr[t][0], pr[t][1] * vsr[t][0], ph01, pl01);
-        split_f16x2(pr[t][2] * vsr[t][1], pr[t][3] * vsr[t][1], ph23, pl23);
+        const float w0 = pr[t][0] * vsr[t][0], w1 = pr[t][1] * vsr[t][0];
+        const float w2 = pr[t][2] * vsr[t][1], w3 = pr[t][3] * vsr[t][1];
+        if constexpr (CT == 2) {
+          vw0 += w0 + w2;
+          vw1 += w1 + w3;
+        }
+        split_f16x2(w0, w1, ph01, pl01);
+        split_f16x2(w2, w3, ph23, pl23);
       }
       pb[t][0] = movmatrix_trans(ph01);
       pb[t][1] = movmatrix_trans(ph23);
@@ -663,11 +676,12 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
               e4m3x4_to_f16x2x2(__byte_perm(r[2 * u], 0u, 0x3120), a0, a1);
               e4m3x4_to_f16x2x2(__byte_perm(r[2 * u + 1], 0u, 0x3120), a2, a3);
             } else {
+              // 1152 + code, exact in f16 (the 1152 comes off at the partition end)
               const uint32_t x0 = r[2 * u] ^ 0x80808080u, x1 = r[2 * u + 1] ^ 0x80808080u;
-              a0 = s8_pair_to_f16x2(x0, 0x5240);
-              a1 = s8_pair_to_f16x2(x0, 0x5341);
-              a2 = s8_pair_to_f16x2(x1, 0x5240);
-              a3 = s8_pair_to_f16x2(x1, 0x5341);
+              a0 = __byte_perm(x0, 0x6464u, 0x5240);
+              a1 = __byte_perm(x0, 0x6464u, 0x5341);
+              a2 = __byte_perm(x1, 0x6464u, 0x5240);
+              a3 = __byte_perm(x1, 0x6464u, 0x5341);
             }
             mma_f16_16816(o[mt + u], a0, a1, a2, a3, pb[t][0], pb[t][1]);
             mma_f16_16816(o[mt + u], a0, a1, a2, a3, pc[t][0], pc[t][1]);
@@ -699,6 +713,21 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
         for (int mt = 0; mt < D / 16; ++mt)
 #pragma unroll
           for (int e = 0; e < 4; ++e) o[mt][e] *= p.v_scale;
+      } else if constexpr (CT == 2) {
+        float vt0 = vw0, vt1 = vw1;
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+          vt0 += __shfl_xor_sync(0xffffffffu, vt0, off);
+          vt1 += __shfl_xor_sync(0xffffffffu, vt1, off);
+        }
+        const float c0 = 1152.f * vt0, c1 = 1152.f * vt1;
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+          o[mt][0] -= c0;
+          o[mt][1] -= c1;
+          o[mt][2] -= c0;
+          o[mt][3] -= c1;
+        }
       }
       float lt0 = l0, lt1 = l1;
 #pragma unroll
