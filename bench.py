@@ -124,6 +124,45 @@ def staged_inputs(t: dict, names, dev, pin: bool = True):
     return dev_buf, host_buf
 
 
+def run_pipelined(n, sets, compute, stream, cs, start_ev=None):
+    """n end-to-end steps over two buffer sets (dev_in, host_in, dev_out,
+    host_out): step i copies host_in -> dev_in of set i % 2 on the copy stream
+    cs, computes on `stream` (compute(b) launches the step over set b), and
+    copies dev_out -> host_out on cs.  Step i+1's input copy is queued before
+    step i's output copy; a set is refilled only after the step two back has
+    read it, and its output is overwritten only after it has been copied."""
+    import torch
+    h2d_ev = [torch.cuda.Event() for _ in range(2)]
+    comp_ev = [torch.cuda.Event() for _ in range(2)]
+    d2h_ev = [torch.cuda.Event() for _ in range(2)]
+
+    def h2d_copy(i):
+        b = i & 1
+        with torch.cuda.stream(cs):
+            if i >= 2:
+                cs.wait_event(comp_ev[b])
+            sets[b][0].copy_(sets[b][1], non_blocking=True)
+            h2d_ev[b].record(cs)
+
+    if start_ev is not None:
+        cs.wait_event(start_ev)
+    h2d_copy(0)
+    for i in range(n):
+        b = i & 1
+        if i + 1 < n:
+            h2d_copy(i + 1)
+        stream.wait_event(h2d_ev[b])
+        if i >= 2:
+            stream.wait_event(d2h_ev[b])
+        compute(b)
+        comp_ev[b].record(stream)
+        with torch.cuda.stream(cs):
+            cs.wait_event(comp_ev[b])
+            sets[b][3].copy_(sets[b][2], non_blocking=True)
+            d2h_ev[b].record(cs)
+    stream.wait_stream(cs)
+
+
 # ---------------------------------------------------------------------------
 # clocks sampled during the timed region
 # ---------------------------------------------------------------------------
@@ -459,32 +498,64 @@ def run_gpu(args):
     del flush
     assert ops.get_device_error(dev) == 0
 
-    # ---- end to end through the public API with host buffers: the step's
-    # inputs come over from the pinned host buffer in one copy, the step runs
-    # as timed above, the output goes back in one copy
-    host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    # ---- end to end through the public API with host buffers.  Every step
+    # copies its inputs from a pinned host buffer (one copy) and reads its
+    # output back (one copy).  The copies run on a second stream against two
+    # sets of staged inputs and outputs, so that step i+1's input copy and
+    # step i's output copy overlap the neighbouring steps' compute.
+    out0, views0 = out, {k: t[k] for k in names}
+    t1 = dict(views0)
+    dev_stage1, host_stage1 = staged_inputs(t1, names, dev)
+    out1 = torch.empty_like(out0)
+    sets = [(dev_stage, host_stage, views0, out0), (dev_stage1, host_stage1, t1, out1)]
+    host_outs = [torch.empty(out0.shape, dtype=out0.dtype, pin_memory=True) for _ in range(2)]
     h2d = host_stage.numel()
-    d2h = host_out.numel() * host_out.element_size()
-    e2e_steps = max(1, min(K, 200))
-
-    def e2e_step():
-        dev_stage.copy_(host_stage, non_blocking=True)
-        if use_graph:
-            g_step.replay()
-        else:
+    d2h = host_outs[0].numel() * host_outs[0].element_size()
+    graphs = [g_step] if use_graph else []
+    if use_graph:
+        # the same step over the second set (closures read t and out when called)
+        for k in names:
+            t[k] = t1[k]
+        out = out1
+        g1 = torch.cuda.CUDAGraph()
+        cap.wait_stream(stream)
+        with torch.cuda.graph(g1, stream=cap):
             prologue()
             attention()
-        host_out.copy_(out, non_blocking=True)
+        stream.wait_stream(cap)
+        graphs.append(g1)
+        for k in names:
+            t[k] = views0[k]
+        out = out0
+        torch.cuda.synchronize(dev)
+    cs = torch.cuda.Stream(dev)
+    pipe_sets = [(sets[i][0], sets[i][1], sets[i][3], host_outs[i]) for i in range(2)]
 
-    for _ in range(3):
-        e2e_step()
+    def e2e_compute(b):
+        nonlocal out
+        if use_graph:
+            graphs[b].replay()
+            return
+        for k in names:
+            t[k] = sets[b][2][k]
+        out = sets[b][3]
+        prologue()
+        attention()
+        for k in names:
+            t[k] = views0[k]
+        out = out0
+
+    def e2e_run(n, start_ev=None):
+        run_pipelined(n, pipe_sets, e2e_compute, stream, cs, start_ev)
+
+    e2e_steps = max(4, min(K, 200))
+    e2e_run(4)
     torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         dist.barrier()
     e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
+    e2e_run(e2e_steps, start_ev=e0)
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
@@ -550,7 +621,10 @@ def run_gpu(args):
         },
         "e2e": {"value": e2e_value, "unit": "GB/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "decode_tokens_per_s_per_layer": world * w.num_seqs / (e2e_ms * 1e-3)},
+                "decode_tokens_per_s_per_layer": world * w.num_seqs / (e2e_ms * 1e-3),
+                "copies": "per step one pinned-host-to-device copy of the inputs and one "
+                          "device-to-pinned-host copy of the output, on a second stream with "
+                          "two staged buffer sets, overlapping the neighbouring steps"},
         "rows": rows,
         "gpu_launches": launches_per_step * K,
         "clocks": clock_info,
@@ -909,24 +983,36 @@ def run_prefill(args):
     attn_ms = sum(a.elapsed_time(b) for a, b in ev) / K
     assert ops.get_device_error(dev) == 0
 
-    # end to end: host buffers in, output back, through the public calls
-    pin = {"q": q.cpu().pin_memory(), "k": k_new.cpu().pin_memory(),
-           "v": v_new.cpu().pin_memory(), "bt": bt.cpu().pin_memory(),
-           "cu": cu.cpu().pin_memory(), "lens": lens.cpu().pin_memory()}
-    dst = {"q": q, "k": k_new, "v": v_new, "bt": bt, "cu": cu, "lens": lens}
-    host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-    h2d = sum(v.numel() * v.element_size() for v in pin.values())
-    d2h = host_out.numel() * host_out.element_size()
-    e2e_steps = max(3, min(K, 50))
+    # end to end through the public calls: every step copies its inputs (q,
+    # the new K/V rows, tables, cu_seqlens, lengths) from one pinned host
+    # buffer and reads its output back, on a second stream with two staged
+    # buffer sets that overlap the neighbouring steps' compute
+    base = {"q": q, "k": k_new, "v": v_new, "bt": bt, "cu": cu, "lens": lens}
+    names = list(base)
+    sets = []
+    for _ in range(2):
+        views = dict(base)
+        dev_in, host_in = staged_inputs(views, names, dev)
+        o = torch.empty_like(out)
+        sets.append((dev_in, host_in, o, torch.empty(o.shape, dtype=o.dtype, pin_memory=True),
+                     views))
+    h2d = sets[0][1].numel()
+    d2h = sets[0][3].numel() * sets[0][3].element_size()
+    cs = torch.cuda.Stream(dev)
+
+    def e2e_compute(b_):
+        x = sets[b_][4]
+        ops.paged_kv_append_varlen(x["k"], x["v"], x["cu"], x["lens"], x["bt"], kc, vc)
+        ops.paged_attention_prefill(x["q"], kc, vc, x["bt"], x["cu"], x["lens"], w.scale, max_q,
+                                    max_len, out=sets[b_][2], workspace=workspace)
+
+    pipe_sets = [st[:4] for st in sets]
+    run_pipelined(3, pipe_sets, e2e_compute, stream, cs)
+    e2e_steps = max(4, min(K, 50))
     torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(e2e_steps):
-        for k_, v_ in pin.items():
-            dst[k_].copy_(v_, non_blocking=True)
-        append()
-        attention()
-        host_out.copy_(out, non_blocking=True)
+    run_pipelined(e2e_steps, pipe_sets, e2e_compute, stream, cs, e0)
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
@@ -981,7 +1067,10 @@ def run_prefill(args):
         "e2e": {"value": world * (flops if tensor_bound else kv_bytes) / (e2e_ms * 1e-3) /
                 (1e12 if tensor_bound else 1e9),
                 "unit": "TFLOP/s" if tensor_bound else "GB/s", "ms_per_step": e2e_ms,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "copies": "per step one pinned-host-to-device copy of the inputs and one "
+                          "device-to-pinned-host copy of the output, on a second stream with "
+                          "two staged buffer sets, overlapping the neighbouring steps"},
         "gpu_launches": launches_per_step * K,
         "clocks": clock_info,
     }
