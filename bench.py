@@ -559,6 +559,10 @@ def run_gpu(args):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    # the same inputs in both sets: the outputs read back equal the timed step's
+    ref_out = out0.cpu()
+    for h in host_outs:
+        assert torch.equal(h.view(torch.int16), ref_out.view(torch.int16)), "e2e output differs"
 
     # ---- max over ranks
     total_ms, e2e_ms, attn_avg_ms = max_over_ranks([total_ms, e2e_ms, attn_avg_ms], dev)
@@ -1016,6 +1020,11 @@ def run_prefill(args):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    # the same inputs in both sets: the outputs read back equal the timed step's
+    ref_out = out.cpu()
+    for st in sets:
+        assert torch.equal(st[3].view(torch.int16), ref_out.view(torch.int16)), \
+            "e2e output differs"
 
     total_ms, attn_ms, e2e_ms = max_over_ranks([total_ms, attn_ms, e2e_ms], dev)
     ms_step = total_ms / K
