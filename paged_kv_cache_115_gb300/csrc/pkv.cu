@@ -442,7 +442,7 @@ pkv_status launch_tc_d(int hpc, const pkv::TcParams& prm, int n, int groups, cud
 // one-byte codes), 128-byte swizzle.
 pkv_status encode_pool_map(CUtensorMap* map, const void* pool, int64_t num_blocks, int K, int H_kv,
                            int D, bool one_byte = false) {
-  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
   pkv_status st = get_encode(&enc);
   if (st != PKV_OK) return st;
   const cuuint64_t eb = one_byte ? 1 : 2;
