@@ -315,13 +315,21 @@ class PrefillWorkload:
 def build_prefill(name: str, seed: int = 0) -> PrefillWorkload:
     """``suffix_prefill``: 32 requests that hit a cached prefix of U[1024, 4096]
     tokens and prefill a 512-token suffix ("推理与 KV Cache 02", 前缀索引与
-    Block Table), Mistral-7B attention shape.  ``speculative_decode``: the
+    Block Table), Mistral-7B attention shape.  ``chunked_prefill``: 64
+    requests with U[1024, 4096] tokens already cached, each prefilling its
+    next 32-token chunk ("KV Cache：长上下文为什么吃显存，PagedAttention 怎么救"
+    §06: a long prompt's prefill cut into small chunks interleaved with decode
+    steps), Mistral-7B attention shape.  ``speculative_decode``: the
     Qwen3-0.6B decode batch (64 sequences, U[512, 4096] cached tokens) with 4
     candidate tokens each ("企业官网建设流程全解析" §8.2)."""
     rng = np.random.default_rng(20_000 + seed)
     if name == "suffix_prefill":
         prefix = rng.integers(1024, 4096 + 1, size=32)
         news = np.full(32, 512)
+        H_q, H_kv, D, K = 32, 8, 128, 16
+    elif name == "chunked_prefill":
+        prefix = rng.integers(1024, 4096 + 1, size=64)
+        news = np.full(64, 32)
         H_q, H_kv, D, K = 32, 8, 128, 16
     elif name == "speculative_decode":
         prefix = rng.integers(512, 4096 + 1, size=64)
@@ -345,4 +353,4 @@ def build_prefill(name: str, seed: int = 0) -> PrefillWorkload:
                            scale=1.0 / math.sqrt(D))
 
 
-PREFILL_NAMES = ("suffix_prefill", "speculative_decode")
+PREFILL_NAMES = ("suffix_prefill", "chunked_prefill", "speculative_decode")

@@ -3,8 +3,9 @@ bench.py times: sampled outputs against the oracle computed one by one.
 
 * FP8 / INT8 pools at the Mistral-7B-shaped decode size (quantizing append +
   attention, automatic kernel choice);
-* the multi-query workloads suffix_prefill (tcgen05 kernel) and
-  speculative_decode (stream-K decode kernel with several query rows);
+* the multi-query workloads suffix_prefill (two-tile tcgen05 kernel),
+  chunked_prefill (single-tile tcgen05 kernel) and speculative_decode
+  (stream-K decode kernel with several query rows);
 * the block swap workload (every other sequence out to pinned host memory and
   back into a permutation of the blocks).
 """
@@ -116,7 +117,7 @@ def test_quant_full_size_sampled(ops, fmt):
         check_attention(outf[s, h], ref, "bf16", f"{fmt} s={s} h={h}")
 
 
-@pytest.mark.parametrize("name", ["suffix_prefill", "speculative_decode"])
+@pytest.mark.parametrize("name", ["suffix_prefill", "chunked_prefill", "speculative_decode"])
 def test_prefill_full_size_sampled(ops, name):
     w = wl.build_prefill(name)
     K, H, D, H_q = w.block_size, w.num_kv_heads, w.head_dim, w.num_q_heads
