@@ -858,12 +858,14 @@ PREFILL_METRIC = "paged multi-query attention (prefill) TFLOP/s and KV GB/s"
 def prefill_kernel(w) -> str:
     """The kernel the automatic prefill plan picks for workload w (mirrors
     the library's plan: up to 8 query rows per KV head -> the stream-K decode
-    kernel; more than 64 -> tcgen05, two query tiles per CTA above 128)."""
+    kernel; more than 64 -> tcgen05, two query tiles per CTA above 128 and
+    one below)."""
     rows = int(w.news.max()) * (w.num_q_heads // w.num_kv_heads)
     if rows <= 8 and w.num_seqs <= 2048:
         return "attn_tc_kernel (stream-K decode kernel, query rows as score columns)"
     if rows > 64 and w.scale > 0:
-        return "attn_prefill_tc05x2_kernel" if rows > 128 else "attn_prefill_tc05_kernel"
+        return ("attn_prefill_tc05x2_kernel" if rows > 128
+                else "attn_prefill_tc05x2_kernel (one query tile per CTA)")
     return "attn_prefill_kernel (mma.sync)"
 
 

@@ -379,8 +379,9 @@ PKV_API pkv_status pkv_attention_decode_quant(
  *                  KV head (max_query_len x num_q_heads / num_kv_heads): up
  *                  to 8 -> the stream-K decode kernel; 9 .. 64, or scale <= 0
  *                  -> mma.sync tiles of 16 / 32 / 64 rows; more -> tcgen05
- *                  tiles of 128 rows (two per CTA, sharing every K/V tile,
- *                  above 128 rows).  1 = tcgen05 (scale > 0, no split),
+ *                  tiles of 128 rows (two per CTA sharing every K/V tile; one
+ *                  per CTA when no KV head has more than 128 rows).
+ *                  1 = tcgen05 (scale > 0, no split),
  *                  2 = mma.sync, 3 = stream-K decode kernel (at most 8 rows
  *                  per KV head, at most 2048 sequences, no split).
  *                  num_splits (mma.sync

@@ -289,46 +289,29 @@ struct PfInst {
 template <int D, int NW> std::once_flag PfInst<D, NW>::flags[kMaxDevices];
 template <int D, int NW> cudaError_t PfInst<D, NW>::errs[kMaxDevices];
 
-template <int D>
-struct T5Inst {
-  using C = pkv::T5Cfg<D>;
-  static std::once_flag flags[kMaxDevices];
-  static cudaError_t errs[kMaxDevices];
-  static pkv_status launch(const pkv::PfParams& prm, int tiles, int H_kv, int S, cudaStream_t st,
-                           int dev) {
-    auto k = pkv::attn_prefill_tc05_kernel<D>;
-    pkv_status s = set_smem_once(k, C::SMEM, flags, errs, dev);
-    if (s != PKV_OK) return s;
-    PKV_CUDA(launch_pdl(k, dim3(tiles, H_kv, S), dim3(C::THREADS), (size_t)C::SMEM, st, prm));
-    return PKV_OK;
-  }
-};
-template <int D> std::once_flag T5Inst<D>::flags[kMaxDevices];
-template <int D> cudaError_t T5Inst<D>::errs[kMaxDevices];
 
-template <int D>
+template <int D, bool SOLO>
 struct X2Inst {
   using C = pkv::X2Cfg<D>;
   static std::once_flag flags[kMaxDevices];
   static cudaError_t errs[kMaxDevices];
   static pkv_status launch(const pkv::PfParams& prm, int pairs, int H_kv, int S, cudaStream_t st,
                            int dev) {
-    auto k = pkv::attn_prefill_tc05x2_kernel<D>;
+    auto k = pkv::attn_prefill_tc05x2_kernel<D, SOLO>;
     pkv_status s = set_smem_once(k, C::SMEM, flags, errs, dev);
     if (s != PKV_OK) return s;
     PKV_CUDA(launch_pdl(k, dim3(pairs, H_kv, S), dim3(C::THREADS), (size_t)C::SMEM, st, prm));
     return PKV_OK;
   }
 };
-template <int D> std::once_flag X2Inst<D>::flags[kMaxDevices];
-template <int D> cudaError_t X2Inst<D>::errs[kMaxDevices];
+template <int D, bool SOLO> std::once_flag X2Inst<D, SOLO>::flags[kMaxDevices];
+template <int D, bool SOLO> cudaError_t X2Inst<D, SOLO>::errs[kMaxDevices];
 
 // Query rows per KV head and tile: 16 per consumer warp, 1, 2 or 4 warps.
 int prefill_warps(int64_t rows) { return rows <= 16 ? 1 : (rows <= 32 ? 2 : 4); }
 
 struct PrefillPlan {
   bool tc05 = false;
-  bool x2 = false;         // tcgen05 kernel with two query tiles per CTA
   bool dec = false;        // stream-K decode kernel with several query rows per sequence
   AttnPlan ap;             // its plan
   int nw = 1;              // mma.sync kernel: consumer warps (16 rows each)
@@ -415,7 +398,6 @@ pkv_status plan_prefill(int num_seqs, int num_tokens, int max_query_len, int max
     }
   }
   // two 128-row tiles per CTA once a KV head has more than one
-  p.x2 = p.tc05 && p.tiles > 1;
   PKV_CHECK(p.tiles * p.nsp <= 2147483647, PKV_ERR_UNSUPPORTED, "too many query rows");
   if (p.nsp > 1) {
     const size_t T = (size_t)num_tokens;
@@ -1235,14 +1217,16 @@ pkv_status pkv_attention_prefill(const void* q, const void* k_cache, const void*
   }
   cudaStream_t strm = as_stream(stream);
   const int grid_x = (int)(plan.tiles * plan.nsp);
-  if (plan.tc05 && plan.x2) {
-    const int pairs = (int)ceil_div(plan.tiles, 2);
-    if (head_dim == 128) return X2Inst<128>::launch(prm, pairs, num_kv_heads, num_seqs, strm, dev);
-    return X2Inst<64>::launch(prm, pairs, num_kv_heads, num_seqs, strm, dev);
-  }
   if (plan.tc05) {
-    if (head_dim == 128) return T5Inst<128>::launch(prm, grid_x, num_kv_heads, num_seqs, strm, dev);
-    return T5Inst<64>::launch(prm, grid_x, num_kv_heads, num_seqs, strm, dev);
+    // two query tiles per CTA sharing each K / V tile; one (SOLO) when every
+    // (sequence, KV head) has a single tile
+    const int pairs = (int)ceil_div(plan.tiles, 2);
+    if (plan.tiles == 1) {
+      if (head_dim == 128) return X2Inst<128, true>::launch(prm, 1, num_kv_heads, num_seqs, strm, dev);
+      return X2Inst<64, true>::launch(prm, 1, num_kv_heads, num_seqs, strm, dev);
+    }
+    if (head_dim == 128) return X2Inst<128, false>::launch(prm, pairs, num_kv_heads, num_seqs, strm, dev);
+    return X2Inst<64, false>::launch(prm, pairs, num_kv_heads, num_seqs, strm, dev);
   }
   const int nw = plan.nw;
   if (head_dim == 128) {

@@ -1,6 +1,6 @@
 // Multi-query paged attention on tcgen05 with two 128-row query tiles per CTA.
-// Same function as attn_prefill_kernel / attn_prefill_tc05_kernel (new token
-// i of n at position len - n + i attends to positions 0 .. itself).
+// Same function as attn_prefill_kernel (new token i of n at position
+// len - n + i attends to positions 0 .. itself), for tiles of 128 query rows.
 //
 // The two query tiles (A: rows r0 .. r0+127, B: the next 128 rows of the same
 // KV head and sequence) share every K and V tile: one TMA load feeds
@@ -55,7 +55,9 @@ struct X2Cfg {
   static constexpr uint32_t IDESC_PV = umma_idesc_bf16(kT5Rows, D, 0, 1);
 };
 
-template <int D>
+// SOLO: every (sequence, KV head) has at most one 128-row query tile; tile B
+// is then never used (its warps only stage their empty Q rows).
+template <int D, bool SOLO>
 __global__ void __launch_bounds__(X2Cfg<D>::THREADS, 1)
 attn_prefill_tc05x2_kernel(const __grid_constant__ PfParams p) {
   using C = X2Cfg<D>;
@@ -128,8 +130,10 @@ attn_prefill_tc05x2_kernel(const __grid_constant__ PfParams p) {
     pmax = L - n + min(R - 1, r0 + 2 * kT5Rows - 1) / G;  // last key any row of the pair sees
     nkt = pmax / kPfBN + 1;
   }
-  // tile B has rows only when R > r0 + 128; without rows it still runs its
-  // (masked) softmax so that every barrier count stays the same
+  // tiles per CTA.  With SOLO only tile A; otherwise both, and a tile B
+  // without rows (R <= r0 + 128) still runs its masked softmax so that every
+  // barrier count stays the same
+  constexpr int ntiles = SOLO ? 1 : 2;
 
   if (warp == 8 || warp == 10) {
     // =================== TMA producers: warp 8 K tiles, warp 10 V tiles ===================
@@ -201,7 +205,7 @@ attn_prefill_tc05x2_kernel(const __grid_constant__ PfParams p) {
             break;
           }
           const uint32_t kb = sbase + C::K_OFF + stage * C::KBYTES;
-          for (int x = 0; x < 2 && ok; ++x) {
+          for (int x = 0; x < ntiles && ok; ++x) {
             // S buffer b of tile x holds P(kt - 2) until O += P(kt - 2) V is done
             if (kt >= 2 && !mbar_wait_bounded(p_free(x, b), ((kt >> 1) - 1) & 1)) {
               ok = false;
@@ -219,6 +223,7 @@ attn_prefill_tc05x2_kernel(const __grid_constant__ PfParams p) {
             umma_commit(s_full(x, b));
             umma_commit(k_empty + 8 * stage);
           }
+          if (SOLO && ok) umma_commit(k_empty + 8 * stage);   // the slot's second arrival
         }
       } else {
         for (int t = 0; t < nkt && ok; ++t) {
@@ -228,7 +233,7 @@ attn_prefill_tc05x2_kernel(const __grid_constant__ PfParams p) {
             break;
           }
           const uint32_t vb = sbase + C::V_OFF + stage * C::KBYTES;
-          for (int x = 0; x < 2 && ok; ++x) {
+          for (int x = 0; x < ntiles && ok; ++x) {
             if (!mbar_wait_bounded(p_full(x, t & 1), (t >> 1) & 1)) {
               ok = false;
               break;
@@ -282,7 +287,8 @@ attn_prefill_tc05x2_kernel(const __grid_constant__ PfParams p) {
     }
     const float sl = p.scale_log2;
     float m_used = 0.f, l = 0.f;
-    for (int kt = 0; kt < nkt && ok; ++kt) {
+    const int my_nkt = x < ntiles ? nkt : 0;     // a tile without rows stops here
+    for (int kt = 0; kt < my_nkt && ok; ++kt) {
       const int b = kt & 1;
       ok = __all_sync(0xffffffffu, mbar_wait_bounded(s_full(x, b), (kt >> 1) & 1));
       if (!ok) break;
@@ -379,7 +385,7 @@ attn_prefill_tc05x2_kernel(const __grid_constant__ PfParams p) {
       mbar_arrive(p_full(x, b));
     }
     // ---- epilogue: O / l from TMEM to the output rows
-    if (active && ok) {
+    if (active && ok && my_nkt > 0) {
       // o_done may still be two phases behind here; the last buffer's P-free
       // commit follows every O += P V of this tile
       ok = __all_sync(0xffffffffu,

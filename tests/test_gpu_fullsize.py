@@ -4,7 +4,7 @@ bench.py times: sampled outputs against the oracle computed one by one.
 * FP8 / INT8 pools at the Mistral-7B-shaped decode size (quantizing append +
   attention, automatic kernel choice);
 * the multi-query workloads suffix_prefill (two-tile tcgen05 kernel),
-  chunked_prefill (single-tile tcgen05 kernel) and speculative_decode
+  chunked_prefill (tcgen05 kernel, one query tile per CTA) and speculative_decode
   (stream-K decode kernel with several query rows);
 * the block swap workload (every other sequence out to pinned host memory and
   back into a permutation of the blocks).
