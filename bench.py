@@ -857,13 +857,14 @@ PREFILL_METRIC = "paged multi-query attention (prefill) TFLOP/s and KV GB/s"
 
 def prefill_kernel(w) -> str:
     """The kernel the automatic prefill plan picks for workload w (mirrors
-    the library's plan: up to 8 query rows per KV head -> the stream-K decode
-    kernel; more than 64 -> tcgen05, two query tiles per CTA above 128 and
-    one below)."""
+    the library's plan on a 152-SM GB300: up to 8 query rows per KV head ->
+    the stream-K decode kernel; more -> tcgen05 (two query tiles per CTA
+    above 128 rows, one below), unless 9 .. 64 rows come with fewer
+    (sequence, KV head) pairs than SMs -> mma.sync)."""
     rows = int(w.news.max()) * (w.num_q_heads // w.num_kv_heads)
     if rows <= 8 and w.num_seqs <= 2048:
         return "attn_tc_kernel (stream-K decode kernel, query rows as score columns)"
-    if rows > 64 and w.scale > 0:
+    if w.scale > 0 and (rows > 64 or w.num_seqs * w.num_kv_heads >= 152):
         return ("attn_prefill_tc05x2_kernel" if rows > 128
                 else "attn_prefill_tc05x2_kernel (one query tile per CTA)")
     return "attn_prefill_kernel (mma.sync)"

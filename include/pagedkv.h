@@ -377,10 +377,11 @@ PKV_API pkv_status pkv_attention_decode_quant(
  *   k_cache, v_cache, block_tables: as pkv_attention_decode.
  *   config:        NULL or kernel 0 = automatic, by the query rows of one
  *                  KV head (max_query_len x num_q_heads / num_kv_heads): up
- *                  to 8 -> the stream-K decode kernel; 9 .. 64, or scale <= 0
- *                  -> mma.sync tiles of 16 / 32 / 64 rows; more -> tcgen05
- *                  tiles of 128 rows (two per CTA sharing every K/V tile; one
- *                  per CTA when no KV head has more than 128 rows).
+ *                  to 8 -> the stream-K decode kernel; more -> tcgen05 tiles
+ *                  of 128 rows (two per CTA sharing every K/V tile; one per
+ *                  CTA when no KV head has more than 128 rows), except that
+ *                  9 .. 64 rows with fewer (sequence, KV head) pairs than SMs,
+ *                  or scale <= 0, take mma.sync tiles of 16 / 32 / 64 rows.
  *                  1 = tcgen05 (scale > 0, no split),
  *                  2 = mma.sync, 3 = stream-K decode kernel (at most 8 rows
  *                  per KV head, at most 2048 sequences, no split).

@@ -378,7 +378,18 @@ pkv_status plan_prefill(int num_seqs, int num_tokens, int max_query_len, int max
   }
   // tcgen05 tiles of 128 rows once a KV head has more than 64 query rows;
   // mma.sync tiles of 16 / 32 / 64 rows below that
-  p.tc05 = cfg.kernel == 1 || (cfg.kernel == 0 && cfg.num_splits <= 1 && rows > 64 && scale > 0.f);
+  // tcgen05 tiles of 128 rows: above 64 rows per KV head always; from 9 rows
+  // when the launch has at least one 128-row tile per SM (padding rows cost
+  // tensor work only, and these launches are bandwidth-bound); below that the
+  // mma.sync kernel, which can split the key range over more CTAs
+  bool tc05_auto = cfg.kernel == 0 && cfg.num_splits <= 1 && rows > 8 && scale > 0.f;
+  if (tc05_auto && rows <= 64) {
+    int dev = 0, sms = 0;
+    pkv_status st = device_facts(&dev, &sms);
+    if (st != PKV_OK) return st;
+    tc05_auto = (int64_t)H_kv * std::max(num_seqs, 1) >= sms;
+  }
+  p.tc05 = cfg.kernel == 1 || tc05_auto;
   p.nw = prefill_warps(rows);
   p.tiles = std::max<int64_t>(1, ceil_div(rows, p.tc05 ? pkv::kT5Rows : 16 * p.nw));
   const int64_t max_tiles = std::max<int64_t>(1, ceil_div(max_context_len, pkv::kPfBN));

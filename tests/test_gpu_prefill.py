@@ -268,3 +268,18 @@ def test_multi_token_decode_kernel_counts(ops):
     with pytest.raises(ops.PagedKVError):
         ops.paged_attention_prefill(d["q"], d["kc"], d["vc"], bt, cu, bad, pb["scale"], 5, 42,
                                     kernel=3)
+
+
+@pytest.mark.parametrize("n", [3, 4, 16])
+def test_few_rows_many_pairs_automatic(ops, n):
+    # 9 .. 64 query rows per KV head with at least as many (sequence, KV head)
+    # pairs as SMs: the automatic plan takes one tcgen05 tile per CTA (mostly
+    # padding rows); the result must match the oracle and the mma.sync kernel
+    S, H_kv, G = 40, 4, 4
+    rng = np.random.default_rng(60 + n)
+    prefix = [int(x) for x in rng.integers(0, 300, size=S)]
+    pb = prefill_problem(prefix, [n] * S, G * H_kv, H_kv, 128, 16, seed=70 + n)
+    full_check(ops, pb, f"automatic n={n}")
+    _, _, out_tc = run_gpu(ops, pb, kernel=1)
+    _, _, out_ms = run_gpu(ops, pb, kernel=2)
+    check_attention(as_f64(out_tc), as_f64(out_ms), "bf16", f"tcgen05 vs mma.sync n={n}")
