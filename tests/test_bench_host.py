@@ -71,6 +71,7 @@ def test_committed_traffic_records_name_their_workload():
 
 
 @pytest.mark.parametrize("name,kernel", [("suffix_prefill", "attn_prefill_tc05x2_kernel"),
+                                         ("chunked_prefill", "attn_prefill_tc05x2_kernel (one"),
                                          ("speculative_decode", "attn_tc_kernel")])
 def test_prefill_kernel_name(name, kernel):
     assert bench.prefill_kernel(wl.build_prefill(name)).startswith(kernel)
