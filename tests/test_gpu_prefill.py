@@ -270,16 +270,17 @@ def test_multi_token_decode_kernel_counts(ops):
                                     kernel=3)
 
 
+@pytest.mark.parametrize("D,K", [(128, 16), (64, 8), (128, 32)])
 @pytest.mark.parametrize("n", [3, 4, 16])
-def test_few_rows_many_pairs_automatic(ops, n):
+def test_few_rows_many_pairs_automatic(ops, n, D, K):
     # 9 .. 64 query rows per KV head with at least as many (sequence, KV head)
     # pairs as SMs: the automatic plan takes one tcgen05 tile per CTA (mostly
     # padding rows); the result must match the oracle and the mma.sync kernel
     S, H_kv, G = 40, 4, 4
     rng = np.random.default_rng(60 + n)
     prefix = [int(x) for x in rng.integers(0, 300, size=S)]
-    pb = prefill_problem(prefix, [n] * S, G * H_kv, H_kv, 128, 16, seed=70 + n)
-    full_check(ops, pb, f"automatic n={n}")
+    pb = prefill_problem(prefix, [n] * S, G * H_kv, H_kv, D, K, seed=70 + n + D + K)
+    full_check(ops, pb, f"automatic n={n} D={D} K={K}")
     _, _, out_tc = run_gpu(ops, pb, kernel=1)
     _, _, out_ms = run_gpu(ops, pb, kernel=2)
-    check_attention(as_f64(out_tc), as_f64(out_ms), "bf16", f"tcgen05 vs mma.sync n={n}")
+    check_attention(as_f64(out_tc), as_f64(out_ms), "bf16", f"tcgen05 vs mma.sync n={n} D={D} K={K}")
