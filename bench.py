@@ -1098,8 +1098,11 @@ def run_prefill(args):
                            cwd=ROOT, timeout=600)
         if r.returncode == 0:
             res = json.loads(r.stdout.strip().splitlines()[-1])
+            # in the line's own unit (K/V bytes taken as the sample's share of FLOPs)
+            cpu_v = (res["flops"] / res["seconds"] / 1e12 if tensor_bound else
+                     res["flops"] / flops * kv_bytes / res["seconds"] / 1e9)
             line["cpu_baseline"] = {
-                "value": res["flops"] / res["seconds"] / 1e12, "unit": "TFLOP/s", "cores": 1,
+                "value": cpu_v, "unit": "TFLOP/s" if tensor_bound else "GB/s", "cores": 1,
                 "kind": "oracle",
                 "sample": f"fp64 numpy oracle, single-threaded, {res['tokens']} of the first "
                           f"sequence's new tokens ({res['seconds']:.1f} s)"}
@@ -1126,17 +1129,25 @@ def run_reference(args):
             r = _prefill_cpu_sample(args.workload, args.seed, per_step)
             fl += r["flops"]
             sec += r["seconds"]
-        value = fl / sec / 1e12
+        # the GPU arm's unit: TFLOP/s when the workload is tensor-bound, else
+        # K/V GB/s, the sample's bytes taken as its share of the workload's FLOPs
+        pw = wl.build_prefill(args.workload, seed=args.seed)
+        total_flops = prefill_flops(pw)
+        total_bytes = int(pw.context_lens.sum()) * pw.num_kv_heads * pw.head_dim * 2 * 2
+        if total_flops / total_bytes > 400:
+            value, unit = fl / sec / 1e12, "TFLOP/s"
+        else:
+            value, unit = fl / total_flops * total_bytes / sec / 1e9, "GB/s"
         return {
-            "impl": "reference", "metric": PREFILL_METRIC, "value": value, "unit": "TFLOP/s",
+            "impl": "reference", "metric": PREFILL_METRIC, "value": value, "unit": unit,
             "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": sec / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": args.workload},
-            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+            "cpu_baseline": {"value": value, "unit": unit, "cores": 1, "kind": "oracle",
                              "sample": "fp64 numpy oracle on the first sequence's last new "
                                        "tokens"},
-            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0},
             "gpu_launches": 0,
         }
