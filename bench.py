@@ -1216,7 +1216,7 @@ def main(argv=None):
     ap.add_argument("--op", choices=["decode", "swap", "prefill"], default="decode",
                     help="decode: the decode step (default); swap: block swap GPU <-> host; "
                          "prefill: multi-query attention (workloads suffix_prefill, "
-                         "speculative_decode)")
+                         "chunked_prefill, speculative_decode)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of CPU work for the oracle baseline sample")

@@ -82,3 +82,26 @@ def test_prefill_flops_closed_form():
     class W:
         prefix = np.array([10]); news = np.array([4]); head_dim = 2; num_q_heads = 3
     assert bench.prefill_flops(W) == 4 * 2 * 3 * (11 + 12 + 13 + 14)
+
+
+def _reference_line(argv, capsys):
+    bench.main(argv)
+    out = capsys.readouterr().out.strip().splitlines()[-1]
+    return json.loads(out)
+
+
+def test_reference_arm_decode(capsys):
+    d = _reference_line(["--impl", "reference", "--workload", "tiny", "--steps", "1",
+                         "--warmup", "1", "--cpu-budget", "1"], capsys)
+    assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
+    assert d["e2e"]["value"] == d["value"] and d["gpu_launches"] == 0
+
+
+@pytest.mark.parametrize("name,unit", [("chunked_prefill", "GB/s"),
+                                       ("speculative_decode", "GB/s")])
+def test_reference_arm_prefill_units(capsys, name, unit):
+    # bandwidth-bound multi-query workloads report K/V GB/s, like the GPU arm
+    d = _reference_line(["--impl", "reference", "--op", "prefill", "--workload", name,
+                         "--steps", "1", "--warmup", "1", "--cpu-budget", "1"], capsys)
+    assert d["unit"] == unit and d["cpu_baseline"]["unit"] == unit and d["value"] > 0
