@@ -17,10 +17,12 @@
 // O += P V issue.  P (split hi + lo bf16) is written by the softmax over the
 // S buffer it came from and read from TMEM by the O += P V product (A operand
 // in tensor memory); the S buffer is free again when that product is done.
-// K and V rings are 5 deep.  The exponent base of a row is raised only when its maximum
-// grows by more than 2^8 (O rescaled in TMEM rarely).  Every wait is bounded
-// and records PKV_DEVERR_TIMEOUT; TMEM is freed on every path after both
-// issuing threads have seen their MMAs complete.
+// K and V rings are 5 deep.  The exponent base of a row is raised only when
+// its maximum grows by more than 2^8 (O rescaled in TMEM rarely).  Compiled
+// with SOLO (every KV head has at most one tile), tile B is switched off: no
+// tile-B products, softmax or barriers.  Every wait is bounded and records
+// PKV_DEVERR_TIMEOUT; TMEM is freed on every path after both issuing threads
+// have seen their MMAs complete.
 #pragma once
 
 #include "pkv_prefill_tc05.cuh"
