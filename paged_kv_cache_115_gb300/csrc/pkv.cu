@@ -249,7 +249,7 @@ pkv::Workspace carve_workspace(void* ws, const AttnPlan& p, int H_q, int D) {
 }
 
 // ---- tensor-core kernel dispatch ------------------------------------------------
-template <int D, int HPC, int CT>
+template <int D, int HPC, int CT, bool B8>
 struct TcInst {
   // stages: as many as fit in ~192 KiB (bf16) / ~203 KiB (one-byte pools)
   // of shared memory, between 2 and 8
@@ -257,19 +257,21 @@ struct TcInst {
   static constexpr int BUDGET = CT ? 217088 - 9216 : 196608;
   static constexpr int NS_FIT = BUDGET / STAGE_BYTES;
   static constexpr int NS = NS_FIT < 2 ? 2 : (NS_FIT > 8 ? 8 : NS_FIT);
-  using C = pkv::TcCfg<D, HPC, NS, CT>;
+  using C = pkv::TcCfg<D, HPC, NS, CT, B8>;
   static std::once_flag flags[kMaxDevices];
   static cudaError_t errs[kMaxDevices];
   static pkv_status launch(const pkv::TcParams& prm, int n, int groups, cudaStream_t st, int dev) {
-    auto k = pkv::attn_tc_kernel<D, HPC, NS, CT>;
+    auto k = pkv::attn_tc_kernel<D, HPC, NS, CT, B8>;
     pkv_status s = set_smem_once(k, C::SMEM, flags, errs, dev);
     if (s != PKV_OK) return s;
     PKV_CUDA(launch_pdl(k, dim3(n, groups), dim3(C::THREADS), (size_t)C::SMEM, st, prm));
     return PKV_OK;
   }
 };
-template <int D, int HPC, int CT> std::once_flag TcInst<D, HPC, CT>::flags[kMaxDevices];
-template <int D, int HPC, int CT> cudaError_t TcInst<D, HPC, CT>::errs[kMaxDevices];
+template <int D, int HPC, int CT, bool B8>
+std::once_flag TcInst<D, HPC, CT, B8>::flags[kMaxDevices];
+template <int D, int HPC, int CT, bool B8>
+cudaError_t TcInst<D, HPC, CT, B8>::errs[kMaxDevices];
 
 // ---- multi-query (prefill) kernel dispatch -----------------------------------------
 template <int D, int NW>
@@ -419,15 +421,24 @@ pkv_status plan_prefill(int num_seqs, int num_tokens, int max_query_len, int max
   return PKV_OK;
 }
 
-template <int D, int CT>
-pkv_status launch_tc_d(int hpc, const pkv::TcParams& prm, int n, int groups, cudaStream_t st,
-                       int dev) {
+template <int D, int CT, bool B8>
+pkv_status launch_tc_hpc(int hpc, const pkv::TcParams& prm, int n, int groups, cudaStream_t st,
+                         int dev) {
   switch (hpc) {
-    case 8: return TcInst<D, 8, CT>::launch(prm, n, groups, st, dev);
-    case 4: return TcInst<D, 4, CT>::launch(prm, n, groups, st, dev);
-    case 2: return TcInst<D, 2, CT>::launch(prm, n, groups, st, dev);
-    default: return TcInst<D, 1, CT>::launch(prm, n, groups, st, dev);
+    case 8: return TcInst<D, 8, CT, B8>::launch(prm, n, groups, st, dev);
+    case 4: return TcInst<D, 4, CT, B8>::launch(prm, n, groups, st, dev);
+    case 2: return TcInst<D, 2, CT, B8>::launch(prm, n, groups, st, dev);
+    default: return TcInst<D, 1, CT, B8>::launch(prm, n, groups, st, dev);
   }
+}
+
+// 8-token blocks take the kernel's B8 layout (tensor maps from
+// encode_pool_map_b8); block sizes that are multiples of 16 the plain one
+template <int D, int CT>
+pkv_status launch_tc_d(int hpc, int block_size, const pkv::TcParams& prm, int n, int groups,
+                       cudaStream_t st, int dev) {
+  return block_size < pkv::kTile ? launch_tc_hpc<D, CT, true>(hpc, prm, n, groups, st, dev)
+                                 : launch_tc_hpc<D, CT, false>(hpc, prm, n, groups, st, dev);
 }
 
 // Tensor map over a pool seen as [rows = num_blocks * K][H_kv][D]: boxes of
@@ -450,6 +461,32 @@ pkv_status encode_pool_map(CUtensorMap* map, const void* pool, int64_t num_block
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   PKV_CHECK(r == CUDA_SUCCESS, PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return PKV_OK;
+}
+
+// Tensor map over a pool of 8-token blocks for the decode kernel's B8
+// layout: dimensions (128-byte column, row = num_blocks * 8, column group,
+// KV head) with byte strides (row H_kv * D * eb, group 128, head D * eb),
+// boxes of 128 bytes x 8 rows x all column groups x hpc heads, 128-byte
+// swizzle.  A box read at a block's first row is that block's hpc heads:
+// hpc * D * eb contiguous bytes per row.
+pkv_status encode_pool_map_b8(CUtensorMap* map, const void* pool, int64_t num_blocks, int H_kv,
+                              int D, int hpc, bool one_byte) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+  pkv_status st = get_encode(&enc);
+  if (st != PKV_OK) return st;
+  const cuuint64_t eb = one_byte ? 1 : 2;
+  const cuuint64_t c0 = 128 / eb;                 // elements of a 128-byte column
+  const cuuint64_t nh = (cuuint64_t)D * eb / 128; // column groups of a head row
+  cuuint64_t dims[4] = {c0, (cuuint64_t)(num_blocks * 8), nh, (cuuint64_t)H_kv};
+  cuuint64_t strides[3] = {(cuuint64_t)H_kv * D * eb, 128, (cuuint64_t)D * eb};
+  cuuint32_t box[4] = {(cuuint32_t)c0, 8, (cuuint32_t)nh, (cuuint32_t)hpc};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(map, one_byte ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                   4, const_cast<void*>(pool), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  PKV_CHECK(r == CUDA_SUCCESS, PKV_ERR_CUDA, "cuTensorMapEncodeTiled (B8) failed (%d)", (int)r);
   return PKV_OK;
 }
 
@@ -969,9 +1006,15 @@ pkv_status attention_impl(const void* q, const void* k_cache, const void* v_cach
     st = device_facts(&dev, &sms);
     if (st != PKV_OK) return st;
     memset(&prm, 0, sizeof(prm));
-    st = encode_pool_map(&prm.tmap_k, k_cache, num_blocks, block_size, H_kv, D, quant != nullptr);
-    if (st != PKV_OK) return st;
-    st = encode_pool_map(&prm.tmap_v, v_cache, num_blocks, block_size, H_kv, D, quant != nullptr);
+    if (block_size < pkv::kTile) {
+      st = encode_pool_map_b8(&prm.tmap_k, k_cache, num_blocks, H_kv, D, plan.hpc, quant != nullptr);
+      if (st != PKV_OK) return st;
+      st = encode_pool_map_b8(&prm.tmap_v, v_cache, num_blocks, H_kv, D, plan.hpc, quant != nullptr);
+    } else {
+      st = encode_pool_map(&prm.tmap_k, k_cache, num_blocks, block_size, H_kv, D, quant != nullptr);
+      if (st != PKV_OK) return st;
+      st = encode_pool_map(&prm.tmap_v, v_cache, num_blocks, block_size, H_kv, D, quant != nullptr);
+    }
     if (st != PKV_OK) return st;
     if (quant) {
       prm.v_scale = quant->format == PKV_KV_FP8_E4M3 ? quant->v_scale : 1.f;
@@ -1000,13 +1043,17 @@ pkv_status attention_impl(const void* q, const void* k_cache, const void* v_cach
       prm.block_size = block_size;
       prm.scale_log2 = sl;
       if (quant == nullptr) {
-        st = D == 64 ? launch_tc_d<64, 0>(plan.hpc, prm, plan.n_per_group, plan.groups, strm, dev)
-                     : launch_tc_d<128, 0>(plan.hpc, prm, plan.n_per_group, plan.groups, strm, dev);
+        st = D == 64 ? launch_tc_d<64, 0>(plan.hpc, block_size, prm, plan.n_per_group, plan.groups,
+                                          strm, dev)
+                     : launch_tc_d<128, 0>(plan.hpc, block_size, prm, plan.n_per_group,
+                                           plan.groups, strm, dev);
       } else if (quant->format == PKV_KV_FP8_E4M3) {
         prm.scale_log2 = (float)((double)scale * log2e * (double)quant->k_scale);
-        st = launch_tc_d<128, 1>(plan.hpc, prm, plan.n_per_group, plan.groups, strm, dev);
+        st = launch_tc_d<128, 1>(plan.hpc, block_size, prm, plan.n_per_group, plan.groups, strm,
+                                 dev);
       } else {
-        st = launch_tc_d<128, 2>(plan.hpc, prm, plan.n_per_group, plan.groups, strm, dev);
+        st = launch_tc_d<128, 2>(plan.hpc, block_size, prm, plan.n_per_group, plan.groups, strm,
+                                 dev);
       }
     } else {
       const SimtArgs a{btb, max_blocks_per_seq, lb, max_context_len, S, H_q, H_kv,
@@ -1183,8 +1230,17 @@ pkv_status pkv_attention_prefill(const void* q, const void* k_cache, const void*
     // several query rows per sequence through the stream-K decode kernel
     pkv::TcParams tp;
     memset(&tp, 0, sizeof(tp));
-    tp.tmap_k = prm.tmap_k;
-    tp.tmap_v = prm.tmap_v;
+    if (block_size < pkv::kTile) {
+      st = encode_pool_map_b8(&tp.tmap_k, k_cache, num_blocks, num_kv_heads, head_dim,
+                              plan.ap.hpc, false);
+      if (st != PKV_OK) return st;
+      st = encode_pool_map_b8(&tp.tmap_v, v_cache, num_blocks, num_kv_heads, head_dim,
+                              plan.ap.hpc, false);
+      if (st != PKV_OK) return st;
+    } else {
+      tp.tmap_k = prm.tmap_k;
+      tp.tmap_v = prm.tmap_v;
+    }
     tp.q = prm.q;
     tp.out = prm.out;
     tp.block_tables = block_tables;
@@ -1208,8 +1264,10 @@ pkv_status pkv_attention_prefill(const void* q, const void* k_cache, const void*
     tp.scale_log2 = prm.scale_log2;
     cudaStream_t strm = as_stream(stream);
     st = head_dim == 64
-             ? launch_tc_d<64, 0>(plan.ap.hpc, tp, plan.ap.n_per_group, plan.ap.groups, strm, dev)
-             : launch_tc_d<128, 0>(plan.ap.hpc, tp, plan.ap.n_per_group, plan.ap.groups, strm,
+             ? launch_tc_d<64, 0>(plan.ap.hpc, block_size, tp, plan.ap.n_per_group,
+                                  plan.ap.groups, strm, dev)
+             : launch_tc_d<128, 0>(plan.ap.hpc, block_size, tp, plan.ap.n_per_group,
+                                   plan.ap.groups, strm,
                                    dev);
     if (st != PKV_OK || plan.ap.pmax <= 1) return st;
     return launch_reduce<__nv_bfloat16>(head_dim, tp.ws, num_tokens, num_q_heads, out, strm);

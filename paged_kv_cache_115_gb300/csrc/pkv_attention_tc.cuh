@@ -76,7 +76,16 @@ struct TcParams {
 // go through ldmatrix into bf16 mma fragments.
 //
 // Stage layout: K boxes [head][tile][column group], then V boxes, then (INT8)
-// the 16 per-slot scales of each tile: K tiles, then V tiles.
+// the 16 per-slot scales of each tile: K tiles, then V tiles.  A box holds
+// 16 token rows of 128 bytes in the 128-byte swizzle (row r's 16-byte chunk
+// c at chunk c ^ (r & 7)).
+//
+// 8-token blocks (B8): one 8-row block of a pool holds every head of the
+// block contiguously, so a single 4-D box brings all HPC heads and column
+// groups of one block half of a tile, laid out [tile][block half][head]
+// [column group][8 rows x 128 bytes]: rows 8..15 of a tile sit UST bytes
+// after rows 0..7 instead of 1024.  Each 8-row group is still a whole
+// 1024-byte swizzle atom, so row r keeps the swizzle phase r & 7.
 // Two int8 codes of a word whose bytes were already XORed with 0x80, chosen
 // by a byte-permute selector that puts them in the low bytes of two f16
 // halves with exponent bits 0x64 (selector nibbles: code byte, 4 = 0x64,
@@ -109,7 +118,18 @@ __device__ __forceinline__ float ex2_approx_ftz(float x) {
   return y;
 }
 
-template <int D, int HPC, int NS, int CT = 0>
+// 4-D tiled load global -> shared, completion counted on an mbarrier.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1, int c2, int c3, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar),
+      "l"(policy)
+      : "memory");
+}
+
+template <int D, int HPC, int NS, int CT = 0, bool B8 = false>
 struct TcCfg {
   static constexpr int TL = CT ? 2 : 1;                   // 16-row tiles per chunk
   static constexpr int CH = kTile * TL;                   // tokens per chunk
@@ -129,9 +149,17 @@ struct TcCfg {
   static_assert(CT == 0 || D == 128, "one-byte pools need head_dim 128");
   static_assert(tc_chunk_tokens(CT) == CH, "chunk size");
   // smem offset of head h's box (tile t, column group half) of K (kv 0) or V
+  static constexpr int UST = HPC * NH * 1024;        // B8: one block half of a tile, all heads
+  static constexpr int RSTEP8 = B8 ? UST : 1024;     // rows 8..15 relative to rows 0..7
+  static constexpr int HSTR = B8 ? 1024 : kBoxBytes; // column group stride
+  // smem offset of row 0 of head h's box (tile t, column group half) of K
+  // (kv 0) or V
   __host__ __device__ static constexpr int box_off(int kv, int h, int t, int half) {
-    return kv * KPART + ((h * TL + t) * NH + half) * kBoxBytes;
+    return B8 ? kv * KPART + t * 2 * UST + (h * NH + half) * 1024
+              : kv * KPART + ((h * TL + t) * NH + half) * kBoxBytes;
   }
+  // offset of row r (0..15) inside a box
+  __host__ __device__ static constexpr int row_off(int r) { return (r & 7) * 128 + (r >> 3) * RSTEP8; }
 };
 
 // Largest CTA index i whose range starts at or before chunk c.
@@ -149,10 +177,10 @@ __device__ __forceinline__ int seq_of_chunk(const int* cstart, int S, int c) {
   return lo;
 }
 
-template <int D, int HPC, int NS, int CT = 0>
-__global__ void __launch_bounds__(TcCfg<D, HPC, NS, CT>::THREADS, 1)
+template <int D, int HPC, int NS, int CT = 0, bool B8 = false>
+__global__ void __launch_bounds__(TcCfg<D, HPC, NS, CT, B8>::THREADS, 1)
 attn_tc_kernel(const __grid_constant__ TcParams p) {
-  using C = TcCfg<D, HPC, NS, CT>;
+  using C = TcCfg<D, HPC, NS, CT, B8>;
   constexpr int TL = C::TL, CH = C::CH;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -267,15 +295,14 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
       prefetch_tensormap(&p.tmap_v);
     }
     const uint64_t policy = l2_policy_evict_first();
-    const int sbl = K < kTile ? 1 : 0;       // log2 of the boxes per tile row
+    constexpr int sbl = B8 ? 1 : 0;          // log2 of the blocks per tile
     int k = 0;
     bool ok = true;
     for (int c0 = cb; c0 < ce && ok; c0 += 32) {
       // pool rows of the tiles of the next 32 chunks, one chunk per lane; a
       // tile past the sequence end (or of an out-of-range block) gets a row
       // that is wholly out of bounds, which TMA fills with zeros.  With
-      // 8-token blocks a tile spans two blocks: two 8-row boxes (u = 0, 1),
-      // each a whole 1024-byte swizzle atom, land where one 16-row box would.
+      // 8-token blocks a tile spans two blocks (u = 0, 1).
       int row[TL][2];
 #pragma unroll
       for (int t = 0; t < TL; ++t) row[t][0] = row[t][1] = -2 * kTile;
@@ -319,32 +346,48 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
         if (lane == 0) mbar_arrive_expect_tx(bar_full + 8 * stage, C::TX);
         __syncwarp();
         uint8_t* sb = smem + stage * C::STAGE;
-        for (int i = lane; i < (C::NCOPY << sbl); i += 32) {
-          const int ci = i >> sbl, u = i & sbl;
-          if (ci < C::NBOX) {
-            const int kv = ci / (HPC * TL * C::NH);
-            const int rem = ci - kv * (HPC * TL * C::NH);
-            const int h = rem / (TL * C::NH);
-            const int rem2 = rem - h * (TL * C::NH);
-            const int t = rem2 / C::NH, half = rem2 - t * C::NH;
-            const int r0 = t ? r[TL - 1][0] : r[0][0];
-            const int r1 = t ? r[TL - 1][1] : r[0][1];
-            tma_load_3d(smem_u32(sb + C::box_off(kv, h, t, half) + u * (kBoxBytes / 2)),
-                        kv ? &p.tmap_v : &p.tmap_k, bar_full + 8 * stage, half * 64, head0 + h,
-                        u ? r1 : r0, policy);
-          } else if constexpr (CT == 2) {
-            // a tile's 16 per-slot scales (64 bytes, or two 32-byte halves
-            // with 8-token blocks); a tile with no rows reads slot 0's
-            // scales, which meet zero codes
-            const int idx = ci - C::NBOX;
-            const int kv = idx / TL, t = idx - kv * TL;
+        if constexpr (B8) {
+          // one 4-D box per (K / V, tile, block half): all heads of the CTA,
+          // all column groups, 8 rows; then (INT8) the scales of each half
+          constexpr int NB = 4 * TL;
+          for (int i = lane; i < NB + (CT == 2 ? NB : 0); i += 32) {
+            const int j = i < NB ? i : i - NB;
+            const int kv = j / (2 * TL), t = (j >> 1) % TL, u = j & 1;
             const int r0 = t ? r[TL - 1][0] : r[0][0];
             const int r1 = t ? r[TL - 1][1] : r[0][1];
             const int rr = u ? r1 : r0;
-            const int nbytes = 64 >> sbl;
-            const float* src = (kv ? p.v_ts : p.k_ts) + (rr >= 0 ? rr : 0);
-            bulk_load(smem_u32(sb + C::SCALE_OFF + (kv * TL + t) * 64 + u * nbytes), src, nbytes,
-                      bar_full + 8 * stage);
+            if (i < NB) {
+              tma_load_4d(smem_u32(sb + kv * C::KPART + (2 * t + u) * C::UST),
+                          kv ? &p.tmap_v : &p.tmap_k, bar_full + 8 * stage, 0, rr, 0, head0,
+                          policy);
+            } else if constexpr (CT == 2) {
+              // a half tile with no rows reads slot 0's scales, which meet zero codes
+              const float* src = (kv ? p.v_ts : p.k_ts) + (rr >= 0 ? rr : 0);
+              bulk_load(smem_u32(sb + C::SCALE_OFF + (kv * TL + t) * 64 + u * 32), src, 32,
+                        bar_full + 8 * stage);
+            }
+          }
+        } else {
+          for (int i = lane; i < C::NCOPY; i += 32) {
+            if (i < C::NBOX) {
+              const int kv = i / (HPC * TL * C::NH);
+              const int rem = i - kv * (HPC * TL * C::NH);
+              const int h = rem / (TL * C::NH);
+              const int rem2 = rem - h * (TL * C::NH);
+              const int t = rem2 / C::NH, half = rem2 - t * C::NH;
+              tma_load_3d(smem_u32(sb + C::box_off(kv, h, t, half)), kv ? &p.tmap_v : &p.tmap_k,
+                          bar_full + 8 * stage, half * 64, head0 + h, t ? r[TL - 1][0] : r[0][0],
+                          policy);
+            } else if constexpr (CT == 2) {
+              // a tile's 16 per-slot scales (64 bytes); a tile with no rows
+              // reads slot 0's scales, which meet zero codes
+              const int idx = i - C::NBOX;
+              const int kv = idx / TL, t = idx - kv * TL;
+              const int rr = t ? r[TL - 1][0] : r[0][0];
+              const float* src = (kv ? p.v_ts : p.k_ts) + (rr >= 0 ? rr : 0);
+              bulk_load(smem_u32(sb + C::SCALE_OFF + (kv * TL + t) * 64), src, 64,
+                        bar_full + 8 * stage);
+            }
           }
         }
         __syncwarp();
@@ -483,7 +526,7 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
         const int r = valid + i / (C::NH * 8);          // chunk row: tile r / 16
         const int rem = i % (C::NH * 8);
         const int half = rem >> 3, ch = rem & 7;
-        *reinterpret_cast<uint4*>(sb + C::box_off(1, w, r / kTile, half) + (r % kTile) * 128 +
+        *reinterpret_cast<uint4*>(sb + C::box_off(1, w, r / kTile, half) + C::row_off(r % kTile) +
                                   ch * 16) = make_uint4(0u, 0u, 0u, 0u);
       }
       fence_proxy_async_smem();
@@ -501,7 +544,7 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
       for (int ks = 0; ks < D / 16; ++ks) {
         const int half = ks >> 2;
         const int ch = ((ks & 3) << 1) + chs;
-        const uint32_t addr = smem_u32(kt + half * kBoxBytes) + r * 128 + ((ch ^ (r & 7)) << 4);
+        const uint32_t addr = smem_u32(kt + half * C::HSTR) + C::row_off(r) + ((ch ^ (r & 7)) << 4);
         uint32_t a0, a1, a2, a3;
         ldmatrix_x4(addr, a0, a1, a2, a3);
         mma_bf16_16816(sacc[0], a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
@@ -516,7 +559,7 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
         for (int t = 0; t < TL; ++t) {
           const uint8_t* kt = sb + C::box_off(0, w, t, 0);
           const uint32_t w0 = *reinterpret_cast<const uint32_t*>(kt + off);
-          const uint32_t w1 = *reinterpret_cast<const uint32_t*>(kt + off + 8 * 128);
+          const uint32_t w1 = *reinterpret_cast<const uint32_t*>(kt + off + C::RSTEP8);
           uint32_t a0, a1, a2, a3;
           if constexpr (CT == 1) {
             e4m3x4_to_f16x2x2(w0, a0, a2);
@@ -662,7 +705,7 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
       const int tok = (lm & 1) * 8 + lr;
 #pragma unroll
       for (int t = 0; t < TL; ++t) {
-        const uint32_t vt = smem_u32(sb + C::box_off(1, w, t, 0)) + tok * 128;
+        const uint32_t vt = smem_u32(sb + C::box_off(1, w, t, 0)) + C::row_off(tok);
 #pragma unroll
         for (int mt = 0; mt < D / 16; mt += 2) {
           uint32_t r[4];
@@ -696,7 +739,7 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
       for (int mt = 0; mt < D / 16; ++mt) {
         const int half = mt >> 2;
         const int ch = ((mt & 3) << 1) + chs;
-        const uint32_t addr = smem_u32(vt + half * kBoxBytes) + r * 128 + ((ch ^ (r & 7)) << 4);
+        const uint32_t addr = smem_u32(vt + half * C::HSTR) + C::row_off(r) + ((ch ^ (r & 7)) << 4);
         uint32_t a0, a1, a2, a3;
         ldmatrix_x4_trans(addr, a0, a1, a2, a3);
         mma_bf16_16816(o[mt], a0, a1, a2, a3, pb[0][0], pb[0][1]);

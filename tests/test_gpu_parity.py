@@ -191,9 +191,10 @@ def test_tc_kernel_split_counts(ops, num_splits):
     full_check(ops, w, kernel=1, num_splits=num_splits)
 
 
+@pytest.mark.parametrize("K", [16, 8])
 @pytest.mark.parametrize("H_kv", [1, 2, 4, 8, 16])
-def test_tc_kernel_head_groups(ops, H_kv):
-    w = wl.build_decode("tc_heads", [70, 300, 5], 2 * H_kv, H_kv, 128, 16, "bf16", seed=H_kv)
+def test_tc_kernel_head_groups(ops, H_kv, K):
+    w = wl.build_decode("tc_heads", [70, 300, 5], 2 * H_kv, H_kv, 128, K, "bf16", seed=H_kv + K)
     full_check(ops, w, kernel=1)
 
 
