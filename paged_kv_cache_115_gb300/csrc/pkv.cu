@@ -432,8 +432,8 @@ pkv_status launch_tc_hpc(int hpc, const pkv::TcParams& prm, int n, int groups, c
   }
 }
 
-// 8-token blocks take the kernel's B8 layout (tensor maps from
-// encode_pool_map_b8); block sizes that are multiples of 16 the plain one
+// 8-token blocks take the kernel's B8 layout; block sizes that are multiples
+// of 16 the plain one (tensor maps from encode_pool_map_heads for both)
 template <int D, int CT>
 pkv_status launch_tc_d(int hpc, int block_size, const pkv::TcParams& prm, int n, int groups,
                        cudaStream_t st, int dev) {
@@ -441,9 +441,9 @@ pkv_status launch_tc_d(int hpc, int block_size, const pkv::TcParams& prm, int n,
                                  : launch_tc_hpc<D, CT, false>(hpc, prm, n, groups, st, dev);
 }
 
-// Tensor map over a pool seen as [rows = num_blocks * K][H_kv][D]: boxes of
-// 128 bytes x 1 head x 16 rows (64 bf16 columns, or a full 128-column row of
-// one-byte codes), 128-byte swizzle.
+// Tensor map over a pool seen as [rows = num_blocks * K][H_kv][D] for the
+// multi-query kernels: boxes of 128 bytes x 1 head x min(K, 16) rows (64 bf16
+// columns, or a full 128-column row of one-byte codes), 128-byte swizzle.
 pkv_status encode_pool_map(CUtensorMap* map, const void* pool, int64_t num_blocks, int K, int H_kv,
                            int D, bool one_byte = false) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
@@ -464,29 +464,29 @@ pkv_status encode_pool_map(CUtensorMap* map, const void* pool, int64_t num_block
   return PKV_OK;
 }
 
-// Tensor map over a pool of 8-token blocks for the decode kernel's B8
-// layout: dimensions (128-byte column, row = num_blocks * 8, column group,
-// KV head) with byte strides (row H_kv * D * eb, group 128, head D * eb),
-// boxes of 128 bytes x 8 rows x all column groups x hpc heads, 128-byte
-// swizzle.  A box read at a block's first row is that block's hpc heads:
-// hpc * D * eb contiguous bytes per row.
-pkv_status encode_pool_map_b8(CUtensorMap* map, const void* pool, int64_t num_blocks, int H_kv,
-                              int D, int hpc, bool one_byte) {
+// Tensor map over a pool for the decode kernel: dimensions (128-byte column,
+// row = num_blocks * K, column group, KV head) with byte strides (row
+// H_kv * D * eb, group 128, head D * eb), boxes of 128 bytes x min(K, 16)
+// rows x all column groups x hpc heads, 128-byte swizzle.  A box is hpc * D
+// * eb contiguous bytes of each of its rows and never crosses a block.
+pkv_status encode_pool_map_heads(CUtensorMap* map, const void* pool, int64_t num_blocks, int K,
+                                 int H_kv, int D, int hpc, bool one_byte) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
   pkv_status st = get_encode(&enc);
   if (st != PKV_OK) return st;
   const cuuint64_t eb = one_byte ? 1 : 2;
   const cuuint64_t c0 = 128 / eb;                 // elements of a 128-byte column
   const cuuint64_t nh = (cuuint64_t)D * eb / 128; // column groups of a head row
-  cuuint64_t dims[4] = {c0, (cuuint64_t)(num_blocks * 8), nh, (cuuint64_t)H_kv};
+  cuuint64_t dims[4] = {c0, (cuuint64_t)(num_blocks * K), nh, (cuuint64_t)H_kv};
   cuuint64_t strides[3] = {(cuuint64_t)H_kv * D * eb, 128, (cuuint64_t)D * eb};
-  cuuint32_t box[4] = {(cuuint32_t)c0, 8, (cuuint32_t)nh, (cuuint32_t)hpc};
+  cuuint32_t box[4] = {(cuuint32_t)c0, (cuuint32_t)std::min(K, pkv::kTile), (cuuint32_t)nh,
+                       (cuuint32_t)hpc};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = enc(map, one_byte ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                    4, const_cast<void*>(pool), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  PKV_CHECK(r == CUDA_SUCCESS, PKV_ERR_CUDA, "cuTensorMapEncodeTiled (B8) failed (%d)", (int)r);
+  PKV_CHECK(r == CUDA_SUCCESS, PKV_ERR_CUDA, "cuTensorMapEncodeTiled (heads) failed (%d)", (int)r);
   return PKV_OK;
 }
 
@@ -1006,15 +1006,11 @@ pkv_status attention_impl(const void* q, const void* k_cache, const void* v_cach
     st = device_facts(&dev, &sms);
     if (st != PKV_OK) return st;
     memset(&prm, 0, sizeof(prm));
-    if (block_size < pkv::kTile) {
-      st = encode_pool_map_b8(&prm.tmap_k, k_cache, num_blocks, H_kv, D, plan.hpc, quant != nullptr);
-      if (st != PKV_OK) return st;
-      st = encode_pool_map_b8(&prm.tmap_v, v_cache, num_blocks, H_kv, D, plan.hpc, quant != nullptr);
-    } else {
-      st = encode_pool_map(&prm.tmap_k, k_cache, num_blocks, block_size, H_kv, D, quant != nullptr);
-      if (st != PKV_OK) return st;
-      st = encode_pool_map(&prm.tmap_v, v_cache, num_blocks, block_size, H_kv, D, quant != nullptr);
-    }
+    st = encode_pool_map_heads(&prm.tmap_k, k_cache, num_blocks, block_size, H_kv, D, plan.hpc,
+                               quant != nullptr);
+    if (st != PKV_OK) return st;
+    st = encode_pool_map_heads(&prm.tmap_v, v_cache, num_blocks, block_size, H_kv, D, plan.hpc,
+                               quant != nullptr);
     if (st != PKV_OK) return st;
     if (quant) {
       prm.v_scale = quant->format == PKV_KV_FP8_E4M3 ? quant->v_scale : 1.f;
@@ -1230,17 +1226,12 @@ pkv_status pkv_attention_prefill(const void* q, const void* k_cache, const void*
     // several query rows per sequence through the stream-K decode kernel
     pkv::TcParams tp;
     memset(&tp, 0, sizeof(tp));
-    if (block_size < pkv::kTile) {
-      st = encode_pool_map_b8(&tp.tmap_k, k_cache, num_blocks, num_kv_heads, head_dim,
-                              plan.ap.hpc, false);
-      if (st != PKV_OK) return st;
-      st = encode_pool_map_b8(&tp.tmap_v, v_cache, num_blocks, num_kv_heads, head_dim,
-                              plan.ap.hpc, false);
-      if (st != PKV_OK) return st;
-    } else {
-      tp.tmap_k = prm.tmap_k;
-      tp.tmap_v = prm.tmap_v;
-    }
+    st = encode_pool_map_heads(&tp.tmap_k, k_cache, num_blocks, block_size, num_kv_heads,
+                               head_dim, plan.ap.hpc, false);
+    if (st != PKV_OK) return st;
+    st = encode_pool_map_heads(&tp.tmap_v, v_cache, num_blocks, block_size, num_kv_heads,
+                               head_dim, plan.ap.hpc, false);
+    if (st != PKV_OK) return st;
     tp.q = prm.q;
     tp.out = prm.out;
     tp.block_tables = block_tables;

@@ -75,17 +75,17 @@ struct TcParams {
 // into f16 mma fragments (e4m3 and int8 codes are exact in f16); bf16 tiles
 // go through ldmatrix into bf16 mma fragments.
 //
-// Stage layout: K boxes [head][tile][column group], then V boxes, then (INT8)
+// Stage layout: K boxes [tile][head][column group], then V boxes, then (INT8)
 // the 16 per-slot scales of each tile: K tiles, then V tiles.  A box holds
 // 16 token rows of 128 bytes in the 128-byte swizzle (row r's 16-byte chunk
-// c at chunk c ^ (r & 7)).
+// c at chunk c ^ (r & 7)).  A row of a pool block holds every KV head
+// contiguously, so one 4-D TMA copy (column, row, column group, head) brings
+// a tile's rows for all HPC heads and column groups of the CTA at once.
 //
-// 8-token blocks (B8): one 8-row block of a pool holds every head of the
-// block contiguously, so a single 4-D box brings all HPC heads and column
-// groups of one block half of a tile, laid out [tile][block half][head]
-// [column group][8 rows x 128 bytes]: rows 8..15 of a tile sit UST bytes
-// after rows 0..7 instead of 1024.  Each 8-row group is still a whole
-// 1024-byte swizzle atom, so row r keeps the swizzle phase r & 7.
+// 8-token blocks (B8): a tile spans two blocks, one copy each, laid out
+// [tile][block half][head][column group][8 rows x 128 bytes]: rows 8..15 of
+// a tile sit UST bytes after rows 0..7 instead of 1024.  Each 8-row group is
+// still a whole 1024-byte swizzle atom, so row r keeps the swizzle phase r & 7.
 // Two int8 codes of a word whose bytes were already XORed with 0x80, chosen
 // by a byte-permute selector that puts them in the low bytes of two f16
 // halves with exponent bits 0x64 (selector nibbles: code byte, 4 = 0x64,
@@ -134,21 +134,19 @@ struct TcCfg {
   static constexpr int TL = CT ? 2 : 1;                   // 16-row tiles per chunk
   static constexpr int CH = kTile * TL;                   // tokens per chunk
   static constexpr int NH = CT ? 1 : D / 64;              // boxes per head row
-  static constexpr int NBOX = 2 * HPC * TL * NH;
   static constexpr int KPART = HPC * TL * NH * kBoxBytes;
   static constexpr int SCALE_OFF = 2 * KPART;
   static constexpr int SCALE_BYTES = CT == 2 ? 2 * TL * kTile * 4 : 0;
-  static constexpr int NCOPY = NBOX + (CT == 2 ? 2 * TL : 0);
   static constexpr int STAGE = ((2 * KPART + SCALE_BYTES + 1023) / 1024) * 1024;
   static constexpr int THREADS = (HPC + 1) * 32;
   static constexpr int BAR_OFF = NS * STAGE;
   static constexpr int CSTART_OFF = BAR_OFF + 2 * NS * 8 + 16;
   static constexpr int SMEM = CSTART_OFF + (kTcMaxSeqs + 1) * 4 + 1024;  // + alignment slack
   static constexpr uint32_t TX = 2 * KPART + SCALE_BYTES;  // bytes landing per stage
-  static_assert(NBOX <= 32, "one box per producer lane");
   static_assert(CT == 0 || D == 128, "one-byte pools need head_dim 128");
   static_assert(tc_chunk_tokens(CT) == CH, "chunk size");
   // smem offset of head h's box (tile t, column group half) of K (kv 0) or V
+  static constexpr int TBOX = HPC * NH * kBoxBytes;  // one tile, all heads of the CTA
   static constexpr int UST = HPC * NH * 1024;        // B8: one block half of a tile, all heads
   static constexpr int RSTEP8 = B8 ? UST : 1024;     // rows 8..15 relative to rows 0..7
   static constexpr int HSTR = B8 ? 1024 : kBoxBytes; // column group stride
@@ -156,7 +154,7 @@ struct TcCfg {
   // (kv 0) or V
   __host__ __device__ static constexpr int box_off(int kv, int h, int t, int half) {
     return B8 ? kv * KPART + t * 2 * UST + (h * NH + half) * 1024
-              : kv * KPART + ((h * TL + t) * NH + half) * kBoxBytes;
+              : kv * KPART + t * TBOX + (h * NH + half) * kBoxBytes;
   }
   // offset of row r (0..15) inside a box
   __host__ __device__ static constexpr int row_off(int r) { return (r & 7) * 128 + (r >> 3) * RSTEP8; }
@@ -368,22 +366,18 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
             }
           }
         } else {
-          for (int i = lane; i < C::NCOPY; i += 32) {
-            if (i < C::NBOX) {
-              const int kv = i / (HPC * TL * C::NH);
-              const int rem = i - kv * (HPC * TL * C::NH);
-              const int h = rem / (TL * C::NH);
-              const int rem2 = rem - h * (TL * C::NH);
-              const int t = rem2 / C::NH, half = rem2 - t * C::NH;
-              tma_load_3d(smem_u32(sb + C::box_off(kv, h, t, half)), kv ? &p.tmap_v : &p.tmap_k,
-                          bar_full + 8 * stage, half * 64, head0 + h, t ? r[TL - 1][0] : r[0][0],
-                          policy);
+          // one 4-D box per (K / V, tile): 16 rows of all heads of the CTA and
+          // all column groups; then (INT8) each tile's 16 per-slot scales
+          constexpr int NB = 2 * TL;
+          for (int i = lane; i < NB + (CT == 2 ? NB : 0); i += 32) {
+            const int j = i < NB ? i : i - NB;
+            const int kv = j / TL, t = j - kv * TL;
+            const int rr = t ? r[TL - 1][0] : r[0][0];
+            if (i < NB) {
+              tma_load_4d(smem_u32(sb + kv * C::KPART + t * C::TBOX), kv ? &p.tmap_v : &p.tmap_k,
+                          bar_full + 8 * stage, 0, rr, 0, head0, policy);
             } else if constexpr (CT == 2) {
-              // a tile's 16 per-slot scales (64 bytes); a tile with no rows
-              // reads slot 0's scales, which meet zero codes
-              const int idx = i - C::NBOX;
-              const int kv = idx / TL, t = idx - kv * TL;
-              const int rr = t ? r[TL - 1][0] : r[0][0];
+              // a tile with no rows reads slot 0's scales, which meet zero codes
               const float* src = (kv ? p.v_ts : p.k_ts) + (rr >= 0 ? rr : 0);
               bulk_load(smem_u32(sb + C::SCALE_OFF + (kv * TL + t) * 64), src, 64,
                         bar_full + 8 * stage);
