@@ -1,0 +1,39 @@
+"""The decode kernel's shared-memory stage layout, checked on the host.
+
+``tests/layout_check.cu`` includes the kernel header and checks, for every
+template configuration, that the consumers' row addresses are where the
+producer's 4-D TMA boxes land, that each row keeps its swizzle phase, and that
+the bytes a stage expects equal the bytes delivered. Built with nvcc for the
+host; no GPU is needed.
+"""
+
+import os
+import shutil
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+CSRC = os.path.join(ROOT, "paged_kv_cache_115_gb300", "csrc")
+
+
+def _nvcc():
+    for cand in (os.environ.get("NVCC"), shutil.which("nvcc"), "/usr/local/cuda/bin/nvcc"):
+        if cand and os.path.exists(cand):
+            return cand
+    return None
+
+
+def test_stage_layout_matches_the_boxes(tmp_path):
+    nvcc = _nvcc()
+    if nvcc is None:
+        pytest.skip("nvcc not available")
+    exe = str(tmp_path / "layout_check")
+    cmd = [nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-std=c++17", "-O1",
+           "-I", os.path.join(ROOT, "include"), "-I", CSRC, "-DPKV_BUILD", "-o", exe,
+           os.path.join(ROOT, "tests", "layout_check.cu")]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stdout + r.stderr
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert "layout ok" in r.stdout
