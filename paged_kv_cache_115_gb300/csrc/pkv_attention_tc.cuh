@@ -70,8 +70,8 @@ struct TcParams {
 };
 
 // Pool formats of the kernel: CT 0 = bf16, 1 = FP8 e4m3 (per-tensor scale),
-// 2 = INT8 (per-slot scale).  A one-byte pool row of D = 128 is one 128-byte
-// box per head; a bf16 row is D / 64 boxes.  One-byte tiles are read straight
+// 2 = INT8 (per-slot scale).  A head's row is one 128-byte column group in a
+// one-byte pool of D = 128, D / 64 groups in a bf16 pool.  One-byte tiles are read straight
 // into f16 mma fragments (e4m3 and int8 codes are exact in f16); bf16 tiles
 // go through ldmatrix into bf16 mma fragments.
 //
@@ -86,6 +86,7 @@ struct TcParams {
 // [tile][block half][head][column group][8 rows x 128 bytes]: rows 8..15 of
 // a tile sit UST bytes after rows 0..7 instead of 1024.  Each 8-row group is
 // still a whole 1024-byte swizzle atom, so row r keeps the swizzle phase r & 7.
+
 // Two int8 codes of a word whose bytes were already XORed with 0x80, chosen
 // by a byte-permute selector that puts them in the low bytes of two f16
 // halves with exponent bits 0x64 (selector nibbles: code byte, 4 = 0x64,
@@ -145,7 +146,6 @@ struct TcCfg {
   static constexpr uint32_t TX = 2 * KPART + SCALE_BYTES;  // bytes landing per stage
   static_assert(CT == 0 || D == 128, "one-byte pools need head_dim 128");
   static_assert(tc_chunk_tokens(CT) == CH, "chunk size");
-  // smem offset of head h's box (tile t, column group half) of K (kv 0) or V
   static constexpr int TBOX = HPC * NH * kBoxBytes;  // one tile, all heads of the CTA
   static constexpr int UST = HPC * NH * 1024;        // B8: one block half of a tile, all heads
   static constexpr int RSTEP8 = B8 ? UST : 1024;     // rows 8..15 relative to rows 0..7
