@@ -161,12 +161,12 @@ struct TcCfg {
 };
 
 // Largest CTA index i whose range starts at or before chunk c.
-__device__ __forceinline__ int cta_of_chunk(long long c, long long T, int n) {
+__host__ __device__ __forceinline__ int cta_of_chunk(long long c, long long T, int n) {
   return (int)(((c + 1) * (long long)n - 1) / T);
 }
 
 // Largest s in [0, S) with cstart[s] <= c (c < cstart[S]).
-__device__ __forceinline__ int seq_of_chunk(const int* cstart, int S, int c) {
+__host__ __device__ __forceinline__ int seq_of_chunk(const int* cstart, int S, int c) {
   int lo = 0, hi = S;   // invariant: cstart[lo] <= c < cstart[hi]
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;

@@ -1,7 +1,8 @@
-// Host-side check of the decode kernel's shared-memory stage layout, for every
-// template configuration the library instantiates.
+// Host-side checks of the decode kernel (attn_tc_kernel): its shared-memory
+// stage layout for every template configuration the library instantiates, and
+// its stream-K bookkeeping.
 //
-// The producer fills a stage with 4-D TMA boxes. A box lands densely as
+// Layout. The producer fills a stage with 4-D TMA boxes. A box lands densely as
 // [head][column group][row][128 bytes], at the destination the producer gives
 // it: kv * KPART + t * TBOX for 16-row tiles, or kv * KPART + (2t + u) * UST
 // for the two 8-row block halves of a B8 tile. The consumers address row r of
@@ -12,9 +13,19 @@
 //     aligned atom;
 //   * no byte is written twice, and the bytes a stage expects (TcCfg::TX)
 //     equal the bytes its copies deliver (boxes, then INT8 scales).
-// It makes no CUDA call, so it runs without a GPU. tests/test_layout_host.py
+//
+// Stream-K. With T chunks over n <= T CTAs, CTA i owns chunks
+// [floor(iT/n), floor((i+1)T/n)). Checked by brute force: cta_of_chunk(c)
+// is the CTA whose range holds chunk c, every CTA owns at least one chunk,
+// seq_of_chunk(c) is the sequence whose chunk range holds c (empty sequences
+// included), and a sequence never spans more CTAs than the partial slots
+// the host plan reserves (min(CTAs per group, ceil(max_len / 16))).
+//
+// It makes no CUDA call, so it runs without a GPU. tests/test_tc_host.py
 // builds and runs it.
+#include <algorithm>
 #include <cstdio>
+#include <random>
 #include <vector>
 
 #include "pkv_attention_tc.cuh"
@@ -74,16 +85,56 @@ int check_hpc() {
          check_layout<D, 4, CT, B8>() + check_layout<D, 8, CT, B8>();
 }
 
-int main() {
+int check_stream_k() {
   int errors = 0;
+  for (long long T = 1; T <= 400; ++T)
+    for (int n = 1; n <= T && n <= 160; ++n) {
+      for (int i = 0; i < n; ++i)
+        if ((long long)(i + 1) * T / n <= (long long)i * T / n) ++errors;   // empty CTA
+      for (long long c = 0; c < T; ++c) {
+        const long long i = pkv::cta_of_chunk(c, T, n);
+        if (i < 0 || i >= n || i * T / n > c || c >= (i + 1) * T / n) ++errors;
+      }
+    }
+  std::mt19937 rng(7);
+  for (int trial = 0; trial < 4000; ++trial) {
+    const int S = 1 + (int)(rng() % 48);
+    const int CH = trial & 1 ? 32 : 16;          // bf16 / one-byte chunk sizes
+    const int max_len = 1 + (int)(rng() % 3000);
+    std::vector<int> cstart(S + 1, 0);
+    for (int s = 0; s < S; ++s) {
+      const int len = rng() % 5 == 0 ? 0 : (int)(rng() % (max_len + 1));
+      cstart[s + 1] = cstart[s] + (len + CH - 1) / CH;
+    }
+    const long long T = cstart[S];
+    if (T == 0) continue;
+    for (int c = 0; c < T; ++c) {
+      const int s = pkv::seq_of_chunk(cstart.data(), S, c);
+      if (s < 0 || s >= S || cstart[s] > c || c >= cstart[s + 1]) ++errors;
+    }
+    const int grid = 1 + (int)(rng() % 160);     // CTAs per KV-head group
+    const int n = (int)(T < grid ? T : grid);
+    const int pmax = std::max(1, std::min(grid, (max_len + 15) / 16));
+    for (int s = 0; s < S; ++s) {
+      if (cstart[s] == cstart[s + 1]) continue;
+      const int np = pkv::cta_of_chunk(cstart[s + 1] - 1, T, n) - pkv::cta_of_chunk(cstart[s], T, n) + 1;
+      if (np < 1 || np > pmax) ++errors;
+    }
+  }
+  if (errors) std::printf("stream-K errors: %d\n", errors);
+  return errors;
+}
+
+int main() {
+  int errors = check_stream_k();
   errors += check_hpc<64, 0, false>() + check_hpc<64, 0, true>();
   errors += check_hpc<128, 0, false>() + check_hpc<128, 0, true>();
   errors += check_hpc<128, 1, false>() + check_hpc<128, 1, true>();
   errors += check_hpc<128, 2, false>() + check_hpc<128, 2, true>();
   if (errors) {
-    std::printf("layout errors: %d\n", errors);
+    std::printf("errors: %d\n", errors);
     return 1;
   }
-  std::printf("layout ok: 32 configurations\n");
+  std::printf("layout ok: 32 configurations; stream-K ok\n");
   return 0;
 }
