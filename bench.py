@@ -64,22 +64,30 @@ def read_peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
 
 
-def read_traffic(name="attention_traffic.json", workload=None):
-    """DRAM bytes per launch of a kernel from a committed ncu summary, valid
-    only while the kernel's sources are unchanged since the capture.  Files
-    with several records are keyed by workload name."""
+def traffic_record(name="attention_traffic.json", workload=None):
+    """(record, note): DRAM bytes per launch of a kernel from a committed ncu
+    summary, valid only while the kernel's sources are unchanged since the
+    capture, and a note saying where the figure comes from or why there is
+    none.  Files with several records are keyed by workload name."""
     try:
         with open(os.path.join(ROOT, "profiles", name)) as f:
             t = json.load(f)
     except OSError:
-        return None
+        return None, f"no ncu record (profiles/{name} missing)"
     if workload is not None:
         t = t.get(workload)
         if t is None:
-            return None
+            return None, f"no ncu record for {workload} in profiles/{name}"
     if t.get("kernel_src_sha") != src_sha(t.get("sources", KERNEL_SRC)):
-        return None
-    return t
+        return None, (f"profiles/{name} was captured on earlier kernel sources; no ncu "
+                      f"capture of the current ones")
+    return t, (f"ncu dram__bytes_read.sum + dram__bytes_write.sum per launch, "
+               f"profiles/{name} (kernel sources unchanged since the capture)")
+
+
+def read_traffic(name="attention_traffic.json", workload=None):
+    """The record of traffic_record, or None."""
+    return traffic_record(name, workload)[0]
 
 
 def workload_desc(w) -> dict:
@@ -580,10 +588,11 @@ def run_gpu(args):
     achieved = kv_bytes / (attn_avg_ms * 1e-3) / 1e9
     for r in rows.values():
         r["frac"] = r["GBps"] / hbm
-    traffic = read_traffic()
+    traffic, traffic_src = traffic_record()
     if traffic and (traffic.get("workload") != w.name or traffic.get("kv_format") != fmt
                     or traffic.get("block_size") != w.block_size):
         traffic = None                  # the record is for another workload
+        traffic_src = "the ncu record is for another workload, pool format or block size"
     cfg = workload_desc(w)
     cfg["l2"] = (f"inputs larger than L2: {kv_bytes / 1e6:.0f} MB of KV read per step "
                  f"vs 129 MB L2; no flush between steps")
@@ -622,6 +631,7 @@ def run_gpu(args):
             "algorithmic_bytes_per_launch": kv_bytes,
             "avg_launch_ms": attn_avg_ms,
             "traffic": traffic["bytes_per_launch"] if traffic else None,
+            "traffic_source": traffic_src,
         },
         "e2e": {"value": e2e_value, "unit": "GB/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -822,7 +832,8 @@ def run_swap(args):
                                     "the same bytes each way (cudaMemcpyAsync via torch)",
                      "unit": "GB/s", "frac": achieved / peak,
                      "algorithmic_bytes_per_launch": dir_bytes,
-                     "avg_launch_ms": (out_ms + in_ms) / 2, "traffic": None},
+                     "avg_launch_ms": (out_ms + in_ms) / 2, "traffic": None,
+                     "traffic_source": "none: the swap is bound by the host link, not DRAM"},
         "rows": {"swap_out": {"median_us": out_ms * 1e3,
                               "GBps": dir_bytes / (out_ms * 1e-3) / 1e9,
                               "contiguous_copy_GBps": dir_bytes / (d2h_ms * 1e-3) / 1e9},
@@ -1050,11 +1061,12 @@ def run_prefill(args):
         peak = float(peaks["hbm_gbs"])
         roof = {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
                 "frac": gbs / peak, "peak_source": f"{peak_src} hbm_gbs (copy, read+write)"}
-    traffic = read_traffic("prefill_traffic.json", w.name)
+    traffic, traffic_src = traffic_record("prefill_traffic.json", w.name)
     roof.update({"kernel": prefill_kernel(w),
                  "algorithmic_flops_per_launch": flops,
                  "algorithmic_bytes_per_launch": kv_bytes, "avg_launch_ms": attn_ms,
-                 "traffic": traffic["bytes_per_launch"] if traffic else None})
+                 "traffic": traffic["bytes_per_launch"] if traffic else None,
+                 "traffic_source": traffic_src})
     value = world * (tflops if tensor_bound else gbs)
     cfg = {"workload": w.name, "num_seqs": w.num_seqs, "new_tokens": T,
            "new_tokens_per_seq": {"min": int(w.news.min()), "max": max_q},

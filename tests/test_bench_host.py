@@ -55,8 +55,12 @@ def test_traffic_record_follows_its_sources(tmp_path, monkeypatch):
     assert bench.read_traffic("t.json", "w1")["bytes_per_launch"] == 123.0
     assert bench.read_traffic("t.json", "w2") is None          # another workload
     assert bench.read_traffic("missing.json", "w1") is None
+    assert "unchanged" in bench.traffic_record("t.json", "w1")[1]
     _write(root, "src/b.cuh", "kernel b, changed")
     assert bench.read_traffic("t.json", "w1") is None          # stale after a change
+    rec, note = bench.traffic_record("t.json", "w1")
+    assert rec is None and "earlier kernel sources" in note
+    assert "no ncu record for w2" in bench.traffic_record("t.json", "w2")[1]
 
 
 def test_committed_traffic_records_name_their_workload():
