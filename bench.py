@@ -31,7 +31,9 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "paged decode attention KV GB/s (% of GB300 HBM peak); decode tokens/s per layer"
-DEFAULT_WORKLOAD = "qwen3_0_6b"
+DEFAULT_WORKLOAD = "mistral_7b"
+# further decode workloads timed by the default run (same protocol, no e2e leg)
+DEFAULT_ALSO = "llama31_70b"
 # sources of the dominant kernel (attn_tc_kernel); a recorded DRAM-traffic
 # figure is used only while these files are unchanged
 KERNEL_SRC = ["paged_kv_cache_115_gb300/csrc/pkv_attention_tc.cuh",
@@ -228,63 +230,220 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # CPU oracle baseline (the only place bench.py runs the oracle)
 # ---------------------------------------------------------------------------
-def _cpu_sample(name: str, seed: int, budget_s: float) -> dict:
+def _host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:          # not Linux
+        return os.cpu_count() or 1
+
+
+def _cpu_items(name: str, seed: int):
+    """The workload and its (sequence, KV head) work items, sequence-major."""
+    from paged_kv_cache_115_gb300 import workloads as wl
+    w = wl.build(name, seed=seed)
+    items = [(s, j) for s in range(w.num_seqs) if int(w.context_lens[s]) > 0
+             for j in range(w.num_kv_heads)]
+    return w, items
+
+
+def _cpu_worker(name: str, seed: int, items, budget_s: float, rounds: int, barrier,
+                queue) -> None:
+    """One process of the CPU baseline: prepares the inputs of its work items
+    (untimed), then for each round waits for every other process and runs the
+    oracle (slot mapping + KV write + attention) over its items until they
+    are done or the budget has passed, reporting (round, bytes, start, end,
+    items, tokens)."""
     import numpy as np
     import torch
     import oracle
     from paged_kv_cache_115_gb300 import accounting, workloads as wl
 
+    torch.set_num_threads(1)
     full = wl.build(name, seed=seed)
-    order = list(range(full.num_seqs))
-    done_bytes, done_tokens, done_seqs, elapsed = 0, 0, 0, 0.0
-    H_kv, D = full.num_kv_heads, full.head_dim
-    eb = full.elem_bytes
-    for s in order:
+    G = full.num_q_heads // full.num_kv_heads
+
+    def st(x):
+        x = x.contiguous()
+        return x.view(torch.int16).numpy().view(np.uint16) if x.dtype == torch.bfloat16 \
+            else x.numpy()
+
+    prepared, cur = [], None
+    for s, j in items:
         L = int(full.context_lens[s])
-        sub = wl.build_decode("sample", [L], full.num_q_heads, H_kv, D, full.block_size,
-                              full.dtype, seed=seed + s)
-        t = wl.materialize(sub, seed=seed + s, canary=False)
+        if cur is None or cur[0] != s:
+            sub = wl.build_decode("sample", [L], full.num_q_heads, full.num_kv_heads,
+                                  full.head_dim, full.block_size, full.dtype, seed=seed + s)
+            t = wl.materialize(sub, seed=seed + s, canary=False)
+            cur = (s, sub, {k: st(t[k]) for k in ("q", "k_cache", "v_cache", "k_new", "v_new")})
+            del t
+        _, sub, a = cur
+        # the head-j slice of the sequence's inputs (query heads j*G .. j*G+G-1)
+        prepared.append((sub, L, np.ascontiguousarray(a["q"][:, j * G:(j + 1) * G]),
+                         np.ascontiguousarray(a["k_cache"][:, :, j:j + 1]),
+                         np.ascontiguousarray(a["v_cache"][:, :, j:j + 1]),
+                         np.ascontiguousarray(a["k_new"][:, j:j + 1]),
+                         np.ascontiguousarray(a["v_new"][:, j:j + 1])))
+    cur = None
+    for r in range(rounds):
+        barrier.wait(timeout=900)
+        t0 = time.monotonic()
+        nbytes = ntok = n = 0
+        for sub, L, q, kc, vc, kn, vn in prepared:
+            slots = oracle.slot_mapping(sub.block_tables, sub.positions, sub.block_size)
+            kc2, vc2 = oracle.kv_write(kc, vc, kn, vn, slots)
+            oracle.paged_attention_decode(q, kc2, vc2, sub.block_tables, sub.context_lens,
+                                          sub.scale, sub.dtype)
+            nbytes += accounting.attention_kv_bytes([L], 1, full.head_dim, full.elem_bytes)
+            ntok += L
+            n += 1
+            if time.monotonic() - t0 >= budget_s:
+                break
+        queue.put((r, nbytes, t0, time.monotonic(), n, ntok))
 
-        def st(x):
-            x = x.contiguous()
-            return x.view(torch.int16).numpy().view(np.uint16) if x.dtype == torch.bfloat16 \
-                else x.numpy()
-        q, kc, vc = st(t["q"]), st(t["k_cache"]), st(t["v_cache"])
-        t0 = time.perf_counter()
-        slots = oracle.slot_mapping(sub.block_tables, sub.positions, sub.block_size)
-        kc, vc = oracle.kv_write(kc, vc, st(t["k_new"]), st(t["v_new"]), slots)
-        oracle.paged_attention_decode(q, kc, vc, sub.block_tables, sub.context_lens, sub.scale,
-                                      sub.dtype)
-        elapsed += time.perf_counter() - t0
-        done_bytes += accounting.attention_kv_bytes([L], H_kv, D, eb)
-        done_tokens += 1
-        done_seqs += 1
-        if elapsed >= budget_s:
-            break
-    return {"bytes": done_bytes, "seconds": elapsed, "seqs": done_seqs,
-            "of_seqs": full.num_seqs, "tokens": int(sum(full.context_lens[:done_seqs]))}
+
+def _deal(items, procs: int, num_seqs: int):
+    """Items per process: whole sequences (all their KV heads) dealt round
+    robin when there are at least two sequences per process, else the
+    (sequence, KV head) items themselves dealt round robin."""
+    if num_seqs >= 2 * procs:
+        by_seq = {}
+        for it in items:
+            by_seq.setdefault(it[0], []).append(it)
+        seqs = sorted(by_seq)
+        return [[it for s in seqs[i::procs] for it in by_seq[s]] for i in range(procs)]
+    return [items[i::procs] for i in range(procs)]
 
 
-def run_cpu_baseline(name: str, seed: int, budget_s: float) -> dict:
+def _cpu_parallel(name: str, seed: int, budget_s: float, procs: int, rounds: int = 1):
+    """The oracle on `procs` spawned host processes, each on its share of the
+    workload's (sequence, KV head) items; per round, throughput = all bytes /
+    wall time from the common start to the last finish.  Returns the last
+    round's result (with the list of all rounds under "rounds")."""
+    import multiprocessing as mp
+    import queue as _queue
+    w, items = _cpu_items(name, seed)
+    ctx = mp.get_context("spawn")
+    procs = max(1, min(procs, len(items)))
+    shares = _deal(items, procs, w.num_seqs)
+    barrier, queue = ctx.Barrier(procs), ctx.Queue()
+    ps = [ctx.Process(target=_cpu_worker,
+                      args=(name, seed, shares[i], budget_s, rounds, barrier, queue))
+          for i in range(procs)]
+    for p_ in ps:
+        p_.start()
+    res, deadline = [], time.monotonic() + 900 + rounds * 20 * budget_s
+    while len(res) < procs * rounds:
+        try:
+            res.append(queue.get(timeout=2))
+        except _queue.Empty:
+            dead = [p_.exitcode for p_ in ps if p_.exitcode not in (None, 0)]
+            if dead or time.monotonic() > deadline:
+                for p_ in ps:
+                    if p_.is_alive():
+                        p_.kill()
+                raise RuntimeError(f"cpu baseline worker failed (exit codes {dead})")
+    for p_ in ps:
+        p_.join(timeout=60)
+    out = []
+    for r in range(rounds):
+        rr = [x for x in res if x[0] == r]
+        wall = max(x[3] for x in rr) - min(x[2] for x in rr)
+        done = sum(x[4] for x in rr)
+        out.append({"bytes": sum(x[1] for x in rr), "seconds": wall, "items": done,
+                    "of_items": len(items), "tokens": sum(x[5] for x in rr), "procs": procs,
+                    "seqs_per_s": done / w.num_kv_heads / wall})
+    last = dict(out[-1])
+    last["rounds"] = out
+    return last
+
+
+def _accuracy(check_path: str) -> dict:
+    """Max-abs / max-rel error of the GPU outputs saved in `check_path`
+    against the oracle run on the same inputs (taken before any library
+    kernel ran): block copies, slot mapping, KV write, then attention, on the
+    sampled sequences and KV heads."""
+    import numpy as np
+    import oracle
+    z = np.load(check_path)
+    fmt, dt = str(z["fmt"]), str(z["dtype"])
+    bt, lens, pos, pairs = z["block_tables"], z["context_lens"], z["positions"], z["copy_pairs"]
+    kc, vc, K = z["k_blocks"], z["v_blocks"], int(z["block_size"])
+    if fmt == "bf16":          # plain pools (bf16 or f32)
+        if len(pairs):
+            kc, vc = oracle.kv_block_copy(kc, vc, pairs)
+        slots = oracle.slot_mapping(bt, pos, K)
+        kc, vc = oracle.kv_write(kc, vc, z["k_new"], z["v_new"], slots)
+        ref = oracle.paged_attention_decode(z["q"], kc, vc, bt, lens, float(z["scale"]), dt)
+    else:
+        from oracle import quant as Q
+        slots = oracle.slot_mapping(bt, pos, K)
+        kf = oracle.decode(z["k_new"], "bf16").astype(np.float32)
+        vf = oracle.decode(z["v_new"], "bf16").astype(np.float32)
+        if fmt == "fp8":
+            ks, vs = float(z["k_scale"]), float(z["v_scale"])
+            kc, vc = Q.kv_write_fp8(kc, vc, kf, vf, slots, ks, vs)
+            ref = Q.paged_attention_decode_quant(z["q"], kc, vc, bt, lens, float(z["scale"]),
+                                                 "bf16", "fp8", k_scale=ks, v_scale=vs)
+        else:
+            kc, vc, kts, vts = Q.kv_write_int8(kc, vc, z["k_ts"], z["v_ts"], kf, vf, slots)
+            ref = Q.paged_attention_decode_quant(z["q"], kc, vc, bt, lens, float(z["scale"]),
+                                                 "bf16", "int8", k_tok_scales=kts,
+                                                 v_tok_scales=vts)
+    got = oracle.decode(z["out"], dt)
+    err = np.abs(got - ref)
+    tol = 2e-3 + 1e-2 * np.abs(ref) if dt == "bf16" else np.full_like(ref, 1e-5)
+    return {"max_abs": float(err.max()), "max_rel": float((err / np.maximum(np.abs(ref), 1e-30)).max()),
+            "elements": int(err.size), "within_tolerance": bool((err <= tol).all()),
+            "tolerance": ("|gpu - oracle| <= 2e-3 + 1e-2 |oracle| element-wise" if dt == "bf16"
+                          else "|gpu - oracle| <= 1e-5 element-wise"),
+            "sample": str(z["sample"])}
+
+
+def _cpu_job(name: str, seed: int, budget_s: float, check_paths: str = "") -> dict:
+    """The CPU leg (CUDA hidden): the accuracy checks of the saved GPU outputs
+    (`check_paths`: JSON object, workload name -> .npz path), then the oracle
+    timed on one core and on every host core."""
+    out = {}
+    if check_paths:
+        out["accuracy"] = {nm: _accuracy(pth) for nm, pth in json.loads(check_paths).items()}
+    cores = _host_cores()
+    out["one_core"] = _cpu_parallel(name, seed, min(budget_s / 3, 5.0), 1)
+    out["all_cores"] = _cpu_parallel(name, seed, budget_s, cores)
+    return out
+
+
+def run_cpu_job(name: str, seed: int, budget_s: float, check_paths: str = "") -> dict:
+    """Runs _cpu_job in a fresh interpreter with CUDA hidden (the oracle never
+    shares a process with the GPU arm) and returns its result."""
     env = dict(os.environ)
     for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         env[k] = "1"
     env["CUDA_VISIBLE_DEVICES"] = ""
     code = ("import json,sys; sys.path.insert(0, %r); import bench; "
-            "print(json.dumps(bench._cpu_sample(%r, %d, %f)))" % (ROOT, name, seed, budget_s))
+            "print(json.dumps(bench._cpu_job(%r, %d, %f, %r)))"
+            % (ROOT, name, seed, budget_s, check_paths))
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
-                       cwd=ROOT, timeout=max(600, budget_s * 20))
+                       cwd=ROOT, timeout=max(900, budget_s * 30))
     if r.returncode != 0:
-        raise RuntimeError("cpu baseline failed: " + r.stderr[-2000:])
-    res = json.loads(r.stdout.strip().splitlines()[-1])
-    gbs = res["bytes"] / res["seconds"] / 1e9
+        raise RuntimeError("cpu leg failed: " + r.stderr[-2000:])
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def cpu_baseline_line(name: str, res: dict) -> dict:
+    """The bench line's cpu_baseline object from a _cpu_job result."""
+    a, o = res["all_cores"], res["one_core"]
+    gbs = a["bytes"] / a["seconds"] / 1e9
     return {
-        "value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
-        "seconds": res["seconds"],
-        "decode_tokens_per_s_per_layer": res["seqs"] / res["seconds"],
-        "sample": (f"fp64 numpy oracle (slot mapping + KV write + attention), single-threaded, "
-                   f"on the first {res['seqs']} of {res['of_seqs']} sequences of {name} "
-                   f"({res['tokens']} cached tokens, {res['bytes'] / 1e6:.1f} MB of KV)"),
+        "value": gbs, "unit": "GB/s", "cores": a["procs"], "kind": "oracle",
+        "seconds": a["seconds"],
+        "decode_tokens_per_s_per_layer": a["seqs_per_s"],
+        "one_core": {"value": o["bytes"] / o["seconds"] / 1e9, "unit": "GB/s",
+                     "seconds": o["seconds"], "items": o["items"]},
+        "sample": (f"fp64 numpy oracle (slot mapping + KV write + attention) over {a['items']} "
+                   f"of the {a['of_items']} (sequence, KV head) items of {name} "
+                   f"({a['tokens']} cached tokens, {a['bytes'] / 1e6:.1f} MB of KV), "
+                   f"{a['procs']} spawned processes, one thread each, items dealt round robin; "
+                   f"time = wall clock from the common start to the last finish"),
     }
 
 
@@ -311,131 +470,253 @@ def rank_seed(base_seed: int, rank: int) -> int:
 # ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
-def run_gpu(args):
+def _pick_samples(w, max_tokens: int = 40000):
+    """Sequences for the accuracy check: the longest, the first, the last and
+    the middle one, as many as fit in `max_tokens` cached tokens (at least
+    one)."""
+    import numpy as np
+    S = w.num_seqs
+    cand = [int(np.argmax(w.context_lens)), 0, S - 1, S // 2]
+    picks, tok = [], 0
+    for s in cand:
+        L = int(w.context_lens[s])
+        if s in picks or L <= 0:
+            continue
+        if picks and tok + L > max_tokens:
+            continue
+        picks.append(s)
+        tok += L
+    return picks
+
+
+def _accuracy_snapshot(w, t, fmt: str, quant_scales) -> dict:
+    """Inputs of the accuracy check, taken before any library kernel touches
+    the pool: the blocks the sampled sequences read (and the sources of the
+    copy-on-write pairs that write them), renumbered into a small pool, two of
+    the KV heads, and the sampled rows of q and of the new tokens."""
     import numpy as np
     import torch
-    import torch.distributed as dist
+    samples = _pick_samples(w)
+    K = w.block_size
+    heads = sorted({0, w.num_kv_heads - 1})
+    G = w.num_q_heads // w.num_kv_heads
+    need = set()
+    for s in samples:
+        need.update(int(b) for b in w.block_tables[s, :-(-int(w.context_lens[s]) // K)])
+    pairs = [tuple(int(x) for x in p) for p in w.copy_pairs]
+    while True:
+        more = {src for src, dst in pairs if dst in need and src not in need}
+        if not more:
+            break
+        need |= more
+    blocks = np.array(sorted(need), np.int64)
+    remap = {int(b): i for i, b in enumerate(blocks)}
+    maxb = max(-(-int(w.context_lens[s]) // K) for s in samples)
+    bt = np.zeros((len(samples), maxb), np.int32)
+    for i, s in enumerate(samples):
+        n = -(-int(w.context_lens[s]) // K)
+        bt[i, :n] = [remap[int(b)] for b in w.block_tables[s, :n]]
+    sel = [(remap[src], remap[dst]) for src, dst in pairs if dst in need]
+    idx = torch.from_numpy(blocks).to(t["k_cache"].device)
+    hsel = torch.tensor(heads, device=idx.device)
+    qh = torch.tensor([j * G + g for j in heads for g in range(G)], device=idx.device)
+    sidx = torch.tensor(samples, device=idx.device)
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
-    torch.cuda.set_device(dev)
+    def host(x):
+        x = x.contiguous().cpu()
+        if x.dtype == torch.bfloat16:
+            return x.view(torch.int16).numpy().view(np.uint16)
+        return x.numpy()
 
-    from paged_kv_cache_115_gb300 import accounting, build, workloads as wl
-    if rank == 0 or world == 1:
-        build.build()
-    if world > 1:
-        dist.barrier()
-    from paged_kv_cache_115_gb300 import ops
+    snap = {
+        "fmt": np.array(fmt), "dtype": np.array(w.dtype), "block_size": np.array(K),
+        "scale": np.array(w.scale),
+        "k_blocks": host(t["k_cache"].index_select(0, idx).index_select(2, hsel)),
+        "v_blocks": host(t["v_cache"].index_select(0, idx).index_select(2, hsel)),
+        "block_tables": bt,
+        "context_lens": w.context_lens[samples].astype(np.int32),
+        "positions": w.positions[samples].astype(np.int32),
+        "copy_pairs": np.array(sel, np.int64).reshape(-1, 2),
+        "q": host(t["q"].index_select(0, sidx).index_select(1, qh)),
+        "k_new": host(t["k_new"].index_select(0, sidx).index_select(1, hsel)),
+        "v_new": host(t["v_new"].index_select(0, sidx).index_select(1, hsel)),
+        "sample": np.array(f"sequences {samples} (of {w.num_seqs}), KV heads {heads} with their "
+                           f"{G} query heads each, {len(blocks)} blocks"),
+        "_samples": samples, "_qh": qh,
+    }
+    if fmt == "fp8":
+        snap["k_scale"], snap["v_scale"] = np.array(quant_scales[0]), np.array(quant_scales[1])
+    elif fmt == "int8":
+        slot_idx = (idx[:, None] * K + torch.arange(K, device=idx.device)[None, :]).reshape(-1)
+        snap["k_ts"] = host(t["k_ts"].index_select(0, slot_idx))
+        snap["v_ts"] = host(t["v_ts"].index_select(0, slot_idx))
+    return snap
 
-    w = wl.build(args.workload, seed=rank_seed(args.seed, rank),
-                 block_size=args.block_size or None)
-    t = wl.materialize(w, device=dev, seed=rank_seed(args.seed, rank), canary=False,
-                       values_device="cuda")
-    fmt = args.kv_format
-    stream = torch.cuda.current_stream(dev)
-    out = torch.empty_like(t["q"])
-    slots = torch.empty(w.num_seqs, dtype=torch.int64, device=dev)
-    has_copy = len(w.copy_pairs) > 0
-    max_len = w.max_context_len
-    if fmt == "bf16":
-        kv_bytes = accounting.attention_kv_bytes(w.context_lens, w.num_kv_heads, w.head_dim,
-                                                 w.elem_bytes)
-        ws_bytes = ops.attention_workspace_bytes(w.num_seqs, w.num_q_heads, w.num_kv_heads,
-                                                 w.head_dim, w.block_size, max_len, t["q"].dtype)
-    else:
-        # one-byte pools of seeded random codes (finite e4m3 codes; int8 codes
-        # with per-slot scales); the bf16 pools are dropped
-        g = torch.Generator(device=dev)
-        g.manual_seed(rank_seed(args.seed, rank) + 7)
-        shape = t["k_cache"].shape
-        del t["k_cache"], t["v_cache"]
-        for name in ("k_cache", "v_cache"):
-            c = torch.randint(0, 256, shape, generator=g, device=dev, dtype=torch.int32)
-            c = torch.where((c & 0x7F) == 0x7F, c - 1, c).to(torch.uint8)
-            t[name] = c if fmt == "fp8" else c.view(torch.int8)
-        if fmt == "int8":
-            n = shape[0] * shape[1]
-            t["k_ts"] = torch.rand(n, generator=g, device=dev) * 0.02 + 0.001
-            t["v_ts"] = torch.rand(n, generator=g, device=dev) * 0.02 + 0.001
-            qd = ops.kv_quant("int8", k_token_scales=t["k_ts"], v_token_scales=t["v_ts"])
-        else:
-            qd = ops.kv_quant("fp8", 0.05, 0.05)
-        kv_bytes = accounting.attention_kv_bytes(w.context_lens, w.num_kv_heads, w.head_dim, 1)
-        if fmt == "int8":
-            kv_bytes += int(w.context_lens.sum()) * 2 * 4      # one K and one V scale per token
-        ws_bytes = ops.attention_quant_workspace_bytes(w.num_seqs, w.num_q_heads,
-                                                       w.num_kv_heads, w.head_dim, w.block_size,
-                                                       max_len, t["q"].dtype, qd)
-    workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
-    use_graph = not args.eager
-    # the step's inputs live back to back in one device buffer with a pinned
-    # host twin, so that the end-to-end leg moves them in one copy
-    names = ["q", "k_new", "v_new", "block_tables", "context_lens", "positions"]
-    if has_copy:
-        names.append("copy_pairs")
-    dev_stage, host_stage = staged_inputs(t, names, dev)
 
-    def attention():
+def _save_snapshot(snap: dict, out) -> str:
+    """Adds the GPU output rows to a snapshot and writes it to a temporary
+    .npz file; returns its path."""
+    import tempfile
+    import numpy as np
+    import torch
+    sidx = torch.tensor(snap["_samples"], device=out.device)
+    rows = out.index_select(0, sidx).index_select(1, snap["_qh"]).contiguous().cpu()
+    data = {k: v for k, v in snap.items() if not k.startswith("_")}
+    data["out"] = rows.view(torch.int16).numpy().view(np.uint16) \
+        if rows.dtype == torch.bfloat16 else rows.numpy()
+    fd, path = tempfile.mkstemp(suffix=".npz", prefix="pkv_check_")
+    os.close(fd)
+    np.savez(path, **data)
+    return path
+
+
+class DecodeCase:
+    """One decode workload set up on the GPU: pools, step inputs staged in
+    one device buffer with a pinned host twin, workspace, and the step's
+    calls (block copy, fused slot mapping + KV write, attention)."""
+
+    def __init__(self, args, name, dev, rank, snapshot: bool):
+        import torch
+        from paged_kv_cache_115_gb300 import accounting, ops, workloads as wl
+        self.ops = ops
+        self.fmt = fmt = args.kv_format
+        self.dev = dev
+        w = self.w = wl.build(name, seed=rank_seed(args.seed, rank),
+                              block_size=args.block_size or None)
+        t = self.t = wl.materialize(w, device=dev, seed=rank_seed(args.seed, rank),
+                                    canary=False, values_device="cuda")
+        self.out = torch.empty_like(t["q"])
+        self.slots = torch.empty(w.num_seqs, dtype=torch.int64, device=dev)
+        self.has_copy = len(w.copy_pairs) > 0
+        self.max_len = max_len = w.max_context_len
+        scales = None
         if fmt == "bf16":
+            self.qd = None
+            self.kv_bytes = accounting.attention_kv_bytes(w.context_lens, w.num_kv_heads,
+                                                          w.head_dim, w.elem_bytes)
+            ws_bytes = ops.attention_workspace_bytes(w.num_seqs, w.num_q_heads, w.num_kv_heads,
+                                                     w.head_dim, w.block_size, max_len,
+                                                     t["q"].dtype)
+        else:
+            # one-byte pools of seeded random codes (finite e4m3 codes; int8
+            # codes with per-slot scales); the bf16 pools are dropped
+            g = torch.Generator(device=dev)
+            g.manual_seed(rank_seed(args.seed, rank) + 7)
+            shape = t["k_cache"].shape
+            del t["k_cache"], t["v_cache"]
+            for nm in ("k_cache", "v_cache"):
+                c = torch.randint(0, 256, shape, generator=g, device=dev, dtype=torch.int32)
+                c = torch.where((c & 0x7F) == 0x7F, c - 1, c).to(torch.uint8)
+                t[nm] = c if fmt == "fp8" else c.view(torch.int8)
+            if fmt == "int8":
+                n = shape[0] * shape[1]
+                t["k_ts"] = torch.rand(n, generator=g, device=dev) * 0.02 + 0.001
+                t["v_ts"] = torch.rand(n, generator=g, device=dev) * 0.02 + 0.001
+                self.qd = ops.kv_quant("int8", k_token_scales=t["k_ts"],
+                                       v_token_scales=t["v_ts"])
+            else:
+                scales = (0.05, 0.05)
+                self.qd = ops.kv_quant("fp8", *scales)
+            self.kv_bytes = accounting.attention_kv_bytes(w.context_lens, w.num_kv_heads,
+                                                          w.head_dim, 1)
+            if fmt == "int8":
+                self.kv_bytes += int(w.context_lens.sum()) * 2 * 4   # a K and a V scale per token
+            ws_bytes = ops.attention_quant_workspace_bytes(w.num_seqs, w.num_q_heads,
+                                                           w.num_kv_heads, w.head_dim,
+                                                           w.block_size, max_len, t["q"].dtype,
+                                                           self.qd)
+        # the accuracy check's inputs, before any library kernel runs
+        self.snap = None
+        if snapshot and not (fmt != "bf16" and self.has_copy):
+            self.snap = _accuracy_snapshot(w, t, fmt, scales)
+        # zeroed once; the library leaves the workspace's counters at zero
+        self.workspace = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+        self.names = ["q", "k_new", "v_new", "block_tables", "context_lens", "positions"]
+        if self.has_copy:
+            self.names.append("copy_pairs")
+        # the step's inputs back to back in one device buffer with a pinned
+        # host twin, so that the end-to-end leg moves them in one copy
+        self.dev_stage, self.host_stage = staged_inputs(t, self.names, dev)
+        attn_launches = ops.attention_launch_count(w.num_seqs, w.num_q_heads, w.num_kv_heads,
+                                                   w.head_dim, w.block_size, max_len,
+                                                   t["q"].dtype)
+        copy_launches = (1 if fmt != "int8" else 2) if self.has_copy else 0
+        self.launches_per_step = copy_launches + 1 + attn_launches
+        pool_eb = w.elem_bytes if fmt == "bf16" else 1
+        n_new = int((w.positions >= 0).sum())
+        self.row_fns = []
+        if self.has_copy:
+            self.row_fns.append(("kv_block_copy", self.copy_fn,
+                                 accounting.block_copy_bytes(len(w.copy_pairs), w.block_size,
+                                                             w.num_kv_heads, w.head_dim,
+                                                             pool_eb)))
+        self.row_fns.append(("paged_kv_append", self.append_fn,
+                             n_new * w.num_kv_heads * w.head_dim * 2 * (w.elem_bytes + pool_eb)))
+        self.row_fns.append(("paged_attention_decode", self.attention, self.kv_bytes))
+
+    # ---- the step's calls (they read self.t / self.out when called) ----
+    def attention(self):
+        t, w, ops = self.t, self.w, self.ops
+        if self.fmt == "bf16":
             ops.paged_attention_decode(t["q"], t["k_cache"], t["v_cache"], t["block_tables"],
-                                       t["context_lens"], w.scale, out=out,
-                                       max_context_len=max_len, workspace=workspace)
+                                       t["context_lens"], w.scale, out=self.out,
+                                       max_context_len=self.max_len, workspace=self.workspace)
         else:
             ops.paged_attention_decode_quant(t["q"], t["k_cache"], t["v_cache"],
-                                             t["block_tables"], t["context_lens"], w.scale, qd,
-                                             out=out, max_context_len=max_len,
-                                             workspace=workspace)
+                                             t["block_tables"], t["context_lens"], w.scale,
+                                             self.qd, out=self.out, max_context_len=self.max_len,
+                                             workspace=self.workspace)
 
-    def copy_fn():
-        if fmt == "bf16":
+    def copy_fn(self):
+        t, ops = self.t, self.ops
+        if self.fmt == "bf16":
             ops.kv_block_copy(t["k_cache"], t["v_cache"], t["copy_pairs"])
         else:
-            ops.kv_block_copy_quant(t["k_cache"], t["v_cache"], t["copy_pairs"], qd)
+            ops.kv_block_copy_quant(t["k_cache"], t["v_cache"], t["copy_pairs"], self.qd)
 
-    def append_fn():
+    def append_fn(self):
         # slot mapping + KV write of the new tokens in one fused launch
-        if fmt == "bf16":
+        t, ops = self.t, self.ops
+        if self.fmt == "bf16":
             ops.paged_kv_append(t["k_new"], t["v_new"], t["block_tables"], t["positions"],
-                                t["k_cache"], t["v_cache"], slots)
+                                t["k_cache"], t["v_cache"], self.slots)
         else:
             ops.paged_kv_append_quant(t["k_new"], t["v_new"], t["block_tables"], t["positions"],
-                                      t["k_cache"], t["v_cache"], qd, slots)
+                                      t["k_cache"], t["v_cache"], self.qd, self.slots)
 
-    def prologue():
-        if has_copy:
-            copy_fn()
-        append_fn()
+    def step(self):
+        if self.has_copy:
+            self.copy_fn()
+        self.append_fn()
+        self.attention()
 
-    # kernels launched per step (ours only)
-    attn_launches = ops.attention_launch_count(w.num_seqs, w.num_q_heads, w.num_kv_heads,
-                                               w.head_dim, w.block_size, max_len, t["q"].dtype)
-    copy_launches = (1 if fmt != "int8" else 2) if has_copy else 0
-    launches_per_step = copy_launches + 1 + attn_launches
+    def release(self):
+        self.t = self.out = self.workspace = self.dev_stage = self.host_stage = None
 
-    for _ in range(max(args.warmup, 3)):
-        prologue()
-        attention()
+
+def _time_case(case, K: int, warmup: int, use_graph: bool, stream, world: int) -> dict:
+    """Warm-up, then K timed steps (graph replays of the whole step, or eager
+    launches) bracketed by events on the launching stream; then K replays of
+    the attention call alone, each between events, for the per-launch
+    roofline; then each row of the step alone with L2 flushed before it."""
+    import torch
+    import torch.distributed as dist
+    dev, ops = case.dev, case.ops
+    for _ in range(max(warmup, 3)):
+        case.step()
     torch.cuda.synchronize(dev)
     assert ops.get_device_error(dev) == 0
-
-    K = args.steps
+    g_step = g_attn = cap = None
     if use_graph:
         # the whole step as one graph; the attention call alone as another
-        # (for the per-launch roofline timing)
         # (capture needs a side stream; replays run on the timing stream)
         g_step, g_attn = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
         cap = torch.cuda.Stream(dev)
         cap.wait_stream(stream)
         with torch.cuda.graph(g_step, stream=cap):
-            prologue()
-            attention()
+            case.step()
         with torch.cuda.graph(g_attn, stream=cap):
-            attention()
+            case.attention()
         stream.wait_stream(cap)
         torch.cuda.synchronize(dev)
         for _ in range(3):
@@ -444,8 +725,6 @@ def run_gpu(args):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(K)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(dev.index) if rank == 0 else None
-    time.sleep(0.2 if clocks else 0)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
@@ -454,9 +733,11 @@ def run_gpu(args):
         if use_graph:
             g_step.replay()
         else:
-            prologue()
+            if case.has_copy:
+                case.copy_fn()
+            case.append_fn()
             ev[i][0].record(stream)
-            attention()
+            case.attention()
             ev[i][1].record(stream)
     stop.record(stream)
     torch.cuda.synchronize(dev)
@@ -466,30 +747,18 @@ def run_gpu(args):
             g_attn.replay()
             ev[i][1].record(stream)
         torch.cuda.synchronize(dev)
-    clock_info = clocks.stop() if clocks else None
     if world > 1:
         dist.barrier()
     total_ms = start.elapsed_time(stop)
-    attn_ms = [a.elapsed_time(b) for a, b in ev]
-    attn_avg_ms = sum(attn_ms) / K
+    attn_avg_ms = sum(a.elapsed_time(b) for a, b in ev) / K
     assert ops.get_device_error(dev) == 0
 
-    # ---- each row of the step alone: events around the row only, L2 flushed
-    # (a 256 MB write) before every timed launch
+    # each row of the step alone: events around the row only, L2 flushed (a
+    # 256 MB write) before every timed launch
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
-    row_fns = []
-    pool_eb = w.elem_bytes if fmt == "bf16" else 1
-    n_new = int((w.positions >= 0).sum())
-    if has_copy:
-        row_fns.append(("kv_block_copy", copy_fn,
-                        accounting.block_copy_bytes(len(w.copy_pairs), w.block_size,
-                                                    w.num_kv_heads, w.head_dim, pool_eb)))
-    row_fns.append(("paged_kv_append", append_fn,
-                    n_new * w.num_kv_heads * w.head_dim * 2 * (w.elem_bytes + pool_eb)))
-    row_fns.append(("paged_attention_decode", attention, kv_bytes))
     rows = {}
     R = max(5, min(50, K))
-    for name, fn, nbytes in row_fns:
+    for nm, fn, nbytes in case.row_fns:
         times = []
         for _ in range(R):
             flush.fill_(1)
@@ -500,58 +769,63 @@ def run_gpu(args):
             torch.cuda.synchronize(dev)
             times.append(a.elapsed_time(b))
         med = statistics.median(times)
-        rows[name] = {"median_us": med * 1e3, "min_us": min(times) * 1e3,
-                      "algorithmic_bytes": nbytes, "GBps": nbytes / (med * 1e-3) / 1e9,
-                      "frac": None}
+        rows[nm] = {"median_us": med * 1e3, "min_us": min(times) * 1e3,
+                    "algorithmic_bytes": nbytes, "GBps": nbytes / (med * 1e-3) / 1e9,
+                    "frac": None, "l2": "flushed before each launch (eager, one launch each)"}
     del flush
     assert ops.get_device_error(dev) == 0
+    return {"total_ms": total_ms, "attn_avg_ms": attn_avg_ms, "rows": rows,
+            "g_step": g_step, "cap": cap}
 
-    # ---- end to end through the public API with host buffers.  Every step
-    # copies its inputs from a pinned host buffer (one copy) and reads its
-    # output back (one copy).  The copies run on a second stream against two
-    # sets of staged inputs and outputs, so that step i+1's input copy and
-    # step i's output copy overlap the neighbouring steps' compute.
-    out0, views0 = out, {k: t[k] for k in names}
+
+def _e2e_case(case, timing: dict, K: int, use_graph: bool, stream, world: int) -> dict:
+    """End to end through the public API with host buffers.  Every step
+    copies its inputs from a pinned host buffer (one copy) and reads its
+    output back (one copy).  The copies run on a second stream against two
+    sets of staged inputs and outputs, so that step i+1's input copy and step
+    i's output copy overlap the neighbouring steps' compute."""
+    import torch
+    import torch.distributed as dist
+    dev, t, names = case.dev, case.t, case.names
+    out0, views0 = case.out, {k: t[k] for k in names}
     t1 = dict(views0)
     dev_stage1, host_stage1 = staged_inputs(t1, names, dev)
     out1 = torch.empty_like(out0)
-    sets = [(dev_stage, host_stage, views0, out0), (dev_stage1, host_stage1, t1, out1)]
+    sets = [(case.dev_stage, case.host_stage, views0, out0), (dev_stage1, host_stage1, t1, out1)]
     host_outs = [torch.empty(out0.shape, dtype=out0.dtype, pin_memory=True) for _ in range(2)]
-    h2d = host_stage.numel()
+    h2d = case.host_stage.numel()
     d2h = host_outs[0].numel() * host_outs[0].element_size()
-    graphs = [g_step] if use_graph else []
+    graphs = [timing["g_step"]] if use_graph else []
     if use_graph:
-        # the same step over the second set (closures read t and out when called)
+        # the same step over the second set (the calls read t and out when called)
         for k in names:
             t[k] = t1[k]
-        out = out1
+        case.out = out1
         g1 = torch.cuda.CUDAGraph()
+        cap = timing["cap"]
         cap.wait_stream(stream)
         with torch.cuda.graph(g1, stream=cap):
-            prologue()
-            attention()
+            case.step()
         stream.wait_stream(cap)
         graphs.append(g1)
         for k in names:
             t[k] = views0[k]
-        out = out0
+        case.out = out0
         torch.cuda.synchronize(dev)
     cs = torch.cuda.Stream(dev)
     pipe_sets = [(sets[i][0], sets[i][1], sets[i][3], host_outs[i]) for i in range(2)]
 
     def e2e_compute(b):
-        nonlocal out
         if use_graph:
             graphs[b].replay()
             return
         for k in names:
             t[k] = sets[b][2][k]
-        out = sets[b][3]
-        prologue()
-        attention()
+        case.out = sets[b][3]
+        case.step()
         for k in names:
             t[k] = views0[k]
-        out = out0
+        case.out = out0
 
     def e2e_run(n, start_ev=None):
         run_pipelined(n, pipe_sets, e2e_compute, stream, cs, start_ev)
@@ -571,9 +845,93 @@ def run_gpu(args):
     ref_out = out0.cpu()
     for h in host_outs:
         assert torch.equal(h.view(torch.int16), ref_out.view(torch.int16)), "e2e output differs"
+    return {"ms": e2e_ms, "h2d": h2d, "d2h": d2h}
+
+
+def _roofline(case, attn_avg_ms: float, hbm: float, peak_src: str) -> dict:
+    w = case.w
+    achieved = case.kv_bytes / (attn_avg_ms * 1e-3) / 1e9
+    traffic, traffic_src = traffic_record()
+    if traffic and (traffic.get("workload") != w.name or traffic.get("kv_format") != case.fmt
+                    or traffic.get("block_size") != w.block_size):
+        traffic = None                  # the record is for another workload
+        traffic_src = "the ncu record is for another workload, pool format or block size"
+    return {
+        "bound": "hbm",
+        "kernel": "pkv_attention_decode (attn_tc_kernel, split-K merge fused)",
+        "achieved": achieved,
+        "peak": hbm,
+        "peak_source": f"{peak_src} hbm_gbs (copy, read+write)",
+        "unit": "GB/s",
+        "frac": achieved / hbm,
+        "algorithmic_bytes_per_launch": case.kv_bytes,
+        "avg_launch_ms": attn_avg_ms,
+        "timing": "CUDA events around back-to-back graph replays of the attention call "
+                  "on the launching stream (L2 warm from the previous replay only where the "
+                  "KV fits in it)",
+        "traffic": traffic["bytes_per_launch"] if traffic else None,
+        "traffic_source": traffic_src,
+    }
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
+    torch.cuda.set_device(dev)
+
+    from paged_kv_cache_115_gb300 import build
+    if rank == 0 or world == 1:
+        build.build()
+    if world > 1:
+        dist.barrier()
+    from paged_kv_cache_115_gb300 import ops  # noqa: F401  (loads the library)
+
+    check = rank == 0 and not args.no_cpu_baseline
+    use_graph = not args.eager
+    stream = torch.cuda.current_stream(dev)
+    K = args.steps
+    also = [n for n in (args.also.split(",") if args.also else []) if n and n != args.workload]
+
+    case = DecodeCase(args, args.workload, dev, rank, snapshot=check)
+    clocks = ClockSampler(dev.index) if rank == 0 else None
+    time.sleep(0.2 if clocks else 0)
+    tm = _time_case(case, K, args.warmup, use_graph, stream, world)
+    e2e = _e2e_case(case, tm, K, use_graph, stream, world)
+    checks = {}
+    if case.snap is not None:
+        checks[case.w.name] = _save_snapshot(case.snap, case.out)
+    head = {"w": case.w, "kv_bytes": case.kv_bytes, "launches": case.launches_per_step,
+            "fmt": case.fmt, "case": case}
+    # further workloads, same protocol (no end-to-end leg)
+    extra = []
+    tm["g_step"] = tm["cap"] = None
+    for nm in also:
+        case.release()
+        torch.cuda.synchronize(dev)
+        torch.cuda.empty_cache()
+        c2 = DecodeCase(args, nm, dev, rank, snapshot=check)
+        tm2 = _time_case(c2, K, args.warmup, use_graph, stream, world)
+        if c2.snap is not None:
+            checks[c2.w.name] = _save_snapshot(c2.snap, c2.out)
+        extra.append((c2, tm2))
+        case = c2
+    clock_info = clocks.stop() if clocks else None
 
     # ---- max over ranks
-    total_ms, e2e_ms, attn_avg_ms = max_over_ranks([total_ms, e2e_ms, attn_avg_ms], dev)
+    vals = [tm["total_ms"], e2e["ms"], tm["attn_avg_ms"]]
+    for _, t2 in extra:
+        vals += [t2["total_ms"], t2["attn_avg_ms"]]
+    vals = max_over_ranks(vals, dev)
+    total_ms, e2e_ms, attn_avg_ms = vals[:3]
+    w, kv_bytes = head["w"], head["kv_bytes"]
     ms_step = total_ms / K
     value = world * kv_bytes / (ms_step * 1e-3) / 1e9
     e2e_value = world * kv_bytes / (e2e_ms * 1e-3) / 1e9
@@ -585,22 +943,16 @@ def run_gpu(args):
 
     peaks, peak_src = read_peaks()
     hbm = float(peaks["hbm_gbs"])
-    achieved = kv_bytes / (attn_avg_ms * 1e-3) / 1e9
-    for r in rows.values():
+    for r in tm["rows"].values():
         r["frac"] = r["GBps"] / hbm
-    traffic, traffic_src = traffic_record()
-    if traffic and (traffic.get("workload") != w.name or traffic.get("kv_format") != fmt
-                    or traffic.get("block_size") != w.block_size):
-        traffic = None                  # the record is for another workload
-        traffic_src = "the ncu record is for another workload, pool format or block size"
     cfg = workload_desc(w)
     cfg["l2"] = (f"inputs larger than L2: {kv_bytes / 1e6:.0f} MB of KV read per step "
                  f"vs 129 MB L2; no flush between steps")
     cfg["parallelism"] = f"replicas x{world}" if world > 1 else "single GPU"
     cfg["launch"] = "CUDA graph replay (one graph per step)" if use_graph else "eager launches"
     blocks_used = int(sum(-(-int(L) // w.block_size) for L in w.context_lens))
-    cfg["kv_reserved_bytes"] = blocks_used * w.block_size * w.num_kv_heads * w.head_dim * 2 * \
-        (w.elem_bytes if fmt == "bf16" else 1)
+    pool_eb = w.elem_bytes if head["fmt"] == "bf16" else 1
+    cfg["kv_reserved_bytes"] = blocks_used * w.block_size * w.num_kv_heads * w.head_dim * 2 * pool_eb
     cfg["tail_waste_tokens"] = blocks_used * w.block_size - int(w.context_lens.sum())
     cfg["block_table_bytes"] = int(w.block_tables.nbytes)
     line = {
@@ -614,40 +966,61 @@ def run_gpu(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": w.dtype if fmt == "bf16" else f"{w.dtype} q / {fmt} KV",
+        "dtype": w.dtype if head["fmt"] == "bf16" else f"{w.dtype} q / {head['fmt']} KV",
         "data": "synthetic: seeded N(0,1) q/k/v rounded to bf16; block tables from a seeded "
                 "shuffled free list; lengths drawn per the workload recipe",
         "config": cfg,
         "hbm_frac": value / world / hbm,
         "decode_tokens_per_s_per_layer": world * w.num_seqs / (ms_step * 1e-3),
-        "roofline": {
-            "bound": "hbm",
-            "kernel": "pkv_attention_decode (partition + split-K reduce)",
-            "achieved": achieved,
-            "peak": hbm,
-            "peak_source": f"{peak_src} hbm_gbs (copy, read+write)",
-            "unit": "GB/s",
-            "frac": achieved / hbm,
-            "algorithmic_bytes_per_launch": kv_bytes,
-            "avg_launch_ms": attn_avg_ms,
-            "traffic": traffic["bytes_per_launch"] if traffic else None,
-            "traffic_source": traffic_src,
-        },
+        "roofline": _roofline(head["case"], attn_avg_ms, hbm, peak_src),
         "e2e": {"value": e2e_value, "unit": "GB/s", "ms_per_step": e2e_ms,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                 "decode_tokens_per_s_per_layer": world * w.num_seqs / (e2e_ms * 1e-3),
                 "copies": "per step one pinned-host-to-device copy of the inputs and one "
                           "device-to-pinned-host copy of the output, on a second stream with "
                           "two staged buffer sets, overlapping the neighbouring steps"},
-        "rows": rows,
-        "gpu_launches": launches_per_step * K,
+        "rows": tm["rows"],
+        "gpu_launches": head["launches"] * K,
         "clocks": clock_info,
     }
-    if not args.no_cpu_baseline:
+    workloads = {}
+    for i, (c2, t2) in enumerate(extra):
+        tot2, att2 = vals[3 + 2 * i], vals[4 + 2 * i]
+        ms2 = tot2 / K
+        for r in t2["rows"].values():
+            r["frac"] = r["GBps"] / hbm
+        workloads[c2.w.name] = {
+            "value": world * c2.kv_bytes / (ms2 * 1e-3) / 1e9, "unit": "GB/s",
+            "ms_per_step": ms2, "steps": K,
+            "hbm_frac": c2.kv_bytes / (ms2 * 1e-3) / 1e9 / hbm,
+            "decode_tokens_per_s_per_layer": world * c2.w.num_seqs / (ms2 * 1e-3),
+            "config": workload_desc(c2.w),
+            "roofline": _roofline(c2, att2, hbm, peak_src),
+            "rows": t2["rows"],
+            "gpu_launches": c2.launches_per_step * K,
+        }
+        line["gpu_launches"] += c2.launches_per_step * K
+    if workloads:
+        line["workloads"] = workloads
+    if check:
         try:
-            line["cpu_baseline"] = run_cpu_baseline(args.workload, args.seed, args.cpu_budget)
+            res = run_cpu_job(args.workload, args.seed, args.cpu_budget,
+                              json.dumps(checks))
+            line["cpu_baseline"] = cpu_baseline_line(args.workload, res)
+            acc = res.get("accuracy", {})
+            if w.name in acc:
+                line["accuracy"] = acc[w.name]
+            for nm, a in acc.items():
+                if nm in workloads:
+                    workloads[nm]["accuracy"] = a
         except Exception as e:  # report, do not hide the GPU number
             line["cpu_baseline"] = {"value": None, "error": str(e)[:300], "kind": "oracle"}
+        finally:
+            for pth in checks.values():
+                try:
+                    os.remove(pth)
+                except OSError:
+                    pass
     if world > 1:
         dist.destroy_process_group()
     return line
@@ -657,23 +1030,6 @@ def run_gpu(args):
 # block swap (GPU <-> pinned host): preempt half the batch and bring it back
 # ---------------------------------------------------------------------------
 SWAP_METRIC = "KV block swap GB/s (GPU pool <-> pinned host pool, out + in)"
-
-
-def swap_plan(w, seed: int):
-    """Every other sequence of the workload is preempted by swap: its blocks
-    (K and V) go to a host pool in a seeded shuffled order, and come back into
-    a seeded permutation of the same GPU blocks (scattered placement)."""
-    import numpy as np
-    rng = np.random.default_rng(seed + 101)
-    blocks = []
-    for s in range(1, w.num_seqs, 2):
-        n = -(-int(w.context_lens[s]) // w.block_size)
-        blocks.extend(int(b) for b in w.block_tables[s, :n])
-    blocks = np.array(blocks, np.int64)
-    host = rng.permutation(len(blocks)).astype(np.int64)
-    out_pairs = np.stack([blocks, host], 1)
-    in_pairs = np.stack([host, rng.permutation(blocks)], 1)
-    return out_pairs, in_pairs
 
 
 def _swap_cpu_sample(budget_s: float) -> dict:
@@ -715,7 +1071,7 @@ def run_swap(args):
     from paged_kv_cache_115_gb300 import ops
 
     w = wl.build(args.workload, seed=rank_seed(args.seed, rank))
-    out_np, in_np = swap_plan(w, rank_seed(args.seed, rank))
+    out_np, in_np = wl.swap_plan(w, rank_seed(args.seed, rank))
     n = len(out_np)
     shape = (w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim)
     td = torch.bfloat16 if w.dtype == "bf16" else torch.float32
@@ -1185,24 +1541,27 @@ def run_reference(args):
                     "d2h_bytes_per_step": 0},
             "gpu_launches": 0,
         }
-    for _ in range(args.warmup):
-        _cpu_sample(args.workload, args.seed, min(per_step, 1.0))
-    tot_bytes, tot_s, seqs = 0, 0.0, 0
-    for _ in range(args.steps):
-        r = _cpu_sample(args.workload, args.seed, per_step)
-        tot_bytes += r["bytes"]
-        tot_s += r["seconds"]
-        seqs += r["seqs"]
+    # each step: the oracle on every host core over the workload's (sequence,
+    # KV head) items, for about per_step seconds (the whole workload when it
+    # finishes sooner); warm-up steps are short
+    cores = _host_cores()
+    r = _cpu_parallel(args.workload, args.seed, per_step, cores, rounds=args.warmup + args.steps)
+    timed = r["rounds"][args.warmup:]
+    tot_bytes = sum(x["bytes"] for x in timed)
+    tot_s = sum(x["seconds"] for x in timed)
+    items = sum(x["items"] for x in timed)
+    procs = r["procs"]
     value = tot_bytes / tot_s / 1e9
     cfg = workload_desc(w)
-    sample = (f"fp64 numpy oracle on the first sequences of {args.workload}, about "
-              f"{per_step:.0f} s of CPU work per step, {seqs} sequences in all")
+    sample = (f"fp64 numpy oracle (slot mapping + KV write + attention) on {procs} spawned "
+              f"processes over the (sequence, KV head) items of {args.workload}, up to about "
+              f"{per_step:.0f} s per step, {items} items in all")
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 0,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_s / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (same recipe as the GPU arm)", "config": cfg,
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": procs, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
@@ -1216,6 +1575,9 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["gpu", "reference"], default="gpu")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--also", default=DEFAULT_ALSO,
+                    help="decode: comma-separated further workloads timed after the headline "
+                         "one (same protocol, reported under \"workloads\"); '' for none")
     ap.add_argument("--kv-format", choices=["bf16", "fp8", "int8"], default="bf16",
                     help="KV pool storage: bf16, FP8 e4m3 (per-tensor scale) or INT8 "
                          "(per-token scale)")

@@ -221,7 +221,12 @@ PKV_API pkv_status pkv_attention_decode(const void* q, const void* k_cache, cons
  * are rejected with PKV_ERR_WORKSPACE_TOO_SMALL before anything is launched.
  * The first call on a device looks up that device's copy of the array
  * (cudaGetSymbolAddress) with the device current; make that first call
- * before any stream capture.  All calls on a device share the one array:
+ * before any stream capture.  The array is part of the library's device
+ * module, which CUDA loads on a device at the library's first launch or
+ * symbol lookup there: make the first call of any pkv_* compute function on
+ * a device before the KV pool claims that device's free memory, or the
+ * module (64 MiB of it this array) cannot be loaded.  A failed lookup
+ * returns PKV_ERR_CUDA and is not remembered: the next call tries again.  All calls on a device share the one array:
  * calls that overlap on the GPU (different streams, no ordering between
  * them) race on it and give undefined results.  No initial contents are
  * needed; whatever a previous call left there is overwritten before use.

@@ -36,6 +36,7 @@ from .paged_attention import (  # noqa: F401
     kv_block_swap,
     gather_kv,
     dense_attention,
+    attention_rows,
     paged_attention_decode,
     paged_attention_decode_one,
     paged_attention_streaming,

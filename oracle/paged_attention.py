@@ -34,6 +34,7 @@ __all__ = [
     "kv_block_swap",
     "gather_kv",
     "dense_attention",
+    "attention_rows",
     "paged_attention_decode",
     "paged_attention_decode_one",
     "paged_attention_streaming",
@@ -200,6 +201,31 @@ def dense_attention(q: np.ndarray, K: np.ndarray, V: np.ndarray,
     w = np.exp(z - z.max())
     w /= w.sum()
     return w @ V
+
+
+def attention_rows(Q: np.ndarray, K: np.ndarray, V: np.ndarray, limits,
+                   scale: float) -> np.ndarray:
+    """:func:`dense_attention` for several query rows over the same contiguous
+    K, V (fp64): row ``i`` attends to keys ``0 .. limits[i]`` inclusive
+    ("KV Cache：长上下文为什么吃显存" §01, the new token at position t sees
+    ``K_{1:t}``).  All scores come from one matrix product; keys past a row's
+    limit get weight zero; each row's maximum is subtracted before
+    exponentiating.  A row with a negative limit sees no key and gives zeros.
+    """
+    Q = np.asarray(Q, dtype=np.float64)
+    lim = np.asarray(limits, dtype=np.int64).reshape(-1)
+    out = np.zeros((Q.shape[0], V.shape[1]), dtype=np.float64)
+    if K.shape[0] == 0 or Q.shape[0] == 0:
+        return out
+    z = scale * (Q @ K.T)                                     # [rows, keys]
+    visible = np.arange(K.shape[0])[None, :] <= lim[:, None]
+    live = visible.any(axis=1)
+    z = np.where(visible, z, -np.inf)
+    m = np.where(live, z.max(axis=1), 0.0)
+    w = np.where(visible, np.exp(z - m[:, None]), 0.0)
+    tot = w.sum(axis=1)
+    out[live] = (w[live] @ V) / tot[live, None]
+    return out
 
 
 def paged_attention_decode_one(q: np.ndarray, k_cache: np.ndarray,

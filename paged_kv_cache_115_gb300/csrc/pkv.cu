@@ -681,22 +681,30 @@ pkv_status check_quant(const pkv_kv_quant* q, bool need_token_scales) {
 static __device__ __align__(256) uint8_t g_noalloc_scratch[PKV_NOALLOC_SCRATCH_BYTES];
 
 struct NoAllocScratch {
-  std::once_flag once;
-  void* ptr = nullptr;
-  cudaError_t err = cudaSuccess;
+  std::mutex mu;
+  void* ptr = nullptr;   // set only once a lookup has succeeded
 };
 NoAllocScratch g_noalloc[kMaxDevices];
 
-// Device address of this device's copy of the scratch array (set up once per
-// device, with that device current).
+// Device address of this device's copy of the scratch array, looked up with
+// that device current.  Only a successful lookup is kept: a failed one (for
+// instance the module could not be loaded because the device's memory was
+// full) returns its error and the next call tries again.
 pkv_status noalloc_scratch(void** ptr) {
   int dev = 0;
   PKV_CUDA(cudaGetDevice(&dev));
   PKV_CHECK(dev >= 0 && dev < kMaxDevices, PKV_ERR_UNSUPPORTED, "device ordinal %d too large", dev);
   NoAllocScratch& sc = g_noalloc[dev];
-  std::call_once(sc.once, [&] { sc.err = cudaGetSymbolAddress(&sc.ptr, g_noalloc_scratch); });
-  if (sc.err != cudaSuccess || sc.ptr == nullptr)
-    return fail(PKV_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(sc.err));
+  std::lock_guard<std::mutex> lock(sc.mu);
+  if (sc.ptr == nullptr) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+      (void)cudaGetLastError();
+      return fail(PKV_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
+    }
+    sc.ptr = p;
+  }
   *ptr = sc.ptr;
   return PKV_OK;
 }

@@ -153,10 +153,30 @@ def _ptr(t: torch.Tensor) -> ctypes.c_void_p:
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _device_call(fn):
+    """Runs a binding with the device of its CUDA tensor arguments current
+    (the library launches on the current device and picks per-device state
+    from it), after checking that all of them live on that one device."""
+    import functools
+
+    @functools.wraps(fn)
+    def wrapper(*args, **kwargs):
+        devs = {a.device for a in list(args) + list(kwargs.values())
+                if isinstance(a, torch.Tensor) and a.is_cuda}
+        if len(devs) > 1:
+            raise ValueError(f"{fn.__name__}: CUDA tensors on several devices {sorted(map(str, devs))}")
+        if not devs:
+            return fn(*args, **kwargs)
+        with torch.cuda.device(devs.pop()):
+            return fn(*args, **kwargs)
+    return wrapper
+
+
 def version() -> int:
     return int(_version())
 
 
+@_device_call
 def slot_mapping(block_tables: torch.Tensor, positions: torch.Tensor, block_size: int,
                  num_blocks: int, out: Optional[torch.Tensor] = None) -> torch.Tensor:
     """int64 slot of each sequence's token at ``positions`` (-1 for padding)."""
@@ -172,6 +192,7 @@ def slot_mapping(block_tables: torch.Tensor, positions: torch.Tensor, block_size
     return out
 
 
+@_device_call
 def paged_kv_write(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
                    k_cache: torch.Tensor, v_cache: torch.Tensor) -> None:
     """k_cache.view(-1, H_kv, D)[slot_mapping[i]] = k[i] (same for v), in place."""
@@ -190,6 +211,7 @@ def paged_kv_write(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
                      H, D, _dtype_code(k_cache), _stream(k_cache.device)), "pkv_kv_write")
 
 
+@_device_call
 def paged_kv_append(k: torch.Tensor, v: torch.Tensor, block_tables: torch.Tensor,
                     positions: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                     slot_mapping_out: Optional[torch.Tensor] = None) -> None:
@@ -223,6 +245,7 @@ def selftest_wait_timeout(limit_cycles: int, device=None) -> None:
     _check(_selftest_timeout(int(limit_cycles), _stream(dev)), "pkv_selftest_wait_timeout")
 
 
+@_device_call
 def kv_block_copy(k_cache: torch.Tensor, v_cache: torch.Tensor,
                   src_dst_pairs: torch.Tensor) -> None:
     """Copy-on-write block copy: block dst <- block src for each row of pairs."""
@@ -311,6 +334,7 @@ def attention_launch_count(num_seqs, num_q_heads, num_kv_heads, head_dim, block_
     return int(out.value)
 
 
+@_device_call
 def paged_attention_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                            block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
                            out: Optional[torch.Tensor] = None,
@@ -353,6 +377,7 @@ def paged_attention_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
     return out
 
 
+@_device_call
 def paged_attention_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor,
                                    v_cache: torch.Tensor, block_tables: torch.Tensor,
                                    context_lens: torch.Tensor, scale: float,
@@ -430,6 +455,7 @@ def _need_pool(t: torch.Tensor, name: str) -> None:
         raise TypeError(f"{name} must hold one-byte codes (uint8 / int8 / float8_e4m3fn)")
 
 
+@_device_call
 def paged_kv_append_quant(k: torch.Tensor, v: torch.Tensor, block_tables: torch.Tensor,
                           positions: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                           quant: KvQuant,
@@ -456,6 +482,7 @@ def paged_kv_append_quant(k: torch.Tensor, v: torch.Tensor, block_tables: torch.
            "pkv_kv_append_quant")
 
 
+@_device_call
 def kv_block_copy_quant(k_cache: torch.Tensor, v_cache: torch.Tensor,
                         src_dst_pairs: torch.Tensor, quant: KvQuant) -> None:
     """Copy-on-write block copy of a quantized pool (codes and, for INT8, scales)."""
@@ -480,6 +507,7 @@ def attention_quant_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_di
     return int(out.value)
 
 
+@_device_call
 def paged_attention_decode_quant(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                                  block_tables: torch.Tensor, context_lens: torch.Tensor,
                                  scale: float, quant: KvQuant,
@@ -522,6 +550,7 @@ def paged_attention_decode_quant(q: torch.Tensor, k_cache: torch.Tensor, v_cache
 # multi-query (prefill) attention over the paged cache
 # ---------------------------------------------------------------------------
 
+@_device_call
 def paged_kv_append_varlen(k: torch.Tensor, v: torch.Tensor, cu_seqlens: torch.Tensor,
                            context_lens: torch.Tensor, block_tables: torch.Tensor,
                            k_cache: torch.Tensor, v_cache: torch.Tensor,
@@ -552,6 +581,7 @@ def paged_kv_append_varlen(k: torch.Tensor, v: torch.Tensor, cu_seqlens: torch.T
                           _stream(k.device)), "pkv_kv_append_varlen")
 
 
+@_device_call
 def paged_attention_prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                             block_tables: torch.Tensor, cu_seqlens: torch.Tensor,
                             context_lens: torch.Tensor, scale: float, max_query_len: int,

@@ -219,6 +219,23 @@ def build(name: str, seed: int = 0, pad="garbage", block_size: Optional[int] = N
 CONFIG_NAMES = ("tiny", "qwen3_0_6b", "mistral_7b", "llama31_70b", "prefix_cow")
 
 
+def swap_plan(w, seed: int):
+    """Every other sequence of the workload is preempted by swap: its blocks
+    (K and V) go to a host pool in a seeded shuffled order, and come back into
+    a seeded permutation of the same GPU blocks (scattered placement)."""
+    import numpy as np
+    rng = np.random.default_rng(seed + 101)
+    blocks = []
+    for s in range(1, w.num_seqs, 2):
+        n = -(-int(w.context_lens[s]) // w.block_size)
+        blocks.extend(int(b) for b in w.block_tables[s, :n])
+    blocks = np.array(blocks, np.int64)
+    host = rng.permutation(len(blocks)).astype(np.int64)
+    out_pairs = np.stack([blocks, host], 1)
+    in_pairs = np.stack([host, rng.permutation(blocks)], 1)
+    return out_pairs, in_pairs
+
+
 # --------------------------------------------------------------------------
 # tensors
 # --------------------------------------------------------------------------

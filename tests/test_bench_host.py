@@ -98,7 +98,8 @@ def test_reference_arm_decode(capsys):
     d = _reference_line(["--impl", "reference", "--workload", "tiny", "--steps", "1",
                          "--warmup", "1", "--cpu-budget", "1"], capsys)
     assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["value"] > 0
-    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
+    assert d["cpu_baseline"]["kind"] == "oracle"
+    assert 1 <= d["cpu_baseline"]["cores"] <= bench._host_cores()
     assert d["e2e"]["value"] == d["value"] and d["gpu_launches"] == 0
 
 
@@ -109,3 +110,53 @@ def test_reference_arm_prefill_units(capsys, name, unit):
     d = _reference_line(["--impl", "reference", "--op", "prefill", "--workload", name,
                          "--steps", "1", "--warmup", "1", "--cpu-budget", "1"], capsys)
     assert d["unit"] == unit and d["cpu_baseline"]["unit"] == unit and d["value"] > 0
+
+
+def test_deal_whole_sequences_or_items():
+    items = [(s, j) for s in range(8) for j in range(2)]
+    shares = bench._deal(items, 4, 8)              # 2 sequences per process: whole sequences
+    assert sorted(it for sh in shares for it in sh) == items
+    assert all(len({s for s, _ in sh}) == 2 and len(sh) == 4 for sh in shares)
+    shares = bench._deal(items, 6, 8)              # fewer: items round robin
+    assert sorted(it for sh in shares for it in sh) == items
+
+
+@pytest.mark.parametrize("name", ["tiny", "prefix_cow"])
+def test_accuracy_check_plumbing(name):
+    """The bench's accuracy check on the CPU: the snapshot of the sampled
+    sequences, the oracle's own step on it, and the comparison.  The stand-in
+    "GPU output" is the oracle's result on the full workload, so the error is
+    0; a perturbed copy is reported out of tolerance."""
+    import numpy as np
+    import torch
+    import oracle
+    from paged_kv_cache_115_gb300 import workloads as wl
+    from tests._helpers import storage
+    w = wl.build(name)
+    if name == "prefix_cow":                        # keep the CPU work small
+        w = wl.build_prefix_cow(num_parents=4, prefix_len=64, suffix_range=(3, 40))
+    t = wl.materialize(w, canary=False)
+    snap = bench._accuracy_snapshot(w, t, "bf16", None)
+    kc, vc = storage(t["k_cache"]), storage(t["v_cache"])
+    if len(w.copy_pairs):
+        kc, vc = oracle.kv_block_copy(kc, vc, w.copy_pairs)
+    slots = oracle.slot_mapping(w.block_tables, w.positions, w.block_size)
+    kc, vc = oracle.kv_write(kc, vc, storage(t["k_new"]), storage(t["v_new"]), slots)
+    ref = oracle.paged_attention_decode(storage(t["q"]), kc, vc, w.block_tables, w.context_lens,
+                                        w.scale, w.dtype)
+    td = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    out = torch.from_numpy(ref).to(td)
+    path = bench._save_snapshot(snap, out)
+    try:
+        a = bench._accuracy(path)
+    finally:
+        os.remove(path)
+    # the stand-in output is the reference rounded to the storage type
+    assert a["within_tolerance"] and a["elements"] > 0
+    bad = out.clone()
+    bad[snap["_samples"][0], 0, 0] += 1.0
+    path = bench._save_snapshot(snap, bad)
+    try:
+        assert not bench._accuracy(path)["within_tolerance"]
+    finally:
+        os.remove(path)

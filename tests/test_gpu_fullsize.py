@@ -1,5 +1,5 @@
 """Full-size parity of the rows past the decode step, in the launch plans
-bench.py times: sampled outputs against the oracle computed one by one.
+bench.py times: every output element against the oracle.
 
 * FP8 / INT8 pools at the Mistral-7B-shaped decode size (quantizing append +
   attention, automatic kernel choice);
@@ -36,14 +36,8 @@ def ops():
     return o
 
 
-def _picks(rng, S, H, longest, n=20):
-    p = {(int(rng.integers(S)), int(rng.integers(H))) for _ in range(n)}
-    p |= {(longest, h) for h in range(H)}
-    return sorted(p | {(0, 0), (S - 1, H - 1)})
-
-
 @pytest.mark.parametrize("fmt", ["fp8", "int8"])
-def test_quant_full_size_sampled(ops, fmt):
+def test_quant_full_size(ops, fmt):
     w = wl.build("mistral_7b")
     rng = np.random.default_rng(17)
     nb, K, H, D = w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim
@@ -100,25 +94,20 @@ def test_quant_full_size_sampled(ops, fmt):
         kts_now, vts_now = dkt.cpu().numpy(), dvt.cpu().numpy()
     outf = as_f64(out)
     assert np.all(np.isfinite(outf))
+    # every output row against the oracle over the pool as it now stands
     qn = storage(q)
-    G = w.num_q_heads // H
-    for s, h in _picks(np.random.default_rng(1), w.num_seqs, w.num_q_heads,
-                       int(np.argmax(w.context_lens))):
-        L = int(w.context_lens[s])
-        t = np.arange(L)
-        sl = w.block_tables[s][t // K].astype(np.int64) * K + t % K
-        if fmt == "fp8":
-            Kj = Q.dequantize_rows(kc_now, sl, h // G, "fp8", tensor_scale=0.05)
-            Vj = Q.dequantize_rows(vc_now, sl, h // G, "fp8", tensor_scale=0.07)
-        else:
-            Kj = Q.dequantize_rows(kc_now, sl, h // G, "int8", tok_scales=kts_now)
-            Vj = Q.dequantize_rows(vc_now, sl, h // G, "int8", tok_scales=vts_now)
-        ref = oracle.dense_attention(oracle.decode(qn[s, h], "bf16"), Kj, Vj, w.scale)
-        check_attention(outf[s, h], ref, "bf16", f"{fmt} s={s} h={h}")
+    if fmt == "fp8":
+        ref = Q.paged_attention_decode_quant(qn, kc_now, vc_now, w.block_tables, w.context_lens,
+                                             w.scale, "bf16", "fp8", k_scale=0.05, v_scale=0.07)
+    else:
+        ref = Q.paged_attention_decode_quant(qn, kc_now, vc_now, w.block_tables, w.context_lens,
+                                             w.scale, "bf16", "int8", k_tok_scales=kts_now,
+                                             v_tok_scales=vts_now)
+    check_attention(outf, ref, "bf16", f"{fmt} full size")
 
 
 @pytest.mark.parametrize("name", ["suffix_prefill", "chunked_prefill", "speculative_decode"])
-def test_prefill_full_size_sampled(ops, name):
+def test_prefill_full_size(ops, name):
     w = wl.build_prefill(name)
     K, H, D, H_q = w.block_size, w.num_kv_heads, w.head_dim, w.num_q_heads
     G = H_q // H
@@ -147,25 +136,26 @@ def test_prefill_full_size_sampled(ops, name):
     assert np.array_equal(storage(dk), okc) and np.array_equal(storage(dv), ovc)
     outf = as_f64(out)
     assert np.all(np.isfinite(outf))
-    qn = storage(q)
-    rng = np.random.default_rng(3)
-    picks = {(int(rng.integers(T)), int(rng.integers(H_q))) for _ in range(24)}
-    last_of_longest = int(w.cu_seqlens[int(np.argmax(w.context_lens)) + 1]) - 1
-    picks |= {(last_of_longest, h) for h in range(H_q)} | {(0, 0), (T - 1, H_q - 1)}
-    for t, h in sorted(picks):
-        s, p = int(seq[t]), int(pos[t])
-        r = np.arange(p + 1)
-        sl = w.block_tables[s][r // K].astype(np.int64) * K + r % K
-        Kj = oracle.decode(okc.reshape(-1, H, D)[sl, h // G], "bf16")
-        Vj = oracle.decode(ovc.reshape(-1, H, D)[sl, h // G], "bf16")
-        ref = oracle.dense_attention(oracle.decode(qn[t, h], "bf16"), Kj, Vj, w.scale)
-        check_attention(outf[t, h], ref, "bf16", f"{name} t={t} h={h}")
+    # every output row: per (sequence, KV head) the rows are gathered once and
+    # each query row (new token i, head of the group) sees keys 0 .. its position
+    qn = oracle.decode(storage(q), "bf16")
+    ref = np.zeros_like(outf)
+    for s_ in range(w.num_seqs):
+        L = int(w.context_lens[s_])
+        t0, t1 = int(w.cu_seqlens[s_]), int(w.cu_seqlens[s_ + 1])
+        for j in range(H):
+            Kj = oracle.gather_kv(okc, w.block_tables[s_], L, j, K, "bf16")
+            Vj = oracle.gather_kv(ovc, w.block_tables[s_], L, j, K, "bf16")
+            rows = qn[t0:t1, j * G:(j + 1) * G].reshape(-1, D)
+            lim = np.repeat(pos[t0:t1], G)
+            ref[t0:t1, j * G:(j + 1) * G] = oracle.attention_rows(
+                rows, Kj, Vj, lim, w.scale).reshape(t1 - t0, G, D)
+    check_attention(outf, ref, "bf16", name)
 
 
 def test_swap_full_size(ops):
-    import bench
     w = wl.build("qwen3_0_6b")
-    out_np, in_np = bench.swap_plan(w, 0)
+    out_np, in_np = wl.swap_plan(w, 0)
     n = len(out_np)
     shape = (w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim)
     g = torch.Generator().manual_seed(29)

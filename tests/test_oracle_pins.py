@@ -357,6 +357,58 @@ def pin_scalar_brute_force():
                 assert np.abs(out[s, h] - np.array(ref)).max() < 1e-13, trial
 
 
+def pin_decode_one():
+    """The single-row oracle (the checker of the full-size GPU tests) against
+    (a) a pure-Python scalar brute force that maps query head h to KV head
+    h // G by itself, on tiny problems, and (b) the whole-batch oracle, row by
+    row, over GQA ratios 1, 2, 4, 8 and block sizes 1, 4, 16 with NaN in every
+    slot without history and garbage past each table row."""
+    rng = np.random.default_rng(29)
+    for G in (1, 2, 4, 8):
+        for K in (1, 4, 16):
+            H_kv = 2
+            H_q = H_kv * G
+            D = 3
+            lens = [1, K + 2, 2 * K + 1, 0]
+            q, kc, vc, bt, cl, Kc, Vc = random_paged_problem(rng, len(lens), H_q, H_kv, D, K,
+                                                             lens)
+            scale = float(rng.uniform(0.2, 1.2))
+            whole = oracle.paged_attention_decode(q, kc, vc, bt, cl, scale, "f32")
+            for s, L in enumerate(lens):
+                for h in range(H_q):
+                    one = oracle.paged_attention_decode_one(q, kc, vc, bt, cl, scale, s, h,
+                                                            "f32")
+                    kvh = h // G
+                    keys = [[float(x) for x in Kc[s][t, kvh]] for t in range(L)]
+                    vals = [[float(x) for x in Vc[s][t, kvh]] for t in range(L)]
+                    ref = scalar_attention([float(x) for x in q[s, h]], keys, vals, scale)
+                    assert np.abs(one - np.array(ref)).max() < 1e-13, (G, K, s, h)
+                    assert np.abs(one - whole[s, h]).max() < 1e-13, (G, K, s, h)
+
+
+def pin_attention_rows():
+    """Several query rows at once, each up to its own inclusive key limit:
+    equal to a pure-Python scalar brute force over keys 0 .. limit (tiny
+    sizes), and a negative limit gives zeros."""
+    rng = np.random.default_rng(30)
+    for trial in range(25):
+        L = int(rng.integers(1, 9))
+        D = int(rng.integers(1, 5))
+        R = int(rng.integers(1, 6))
+        Kd = rng.standard_normal((L, D)) * 1.5
+        Vd = rng.standard_normal((L, D))
+        Qd = rng.standard_normal((R, D))
+        lim = rng.integers(-1, L, size=R)
+        scale = float(rng.uniform(0.2, 1.3))
+        got = oracle.attention_rows(Qd, Kd, Vd, lim, scale)
+        for i in range(R):
+            n = int(lim[i]) + 1
+            keys = [[float(x) for x in Kd[t]] for t in range(n)]
+            vals = [[float(x) for x in Vd[t]] for t in range(n)]
+            ref = scalar_attention([float(x) for x in Qd[i]], keys, vals, scale)
+            assert np.abs(got[i] - np.array(ref)).max() < 1e-13, (trial, i)
+
+
 def pin_bf16_path():
     """bf16 storage decodes exactly: the oracle on bf16 bit patterns equals
     the oracle on the same numbers stored as f32."""
@@ -423,6 +475,8 @@ def test_attention_pins(golden):
     pin_closed_forms()
     pin_streaming_matches_two_pass()
     pin_scalar_brute_force()
+    pin_decode_one()
+    pin_attention_rows()
     pin_bf16_path()
 
 
@@ -457,6 +511,22 @@ def _mut_gqa_modulo(q, k_cache, v_cache, bt, cl, scale, dtype):
     return out
 
 
+def _mut_one_gqa_modulo(q, k_cache, v_cache, bt, cl, scale, s, h, dtype):
+    H_kv = k_cache.shape[2]
+    j = h % H_kv                                             # wrong head map
+    Kj = opa.gather_kv(k_cache, bt[s], int(cl[s]), j, k_cache.shape[1], dtype)
+    Vj = opa.gather_kv(v_cache, bt[s], int(cl[s]), j, k_cache.shape[1], dtype)
+    return opa.dense_attention(opa.decode(q[s, h], dtype), Kj, Vj, scale)
+
+
+def _mut_rows_exclusive(Q, K, V, limits, scale):
+    lim = np.asarray(limits, np.int64) - 1                   # exclusive bound
+    return _orig_attention_rows(Q, K, V, lim, scale)
+
+
+_orig_attention_rows = opa.attention_rows
+
+
 def _mut_dense_no_scale(q, K, V, scale):
     if K.shape[0] == 0:
         return np.zeros(V.shape[1])
@@ -483,6 +553,8 @@ def _mut_slot_wrong(bt, positions, K):
 @pytest.mark.parametrize("target,replacement,check", [
     ("gather_kv", _mut_gather_offset_swapped, "attention"),
     ("paged_attention_decode", _mut_gqa_modulo, "gqa"),
+    ("paged_attention_decode_one", _mut_one_gqa_modulo, "one"),
+    ("attention_rows", _mut_rows_exclusive, "rows"),
     ("dense_attention", _mut_dense_no_scale, "attention"),
     ("dense_attention", _mut_dense_kv_swapped, "attention"),
     ("slot_mapping", _mut_slot_wrong, "slot"),
@@ -495,6 +567,10 @@ def test_mutations_are_caught(monkeypatch, golden, target, replacement, check):
             _all_attention_pins(golden)
         elif check == "gqa":
             pin_gqa_equals_mha()
+        elif check == "one":
+            pin_decode_one()
+        elif check == "rows":
+            pin_attention_rows()
         else:
             pin_slot_p3_example(golden("p3_block_table_example.json"))
 

@@ -43,16 +43,20 @@ def test_noalloc_matches_regular_entry_point(ops, case):
                                          w.block_size, w.max_context_len, t["q"].dtype)
     assert need <= ops.NOALLOC_SCRATCH_BYTES
     out_fixed = torch.empty_like(t["q"])
+    # CUDA-core kernel: 4 tokens per partition, so that the tiny sequences
+    # (up to 16 tokens) split and the partials and the reduce go through the
+    # fixed scratch too
+    kw = {} if case == "tc_bf16" else {"kernel": 2, "num_splits": 4}
     g = torch.Generator(device="cpu").manual_seed(5)
     for call in range(2):
         if call == 1:   # new queries: the second call must not depend on the first's scratch
             t["q"].copy_(torch.randn(t["q"].shape, generator=g).to(t["q"].dtype))
         ref = ops.paged_attention_decode(t["q"], t["k_cache"], t["v_cache"], t["block_tables"],
                                          t["context_lens"], w.scale,
-                                         max_context_len=w.max_context_len)
+                                         max_context_len=w.max_context_len, **kw)
         ops.paged_attention_decode_noalloc(t["q"], t["k_cache"], t["v_cache"], t["block_tables"],
                                            t["context_lens"], w.scale, out_fixed,
-                                           w.max_context_len)
+                                           w.max_context_len, **kw)
         torch.cuda.synchronize(dev)
         assert ops.get_device_error(dev) == 0
         check_attention(as_f64(out_fixed), as_f64(ref), w.dtype, f"{case} call {call}")
