@@ -470,6 +470,18 @@ def rank_seed(base_seed: int, rank: int) -> int:
 # ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
+def shares_blocks(w) -> bool:
+    """Whether two sequences of the step read the same physical block."""
+    seen = set()
+    for s in range(w.num_seqs):
+        n = -(-int(w.context_lens[s]) // w.block_size)
+        row = set(int(b) for b in w.block_tables[s, :n])
+        if seen & row:
+            return True
+        seen |= row
+    return False
+
+
 def _pick_samples(w, max_tokens: int = 40000):
     """Sequences for the accuracy check: the longest, the first, the last and
     the middle one, as many as fit in `max_tokens` cached tokens (at least
@@ -589,6 +601,9 @@ class DecodeCase:
         self.slots = torch.empty(w.num_seqs, dtype=torch.int64, device=dev)
         self.has_copy = len(w.copy_pairs) > 0
         self.max_len = max_len = w.max_context_len
+        # shared-prefix groups: on when the tables share blocks (auto) or asked
+        self.share = fmt == "bf16" and (args.share_prefix == "on" or
+                                        (args.share_prefix == "auto" and shares_blocks(w)))
         scales = None
         if fmt == "bf16":
             self.qd = None
@@ -596,7 +611,7 @@ class DecodeCase:
                                                           w.head_dim, w.elem_bytes)
             ws_bytes = ops.attention_workspace_bytes(w.num_seqs, w.num_q_heads, w.num_kv_heads,
                                                      w.head_dim, w.block_size, max_len,
-                                                     t["q"].dtype)
+                                                     t["q"].dtype, share_prefix=self.share)
         else:
             # one-byte pools of seeded random codes (finite e4m3 codes; int8
             # codes with per-slot scales); the bf16 pools are dropped
@@ -639,7 +654,7 @@ class DecodeCase:
         self.dev_stage, self.host_stage = staged_inputs(t, self.names, dev)
         attn_launches = ops.attention_launch_count(w.num_seqs, w.num_q_heads, w.num_kv_heads,
                                                    w.head_dim, w.block_size, max_len,
-                                                   t["q"].dtype)
+                                                   t["q"].dtype, share_prefix=self.share)
         copy_launches = (1 if fmt != "int8" else 2) if self.has_copy else 0
         self.launches_per_step = copy_launches + 1 + attn_launches
         pool_eb = w.elem_bytes if fmt == "bf16" else 1
@@ -660,7 +675,8 @@ class DecodeCase:
         if self.fmt == "bf16":
             ops.paged_attention_decode(t["q"], t["k_cache"], t["v_cache"], t["block_tables"],
                                        t["context_lens"], w.scale, out=self.out,
-                                       max_context_len=self.max_len, workspace=self.workspace)
+                                       max_context_len=self.max_len, workspace=self.workspace,
+                                       share_prefix=self.share)
         else:
             ops.paged_attention_decode_quant(t["q"], t["k_cache"], t["v_cache"],
                                              t["block_tables"], t["context_lens"], w.scale,
@@ -848,6 +864,20 @@ def _e2e_case(case, timing: dict, K: int, use_graph: bool, stream, world: int) -
     return {"ms": e2e_ms, "h2d": h2d, "d2h": d2h}
 
 
+def unique_kv_bytes(w, pool_eb: int) -> int:
+    """K and V bytes of the distinct token slots the step's sequences read
+    (each physical slot once, however many tables point at its block)."""
+    import numpy as np
+    slots = []
+    for s in range(w.num_seqs):
+        L = int(w.context_lens[s])
+        t = np.arange(L, dtype=np.int64)
+        slots.append(w.block_tables[s][t // w.block_size].astype(np.int64) * w.block_size
+                     + t % w.block_size)
+    n = len(np.unique(np.concatenate(slots))) if slots else 0
+    return n * w.num_kv_heads * w.head_dim * 2 * pool_eb
+
+
 def _roofline(case, attn_avg_ms: float, hbm: float, peak_src: str) -> dict:
     w = case.w
     achieved = case.kv_bytes / (attn_avg_ms * 1e-3) / 1e9
@@ -856,9 +886,23 @@ def _roofline(case, attn_avg_ms: float, hbm: float, peak_src: str) -> dict:
                     or traffic.get("block_size") != w.block_size):
         traffic = None                  # the record is for another workload
         traffic_src = "the ncu record is for another workload, pool format or block size"
+    extra = {}
+    if shares_blocks(w):
+        # the logical bytes count a shared block once per table that reads it;
+        # DRAM need deliver each physical slot only once
+        ub = unique_kv_bytes(w, w.elem_bytes if case.fmt == "bf16" else 1)
+        extra = {"unique_bytes_per_launch": ub,
+                 "unique_GBps": ub / (attn_avg_ms * 1e-3) / 1e9,
+                 "unique_frac": ub / (attn_avg_ms * 1e-3) / 1e9 / hbm,
+                 "note": "achieved counts logical bytes (each table's reads); shared blocks can "
+                         "come from L2 or be staged once per group, so achieved may exceed the "
+                         "DRAM peak; unique_* count each physical slot once"}
     return {
+        **extra,
         "bound": "hbm",
-        "kernel": "pkv_attention_decode (attn_tc_kernel, split-K merge fused)",
+        "kernel": ("pkv_attention_decode (share_prefix_kernel + attn_tc_kernel shared-prefix "
+                   "groups + attn_reduce_kernel)" if case.share else
+                   "pkv_attention_decode (attn_tc_kernel + attn_reduce_kernel)"),
         "achieved": achieved,
         "peak": hbm,
         "peak_source": f"{peak_src} hbm_gbs (copy, read+write)",
@@ -946,6 +990,7 @@ def run_gpu(args):
     for r in tm["rows"].values():
         r["frac"] = r["GBps"] / hbm
     cfg = workload_desc(w)
+    cfg["share_prefix"] = head["case"].share
     cfg["l2"] = (f"inputs larger than L2: {kv_bytes / 1e6:.0f} MB of KV read per step "
                  f"vs 129 MB L2; no flush between steps")
     cfg["parallelism"] = f"replicas x{world}" if world > 1 else "single GPU"
@@ -994,7 +1039,7 @@ def run_gpu(args):
             "ms_per_step": ms2, "steps": K,
             "hbm_frac": c2.kv_bytes / (ms2 * 1e-3) / 1e9 / hbm,
             "decode_tokens_per_s_per_layer": world * c2.w.num_seqs / (ms2 * 1e-3),
-            "config": workload_desc(c2.w),
+            "config": dict(workload_desc(c2.w), share_prefix=c2.share),
             "roofline": _roofline(c2, att2, hbm, peak_src),
             "rows": t2["rows"],
             "gpu_launches": c2.launches_per_step * K,
@@ -1591,6 +1636,9 @@ def main(argv=None):
                     help="decode: the decode step (default); swap: block swap GPU <-> host; "
                          "prefill: multi-query attention (workloads suffix_prefill, "
                          "chunked_prefill, speculative_decode)")
+    ap.add_argument("--share-prefix", choices=["auto", "on", "off"], default="auto",
+                    help="decode: shared-prefix groups in the attention call (auto: on when "
+                         "the step's block tables share blocks)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of CPU work for the oracle baseline sample")

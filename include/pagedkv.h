@@ -147,7 +147,24 @@ typedef struct {
   int32_t num_splits;    /* kernel 1: CTAs sharing the token range of one KV-head
                             group (0 = SM count x CTAs per SM).  kernel 2:
                             tokens per partition (0 = automatic).              */
-  int32_t reserved[6];   /* must be zero */
+  int32_t share_prefix;  /* 0 = off.  1 = shared-prefix groups (decode with the
+                            tensor-core kernel on bf16 pools; ignored by the
+                            other plans): consecutive sequences are taken in
+                            aligned groups of m = 16 / G (G = num_q_heads /
+                            num_kv_heads, so G <= 8 gives m >= 2); the
+                            leading tokens whose block-table entries are the
+                            same physical blocks in every member's row
+                            ("推理与 KV Cache 02", 前缀索引与 Block Table: whole
+                            blocks shared through the table) are staged once
+                            per group, one tile serving the query heads of
+                            all members, and each member's remaining tokens
+                            are read on their own; the partial states merge
+                            in the split-K reduce.  Put the sequences that
+                            share blocks (forks of one request, requests of
+                            one prompt) next to each other.  Adds one small
+                            launch that compares the table rows, and at most
+                            1024 sequences go into one partition launch.   */
+  int32_t reserved[5];   /* must be zero */
 } pkv_attention_config;
 
 /*
@@ -162,8 +179,9 @@ PKV_API pkv_status pkv_attention_workspace_bytes(int32_t num_seqs, int32_t num_q
 
 /*
  * Number of kernel launches pkv_attention_decode makes for these sizes
- * (written to *launches): one partition launch per batch of sequences plus
- * one split-K reduce launch per batch when any sequence may be split.
+ * (written to *launches): one partition launch per batch of sequences, one
+ * split-K reduce launch per batch when any sequence may be split, and with
+ * share_prefix one table-comparison launch per batch.
  */
 PKV_API pkv_status pkv_attention_launch_count(int32_t num_seqs, int32_t num_q_heads,
                                               int32_t num_kv_heads, int32_t head_dim,

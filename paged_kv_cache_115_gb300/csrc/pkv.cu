@@ -137,6 +137,7 @@ struct AttnPlan {
   int kind = 0;
   int hpc = 0, groups = 0, n_per_group = 0;  // tensor-core kernel
   int ps = 0;                                // CUDA-core kernel: tokens per partition
+  int share_m = 1;                           // tensor-core kernel: sequences per shared-prefix group
   int pmax = 1;
   int seq_batch = 0;
   size_t ws_bytes = 0;
@@ -167,8 +168,9 @@ pkv_status plan_attention(int S, int H_q, int H_kv, int D, int K, int max_len, i
   pkv_attention_config c = {};
   if (cfg) c = *cfg;
   for (int r : c.reserved) PKV_CHECK(r == 0, PKV_ERR_INVALID_ARGUMENT, "reserved config fields must be 0");
-  PKV_CHECK(c.kernel >= 0 && c.kernel <= 2 && c.num_splits >= 0, PKV_ERR_INVALID_ARGUMENT,
-            "bad attention config");
+  PKV_CHECK(c.kernel >= 0 && c.kernel <= 2 && c.num_splits >= 0 &&
+                (c.share_prefix == 0 || c.share_prefix == 1),
+            PKV_ERR_INVALID_ARGUMENT, "bad attention config");
   const int G = H_q / H_kv;
   const bool tc_ok = tc_shape_ok(G, D, K, num_blocks, dt) && tma_aligned;
   AttnPlan p;
@@ -187,6 +189,13 @@ pkv_status plan_attention(int S, int H_q, int H_kv, int D, int K, int max_len, i
     const int max_chunks = (int)ceil_div(max_len, pkv::kTcChunk);
     p.pmax = std::max(1, std::min(p.n_per_group, max_chunks));
     p.seq_batch = std::min(S, pkv::kTcMaxSeqs);
+    if (c.share_prefix && G <= 8) {
+      // groups of 16 / G sequences fill the kernel's two 8-column blocks; a
+      // sequence's partials are its group's shared unit's, then its own's
+      p.share_m = 16 / G;
+      p.pmax *= 2;
+      p.seq_batch = std::min(S, pkv::kTcMaxShareSeqs);
+    }
   } else {
     PKV_CHECK(simt_shape_ok(G, D), PKV_ERR_UNSUPPORTED,
               "unsupported shape: head_dim must be 32/64/128/256 and G <= 16");
@@ -201,6 +210,7 @@ pkv_status plan_attention(int S, int H_q, int H_kv, int D, int K, int max_len, i
   const size_t sb = (size_t)std::max(p.seq_batch, 1);
   p.ws_bytes = align256(sb * 4) + align256(sb * p.pmax * H_q * sizeof(float2)) +
                align256(sb * p.pmax * H_q * (size_t)D * sizeof(float));
+  if (p.share_m > 1) p.ws_bytes += align256(ceil_div((int64_t)sb, p.share_m) * 4);
   *plan = p;
   return PKV_OK;
 }
@@ -229,9 +239,11 @@ pkv_status plan_attention_quant(int S, int H_q, int H_kv, int D, int K, int max_
               "tensor-core kernel on a one-byte pool needs bf16 queries, head_dim 128, G <= 8, "
               "block_size 8 or a multiple of 16 and 16-byte aligned pools and scales");
     c.kernel = 1;
+    c.share_prefix = 0;   // shared-prefix groups are a bf16-pool mode
     return plan_attention(S, H_q, H_kv, D, K, max_len, num_blocks, PKV_BF16, &c, true, plan);
   }
   c.kernel = 2;
+  c.share_prefix = 0;
   return plan_attention(S, H_q, H_kv, D, K, max_len, 1, q_dt, &c, false, plan);
 }
 
@@ -248,8 +260,16 @@ pkv::Workspace carve_workspace(void* ws, const AttnPlan& p, int H_q, int D) {
   return w;
 }
 
+// Shared-prefix mode: the per-group shared lengths follow the partial outputs.
+int* carve_glen(void* ws, const AttnPlan& p, int H_q, int D) {
+  const size_t sb = (size_t)std::max(p.seq_batch, 1);
+  return reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + align256(sb * 4) +
+                                align256(sb * p.pmax * H_q * sizeof(float2)) +
+                                align256(sb * p.pmax * H_q * (size_t)D * sizeof(float)));
+}
+
 // ---- tensor-core kernel dispatch ------------------------------------------------
-template <int D, int HPC, int CT, bool B8>
+template <int D, int HPC, int CT, bool B8, bool SH = false>
 struct TcInst {
   // stages: as many as fit in ~192 KiB (bf16) / ~203 KiB (one-byte pools)
   // of shared memory, between 2 and 8
@@ -261,17 +281,17 @@ struct TcInst {
   static std::once_flag flags[kMaxDevices];
   static cudaError_t errs[kMaxDevices];
   static pkv_status launch(const pkv::TcParams& prm, int n, int groups, cudaStream_t st, int dev) {
-    auto k = pkv::attn_tc_kernel<D, HPC, NS, CT, B8>;
+    auto k = pkv::attn_tc_kernel<D, HPC, NS, CT, B8, SH>;
     pkv_status s = set_smem_once(k, C::SMEM, flags, errs, dev);
     if (s != PKV_OK) return s;
     PKV_CUDA(launch_pdl(k, dim3(n, groups), dim3(C::THREADS), (size_t)C::SMEM, st, prm));
     return PKV_OK;
   }
 };
-template <int D, int HPC, int CT, bool B8>
-std::once_flag TcInst<D, HPC, CT, B8>::flags[kMaxDevices];
-template <int D, int HPC, int CT, bool B8>
-cudaError_t TcInst<D, HPC, CT, B8>::errs[kMaxDevices];
+template <int D, int HPC, int CT, bool B8, bool SH>
+std::once_flag TcInst<D, HPC, CT, B8, SH>::flags[kMaxDevices];
+template <int D, int HPC, int CT, bool B8, bool SH>
+cudaError_t TcInst<D, HPC, CT, B8, SH>::errs[kMaxDevices];
 
 // ---- multi-query (prefill) kernel dispatch -----------------------------------------
 template <int D, int NW>
@@ -361,6 +381,7 @@ pkv_status plan_prefill(int num_seqs, int num_tokens, int max_query_len, int max
   // up to 8 query rows per KV head: the stream-K decode kernel, queries as the
   // 8 score columns of its tensor-core tiles
   const bool dec_ok = rows <= 8 && num_seqs <= pkv::kTcMaxSeqs &&
+                      (int64_t)num_tokens * H_q < (int64_t(1) << 31) &&
                       tc_shape_ok((int)std::max<int64_t>(rows, 1), D, K, num_blocks, dtype);
   PKV_CHECK(cfg.kernel != 3 || (dec_ok && cfg.num_splits == 0), PKV_ERR_UNSUPPORTED,
             "kernel 3 needs at most 8 query rows per KV head (max_query_len x G), at most "
@@ -421,22 +442,29 @@ pkv_status plan_prefill(int num_seqs, int num_tokens, int max_query_len, int max
   return PKV_OK;
 }
 
-template <int D, int CT, bool B8>
+template <int D, int CT, bool B8, bool SH = false>
 pkv_status launch_tc_hpc(int hpc, const pkv::TcParams& prm, int n, int groups, cudaStream_t st,
                          int dev) {
   switch (hpc) {
-    case 8: return TcInst<D, 8, CT, B8>::launch(prm, n, groups, st, dev);
-    case 4: return TcInst<D, 4, CT, B8>::launch(prm, n, groups, st, dev);
-    case 2: return TcInst<D, 2, CT, B8>::launch(prm, n, groups, st, dev);
-    default: return TcInst<D, 1, CT, B8>::launch(prm, n, groups, st, dev);
+    case 8: return TcInst<D, 8, CT, B8, SH>::launch(prm, n, groups, st, dev);
+    case 4: return TcInst<D, 4, CT, B8, SH>::launch(prm, n, groups, st, dev);
+    case 2: return TcInst<D, 2, CT, B8, SH>::launch(prm, n, groups, st, dev);
+    default: return TcInst<D, 1, CT, B8, SH>::launch(prm, n, groups, st, dev);
   }
 }
 
 // 8-token blocks take the kernel's B8 layout; block sizes that are multiples
-// of 16 the plain one (tensor maps from encode_pool_map_heads for both)
+// of 16 the plain one (tensor maps from encode_pool_map_heads for both).
+// Shared-prefix groups (prm.share_m > 1) exist for bf16 pools only.
 template <int D, int CT>
 pkv_status launch_tc_d(int hpc, int block_size, const pkv::TcParams& prm, int n, int groups,
                        cudaStream_t st, int dev) {
+  if constexpr (CT == 0) {
+    if (prm.share_m > 1)
+      return block_size < pkv::kTile
+                 ? launch_tc_hpc<D, CT, true, true>(hpc, prm, n, groups, st, dev)
+                 : launch_tc_hpc<D, CT, false, true>(hpc, prm, n, groups, st, dev);
+  }
   return block_size < pkv::kTile ? launch_tc_hpc<D, CT, true>(hpc, prm, n, groups, st, dev)
                                  : launch_tc_hpc<D, CT, false>(hpc, prm, n, groups, st, dev);
 }
@@ -961,7 +989,7 @@ pkv_status pkv_attention_launch_count(int32_t num_seqs, int32_t num_q_heads,
                                  max_context_len, 1, dtype, config, true, &plan);
   if (st != PKV_OK) return st;
   const int batches = num_seqs == 0 ? 0 : (int)ceil_div(num_seqs, plan.seq_batch);
-  *launches = batches * (plan.pmax > 1 ? 2 : 1);
+  *launches = batches * ((plan.pmax > 1 ? 2 : 1) + (plan.share_m > 1 ? 1 : 0));
   return PKV_OK;
 }
 
@@ -1046,6 +1074,18 @@ pkv_status attention_impl(const void* q, const void* k_cache, const void* v_cach
       prm.G = H_q / H_kv;
       prm.block_size = block_size;
       prm.scale_log2 = sl;
+      prm.share_m = plan.share_m;
+      prm.glen = nullptr;
+      if (plan.share_m > 1) {
+        // the groups' shared lengths, from the table rows
+        int* glen = carve_glen(workspace, plan, H_q, D);
+        const int ngroups = (int)ceil_div(S, plan.share_m);
+        PKV_CUDA(launch_pdl(pkv::share_prefix_kernel,
+                            dim3((unsigned)ceil_div(ngroups, pkv::kShareWarps)),
+                            dim3(pkv::kShareWarps * 32), 0, strm, btb, max_blocks_per_seq, lb,
+                            max_context_len, S, block_size, plan.share_m, glen));
+        prm.glen = glen;
+      }
       if (quant == nullptr) {
         st = D == 64 ? launch_tc_d<64, 0>(plan.hpc, block_size, prm, plan.n_per_group, plan.groups,
                                           strm, dev)
@@ -1234,6 +1274,7 @@ pkv_status pkv_attention_prefill(const void* q, const void* k_cache, const void*
     // several query rows per sequence through the stream-K decode kernel
     pkv::TcParams tp;
     memset(&tp, 0, sizeof(tp));
+    tp.share_m = 1;
     st = encode_pool_map_heads(&tp.tmap_k, k_cache, num_blocks, block_size, num_kv_heads,
                                head_dim, plan.ap.hpc, false);
     if (st != PKV_OK) return st;

@@ -36,6 +36,9 @@ namespace pkv {
 constexpr int kTile = 16;          // token rows per TMA box and per mma tile
 constexpr int kTcChunk = kTile;    // chunk of the bf16 kernel
 constexpr int kTcMaxSeqs = 2048;
+// shared-prefix mode: sequences per launch, so that the units (at most
+// 3/2 of them with groups of two or more) fit the kTcMaxSeqs + 1 chunk starts
+constexpr int kTcMaxShareSeqs = 1024;
 constexpr int kBoxBytes = kTile * 128;
 
 // tokens per stream-K chunk for a pool format (0 bf16, 1 FP8, 2 INT8)
@@ -67,6 +70,12 @@ struct TcParams {
   // n * G <= 8.  Outputs and partials are indexed by query row.  nullptr:
   // one query per sequence, row s (decode).
   const int32_t* cu_seqlens;
+  // shared-prefix groups (bf16 decode, kernel instantiated with SH): share_m
+  // consecutive sequences form a group; glen[g] = tokens at the start of
+  // every member's context that sit in the same physical blocks (a multiple
+  // of 16, written by share_prefix_kernel).  share_m = 1 otherwise.
+  int share_m;
+  const int* glen;
 };
 
 // Pool formats of the kernel: CT 0 = bf16, 1 = FP8 e4m3 (per-tensor scale),
@@ -175,11 +184,54 @@ __host__ __device__ __forceinline__ int seq_of_chunk(const int* cstart, int S, i
   return lo;
 }
 
-template <int D, int HPC, int NS, int CT = 0, bool B8 = false>
+// ---------------------------------------------------------------------------
+// Units of a launch: the stream-K chunks run over units, not sequences.
+// Plain mode (m = 1): unit u is sequence u.  Shared-prefix mode (m >= 2):
+// sequences are taken in aligned groups of m consecutive ones; group g owns
+// units g (m + 1) .. g (m + 1) + m: first its shared unit (the first glen[g]
+// tokens, which sit in the same physical blocks in every member's table, so
+// that one staged tile serves the query columns of all members at once),
+// then one private unit per member s (tokens glen[g] .. L_s).  A unit without
+// tokens (or past the last sequence) has no chunks.  A sequence's partial
+// states are those of its group's shared unit, then those of its private
+// unit, one per CTA that holds chunks of the unit.
+// ---------------------------------------------------------------------------
+__host__ __device__ __forceinline__ int tc_num_units(int S, int m) {
+  return m == 1 ? S : ((S + m - 1) / m) * (m + 1);
+}
+__host__ __device__ __forceinline__ int tc_shared_unit(int s, int m) { return (s / m) * (m + 1); }
+__host__ __device__ __forceinline__ int tc_private_unit(int s, int m) {
+  return m == 1 ? s : (s / m) * (m + 1) + s % m + 1;
+}
+// CTAs holding chunks of unit u (0 for a unit without chunks)
+__host__ __device__ __forceinline__ int tc_unit_parts(const int* cstart, int u, long long T,
+                                                      int n) {
+  const int a = cstart[u], b = cstart[u + 1];
+  return a < b ? cta_of_chunk(b - 1, T, n) - cta_of_chunk(a, T, n) + 1 : 0;
+}
+// Partial states of sequence s, and the slot CTA `cta` writes for it from
+// unit u (one of s's units, holding chunks in that CTA).
+__host__ __device__ __forceinline__ int tc_seq_parts(const int* cstart, int s, int m, long long T,
+                                                     int n) {
+  const int pu = tc_unit_parts(cstart, tc_private_unit(s, m), T, n);
+  return m == 1 ? pu : pu + tc_unit_parts(cstart, tc_shared_unit(s, m), T, n);
+}
+__host__ __device__ __forceinline__ int tc_part_slot(const int* cstart, int s, int u, int m,
+                                                     int cta, long long T, int n) {
+  const int base = (m > 1 && u != tc_shared_unit(s, m))
+                       ? tc_unit_parts(cstart, tc_shared_unit(s, m), T, n) : 0;
+  return base + cta - cta_of_chunk(cstart[u], T, n);
+}
+
+template <int D, int HPC, int NS, int CT = 0, bool B8 = false, bool SH = false>
 __global__ void __launch_bounds__(TcCfg<D, HPC, NS, CT, B8>::THREADS, 1)
 attn_tc_kernel(const __grid_constant__ TcParams p) {
   using C = TcCfg<D, HPC, NS, CT, B8>;
   constexpr int TL = C::TL, CH = C::CH;
+  // 8-column blocks of the score tile: two in shared-prefix mode (the query
+  // heads of a group's members side by side), one otherwise
+  constexpr int NB = SH ? 2 : 1;
+  static_assert(!SH || CT == 0, "shared-prefix groups need bf16 pools");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -192,18 +244,49 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
   const int S = p.num_seqs;
   const int K = p.block_size;
   const int row_tokens = p.max_blocks_per_seq * K;
-  // chunks of sequence s (none for a sequence without query rows)
-  auto nchunks = [&](int s) -> int {
-    const int L = effective_len(p.context_lens[s], p.max_len, row_tokens);
+  const int M = SH ? p.share_m : 1;
+  const int NU = SH ? tc_num_units(S, M) : S;
+  auto seq_len = [&](int s) -> int {
+    return effective_len(p.context_lens[s], p.max_len, row_tokens);
+  };
+  // unit u: first sequence s0 (its table row and first query row), sequences
+  // it serves (0: none), tokens [t0, end) of the sequence
+  auto unit = [&](int u, int& s0, int& rows, int& t0, int& end) {
+    if constexpr (!SH) {
+      s0 = u;
+      rows = 1;
+      t0 = 0;
+      end = seq_len(u);
+    } else {
+      const int g = u / (M + 1), k = u - g * (M + 1);
+      const int lg = p.glen[g];
+      if (k == 0) {
+        s0 = g * M;
+        rows = min(M, S - s0);
+        t0 = 0;
+        end = lg;
+      } else {
+        s0 = g * M + k - 1;
+        rows = s0 < S ? 1 : 0;
+        t0 = lg;
+        end = rows ? max(seq_len(s0), lg) : lg;
+      }
+    }
+  };
+  // chunks of unit u (none for a sequence without query rows)
+  auto nchunks = [&](int u) -> int {
+    int s0, rows, t0, end;
+    unit(u, s0, rows, t0, end);
+    if (rows == 0) return 0;
     if (p.cu_seqlens != nullptr) {
-      const int nq = p.cu_seqlens[s + 1] - p.cu_seqlens[s];
-      if (nq < 0 || nq > L) {
+      const int nq = p.cu_seqlens[s0 + 1] - p.cu_seqlens[s0];
+      if (nq < 0 || nq > end) {
         record_error(PKV_DEVERR_CONTEXT_LEN);
         return 0;
       }
       if (nq == 0) return 0;
     }
-    return (L + CH - 1) / CH;
+    return (end - t0 + CH - 1) / CH;
   };
 
   if (tid == 0) {
@@ -215,12 +298,12 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
   }
   pdl_wait_primary();
 
-  // ---- chunk prefix sums over the batch: cstart[s] = sum_{s'<s} ceil(L/CH)
+  // ---- chunk prefix sums over the units: cstart[u] = sum_{u'<u} chunks(u')
   {
-    const int per = (S + C::THREADS - 1) / C::THREADS;
-    const int a = min(S, tid * per), b = min(S, a + per);
+    const int per = (NU + C::THREADS - 1) / C::THREADS;
+    const int a = min(NU, tid * per), b = min(NU, a + per);
     int local = 0;
-    for (int s = a; s < b; ++s) local += nchunks(s);
+    for (int u = a; u < b; ++u) local += nchunks(u);
     int incl = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -240,19 +323,19 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
     }
     __syncthreads();
     int run = (warp ? s_wsum[warp - 1] : 0) + incl - local;
-    for (int s = a; s < b; ++s) {
-      cstart[s] = run;
-      run += nchunks(s);
+    for (int u = a; u < b; ++u) {
+      cstart[u] = run;
+      run += nchunks(u);
     }
-    if (tid == C::THREADS - 1) cstart[S] = run;
+    if (tid == C::THREADS - 1) cstart[NU] = run;
     __syncthreads();
   }
   pdl_launch_dependents();
 
-  const long long T = cstart[S];
+  const long long T = cstart[NU];
   // Split over at most T CTAs so that every working CTA owns >= 1 chunk and a
-  // sequence's partial index (CTA - first CTA of the sequence) stays below
-  // min(n, chunks of the sequence) <= Pmax.  CTAs past n only do bookkeeping.
+  // unit's partial index (CTA - first CTA of the unit) stays below min(n,
+  // chunks of the unit).  CTAs past n only do bookkeeping.
   const int n = (int)(T < (long long)gridDim.x ? (T > 0 ? T : 1) : (long long)gridDim.x);
   const int cta = blockIdx.x, group = blockIdx.y;
   const int head0 = group * HPC;
@@ -262,8 +345,10 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
 
   // ---- bookkeeping: partial counts and zero outputs of empty sequences
   for (int s = tid; s < S; s += C::THREADS) {
-    const int a = cstart[s], b = cstart[s + 1];
-    if (a == b) {
+    const int up = tc_private_unit(s, M);
+    const int a = cstart[up], b = cstart[up + 1];
+    const int np = SH ? tc_seq_parts(cstart, s, M, T, n) : (a < b ? 1 : 0);
+    if (np == 0) {
       // empty context: zero output (decode); a sequence without query rows
       // has no output
       const int owner = a < T ? cta_of_chunk(a, T, n) : n - 1;
@@ -273,13 +358,15 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
         for (int i = 0; i < HPC * G * D; ++i) o[i] = __float2bfloat16_rn(0.f);
       }
     } else if (group == 0) {
-      const int first = cta_of_chunk(a, T, n);
-      if (first == cta) {
-        const int np = cta_of_chunk(b - 1, T, n) - first + 1;
+      // written by the first CTA of the sequence's private unit (of its
+      // group's shared unit when the private one is empty)
+      const int uo = a < b ? up : tc_shared_unit(s, M);
+      if (cta_of_chunk(cstart[uo], T, n) == cta) {
+        const int parts = tc_seq_parts(cstart, s, M, T, n);
         if (p.cu_seqlens == nullptr) {
-          p.ws.nparts[s] = np;
+          p.ws.nparts[s] = parts;
         } else {
-          for (int r = p.cu_seqlens[s]; r < p.cu_seqlens[s + 1]; ++r) p.ws.nparts[r] = np;
+          for (int r = p.cu_seqlens[s]; r < p.cu_seqlens[s + 1]; ++r) p.ws.nparts[r] = parts;
         }
       }
     }
@@ -298,7 +385,7 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
     bool ok = true;
     for (int c0 = cb; c0 < ce && ok; c0 += 32) {
       // pool rows of the tiles of the next 32 chunks, one chunk per lane; a
-      // tile past the sequence end (or of an out-of-range block) gets a row
+      // tile past the unit's end (or of an out-of-range block) gets a row
       // that is wholly out of bounds, which TMA fills with zeros.  With
       // 8-token blocks a tile spans two blocks (u = 0, 1).
       int row[TL][2];
@@ -306,21 +393,22 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
       for (int t = 0; t < TL; ++t) row[t][0] = row[t][1] = -2 * kTile;
       const int c = c0 + lane;
       if (c < ce) {
-        const int s = seq_of_chunk(cstart, S, c);
-        const int L = (TL > 1 || sbl) ? effective_len(p.context_lens[s], p.max_len, row_tokens)
-                                      : 1 << 30;
+        const int u = seq_of_chunk(cstart, NU, c);
+        int s0, rows, t0, end;
+        unit(u, s0, rows, t0, end);
+        const int L = (TL > 1 || sbl || SH) ? end : 1 << 30;
 #pragma unroll
         for (int t = 0; t < TL; ++t) {
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int tok = (c - cstart[s]) * CH + t * kTile + u * K;
-            if (u <= sbl && tok < L) {
+          for (int uu = 0; uu < 2; ++uu) {
+            const int tok = t0 + (c - cstart[u]) * CH + t * kTile + uu * K;
+            if (uu <= sbl && tok < L) {
               const int lb = tok / K;
-              const long long phys = p.block_tables[(int64_t)s * p.max_blocks_per_seq + lb];
+              const long long phys = p.block_tables[(int64_t)s0 * p.max_blocks_per_seq + lb];
               if (phys < 0 || phys >= p.num_blocks) {
                 record_error(PKV_DEVERR_BLOCK_ID);
               } else {
-                row[t][u] = (int)(phys * K + (tok - lb * K));
+                row[t][uu] = (int)(phys * K + (tok - lb * K));
               }
             }
           }
@@ -401,46 +489,61 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
   const int g = lane >> 2, tq = lane & 3;
   const float sl = p.scale_log2;
 
-  uint32_t qf[D / 16][2];
-  float o[D / 16][4];
+  uint32_t qf[NB][D / 16][2];
+  float o[NB][D / 16][4];
   float slc0 = sl, slc1 = sl;   // per score column (one-byte pools: q's 2^e folded in)
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  float m0[NB], m1[NB], l0[NB], l1[NB];
   // INT8 pools: V enters the tensor core as 1152 + code (the exact f16 the
   // byte permute makes, without the subtraction); vw = sum of weight x V
   // scale per column, so that 1152 vw is taken off o at the partition end
   float vw0 = 0.f, vw1 = 0.f;
-  int s = seq_of_chunk(cstart, S, cb);
-  int len_s = 0;
-  // this thread's score columns 2tq and 2tq+1: their query rows (-1: padding
-  // column) and last visible key positions
-  int64_t rowA = -1, rowB = -1;
-  int limA = 0, limB = 0;
+  int u = seq_of_chunk(cstart, NU, cb);
+  int ut0 = 0, uend = 0, ulim = 0;   // the unit's tokens [ut0, uend); min column limit
+  int nbv = 1;                       // column blocks holding valid columns
+  // this thread's score columns 8 nb + 2tq and 8 nb + 2tq + 1: their query
+  // rows (-1: padding column) and last visible key positions
+  int rowA[NB], rowB[NB];
+  int limA[NB], limB[NB];
   int k = 0;
   for (int c = cb; c < ce; ++c, ++k) {
-    while (c >= cstart[s + 1]) ++s;
-    const int a = cstart[s], b = cstart[s + 1];
+    while (c >= cstart[u + 1]) ++u;
+    const int a = cstart[u], b = cstart[u + 1];
     if (c == cb || c == a) {
-      // ---- new partition: load the q-group as the B fragments of Q^T
-      len_s = effective_len(p.context_lens[s], p.max_len, row_tokens);
-      const int qr0 = p.cu_seqlens ? p.cu_seqlens[s] : s;           // first query row
-      const int nq = p.cu_seqlens ? p.cu_seqlens[s + 1] - qr0 : 1;  // query rows
-      const int ncol = nq * G;                                     // valid score columns
-      const int cA = 2 * tq, cB = 2 * tq + 1;
-      rowA = cA < ncol ? (int64_t)(qr0 + cA / G) * H_q + j * G + cA % G : -1;
-      rowB = cB < ncol ? (int64_t)(qr0 + cB / G) * H_q + j * G + cB % G : -1;
-      limA = cA < ncol ? len_s - nq + cA / G : len_s - 1;
-      limB = cB < ncol ? len_s - nq + cB / G : len_s - 1;
-      // this lane's B-fragment column g
-      const __nv_bfloat16* qrow =
-          p.q + ((int64_t)(qr0 + (g < ncol ? g / G : 0)) * H_q + j * G + g % G) * D;
+      // ---- new partition: load the q-group(s) as the B fragments of Q^T
+      int s0, rows;
+      unit(u, s0, rows, ut0, uend);
+      const int qr0 = p.cu_seqlens ? p.cu_seqlens[s0] : s0;           // first query row
+      const int nq = p.cu_seqlens ? p.cu_seqlens[s0 + 1] - qr0 : rows; // query rows
+      const int ncol = nq * G;                                        // valid score columns
+      nbv = ncol > 8 ? NB : 1;
+      ulim = uend - 1;
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) {
+        const int cA = 8 * nb + 2 * tq, cB = cA + 1;
+        rowA[nb] = cA < ncol ? (qr0 + cA / G) * H_q + j * G + cA % G : -1;
+        rowB[nb] = cB < ncol ? (qr0 + cB / G) * H_q + j * G + cB % G : -1;
+        // several query tokens of one sequence: token i sees keys up to
+        // len - n + i; otherwise every column sees the unit's keys
+        limA[nb] = cA < ncol && p.cu_seqlens ? uend - nq + cA / G : uend - 1;
+        limB[nb] = cB < ncol && p.cu_seqlens ? uend - nq + cB / G : uend - 1;
+        ulim = min(ulim, min(limA[nb], limB[nb]));
+      }
       if constexpr (CT == 0) {
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          if (g < ncol) {
-            qf[ks][0] = __ldg(reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 2 * tq));
-            qf[ks][1] = __ldg(reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 8 + 2 * tq));
-          } else {
-            qf[ks][0] = qf[ks][1] = 0u;
+        for (int nb = 0; nb < NB; ++nb) {
+          // this lane's B-fragment column 8 nb + g
+          const int cq = 8 * nb + g;
+          const __nv_bfloat16* qrow =
+              p.q + ((int64_t)(qr0 + (cq < ncol ? cq / G : 0)) * H_q + j * G + cq % G) * D;
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            if (cq < ncol) {
+              qf[nb][ks][0] = __ldg(reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 2 * tq));
+              qf[nb][ks][1] =
+                  __ldg(reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 8 + 2 * tq));
+            } else {
+              qf[nb][ks][0] = qf[nb][ks][1] = 0u;
+            }
           }
         }
       } else {
@@ -450,6 +553,8 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
         // Each head is scaled by a power of two 2^-e that puts its largest
         // |q| in [2^14, 2^15): exact, and far inside the f16 range; the
         // scores are multiplied back by 2^e.
+        const __nv_bfloat16* qrow =
+            p.q + ((int64_t)(qr0 + (g < ncol ? g / G : 0)) * H_q + j * G + g % G) * D;
         float qv[D / 16][4];
         float amax = 0.f;
 #pragma unroll
@@ -471,8 +576,8 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
         const float down = ldexpf(1.f, -eg);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          qf[ks][0] = pack_f16x2(qv[ks][0] * down, qv[ks][1] * down);
-          qf[ks][1] = pack_f16x2(qv[ks][2] * down, qv[ks][3] * down);
+          qf[0][ks][0] = pack_f16x2(qv[ks][0] * down, qv[ks][1] * down);
+          qf[0][ks][1] = pack_f16x2(qv[ks][2] * down, qv[ks][3] * down);
         }
         // score columns of this thread are heads 2tq, 2tq+1 (held by lanes 8tq, 8tq+4)
         const int e0 = __shfl_sync(0xffffffffu, eg, 8 * tq);
@@ -481,12 +586,17 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
         slc1 = ldexpf(sl, e1);
       }
 #pragma unroll
-      for (int mt = 0; mt < D / 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
-      m0 = m1 = -INFINITY;
-      l0 = l1 = 0.f;
+      for (int nb = 0; nb < NB; ++nb) {
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt)
+          o[nb][mt][0] = o[nb][mt][1] = o[nb][mt][2] = o[nb][mt][3] = 0.f;
+        m0[nb] = m1[nb] = -INFINITY;
+        l0[nb] = l1[nb] = 0.f;
+      }
       vw0 = vw1 = 0.f;
     }
-    const int valid = min(CH, len_s - (c - a) * CH);   // tokens of this chunk
+    const int cpos = ut0 + (c - a) * CH;                 // key position of chunk row 0
+    const int valid = min(CH, uend - cpos);             // tokens of this chunk
     const int stage = k % NS;
     if (!mbar_wait_bounded(bar_full + 8 * stage, (k / NS) & 1)) {
       record_error(PKV_DEVERR_TIMEOUT);
@@ -526,10 +636,13 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
       fence_proxy_async_smem();
       __syncwarp();
     }
-    // ---- S^T[16 tok x 8 heads] = K_tile[16 x D] . Q^T[D x 8], per tile
-    float sacc[TL][4];
+    // ---- S^T[16 tok x 8 columns] = K_tile[16 x D] . Q^T[D x 8], per tile and
+    // column block (one K fragment feeds every column block)
+    float sacc[NB][TL][4];
 #pragma unroll
-    for (int t = 0; t < TL; ++t) sacc[t][0] = sacc[t][1] = sacc[t][2] = sacc[t][3] = 0.f;
+    for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+      for (int t = 0; t < TL; ++t) sacc[nb][t][0] = sacc[nb][t][1] = sacc[nb][t][2] = sacc[nb][t][3] = 0.f;
     if constexpr (CT == 0) {
       const int r = (lane & 7) + ((lane >> 3) & 1) * 8;
       const int chs = lane >> 4;
@@ -541,7 +654,9 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
         const uint32_t addr = smem_u32(kt + half * C::HSTR) + C::row_off(r) + ((ch ^ (r & 7)) << 4);
         uint32_t a0, a1, a2, a3;
         ldmatrix_x4(addr, a0, a1, a2, a3);
-        mma_bf16_16816(sacc[0], a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb)
+          if (nb < nbv) mma_bf16_16816(sacc[nb][0], a0, a1, a2, a3, qf[nb][ks][0], qf[nb][ks][1]);
       }
     } else {
       // byte tiles: rows g and g+8 share a swizzle phase; the 16-code chunk
@@ -565,130 +680,136 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
             a1 = s8_pair_to_f16x2(x1, 0x5140);
             a3 = s8_pair_to_f16x2(x1, 0x5342);
           }
-          mma_f16_16816(sacc[t], a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+          mma_f16_16816(sacc[0][t], a0, a1, a2, a3, qf[0][ks][0], qf[0][ks][1]);
         }
       }
     }
-    // ---- online softmax on (tok 16t+g / 16t+g+8) x (head 2tq / 2tq+1)
-    const bool cmask = (c - a) * CH + CH - 1 > min(limA, limB);
-    float x[TL][4];
-    float mx0 = -INFINITY, mx1 = -INFINITY;
+    // ---- online softmax on (tok 16t+g / 16t+g+8) x (column 8nb+2tq / 8nb+2tq+1)
+    const bool cmask = cpos + CH - 1 > ulim;
+    uint32_t pb[NB][TL][2], pc[NB][TL][2];
 #pragma unroll
-    for (int t = 0; t < TL; ++t) {
-      x[t][0] = sacc[t][0] * slc0 * ksr[t][0];
-      x[t][1] = sacc[t][1] * slc1 * ksr[t][0];
-      x[t][2] = sacc[t][2] * slc0 * ksr[t][1];
-      x[t][3] = sacc[t][3] * slc1 * ksr[t][1];
-      // causal limit of each score column (decode: the sequence end); a
-      // chunk wholly below both limits needs no mask
-      if (cmask) {
-        const int kp = (c - a) * CH + t * kTile + g;   // key position of row g
-        if (kp > limA) x[t][0] = -INFINITY;
-        if (kp > limB) x[t][1] = -INFINITY;
-        if (kp + 8 > limA) x[t][2] = -INFINITY;
-        if (kp + 8 > limB) x[t][3] = -INFINITY;
-      }
-      mx0 = fmaxf(mx0, fmaxf(x[t][0], x[t][2]));
-      mx1 = fmaxf(mx1, fmaxf(x[t][1], x[t][3]));
-    }
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-    }
-    float pr[TL][4];
-    float ps0 = 0.f, ps1 = 0.f;
-    if constexpr (CT == 0) {
-      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-      // a column may have seen no visible key yet (several query rows): keep
-      // its state (-inf, 0, 0) instead of forming -inf - -inf
-      const float mu0 = mn0 == -INFINITY ? 0.f : mn0, mu1 = mn1 == -INFINITY ? 0.f : mn1;
-      const float al0 = exp2f(m0 - mu0), al1 = exp2f(m1 - mu1);
+    for (int nb = 0; nb < NB; ++nb) {
+      if (nb >= nbv) continue;
+      float x[TL][4];
+      float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
       for (int t = 0; t < TL; ++t) {
-        pr[t][0] = exp2f(x[t][0] - mu0);
-        pr[t][1] = exp2f(x[t][1] - mu1);
-        pr[t][2] = exp2f(x[t][2] - mu0);
-        pr[t][3] = exp2f(x[t][3] - mu1);
-        ps0 += pr[t][0] + pr[t][2];
-        ps1 += pr[t][1] + pr[t][3];
+        x[t][0] = sacc[nb][t][0] * slc0 * ksr[t][0];
+        x[t][1] = sacc[nb][t][1] * slc1 * ksr[t][0];
+        x[t][2] = sacc[nb][t][2] * slc0 * ksr[t][1];
+        x[t][3] = sacc[nb][t][3] * slc1 * ksr[t][1];
+        // causal limit of each score column (decode: the unit's end); a
+        // chunk wholly below every column's limit needs no mask
+        if (cmask) {
+          const int kp = cpos + t * kTile + g;   // key position of row g
+          if (kp > limA[nb]) x[t][0] = -INFINITY;
+          if (kp > limB[nb]) x[t][1] = -INFINITY;
+          if (kp + 8 > limA[nb]) x[t][2] = -INFINITY;
+          if (kp + 8 > limB[nb]) x[t][3] = -INFINITY;
+        }
+        mx0 = fmaxf(mx0, fmaxf(x[t][0], x[t][2]));
+        mx1 = fmaxf(mx1, fmaxf(x[t][1], x[t][3]));
       }
-      l0 = l0 * al0 + ps0;
-      l1 = l1 * al1 + ps1;
-      m0 = mn0;
-      m1 = mn1;
 #pragma unroll
-      for (int mt = 0; mt < D / 16; ++mt) {
-        o[mt][0] *= al0;
-        o[mt][1] *= al1;
-        o[mt][2] *= al0;
-        o[mt][3] *= al1;
+      for (int off = 4; off < 32; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
       }
-    } else {
-      // one-byte pools (consumer-bound): the exponent base m of a column is
-      // raised only when a score exceeds it by more than 2^kQuantSlack, so
-      // o and l are rescaled rarely; the weights stay below 2^kQuantSlack and
-      // the final o / l is the same softmax.  A column that has seen no
-      // visible key keeps (-inf, 0, 0).
-      const bool need = mx0 > m0 + kQuantSlack || mx1 > m1 + kQuantSlack;
-      if (__any_sync(0xffffffffu, need)) {
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+      float pr[TL][4];
+      float ps0 = 0.f, ps1 = 0.f;
+      if constexpr (CT == 0) {
+        const float mn0 = fmaxf(m0[nb], mx0), mn1 = fmaxf(m1[nb], mx1);
+        // a column may have seen no visible key yet (several query rows): keep
+        // its state (-inf, 0, 0) instead of forming -inf - -inf
         const float mu0 = mn0 == -INFINITY ? 0.f : mn0, mu1 = mn1 == -INFINITY ? 0.f : mn1;
-        const float al0 = exp2f(m0 - mu0), al1 = exp2f(m1 - mu1);
-        l0 *= al0;
-        l1 *= al1;
-        vw0 *= al0;
-        vw1 *= al1;
-        m0 = mn0;
-        m1 = mn1;
+        const float al0 = exp2f(m0[nb] - mu0), al1 = exp2f(m1[nb] - mu1);
+#pragma unroll
+        for (int t = 0; t < TL; ++t) {
+          pr[t][0] = exp2f(x[t][0] - mu0);
+          pr[t][1] = exp2f(x[t][1] - mu1);
+          pr[t][2] = exp2f(x[t][2] - mu0);
+          pr[t][3] = exp2f(x[t][3] - mu1);
+          ps0 += pr[t][0] + pr[t][2];
+          ps1 += pr[t][1] + pr[t][3];
+        }
+        l0[nb] = l0[nb] * al0 + ps0;
+        l1[nb] = l1[nb] * al1 + ps1;
+        m0[nb] = mn0;
+        m1[nb] = mn1;
 #pragma unroll
         for (int mt = 0; mt < D / 16; ++mt) {
-          o[mt][0] *= al0;
-          o[mt][1] *= al1;
-          o[mt][2] *= al0;
-          o[mt][3] *= al1;
+          o[nb][mt][0] *= al0;
+          o[nb][mt][1] *= al1;
+          o[nb][mt][2] *= al0;
+          o[nb][mt][3] *= al1;
         }
+      } else {
+        // one-byte pools (consumer-bound): the exponent base m of a column is
+        // raised only when a score exceeds it by more than 2^kQuantSlack, so
+        // o and l are rescaled rarely; the weights stay below 2^kQuantSlack and
+        // the final o / l is the same softmax.  A column that has seen no
+        // visible key keeps (-inf, 0, 0).
+        const bool need = mx0 > m0[0] + kQuantSlack || mx1 > m1[0] + kQuantSlack;
+        if (__any_sync(0xffffffffu, need)) {
+          const float mn0 = fmaxf(m0[0], mx0), mn1 = fmaxf(m1[0], mx1);
+          const float mu0 = mn0 == -INFINITY ? 0.f : mn0, mu1 = mn1 == -INFINITY ? 0.f : mn1;
+          const float al0 = exp2f(m0[0] - mu0), al1 = exp2f(m1[0] - mu1);
+          l0[0] *= al0;
+          l1[0] *= al1;
+          vw0 *= al0;
+          vw1 *= al1;
+          m0[0] = mn0;
+          m1[0] = mn1;
+#pragma unroll
+          for (int mt = 0; mt < D / 16; ++mt) {
+            o[0][mt][0] *= al0;
+            o[0][mt][1] *= al1;
+            o[0][mt][2] *= al0;
+            o[0][mt][3] *= al1;
+          }
+        }
+        const float mu0 = m0[0] == -INFINITY ? 0.f : m0[0];
+        const float mu1 = m1[0] == -INFINITY ? 0.f : m1[0];
+#pragma unroll
+        for (int t = 0; t < TL; ++t) {
+          pr[t][0] = ex2_approx_ftz(x[t][0] - mu0);
+          pr[t][1] = ex2_approx_ftz(x[t][1] - mu1);
+          pr[t][2] = ex2_approx_ftz(x[t][2] - mu0);
+          pr[t][3] = ex2_approx_ftz(x[t][3] - mu1);
+          ps0 += pr[t][0] + pr[t][2];
+          ps1 += pr[t][1] + pr[t][3];
+        }
+        l0[0] += ps0;
+        l1[0] += ps1;
       }
-      const float mu0 = m0 == -INFINITY ? 0.f : m0, mu1 = m1 == -INFINITY ? 0.f : m1;
+      // P enters the tensor core as a hi + lo pair of 16-bit terms so that the
+      // product carries ~16 significant bits of each weight (one bf16 rounding
+      // of P costs up to 2^-9 relative per weight); one-byte pools: f16 terms
+      // of P times the V scale of its token
 #pragma unroll
       for (int t = 0; t < TL; ++t) {
-        pr[t][0] = ex2_approx_ftz(x[t][0] - mu0);
-        pr[t][1] = ex2_approx_ftz(x[t][1] - mu1);
-        pr[t][2] = ex2_approx_ftz(x[t][2] - mu0);
-        pr[t][3] = ex2_approx_ftz(x[t][3] - mu1);
-        ps0 += pr[t][0] + pr[t][2];
-        ps1 += pr[t][1] + pr[t][3];
-      }
-      l0 += ps0;
-      l1 += ps1;
-    }
-    // P enters the tensor core as a hi + lo pair of 16-bit terms so that the
-    // product carries ~16 significant bits of each weight (one bf16 rounding
-    // of P costs up to 2^-9 relative per weight); one-byte pools: f16 terms
-    // of P times the V scale of its token
-    uint32_t pb[TL][2], pc[TL][2];
-#pragma unroll
-    for (int t = 0; t < TL; ++t) {
-      uint32_t ph01, pl01, ph23, pl23;
-      if constexpr (CT == 0) {
-        split_bf16x2(pr[t][0], pr[t][1], ph01, pl01);
-        split_bf16x2(pr[t][2], pr[t][3], ph23, pl23);
-      } else {
-        const float w0 = pr[t][0] * vsr[t][0], w1 = pr[t][1] * vsr[t][0];
-        const float w2 = pr[t][2] * vsr[t][1], w3 = pr[t][3] * vsr[t][1];
-        if constexpr (CT == 2) {
-          vw0 += w0 + w2;
-          vw1 += w1 + w3;
+        uint32_t ph01, pl01, ph23, pl23;
+        if constexpr (CT == 0) {
+          split_bf16x2(pr[t][0], pr[t][1], ph01, pl01);
+          split_bf16x2(pr[t][2], pr[t][3], ph23, pl23);
+        } else {
+          const float w0 = pr[t][0] * vsr[t][0], w1 = pr[t][1] * vsr[t][0];
+          const float w2 = pr[t][2] * vsr[t][1], w3 = pr[t][3] * vsr[t][1];
+          if constexpr (CT == 2) {
+            vw0 += w0 + w2;
+            vw1 += w1 + w3;
+          }
+          split_f16x2(w0, w1, ph01, pl01);
+          split_f16x2(w2, w3, ph23, pl23);
         }
-        split_f16x2(w0, w1, ph01, pl01);
-        split_f16x2(w2, w3, ph23, pl23);
+        pb[nb][t][0] = movmatrix_trans(ph01);
+        pb[nb][t][1] = movmatrix_trans(ph23);
+        pc[nb][t][0] = movmatrix_trans(pl01);
+        pc[nb][t][1] = movmatrix_trans(pl23);
       }
-      pb[t][0] = movmatrix_trans(ph01);
-      pb[t][1] = movmatrix_trans(ph23);
-      pc[t][0] = movmatrix_trans(pl01);
-      pc[t][1] = movmatrix_trans(pl23);
     }
-    // ---- O^T[D x 8] += V^T[D x 16 tok] . P^T[16 tok x 8], per tile
+    // ---- O^T[D x 8] += V^T[D x 16 tok] . P^T[16 tok x 8], per tile and
+    // column block (one V fragment feeds every column block)
     if constexpr (CT != 0) {
       // byte tiles; the rows of each 16-row m tile are permuted: row g -> d =
       // 16 mt + 2g, row g + 8 -> d = 16 mt + 2g + 1.  ldmatrix.trans over 8
@@ -705,23 +826,23 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
           uint32_t r[4];
           ldmatrix_x4_trans(vt + (((mt + (lm >> 1)) ^ (tok & 7)) << 4), r[0], r[1], r[2], r[3]);
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            // r[2u]: tokens 2tq, 2tq+1 of m tile mt + u; r[2u+1]: tokens + 8
+          for (int uu = 0; uu < 2; ++uu) {
+            // r[2uu]: tokens 2tq, 2tq+1 of m tile mt + uu; r[2uu+1]: tokens + 8
             uint32_t a0, a1, a2, a3;
             if constexpr (CT == 1) {
               // one permute makes both pairs: bytes (0, 2) low, (1, 3) high
-              e4m3x4_to_f16x2x2(__byte_perm(r[2 * u], 0u, 0x3120), a0, a1);
-              e4m3x4_to_f16x2x2(__byte_perm(r[2 * u + 1], 0u, 0x3120), a2, a3);
+              e4m3x4_to_f16x2x2(__byte_perm(r[2 * uu], 0u, 0x3120), a0, a1);
+              e4m3x4_to_f16x2x2(__byte_perm(r[2 * uu + 1], 0u, 0x3120), a2, a3);
             } else {
               // 1152 + code, exact in f16 (the 1152 comes off at the partition end)
-              const uint32_t x0 = r[2 * u] ^ 0x80808080u, x1 = r[2 * u + 1] ^ 0x80808080u;
+              const uint32_t x0 = r[2 * uu] ^ 0x80808080u, x1 = r[2 * uu + 1] ^ 0x80808080u;
               a0 = __byte_perm(x0, 0x6464u, 0x5240);
               a1 = __byte_perm(x0, 0x6464u, 0x5341);
               a2 = __byte_perm(x1, 0x6464u, 0x5240);
               a3 = __byte_perm(x1, 0x6464u, 0x5341);
             }
-            mma_f16_16816(o[mt + u], a0, a1, a2, a3, pb[t][0], pb[t][1]);
-            mma_f16_16816(o[mt + u], a0, a1, a2, a3, pc[t][0], pc[t][1]);
+            mma_f16_16816(o[0][mt + uu], a0, a1, a2, a3, pb[0][t][0], pb[0][t][1]);
+            mma_f16_16816(o[0][mt + uu], a0, a1, a2, a3, pc[0][t][0], pc[0][t][1]);
           }
         }
       }
@@ -736,20 +857,26 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
         const uint32_t addr = smem_u32(vt + half * C::HSTR) + C::row_off(r) + ((ch ^ (r & 7)) << 4);
         uint32_t a0, a1, a2, a3;
         ldmatrix_x4_trans(addr, a0, a1, a2, a3);
-        mma_bf16_16816(o[mt], a0, a1, a2, a3, pb[0][0], pb[0][1]);
-        mma_bf16_16816(o[mt], a0, a1, a2, a3, pc[0][0], pc[0][1]);
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+          if (nb < nbv) {
+            mma_bf16_16816(o[nb][mt], a0, a1, a2, a3, pb[nb][0][0], pb[nb][0][1]);
+            mma_bf16_16816(o[nb][mt], a0, a1, a2, a3, pc[nb][0][0], pc[nb][0][1]);
+          }
+        }
       }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_empty + 8 * stage);
 
     if (c == ce - 1 || c == b - 1) {
-      // ---- end of partition: write the final output or a partial state
+      // ---- end of partition: write the final output or a partial state of
+      // each valid column
       if constexpr (CT == 1) {
 #pragma unroll
         for (int mt = 0; mt < D / 16; ++mt)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) o[mt][e] *= p.v_scale;
+          for (int e = 0; e < 4; ++e) o[0][mt][e] *= p.v_scale;
       } else if constexpr (CT == 2) {
         float vt0 = vw0, vt1 = vw1;
 #pragma unroll
@@ -760,65 +887,115 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
         const float c0 = 1152.f * vt0, c1 = 1152.f * vt1;
 #pragma unroll
         for (int mt = 0; mt < D / 16; ++mt) {
-          o[mt][0] -= c0;
-          o[mt][1] -= c1;
-          o[mt][2] -= c0;
-          o[mt][3] -= c1;
+          o[0][mt][0] -= c0;
+          o[0][mt][1] -= c1;
+          o[0][mt][2] -= c0;
+          o[0][mt][3] -= c1;
         }
       }
-      float lt0 = l0, lt1 = l1;
 #pragma unroll
-      for (int off = 4; off < 32; off <<= 1) {
-        lt0 += __shfl_xor_sync(0xffffffffu, lt0, off);
-        lt1 += __shfl_xor_sync(0xffffffffu, lt1, off);
-      }
-      const int first = cta_of_chunk(a, T, n);
-      const int np = cta_of_chunk(b - 1, T, n) - first + 1;
-      const int part = cta - first;
-      if (np == 1) {
-        const float i0 = 1.f / lt0, i1 = 1.f / lt1;
-        __nv_bfloat16* oa = p.out + (rowA >= 0 ? rowA : 0) * D;
-        __nv_bfloat16* obb = p.out + (rowB >= 0 ? rowB : 0) * D;
+      for (int nb = 0; nb < NB; ++nb) {
+        if (nb >= nbv) continue;
+        float lt0 = l0[nb], lt1 = l1[nb];
 #pragma unroll
-        for (int mt = 0; mt < D / 16; ++mt) {
-          // O^T rows g and g+8 of tile mt are d0 and d1 (see the PV product)
-          const int d0 = CT == 0 ? mt * 16 + g : mt * 16 + 2 * g;
-          const int d1 = CT == 0 ? d0 + 8 : d0 + 1;
-          if (rowA >= 0) {
-            oa[d0] = __float2bfloat16_rn(o[mt][0] * i0);
-            oa[d1] = __float2bfloat16_rn(o[mt][2] * i0);
-          }
-          if (rowB >= 0) {
-            obb[d0] = __float2bfloat16_rn(o[mt][1] * i1);
-            obb[d1] = __float2bfloat16_rn(o[mt][3] * i1);
-          }
+        for (int off = 4; off < 32; off <<= 1) {
+          lt0 += __shfl_xor_sync(0xffffffffu, lt0, off);
+          lt1 += __shfl_xor_sync(0xffffffffu, lt1, off);
         }
-      } else if (part < p.ws.pmax) {
-        // partial of (query row, head) at ((row * Pmax + part) * H_q + head)
-        const int64_t pa = rowA >= 0 ? (rowA / H_q * p.ws.pmax + part) * H_q + rowA % H_q : 0;
-        const int64_t pb = rowB >= 0 ? (rowB / H_q * p.ws.pmax + part) * H_q + rowB % H_q : 0;
-        float* oa = p.ws.o + pa * D;
-        float* obb = p.ws.o + pb * D;
 #pragma unroll
-        for (int mt = 0; mt < D / 16; ++mt) {
-          const int d0 = CT == 0 ? mt * 16 + g : mt * 16 + 2 * g;
-          const int d1 = CT == 0 ? d0 + 8 : d0 + 1;
-          if (rowA >= 0) {
-            oa[d0] = o[mt][0];
-            oa[d1] = o[mt][2];
+        for (int col = 0; col < 2; ++col) {
+          const int row = col ? rowB[nb] : rowA[nb];
+          if (row < 0) continue;
+          // the column's sequence: its query row in decode; the unit's
+          // sequence for several query tokens per sequence
+          const int sq = p.cu_seqlens ? u : (int)(row / H_q);
+          const int np = tc_seq_parts(cstart, sq, M, T, n);
+          const int part = tc_part_slot(cstart, sq, u, M, cta, T, n);
+          const float lt = col ? lt1 : lt0;
+          const float mm = col ? m1[nb] : m0[nb];
+          if (np == 1) {
+            const float inv = 1.f / lt;
+            __nv_bfloat16* orow = p.out + (int64_t)row * D;
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt) {
+              // O^T rows g and g+8 of tile mt are d0 and d1 (see the PV product)
+              const int d0 = CT == 0 ? mt * 16 + g : mt * 16 + 2 * g;
+              const int d1 = CT == 0 ? d0 + 8 : d0 + 1;
+              orow[d0] = __float2bfloat16_rn(o[nb][mt][col] * inv);
+              orow[d1] = __float2bfloat16_rn(o[nb][mt][2 + col] * inv);
+            }
+          } else if (part < p.ws.pmax) {
+            // partial of (query row, head) at ((row * Pmax + part) * H_q + head)
+            const int64_t pa = ((int64_t)(row / H_q) * p.ws.pmax + part) * H_q + row % H_q;
+            float* orow = p.ws.o + pa * D;
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt) {
+              const int d0 = CT == 0 ? mt * 16 + g : mt * 16 + 2 * g;
+              const int d1 = CT == 0 ? d0 + 8 : d0 + 1;
+              orow[d0] = o[nb][mt][col];
+              orow[d1] = o[nb][mt][2 + col];
+            }
+            if (g == 0) p.ws.ml[pa] = make_float2(mm, lt);
           }
-          if (rowB >= 0) {
-            obb[d0] = o[mt][1];
-            obb[d1] = o[mt][3];
-          }
-        }
-        if (g == 0) {
-          if (rowA >= 0) p.ws.ml[pa] = make_float2(m0, lt0);
-          if (rowB >= 0) p.ws.ml[pb] = make_float2(m1, lt1);
         }
       }
     }
   }
+}
+
+// ===========================================================================
+// Shared-prefix groups: for group g (sequences g m .. g m + m - 1 below S),
+// glen[g] = the number of leading tokens that every member reads from the
+// same physical blocks: the leading run of block-table entries equal in all
+// members' rows, times the block size, capped at the shortest member's length
+// and rounded down to whole 16-token chunks (0 for a group of one).  One warp
+// per group compares 32 entries at a time and stops at the first difference;
+// only entries inside every member's length are read.  Lengths are clamped as
+// the attention kernel clamps them (which also reports them).
+// ===========================================================================
+constexpr int kShareWarps = 8;
+
+__global__ void __launch_bounds__(kShareWarps * 32)
+share_prefix_kernel(const int32_t* __restrict__ block_tables, int max_blocks_per_seq,
+                    const int32_t* __restrict__ context_lens, int max_len, int S, int K, int m,
+                    int* __restrict__ glen) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = blockIdx.x * kShareWarps + warp;
+  const int ngroups = (S + m - 1) / m;
+  const int cap = min(max_len, max_blocks_per_seq * K);
+  int lg = 0;
+  if (g < ngroups) {
+    const int s0 = g * m, cnt = min(m, S - s0);
+    if (cnt >= 2) {
+      int lmin = cap;
+      for (int i = 0; i < cnt; ++i) {
+        const int L = context_lens[s0 + i];
+        lmin = min(lmin, L < 0 ? 0 : min(L, cap));
+      }
+      const int nblk = (lmin + K - 1) / K;
+      int run = nblk;
+      for (int b0 = 0; b0 < nblk; b0 += 32) {
+        const int b = b0 + lane;
+        bool same = true;
+        if (b < nblk) {
+          const int e0 = block_tables[(int64_t)s0 * max_blocks_per_seq + b];
+          for (int i = 1; i < cnt; ++i)
+            same = same && block_tables[(int64_t)(s0 + i) * max_blocks_per_seq + b] == e0;
+        }
+        const unsigned diff = __ballot_sync(0xffffffffu, !same);
+        if (diff) {
+          run = b0 + __ffs(diff) - 1;
+          break;
+        }
+      }
+      lg = min(run * K, lmin) / kTile * kTile;
+    }
+  }
+  // the tables and lengths are inputs no kernel of this library writes; the
+  // workspace may still be read by the previous launch
+  pdl_wait_primary();
+  pdl_launch_dependents();
+  if (g < ngroups && lane == 0) glen[g] = lg;
 }
 
 }  // namespace pkv

@@ -40,7 +40,8 @@ c_i32, c_i64, c_vp, c_sz, c_f = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p,
 
 
 class AttentionConfig(ctypes.Structure):
-    _fields_ = [("kernel", c_i32), ("num_splits", c_i32), ("reserved", c_i32 * 6)]
+    _fields_ = [("kernel", c_i32), ("num_splits", c_i32), ("share_prefix", c_i32),
+                ("reserved", c_i32 * 5)]
 
 
 class KvQuant(ctypes.Structure):
@@ -303,18 +304,19 @@ def kv_block_swap(src_k: torch.Tensor, src_v: Optional[torch.Tensor], dst_k: tor
                            _stream(dev)), "pkv_kv_block_swap")
 
 
-def _cfg(kernel: int, num_splits: int) -> AttentionConfig:
+def _cfg(kernel: int, num_splits: int, share_prefix: bool = False) -> AttentionConfig:
     c = AttentionConfig()
     c.kernel = kernel
     c.num_splits = num_splits
+    c.share_prefix = 1 if share_prefix else 0
     return c
 
 
 def attention_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                               max_context_len, dtype: torch.dtype, kernel: int = 0,
-                              num_splits: int = 0) -> int:
+                              num_splits: int = 0, share_prefix: bool = False) -> int:
     out = c_sz(0)
-    cfg = _cfg(kernel, num_splits)
+    cfg = _cfg(kernel, num_splits, share_prefix)
     code = PKV_BF16 if dtype == torch.bfloat16 else PKV_F32
     _check(_ws_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_context_len,
                      code, ctypes.byref(cfg), ctypes.byref(out)), "pkv_attention_workspace_bytes")
@@ -323,10 +325,10 @@ def attention_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, blo
 
 def attention_launch_count(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                            max_context_len, dtype: torch.dtype, kernel: int = 0,
-                           num_splits: int = 0) -> int:
+                           num_splits: int = 0, share_prefix: bool = False) -> int:
     """Kernel launches one paged_attention_decode call makes for these sizes."""
     out = c_i32(0)
-    cfg = _cfg(kernel, num_splits)
+    cfg = _cfg(kernel, num_splits, share_prefix)
     code = PKV_BF16 if dtype == torch.bfloat16 else PKV_F32
     _check(_launch_count(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                          max_context_len, code, ctypes.byref(cfg), ctypes.byref(out)),
@@ -340,13 +342,16 @@ def paged_attention_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
                            out: Optional[torch.Tensor] = None,
                            max_context_len: Optional[int] = None,
                            workspace: Optional[torch.Tensor] = None,
-                           kernel: int = 0, num_splits: int = 0) -> torch.Tensor:
+                           kernel: int = 0, num_splits: int = 0,
+                           share_prefix: bool = False) -> torch.Tensor:
     """Decode attention over the paged cache (GQA, split-K).
 
     ``max_context_len`` is a host-side bound on ``context_lens``; when omitted
     it is read from the device (one synchronising copy).  ``workspace`` is a
-    uint8 CUDA tensor of at least :func:`attention_workspace_bytes` bytes;
-    when omitted one is allocated with torch.
+    uint8 CUDA tensor of at least :func:`attention_workspace_bytes` bytes
+    (for the same ``kernel``, ``num_splits`` and ``share_prefix``); when
+    omitted one is allocated with torch.  ``share_prefix``: stage blocks that
+    consecutive sequences share once per group (see pkv_attention_config).
     """
     _need(q, "q", None, 3)
     _need(k_cache, "k_cache", q.dtype, 4)
@@ -364,11 +369,11 @@ def paged_attention_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
     if max_context_len is None:
         max_context_len = int(context_lens.max().item()) if S else 0
     need = attention_workspace_bytes(S, H_q, H_kv, D, K, max_context_len, q.dtype, kernel,
-                                     num_splits)
+                                     num_splits, share_prefix)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
     _need(workspace, "workspace", torch.uint8, 1)
-    cfg = _cfg(kernel, num_splits)
+    cfg = _cfg(kernel, num_splits, share_prefix)
     _check(_attention(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                       block_tables.shape[1], _ptr(context_lens), max_context_len, S, H_q, H_kv, D,
                       K, nb, float(scale), _ptr(out), _ptr(workspace), workspace.numel(),

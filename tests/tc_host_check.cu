@@ -125,8 +125,99 @@ int check_stream_k() {
   return errors;
 }
 
+// Shared-prefix units: for random batches (groups of m = 16 / G sequences,
+// shared lengths glen[g] that are multiples of 16 and at most the shortest
+// member's length, 0 for a group of one) and grid sizes, every CTA's runs of
+// one unit are that CTA's partitions; each member of the unit gets the slot
+// `slot(...)`.  Checked: a sequence's slots are exactly 0 .. parts - 1, each
+// once; slots stay below the plan's Pmax (twice the plain bound); the tokens
+// the partitions cover add up to the sequence's length.  `slot` is
+// pkv::tc_part_slot, or a planted variant that must fail.
+template <typename Slot>
+int check_shared_units(Slot slot, int trials) {
+  int errors = 0;
+  std::mt19937 rng(11);
+  for (int trial = 0; trial < trials; ++trial) {
+    const int G = 1 << (rng() % 4);
+    const int m = trial % 5 == 0 ? 1 : 16 / G;    // plain mode too
+    const int S = 1 + (int)(rng() % 40);
+    const int max_len = 1 + (int)(rng() % 2000);
+    std::vector<int> len(S), glen((S + m - 1) / m, 0);
+    for (int s = 0; s < S; ++s) len[s] = rng() % 7 == 0 ? 0 : (int)(rng() % (max_len + 1));
+    if (m > 1) {
+      for (int g = 0; g * m < S; ++g) {
+        const int cnt = std::min(m, S - g * m);
+        int lmin = max_len;
+        for (int i = 0; i < cnt; ++i) lmin = std::min(lmin, len[g * m + i]);
+        glen[g] = cnt >= 2 && rng() % 4 ? (int)(rng() % (lmin + 1)) / 16 * 16 : 0;
+      }
+    }
+    const int NU = pkv::tc_num_units(S, m);
+    std::vector<int> cstart(NU + 1, 0), ut0(NU), uend(NU), us0(NU), urows(NU);
+    for (int u = 0; u < NU; ++u) {
+      int s0 = u, rows = 1, t0 = 0, end = m == 1 ? len[u] : 0;
+      if (m > 1) {
+        const int g = u / (m + 1), k = u % (m + 1);
+        if (k == 0) {
+          s0 = g * m; rows = std::min(m, S - s0); t0 = 0; end = glen[g];
+        } else {
+          s0 = g * m + k - 1; rows = s0 < S; t0 = glen[g];
+          end = rows ? std::max(len[s0], t0) : t0;
+        }
+      }
+      us0[u] = s0; urows[u] = rows; ut0[u] = t0; uend[u] = end;
+      cstart[u + 1] = cstart[u] + (rows ? (end - t0 + 15) / 16 : 0);
+    }
+    const long long T = cstart[NU];
+    if (T == 0) continue;
+    const int grid = 1 + (int)(rng() % 160);
+    const int n = (int)(T < grid ? T : grid);
+    const int pmax = std::max(1, std::min(grid, (max_len + 15) / 16)) * (m > 1 ? 2 : 1);
+    std::vector<std::vector<int>> slots(S);
+    std::vector<long long> covered(S, 0);
+    for (int cta = 0; cta < n; ++cta) {
+      const int cb = (int)((long long)cta * T / n), ce = (int)((long long)(cta + 1) * T / n);
+      for (int c = cb; c < ce; ++c) {
+        const int u = pkv::seq_of_chunk(cstart.data(), NU, c);
+        if (c != cb && c != cstart[u]) continue;            // not a partition start
+        const int last = std::min(ce, cstart[u + 1]);       // partition: chunks c .. last - 1
+        const long long tok = std::min<long long>(uend[u], ut0[u] + (long long)(last - cstart[u]) * 16) -
+                              (ut0[u] + (long long)(c - cstart[u]) * 16);
+        for (int r = 0; r < urows[u]; ++r) {
+          const int s = us0[u] + r;
+          slots[s].push_back(slot(cstart.data(), s, u, m, cta, T, n));
+          covered[s] += tok;
+        }
+      }
+    }
+    for (int s = 0; s < S; ++s) {
+      const int parts = pkv::tc_seq_parts(cstart.data(), s, m, T, n);
+      std::vector<int> got = slots[s];
+      std::sort(got.begin(), got.end());
+      bool ok = (int)got.size() == parts && covered[s] == len[s];
+      for (int i = 0; ok && i < (int)got.size(); ++i) ok = got[i] == i && got[i] < pmax;
+      if (!ok) ++errors;
+    }
+  }
+  return errors;
+}
+
 int main() {
   int errors = check_stream_k();
+  {
+    const int e = check_shared_units(
+        [](const int* cs, int s, int u, int m, int cta, long long T, int n) {
+          return pkv::tc_part_slot(cs, s, u, m, cta, T, n);
+        }, 6000);
+    // planted mistake: private-unit slots without the shared unit's offset
+    const int planted = check_shared_units(
+        [](const int* cs, int s, int u, int m, int cta, long long T, int n) {
+          return cta - pkv::cta_of_chunk(cs[u], T, n);
+        }, 600);
+    if (e) std::printf("shared-prefix unit errors: %d\n", e);
+    if (planted == 0) std::printf("planted slot mistake not caught\n");
+    errors += e + (planted == 0);
+  }
   errors += check_hpc<64, 0, false>() + check_hpc<64, 0, true>();
   errors += check_hpc<128, 0, false>() + check_hpc<128, 0, true>();
   errors += check_hpc<128, 1, false>() + check_hpc<128, 1, true>();
@@ -135,6 +226,6 @@ int main() {
     std::printf("errors: %d\n", errors);
     return 1;
   }
-  std::printf("layout ok: 32 configurations; stream-K ok\n");
+  std::printf("layout ok: 32 configurations; stream-K ok; shared-prefix units ok\n");
   return 0;
 }

@@ -103,3 +103,13 @@ def test_attention_plan_validation(lib):
     # reserved fields must be zero
     cfg.reserved[0] = 1
     assert f(4, 4, 2, 64, 4, 16, 0, ctypes.byref(cfg), ctypes.byref(sz)) == 1
+    cfg.reserved[0] = 0
+    # share_prefix is 0 or 1; the CUDA-core plan ignores it (same workspace)
+    cfg.share_prefix = 2
+    assert f(4, 4, 2, 64, 4, 16, 0, ctypes.byref(cfg), ctypes.byref(sz)) == 1
+    base = ctypes.c_size_t(0)
+    cfg.share_prefix = 0
+    assert f(4, 4, 2, 64, 4, 16, 0, ctypes.byref(cfg), ctypes.byref(base)) == 0
+    cfg.share_prefix = 1
+    assert f(4, 4, 2, 64, 4, 16, 0, ctypes.byref(cfg), ctypes.byref(sz)) == 0
+    assert sz.value == base.value
