@@ -245,6 +245,8 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
   const int K = p.block_size;
   const int row_tokens = p.max_blocks_per_seq * K;
   const int M = SH ? p.share_m : 1;
+  // several query tokens per sequence (never with shared-prefix groups)
+  const int32_t* const cu = SH ? nullptr : p.cu_seqlens;
   const int NU = SH ? tc_num_units(S, M) : S;
   auto seq_len = [&](int s) -> int {
     return effective_len(p.context_lens[s], p.max_len, row_tokens);
@@ -278,8 +280,8 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
     int s0, rows, t0, end;
     unit(u, s0, rows, t0, end);
     if (rows == 0) return 0;
-    if (p.cu_seqlens != nullptr) {
-      const int nq = p.cu_seqlens[s0 + 1] - p.cu_seqlens[s0];
+    if (cu != nullptr) {
+      const int nq = cu[s0 + 1] - cu[s0];
       if (nq < 0 || nq > end) {
         record_error(PKV_DEVERR_CONTEXT_LEN);
         return 0;
@@ -352,7 +354,7 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
       // empty context: zero output (decode); a sequence without query rows
       // has no output
       const int owner = a < T ? cta_of_chunk(a, T, n) : n - 1;
-      if (owner == cta && p.cu_seqlens == nullptr) {
+      if (owner == cta && cu == nullptr) {
         if (group == 0) p.ws.nparts[s] = 0;
         __nv_bfloat16* o = p.out + ((int64_t)s * H_q + head0 * G) * D;
         for (int i = 0; i < HPC * G * D; ++i) o[i] = __float2bfloat16_rn(0.f);
@@ -363,10 +365,10 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
       const int uo = a < b ? up : tc_shared_unit(s, M);
       if (cta_of_chunk(cstart[uo], T, n) == cta) {
         const int parts = tc_seq_parts(cstart, s, M, T, n);
-        if (p.cu_seqlens == nullptr) {
+        if (cu == nullptr) {
           p.ws.nparts[s] = parts;
         } else {
-          for (int r = p.cu_seqlens[s]; r < p.cu_seqlens[s + 1]; ++r) p.ws.nparts[r] = parts;
+          for (int r = cu[s]; r < cu[s + 1]; ++r) p.ws.nparts[r] = parts;
         }
       }
     }
@@ -499,11 +501,14 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
   float vw0 = 0.f, vw1 = 0.f;
   int u = seq_of_chunk(cstart, NU, cb);
   int ut0 = 0, uend = 0, ulim = 0;   // the unit's tokens [ut0, uend); min column limit
+  int qr0 = 0, nq = 0, ncol = 0;     // first query row, query rows, valid score columns
   int nbv = 1;                       // column blocks holding valid columns
-  // this thread's score columns 8 nb + 2tq and 8 nb + 2tq + 1: their query
-  // rows (-1: padding column) and last visible key positions
-  int rowA[NB], rowB[NB];
-  int limA[NB], limB[NB];
+  // score column c (query row qr0 + c / G, head j G + c % G; c >= ncol is
+  // padding) sees keys up to its limit: len - n + i for new token i of n
+  // (several query tokens per sequence), else the unit's last key
+  auto col_lim = [&](int cc) -> int {
+    return cc < ncol && cu ? uend - nq + cc / G : uend - 1;
+  };
   int k = 0;
   for (int c = cb; c < ce; ++c, ++k) {
     while (c >= cstart[u + 1]) ++u;
@@ -512,22 +517,14 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
       // ---- new partition: load the q-group(s) as the B fragments of Q^T
       int s0, rows;
       unit(u, s0, rows, ut0, uend);
-      const int qr0 = p.cu_seqlens ? p.cu_seqlens[s0] : s0;           // first query row
-      const int nq = p.cu_seqlens ? p.cu_seqlens[s0 + 1] - qr0 : rows; // query rows
-      const int ncol = nq * G;                                        // valid score columns
+      qr0 = cu ? cu[s0] : s0;
+      nq = cu ? cu[s0 + 1] - qr0 : rows;
+      ncol = nq * G;
       nbv = ncol > 8 ? NB : 1;
       ulim = uend - 1;
 #pragma unroll
-      for (int nb = 0; nb < NB; ++nb) {
-        const int cA = 8 * nb + 2 * tq, cB = cA + 1;
-        rowA[nb] = cA < ncol ? (qr0 + cA / G) * H_q + j * G + cA % G : -1;
-        rowB[nb] = cB < ncol ? (qr0 + cB / G) * H_q + j * G + cB % G : -1;
-        // several query tokens of one sequence: token i sees keys up to
-        // len - n + i; otherwise every column sees the unit's keys
-        limA[nb] = cA < ncol && p.cu_seqlens ? uend - nq + cA / G : uend - 1;
-        limB[nb] = cB < ncol && p.cu_seqlens ? uend - nq + cB / G : uend - 1;
-        ulim = min(ulim, min(limA[nb], limB[nb]));
-      }
+      for (int nb = 0; nb < NB; ++nb)
+        ulim = min(ulim, min(col_lim(8 * nb + 2 * tq), col_lim(8 * nb + 2 * tq + 1)));
       if constexpr (CT == 0) {
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb) {
@@ -702,10 +699,11 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
         // chunk wholly below every column's limit needs no mask
         if (cmask) {
           const int kp = cpos + t * kTile + g;   // key position of row g
-          if (kp > limA[nb]) x[t][0] = -INFINITY;
-          if (kp > limB[nb]) x[t][1] = -INFINITY;
-          if (kp + 8 > limA[nb]) x[t][2] = -INFINITY;
-          if (kp + 8 > limB[nb]) x[t][3] = -INFINITY;
+          const int limA = col_lim(8 * nb + 2 * tq), limB = col_lim(8 * nb + 2 * tq + 1);
+          if (kp > limA) x[t][0] = -INFINITY;
+          if (kp > limB) x[t][1] = -INFINITY;
+          if (kp + 8 > limA) x[t][2] = -INFINITY;
+          if (kp + 8 > limB) x[t][3] = -INFINITY;
         }
         mx0 = fmaxf(mx0, fmaxf(x[t][0], x[t][2]));
         mx1 = fmaxf(mx1, fmaxf(x[t][1], x[t][3]));
@@ -825,45 +823,63 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
         for (int mt = 0; mt < D / 16; mt += 2) {
           uint32_t r[4];
           ldmatrix_x4_trans(vt + (((mt + (lm >> 1)) ^ (tok & 7)) << 4), r[0], r[1], r[2], r[3]);
+          uint32_t af[2][4];
 #pragma unroll
           for (int uu = 0; uu < 2; ++uu) {
             // r[2uu]: tokens 2tq, 2tq+1 of m tile mt + uu; r[2uu+1]: tokens + 8
-            uint32_t a0, a1, a2, a3;
             if constexpr (CT == 1) {
               // one permute makes both pairs: bytes (0, 2) low, (1, 3) high
-              e4m3x4_to_f16x2x2(__byte_perm(r[2 * uu], 0u, 0x3120), a0, a1);
-              e4m3x4_to_f16x2x2(__byte_perm(r[2 * uu + 1], 0u, 0x3120), a2, a3);
+              e4m3x4_to_f16x2x2(__byte_perm(r[2 * uu], 0u, 0x3120), af[uu][0], af[uu][1]);
+              e4m3x4_to_f16x2x2(__byte_perm(r[2 * uu + 1], 0u, 0x3120), af[uu][2], af[uu][3]);
             } else {
               // 1152 + code, exact in f16 (the 1152 comes off at the partition end)
               const uint32_t x0 = r[2 * uu] ^ 0x80808080u, x1 = r[2 * uu + 1] ^ 0x80808080u;
-              a0 = __byte_perm(x0, 0x6464u, 0x5240);
-              a1 = __byte_perm(x0, 0x6464u, 0x5341);
-              a2 = __byte_perm(x1, 0x6464u, 0x5240);
-              a3 = __byte_perm(x1, 0x6464u, 0x5341);
+              af[uu][0] = __byte_perm(x0, 0x6464u, 0x5240);
+              af[uu][1] = __byte_perm(x0, 0x6464u, 0x5341);
+              af[uu][2] = __byte_perm(x1, 0x6464u, 0x5240);
+              af[uu][3] = __byte_perm(x1, 0x6464u, 0x5341);
             }
-            mma_f16_16816(o[0][mt + uu], a0, a1, a2, a3, pb[0][t][0], pb[0][t][1]);
-            mma_f16_16816(o[0][mt + uu], a0, a1, a2, a3, pc[0][t][0], pc[0][t][1]);
           }
+          // the hi products of both m tiles before the lo ones (consecutive
+          // mma instructions accumulate into different tiles)
+#pragma unroll
+          for (int lo = 0; lo < 2; ++lo)
+#pragma unroll
+            for (int uu = 0; uu < 2; ++uu) {
+              const uint32_t* pp = lo ? pc[0][t] : pb[0][t];
+              mma_f16_16816(o[0][mt + uu], af[uu][0], af[uu][1], af[uu][2], af[uu][3], pp[0],
+                            pp[1]);
+            }
         }
       }
     } else {
+      // two m tiles at a time, the hi products of both before the lo ones, so
+      // that consecutive mma instructions accumulate into different tiles
       const int r = (lane & 7) + (lane >> 4) * 8;
       const int chs = (lane >> 3) & 1;
       const uint8_t* vt = sb + C::box_off(1, w, 0, 0);
 #pragma unroll
-      for (int mt = 0; mt < D / 16; ++mt) {
-        const int half = mt >> 2;
-        const int ch = ((mt & 3) << 1) + chs;
-        const uint32_t addr = smem_u32(vt + half * C::HSTR) + C::row_off(r) + ((ch ^ (r & 7)) << 4);
-        uint32_t a0, a1, a2, a3;
-        ldmatrix_x4_trans(addr, a0, a1, a2, a3);
+      for (int mt = 0; mt < D / 16; mt += 2) {
+        uint32_t a[2][4];
 #pragma unroll
-        for (int nb = 0; nb < NB; ++nb) {
-          if (nb < nbv) {
-            mma_bf16_16816(o[nb][mt], a0, a1, a2, a3, pb[nb][0][0], pb[nb][0][1]);
-            mma_bf16_16816(o[nb][mt], a0, a1, a2, a3, pc[nb][0][0], pc[nb][0][1]);
-          }
+        for (int uu = 0; uu < 2; ++uu) {
+          const int half = (mt + uu) >> 2;
+          const int ch = (((mt + uu) & 3) << 1) + chs;
+          const uint32_t addr =
+              smem_u32(vt + half * C::HSTR) + C::row_off(r) + ((ch ^ (r & 7)) << 4);
+          ldmatrix_x4_trans(addr, a[uu][0], a[uu][1], a[uu][2], a[uu][3]);
         }
+#pragma unroll
+        for (int lo = 0; lo < 2; ++lo)
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+            for (int uu = 0; uu < 2; ++uu)
+              if (nb < nbv) {
+                const uint32_t* pp = lo ? pc[nb][0] : pb[nb][0];
+                mma_bf16_16816(o[nb][mt + uu], a[uu][0], a[uu][1], a[uu][2], a[uu][3], pp[0],
+                               pp[1]);
+              }
       }
     }
     __syncwarp();
@@ -904,11 +920,12 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
         }
 #pragma unroll
         for (int col = 0; col < 2; ++col) {
-          const int row = col ? rowB[nb] : rowA[nb];
-          if (row < 0) continue;
+          const int cc = 8 * nb + 2 * tq + col;
+          if (cc >= ncol) continue;              // padding column
+          const int row = (qr0 + cc / G) * H_q + j * G + cc % G;
           // the column's sequence: its query row in decode; the unit's
           // sequence for several query tokens per sequence
-          const int sq = p.cu_seqlens ? u : (int)(row / H_q);
+          const int sq = cu ? u : (int)(row / H_q);
           const int np = tc_seq_parts(cstart, sq, M, T, n);
           const int part = tc_part_slot(cstart, sq, u, M, cta, T, n);
           const float lt = col ? lt1 : lt0;

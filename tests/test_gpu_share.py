@@ -96,13 +96,16 @@ def test_full_size_prefix_cow(ops):
 
 
 def _duplicate_rows(w, reps):
-    """Attention-only workload whose consecutive rows repeat each sequence
-    `reps` times (identical tables and lengths: the whole context shared, a
-    member with no private tokens); no new tokens are written."""
+    """Workload whose consecutive rows repeat each sequence `reps` times
+    (identical tables and lengths: the whole context shared, members with no
+    private tokens); the first copy of each sequence writes its new token,
+    the others write nothing."""
     idx = np.repeat(np.arange(w.num_seqs), reps)
+    first = np.zeros(len(idx), bool)
+    first[::reps] = True
     w.block_tables = w.block_tables[idx].copy()
     w.context_lens = w.context_lens[idx].copy()
-    w.positions = np.full(len(idx), -1, np.int32)
+    w.positions = np.where(first, w.positions[idx], -1).astype(np.int32)
     w.num_seqs = len(idx)
     return w
 
@@ -116,18 +119,10 @@ def test_identical_rows(ops, lens, G):
     H_kv = 2
     base = wl.build_decode("dup", lens, G * H_kv, H_kv, 128, 16, "bf16", seed=len(lens) + G)
     w = _duplicate_rows(base, 16 // G)
-    c = wl.materialize(w, seed=3)
-    d = {k: v.to(DEV) for k, v in c.items()}
-    out = ops.paged_attention_decode(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
-                                     d["context_lens"], w.scale,
-                                     max_context_len=w.max_context_len, share_prefix=True)
-    torch.cuda.synchronize()
-    assert ops.get_device_error() == 0
-    ref = oracle.paged_attention_decode(storage(c["q"]), storage(c["k_cache"]),
-                                        storage(c["v_cache"]), w.block_tables, w.context_lens,
-                                        w.scale, "bf16")
-    check_attention(as_f64(out), ref, "bf16", "identical rows")
-    assert np.array_equal(as_f64(out)[w.context_lens == 0], np.zeros_like(ref[w.context_lens == 0]))
+    plain, shared, ref = _step_both(ops, w, seed=3)
+    check_attention(shared, ref, "bf16", "identical rows")
+    check_attention(plain, ref, "bf16", "identical rows, plain")
+    assert np.array_equal(shared[w.context_lens == 0], np.zeros_like(ref[w.context_lens == 0]))
 
 
 def test_no_sharing_and_split_counts(ops):
