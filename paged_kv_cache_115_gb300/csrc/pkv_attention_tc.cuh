@@ -298,7 +298,11 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
     }
     fence_barrier_init();
   }
-  pdl_wait_primary();
+  // The prefix sums read only the lengths (and, with several query tokens,
+  // cu_seqlens), which no kernel of this library writes, so they overlap the
+  // previous kernel's tail; shared-prefix groups also need the group lengths
+  // the previous kernel (share_prefix_kernel) writes.
+  if constexpr (SH) pdl_wait_primary();
 
   // ---- chunk prefix sums over the units: cstart[u] = sum_{u'<u} chunks(u')
   {
@@ -345,6 +349,44 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
   const int cb = cta < n ? (int)((long long)cta * T / n) : 0;
   const int ce = cta < n ? (int)((long long)(cta + 1) * T / n) : 0;
 
+  // pool rows of the tiles of 32 chunks from c0, one chunk per lane; a tile
+  // past the unit's end (or of an out-of-range block) gets a row that is
+  // wholly out of bounds, which TMA fills with zeros.  With 8-token blocks a
+  // tile spans two blocks (uu = 0, 1).
+  constexpr int sbl = B8 ? 1 : 0;          // log2 of the blocks per tile
+  auto tile_rows = [&](int c0, int (&row)[TL][2]) {
+#pragma unroll
+    for (int t = 0; t < TL; ++t) row[t][0] = row[t][1] = -2 * kTile;
+    const int c = c0 + lane;
+    if (c < ce) {
+      const int u = seq_of_chunk(cstart, NU, c);
+      int s0, rows, t0, end;
+      unit(u, s0, rows, t0, end);
+      const int L = (TL > 1 || sbl || SH) ? end : 1 << 30;
+#pragma unroll
+      for (int t = 0; t < TL; ++t) {
+#pragma unroll
+        for (int uu = 0; uu < 2; ++uu) {
+          const int tok = t0 + (c - cstart[u]) * CH + t * kTile + uu * K;
+          if (uu <= sbl && tok < L) {
+            const int lb = tok / K;
+            const long long phys = p.block_tables[(int64_t)s0 * p.max_blocks_per_seq + lb];
+            if (phys < 0 || phys >= p.num_blocks) {
+              record_error(PKV_DEVERR_BLOCK_ID);
+            } else {
+              row[t][uu] = (int)(phys * K + (tok - lb * K));
+            }
+          }
+        }
+      }
+    }
+  };
+  // the producer reads its first table entries (no kernel of this library
+  // writes the tables) before waiting for the previous kernel
+  int row[TL][2];
+  if (warp == HPC && cb < ce) tile_rows(cb, row);
+  if constexpr (!SH) pdl_wait_primary();
+
   // ---- bookkeeping: partial counts and zero outputs of empty sequences
   for (int s = tid; s < S; s += C::THREADS) {
     const int up = tc_private_unit(s, M);
@@ -382,40 +424,10 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
       prefetch_tensormap(&p.tmap_v);
     }
     const uint64_t policy = l2_policy_evict_first();
-    constexpr int sbl = B8 ? 1 : 0;          // log2 of the blocks per tile
     int k = 0;
     bool ok = true;
     for (int c0 = cb; c0 < ce && ok; c0 += 32) {
-      // pool rows of the tiles of the next 32 chunks, one chunk per lane; a
-      // tile past the unit's end (or of an out-of-range block) gets a row
-      // that is wholly out of bounds, which TMA fills with zeros.  With
-      // 8-token blocks a tile spans two blocks (u = 0, 1).
-      int row[TL][2];
-#pragma unroll
-      for (int t = 0; t < TL; ++t) row[t][0] = row[t][1] = -2 * kTile;
-      const int c = c0 + lane;
-      if (c < ce) {
-        const int u = seq_of_chunk(cstart, NU, c);
-        int s0, rows, t0, end;
-        unit(u, s0, rows, t0, end);
-        const int L = (TL > 1 || sbl || SH) ? end : 1 << 30;
-#pragma unroll
-        for (int t = 0; t < TL; ++t) {
-#pragma unroll
-          for (int uu = 0; uu < 2; ++uu) {
-            const int tok = t0 + (c - cstart[u]) * CH + t * kTile + uu * K;
-            if (uu <= sbl && tok < L) {
-              const int lb = tok / K;
-              const long long phys = p.block_tables[(int64_t)s0 * p.max_blocks_per_seq + lb];
-              if (phys < 0 || phys >= p.num_blocks) {
-                record_error(PKV_DEVERR_BLOCK_ID);
-              } else {
-                row[t][uu] = (int)(phys * K + (tok - lb * K));
-              }
-            }
-          }
-        }
-      }
+      if (c0 != cb) tile_rows(c0, row);
       const int cnt = min(32, ce - c0);
       for (int b = 0; b < cnt; ++b, ++k) {
         int r[TL][2];
@@ -644,6 +656,10 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
       const int r = (lane & 7) + ((lane >> 3) & 1) * 8;
       const int chs = lane >> 4;
       const uint8_t* kt = sb + C::box_off(0, w, 0, 0);
+      // one column block: odd k steps accumulate apart and are added at the
+      // end, two independent mma chains instead of one (two column blocks
+      // are two chains already)
+      float sodd[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) {
         const int half = ks >> 2;
@@ -651,9 +667,17 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
         const uint32_t addr = smem_u32(kt + half * C::HSTR) + C::row_off(r) + ((ch ^ (r & 7)) << 4);
         uint32_t a0, a1, a2, a3;
         ldmatrix_x4(addr, a0, a1, a2, a3);
+        if (NB == 1 && (ks & 1)) {
+          mma_bf16_16816(sodd, a0, a1, a2, a3, qf[0][ks][0], qf[0][ks][1]);
+        } else {
 #pragma unroll
-        for (int nb = 0; nb < NB; ++nb)
-          if (nb < nbv) mma_bf16_16816(sacc[nb][0], a0, a1, a2, a3, qf[nb][ks][0], qf[nb][ks][1]);
+          for (int nb = 0; nb < NB; ++nb)
+            if (nb < nbv) mma_bf16_16816(sacc[nb][0], a0, a1, a2, a3, qf[nb][ks][0], qf[nb][ks][1]);
+        }
+      }
+      if (NB == 1) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sacc[0][0][e] += sodd[e];
       }
     } else {
       // byte tiles: rows g and g+8 share a swizzle phase; the 16-code chunk

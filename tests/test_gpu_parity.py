@@ -334,3 +334,27 @@ def test_bounded_wait_gives_up_and_context_survives(ops):
     assert ops.get_device_error() == 6
     assert ops.get_device_error() == 0                # the word was cleared
     full_check(ops, wl.build("tiny"))                 # the context still works
+
+
+# ---------------------------------------------------------------------------
+# one very long sequence among short ones: its partials come from most of
+# the grid (more than the reduce's all-at-once fast path holds)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("share", [False, True])
+def test_many_partials(ops, share):
+    lens = [16, 3, 65536, 40] + [16 + 7 * i for i in range(36)]
+    w = wl.build_decode("skew", lens, 32, 8, 128, 16, "bf16", seed=9)
+    c = wl.materialize(w)
+    d = to_dev(c)
+    slots = ops.slot_mapping(d["block_tables"], d["positions"], w.block_size, w.num_blocks)
+    ops.paged_kv_write(d["k_new"], d["v_new"], slots, d["k_cache"], d["v_cache"])
+    out = ops.paged_attention_decode(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                                     d["context_lens"], w.scale,
+                                     max_context_len=w.max_context_len, share_prefix=share)
+    torch.cuda.synchronize()
+    assert ops.get_device_error() == 0
+    _, okc, ovc = oracle_step_pool(w, c)
+    ref = oracle.paged_attention_decode(storage(c["q"]), okc, ovc, w.block_tables,
+                                        w.context_lens, w.scale, "bf16")
+    check_attention(as_f64(out), ref, "bf16", "many partials")
