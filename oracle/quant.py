@@ -17,6 +17,13 @@ Readings: the INT8 "token vector" is the token's whole row in this layer's
 pool (all KV heads x head_dim); the scale and the division are float32
 (IEEE, as the page's fp16 inputs are widened), rounding is half to even; an
 all-zero row gets scale 0 and codes 0.
+
+A third pool pair keeps K at higher precision than V ("19.2 KV Cache
+系统化管理" §19.2.4: K is more sensitive to quantization than V, so it is
+kept more precise): K in bfloat16, V in FP8 e4m3 with one scale per tensor.
+Reading: "more precise" is the pool's 16-bit storage type (bf16), the V
+format the FP8 one above; a K row given in float32 is rounded to bfloat16 to
+nearest, ties to even.
 """
 
 from __future__ import annotations
@@ -24,7 +31,9 @@ from __future__ import annotations
 import numpy as np
 
 __all__ = ["E4M3_MAX", "e4m3_values", "e4m3_decode", "e4m3_encode",
-           "int8_token_quantize", "int8_decode"]
+           "int8_token_quantize", "int8_decode", "bf16_encode", "kv_write_fp8",
+           "kv_write_int8", "kv_write_k16v8", "dequantize_rows",
+           "paged_attention_decode_quant"]
 
 E4M3_MAX = 448.0
 
@@ -101,6 +110,24 @@ def int8_decode(codes: np.ndarray, scale) -> np.ndarray:
     return np.asarray(codes, dtype=np.int8).astype(np.float64) * float(scale)
 
 
+def bf16_encode(x: np.ndarray) -> np.ndarray:
+    """bfloat16 bit patterns (uint16) of float32 values, rounded to nearest
+    with ties to the even pattern.
+
+    A bfloat16 number is the upper 16 bits of a binary32 one.  Rounding the
+    32-bit pattern u to its upper half: add 0x7FFF plus the lowest kept bit
+    (bit 16) and drop the low 16 bits; a carry out of the mantissa moves into
+    the exponent, which is the next representable value (and the largest
+    finite values round up to infinity).  NaNs keep their sign and upper
+    payload with the quiet bit set.
+    """
+    u = np.asarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    nan = np.isnan(np.asarray(x, dtype=np.float32))
+    rounded = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16) & 0xFFFF
+    quiet = ((u >> 16) | 0x0040) & 0xFFFF
+    return np.where(nan, quiet, rounded).astype(np.uint16)
+
+
 # --------------------------------------------------------------------------
 # quantized KV write and attention over a quantized pool
 # --------------------------------------------------------------------------
@@ -139,10 +166,30 @@ def kv_write_int8(k_pool, v_pool, k_tok_scales, v_tok_scales, k_rows, v_rows, sl
     return kp, vp, kts, vts
 
 
+def kv_write_k16v8(k_pool, v_pool, k_rows, v_rows, slots, v_scale):
+    """K pool (bfloat16 bit patterns, uint16 [nb, K, H, D]) and V pool (e4m3
+    codes, uint8) after storing token i's rows (float32 values [T, H, D]) at
+    slots[i]: K = bfloat16(x) to nearest even, V = e4m3(float32(x / v_scale)).
+    Slot -1 skips the token."""
+    kp, vp = k_pool.copy(), v_pool.copy()
+    kf, vf = _flat(kp), _flat(vp)
+    vs = np.float32(v_scale)
+    for i, s in enumerate(np.asarray(slots)):
+        if s < 0:
+            continue
+        kf[s] = bf16_encode(np.asarray(k_rows[i], np.float32))
+        vf[s] = e4m3_encode(np.asarray(v_rows[i], np.float32) / vs)
+    return kp, vp
+
+
 def dequantize_rows(pool, rows_slot, kv_head, fmt, tensor_scale=None, tok_scales=None):
-    """float64 values of pool rows (flattened slots ``rows_slot``) for one KV head."""
+    """float64 values of pool rows (flattened slots ``rows_slot``) for one KV
+    head: ``fmt`` "fp8", "int8", or "bf16" (bit patterns, exact)."""
     flat = _flat(pool)
     codes = flat[np.asarray(rows_slot, np.int64), kv_head, :]
+    if fmt == "bf16":
+        bits = np.asarray(codes).view(np.uint16).astype(np.uint32) << np.uint32(16)
+        return bits.view(np.float32).astype(np.float64)
     if fmt == "fp8":
         return e4m3_decode(codes) * float(np.float32(tensor_scale))
     if fmt == "int8":
@@ -156,7 +203,9 @@ def paged_attention_decode_quant(q, k_pool, v_pool, block_tables, context_lens, 
                                  v_tok_scales=None):
     """Decode attention over a quantized pool: gather through the block table,
     dequantize (code * scale, exactly in float64), then the dense definition
-    of "KV Cache：长上下文为什么吃显存" §01 with GQA head h -> h // G."""
+    of "KV Cache：长上下文为什么吃显存" §01 with GQA head h -> h // G.
+    ``fmt`` "fp8", "int8", or "k16v8" (K pool bfloat16, V pool e4m3 with
+    ``v_scale``)."""
     from .paged_attention import decode, dense_attention
     S, H_q, D = q.shape
     H_kv, K = k_pool.shape[2], k_pool.shape[1]
@@ -168,8 +217,9 @@ def paged_attention_decode_quant(q, k_pool, v_pool, block_tables, context_lens, 
         t = np.arange(L, dtype=np.int64)
         slots = np.asarray(block_tables[s], np.int64)[t // K] * K + t % K
         for j in range(H_kv):
-            Kj = dequantize_rows(k_pool, slots, j, fmt, k_scale, k_tok_scales)
-            Vj = dequantize_rows(v_pool, slots, j, fmt, v_scale, v_tok_scales)
+            kf, vf = ("bf16", "fp8") if fmt == "k16v8" else (fmt, fmt)
+            Kj = dequantize_rows(k_pool, slots, j, kf, k_scale, k_tok_scales)
+            Vj = dequantize_rows(v_pool, slots, j, vf, v_scale, v_tok_scales)
             for h in range(j * G, (j + 1) * G):
                 out[s, h] = dense_attention(q64[s, h], Kj, Vj, scale)
     return out

@@ -179,3 +179,98 @@ def test_quant_attention_equals_plain_attention_on_grid_values():
     vd = (vi.astype(np.float64) * vts.reshape(nb, K)[:, :, None, None]).astype(np.float32)
     ref = oracle.paged_attention_decode(q, kd, vd, bt, lens, 0.3, "f32")
     assert np.abs(got - ref).max() < 1e-12
+
+
+# --------------------------------------------------------------------------
+# K at higher precision than V ("19.2 KV Cache 系统化管理" §19.2.4): bf16 K,
+# FP8 e4m3 V
+# --------------------------------------------------------------------------
+
+def test_bf16_encode_matches_torch_cast():
+    """Round to nearest even from float32 to bfloat16 is a library routine
+    (torch's cast): the oracle's encoder agrees on specials, exact ties with
+    even and odd kept bits, mantissa carries into the exponent, overflow to
+    infinity and random values over the whole exponent range."""
+    torch = pytest.importorskip("torch")
+    specials = np.array([0.0, -0.0, 1.0, -2.5, np.inf, -np.inf, 3.3895314e38,
+                         np.finfo(np.float32).max, np.finfo(np.float32).tiny, 1e-45],
+                        np.float32)
+    ties = np.array([0x3F808000, 0x3F818000, 0x3F80FFFF, 0x3F807FFF, 0x3FFF8000, 0x7F7F8000,
+                     0x80008000, 0x00018000], np.uint32).view(np.float32)
+    rng = np.random.default_rng(40)
+    rnd = rng.integers(0, 2**32, size=20000, dtype=np.uint64).astype(np.uint32).view(np.float32)
+    rnd = rnd[~np.isnan(rnd)]
+    x = np.concatenate([specials, ties, rnd])
+    want = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(Q.bf16_encode(x), want)
+    # a NaN stays a NaN (sign kept, quiet bit set)
+    n = Q.bf16_encode(np.array([np.nan], np.float32))[0]
+    assert (n & 0x7F80) == 0x7F80 and (n & 0x007F) != 0
+
+
+def test_bf16_encode_planted_truncation_fails():
+    """Truncation instead of rounding disagrees with the cast on ties and
+    above-half cases (the pin above would catch such a mistake)."""
+    torch = pytest.importorskip("torch")
+    x = np.array([0x3F80C000, 0x3F818000], np.uint32).view(np.float32)
+    trunc = (x.view(np.uint32) >> 16).astype(np.uint16)
+    want = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert not np.array_equal(trunc, want)
+    assert np.array_equal(Q.bf16_encode(x), want)
+
+
+def test_kv_write_k16v8_brute_force():
+    rng = np.random.default_rng(41)
+    nb, K, H, D, T = 5, 4, 2, 3, 6
+    slots = rng.choice(nb * K, size=T, replace=False).astype(np.int64)
+    slots[2] = -1
+    k = (rng.standard_normal((T, H, D)) * 3).astype(np.float32)
+    v = (rng.standard_normal((T, H, D)) * 3).astype(np.float32)
+    kp = np.full((nb, K, H, D), 0x7FC1, np.uint16)      # NaN canaries
+    vp = np.full((nb, K, H, D), 0x7F, np.uint8)
+    ok, ov = Q.kv_write_k16v8(kp, vp, k, v, slots, 0.75)
+    for i, s in enumerate(slots):
+        if s < 0:
+            continue
+        b, o = divmod(int(s), K)
+        for h in range(H):
+            for d in range(D):
+                assert ok[b, o, h, d] == Q.bf16_encode(np.array([k[i, h, d]]))[0]
+                assert ov[b, o, h, d] == Q.e4m3_encode(np.array([v[i, h, d] / np.float32(0.75)]))[0]
+    written = {int(s) for s in slots if s >= 0}
+    for flat in range(nb * K):
+        if flat not in written:
+            assert np.all(ok.reshape(nb * K, H, D)[flat] == 0x7FC1)
+            assert np.all(ov.reshape(nb * K, H, D)[flat] == 0x7F)
+
+
+def test_k16v8_attention_equals_plain_attention():
+    """K values exact in bf16 and V values exactly e4m3 codes times a power-of-
+    two scale: attention over the pool pair equals the plain oracle on those
+    values; a K pool read as FP8 (a format mix-up) does not."""
+    rng = np.random.default_rng(42)
+    S, H_q, H_kv, D, K = 3, 8, 2, 8, 4
+    lens = [6, 11, 1]
+    nb = sum(-(-L // K) for L in lens) + 2
+    order = rng.permutation(nb)
+    bt = np.full((S, 4), 10**6, np.int64)
+    p = 0
+    for s, L in enumerate(lens):
+        for i in range(-(-L // K)):
+            bt[s, i] = order[p]
+            p += 1
+    q = rng.standard_normal((S, H_q, D)).astype(np.float32)
+    kbits = Q.bf16_encode(rng.standard_normal((nb, K, H_kv, D)).astype(np.float32))
+    v = Q.e4m3_values()
+    finite = np.array([c for c in range(256) if not np.isnan(v[c]) and abs(v[c]) <= 8],
+                      np.uint8)
+    vc = rng.choice(finite, size=(nb, K, H_kv, D)).astype(np.uint8)
+    got = Q.paged_attention_decode_quant(q, kbits, vc, bt, lens, 0.3, "f32", "k16v8",
+                                         v_scale=0.5)
+    kf = (kbits.astype(np.uint32) << 16).view(np.float32)
+    ref = oracle.paged_attention_decode(q, kf, (Q.e4m3_decode(vc) * 0.5).astype(np.float32),
+                                        bt, lens, 0.3, "f32")
+    assert np.abs(got - ref).max() < 1e-12
+    wrong = Q.paged_attention_decode_quant(q, (kbits & 0xFF).astype(np.uint8), vc, bt, lens, 0.3,
+                                           "f32", "fp8", k_scale=1.0, v_scale=0.5)
+    assert not np.all(np.abs(wrong - ref) < 1e-3)
