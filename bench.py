@@ -384,6 +384,11 @@ def _accuracy(check_path: str) -> dict:
             kc, vc = Q.kv_write_fp8(kc, vc, kf, vf, slots, ks, vs)
             ref = Q.paged_attention_decode_quant(z["q"], kc, vc, bt, lens, float(z["scale"]),
                                                  "bf16", "fp8", k_scale=ks, v_scale=vs)
+        elif fmt == "k16v8":
+            vs = float(z["v_scale"])
+            kc, vc = Q.kv_write_k16v8(kc, vc, kf, vf, slots, vs)
+            ref = Q.paged_attention_decode_quant(z["q"], kc, vc, bt, lens, float(z["scale"]),
+                                                 "bf16", "k16v8", v_scale=vs)
         else:
             kc, vc, kts, vts = Q.kv_write_int8(kc, vc, z["k_ts"], z["v_ts"], kf, vf, slots)
             ref = Q.paged_attention_decode_quant(z["q"], kc, vc, bt, lens, float(z["scale"]),
@@ -556,7 +561,7 @@ def _accuracy_snapshot(w, t, fmt: str, quant_scales) -> dict:
                            f"{G} query heads each, {len(blocks)} blocks"),
         "_samples": samples, "_qh": qh,
     }
-    if fmt == "fp8":
+    if fmt in ("fp8", "k16v8"):
         snap["k_scale"], snap["v_scale"] = np.array(quant_scales[0]), np.array(quant_scales[1])
     elif fmt == "int8":
         slot_idx = (idx[:, None] * K + torch.arange(K, device=idx.device)[None, :]).reshape(-1)
@@ -618,22 +623,30 @@ class DecodeCase:
             g = torch.Generator(device=dev)
             g.manual_seed(rank_seed(args.seed, rank) + 7)
             shape = t["k_cache"].shape
-            del t["k_cache"], t["v_cache"]
-            for nm in ("k_cache", "v_cache"):
+            # k16v8: the bf16 K pool stays, only V becomes one-byte codes
+            one_byte = ("v_cache",) if fmt == "k16v8" else ("k_cache", "v_cache")
+            for nm in one_byte:
+                del t[nm]
                 c = torch.randint(0, 256, shape, generator=g, device=dev, dtype=torch.int32)
                 c = torch.where((c & 0x7F) == 0x7F, c - 1, c).to(torch.uint8)
-                t[nm] = c if fmt == "fp8" else c.view(torch.int8)
+                t[nm] = c.view(torch.int8) if fmt == "int8" else c
             if fmt == "int8":
                 n = shape[0] * shape[1]
                 t["k_ts"] = torch.rand(n, generator=g, device=dev) * 0.02 + 0.001
                 t["v_ts"] = torch.rand(n, generator=g, device=dev) * 0.02 + 0.001
                 self.qd = ops.kv_quant("int8", k_token_scales=t["k_ts"],
                                        v_token_scales=t["v_ts"])
+            elif fmt == "k16v8":
+                scales = (1.0, 0.05)
+                self.qd = ops.kv_quant("k16v8", v_scale=scales[1])
             else:
                 scales = (0.05, 0.05)
                 self.qd = ops.kv_quant("fp8", *scales)
+            # K and V bytes per token row: 1 + 1, or 2 + 1 with the bf16 K pool
             self.kv_bytes = accounting.attention_kv_bytes(w.context_lens, w.num_kv_heads,
                                                           w.head_dim, 1)
+            if fmt == "k16v8":
+                self.kv_bytes = self.kv_bytes * 3 // 2
             if fmt == "int8":
                 self.kv_bytes += int(w.context_lens.sum()) * 2 * 4   # a K and a V scale per token
             ws_bytes = ops.attention_quant_workspace_bytes(w.num_seqs, w.num_q_heads,
@@ -654,18 +667,19 @@ class DecodeCase:
         attn_launches = ops.attention_launch_count(w.num_seqs, w.num_q_heads, w.num_kv_heads,
                                                    w.head_dim, w.block_size, max_len,
                                                    t["q"].dtype, share_prefix=self.share)
-        copy_launches = (1 if fmt != "int8" else 2) if self.has_copy else 0
+        copy_launches = (2 if fmt in ("int8", "k16v8") else 1) if self.has_copy else 0
         self.launches_per_step = copy_launches + 1 + attn_launches
-        pool_eb = w.elem_bytes if fmt == "bf16" else 1
+        pool_eb = pool_elem_bytes(fmt, w)
         n_new = int((w.positions >= 0).sum())
         self.row_fns = []
         if self.has_copy:
             self.row_fns.append(("kv_block_copy", self.copy_fn,
-                                 accounting.block_copy_bytes(len(w.copy_pairs), w.block_size,
-                                                             w.num_kv_heads, w.head_dim,
-                                                             pool_eb)))
+                                 int(accounting.block_copy_bytes(len(w.copy_pairs),
+                                                                 w.block_size, w.num_kv_heads,
+                                                                 w.head_dim, pool_eb))))
         self.row_fns.append(("paged_kv_append", self.append_fn,
-                             n_new * w.num_kv_heads * w.head_dim * 2 * (w.elem_bytes + pool_eb)))
+                             int(n_new * w.num_kv_heads * w.head_dim * 2 *
+                                 (w.elem_bytes + pool_eb))))
         self.row_fns.append(("paged_attention_decode", self.attention, self.kv_bytes))
 
     # ---- the step's calls (they read self.t / self.out when called) ----
@@ -863,7 +877,13 @@ def _e2e_case(case, timing: dict, K: int, use_graph: bool, stream, world: int) -
     return {"ms": e2e_ms, "h2d": h2d, "d2h": d2h}
 
 
-def unique_kv_bytes(w, pool_eb: int) -> int:
+def pool_elem_bytes(fmt: str, w) -> float:
+    """Mean bytes per K / V element of the pools: the workload's dtype, one
+    byte for FP8 / INT8, 1.5 for the bf16-K / FP8-V pair."""
+    return {"bf16": w.elem_bytes, "k16v8": 1.5}.get(fmt, 1)
+
+
+def unique_kv_bytes(w, pool_eb: float) -> int:
     """K and V bytes of the distinct token slots the step's sequences read
     (each physical slot once, however many tables point at its block)."""
     import numpy as np
@@ -874,7 +894,7 @@ def unique_kv_bytes(w, pool_eb: int) -> int:
         slots.append(w.block_tables[s][t // w.block_size].astype(np.int64) * w.block_size
                      + t % w.block_size)
     n = len(np.unique(np.concatenate(slots))) if slots else 0
-    return n * w.num_kv_heads * w.head_dim * 2 * pool_eb
+    return int(n * w.num_kv_heads * w.head_dim * 2 * pool_eb)
 
 
 def _roofline(case, attn_avg_ms: float, hbm: float, peak_src: str) -> dict:
@@ -889,7 +909,7 @@ def _roofline(case, attn_avg_ms: float, hbm: float, peak_src: str) -> dict:
     if shares_blocks(w):
         # the logical bytes count a shared block once per table that reads it;
         # DRAM need deliver each physical slot only once
-        ub = unique_kv_bytes(w, w.elem_bytes if case.fmt == "bf16" else 1)
+        ub = unique_kv_bytes(w, pool_elem_bytes(case.fmt, w))
         extra = {"unique_bytes_per_launch": ub,
                  "unique_GBps": ub / (attn_avg_ms * 1e-3) / 1e9,
                  "unique_frac": ub / (attn_avg_ms * 1e-3) / 1e9 / hbm,
@@ -995,8 +1015,9 @@ def run_gpu(args):
     cfg["parallelism"] = f"replicas x{world}" if world > 1 else "single GPU"
     cfg["launch"] = "CUDA graph replay (one graph per step)" if use_graph else "eager launches"
     blocks_used = int(sum(-(-int(L) // w.block_size) for L in w.context_lens))
-    pool_eb = w.elem_bytes if head["fmt"] == "bf16" else 1
-    cfg["kv_reserved_bytes"] = blocks_used * w.block_size * w.num_kv_heads * w.head_dim * 2 * pool_eb
+    pool_eb = pool_elem_bytes(head["fmt"], w)
+    cfg["kv_reserved_bytes"] = int(blocks_used * w.block_size * w.num_kv_heads * w.head_dim * 2 *
+                                   pool_eb)
     cfg["tail_waste_tokens"] = blocks_used * w.block_size - int(w.context_lens.sum())
     cfg["block_table_bytes"] = int(w.block_tables.nbytes)
     line = {
@@ -1622,9 +1643,9 @@ def main(argv=None):
     ap.add_argument("--also", default=DEFAULT_ALSO,
                     help="decode: comma-separated further workloads timed after the headline "
                          "one (same protocol, reported under \"workloads\"); '' for none")
-    ap.add_argument("--kv-format", choices=["bf16", "fp8", "int8"], default="bf16",
-                    help="KV pool storage: bf16, FP8 e4m3 (per-tensor scale) or INT8 "
-                         "(per-token scale)")
+    ap.add_argument("--kv-format", choices=["bf16", "fp8", "int8", "k16v8"], default="bf16",
+                    help="KV pool storage: bf16, FP8 e4m3 (per-tensor scale), INT8 "
+                         "(per-token scale), or k16v8 (bf16 K pool, FP8 V pool)")
     ap.add_argument("--block-size", type=int, default=0,
                     help="override the workload's block size (block-size sweep); 0 keeps it")
     ap.add_argument("--eager", action="store_true",

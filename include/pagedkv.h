@@ -287,8 +287,19 @@ PKV_API pkv_status pkv_selftest_wait_timeout(int64_t limit_cycles, void* stream)
  *   The tensor-core attention kernel forms each softmax weight times its
  *   token's V scale in f16: V scales must stay below 2048 (|v| below about
  *   260,000); larger ones may overflow to inf in the output.
+ * PKV_KV_BF16K_FP8V: K kept more precise than V ("19.2 KV Cache 系统化管理"
+ *   §19.2.4: K is the more sensitive of the two): the K pool holds bfloat16
+ *   values (2 bytes per element; a float32 K row is rounded to nearest even),
+ *   the V pool e4m3 codes of x / v_scale as in PKV_KV_FP8_E4M3 (k_scale is
+ *   not used).  The tensor-core kernel needs a block size that is a multiple
+ *   of 16; other shapes use the CUDA-core kernel.
  */
-typedef enum { PKV_KV_PLAIN = 0, PKV_KV_FP8_E4M3 = 1, PKV_KV_INT8_TOKEN = 2 } pkv_kv_format;
+typedef enum {
+  PKV_KV_PLAIN = 0,
+  PKV_KV_FP8_E4M3 = 1,
+  PKV_KV_INT8_TOKEN = 2,
+  PKV_KV_BF16K_FP8V = 3
+} pkv_kv_format;
 
 typedef struct {
   int32_t format;          /* pkv_kv_format */

@@ -233,11 +233,13 @@ pkv_status plan_attention_quant(int S, int H_q, int H_kv, int D, int K, int max_
     scales_ok = aligned(quant->k_token_scales, 16) && aligned(quant->v_token_scales, 16);
   const bool tc_ok = q_dt == PKV_BF16 && D == 128 && tc_shape_ok(H_q / H_kv, D, K, num_blocks,
                                                                   PKV_BF16) &&
-                     aligned_ok && scales_ok;
+                     aligned_ok && scales_ok &&
+                     (quant->format != PKV_KV_BF16K_FP8V || K % 16 == 0);
   if (c.kernel == 1 || (c.kernel == 0 && tc_ok)) {
     PKV_CHECK(tc_ok, PKV_ERR_UNSUPPORTED,
               "tensor-core kernel on a one-byte pool needs bf16 queries, head_dim 128, G <= 8, "
-              "block_size 8 or a multiple of 16 and 16-byte aligned pools and scales");
+              "block_size 8 or a multiple of 16 (a multiple of 16 with a bf16 K pool) and "
+              "16-byte aligned pools and scales");
     c.kernel = 1;
     c.share_prefix = 0;   // shared-prefix groups are a bf16-pool mode
     return plan_attention(S, H_q, H_kv, D, K, max_len, num_blocks, PKV_BF16, &c, true, plan);
@@ -459,14 +461,19 @@ pkv_status launch_tc_hpc(int hpc, const pkv::TcParams& prm, int n, int groups, c
 template <int D, int CT>
 pkv_status launch_tc_d(int hpc, int block_size, const pkv::TcParams& prm, int n, int groups,
                        cudaStream_t st, int dev) {
+  if constexpr (CT == 3) {
+    return launch_tc_hpc<D, CT, false>(hpc, prm, n, groups, st, dev);   // 16-row tiles only
+  }
   if constexpr (CT == 0) {
     if (prm.share_m > 1)
       return block_size < pkv::kTile
                  ? launch_tc_hpc<D, CT, true, true>(hpc, prm, n, groups, st, dev)
                  : launch_tc_hpc<D, CT, false, true>(hpc, prm, n, groups, st, dev);
   }
-  return block_size < pkv::kTile ? launch_tc_hpc<D, CT, true>(hpc, prm, n, groups, st, dev)
-                                 : launch_tc_hpc<D, CT, false>(hpc, prm, n, groups, st, dev);
+  if constexpr (CT != 3) {
+    return block_size < pkv::kTile ? launch_tc_hpc<D, CT, true>(hpc, prm, n, groups, st, dev)
+                                   : launch_tc_hpc<D, CT, false>(hpc, prm, n, groups, st, dev);
+  }
 }
 
 // Tensor map over a pool seen as [rows = num_blocks * K][H_kv][D] for the
@@ -578,6 +585,10 @@ pkv_status launch_simt_typed(const pkv_kv_quant* quant, int D, const void* q, co
     return launch_simt_q<T>(D, q, pkv::KvFp8{static_cast<const uint8_t*>(kc),
                                               static_cast<const uint8_t*>(vc), quant->k_scale,
                                               quant->v_scale}, out, a, st);
+  if (quant->format == PKV_KV_BF16K_FP8V)
+    return launch_simt_q<T>(D, q, pkv::KvBf16Fp8{static_cast<const __nv_bfloat16*>(kc),
+                                                  static_cast<const uint8_t*>(vc),
+                                                  quant->v_scale}, out, a, st);
   return launch_simt_q<T>(D, q, pkv::KvInt8{static_cast<const int8_t*>(kc),
                                              static_cast<const int8_t*>(vc),
                                              quant->k_token_scales, quant->v_token_scales},
@@ -688,12 +699,16 @@ pkv_status device_view(const void* p, const char* what, const void** out) {
 // Validates a quantized-pool description (token scales required for INT8).
 pkv_status check_quant(const pkv_kv_quant* q, bool need_token_scales) {
   PKV_CHECK(q != nullptr, PKV_ERR_INVALID_ARGUMENT, "null quant description");
-  PKV_CHECK(q->format == PKV_KV_FP8_E4M3 || q->format == PKV_KV_INT8_TOKEN,
-            PKV_ERR_INVALID_ARGUMENT, "quant format must be FP8_E4M3 or INT8_TOKEN");
+  PKV_CHECK(q->format == PKV_KV_FP8_E4M3 || q->format == PKV_KV_INT8_TOKEN ||
+                q->format == PKV_KV_BF16K_FP8V,
+            PKV_ERR_INVALID_ARGUMENT, "quant format must be FP8_E4M3, INT8_TOKEN or BF16K_FP8V");
   if (q->format == PKV_KV_FP8_E4M3) {
     PKV_CHECK(std::isfinite(q->k_scale) && std::isfinite(q->v_scale) && q->k_scale > 0.f &&
                   q->v_scale > 0.f,
               PKV_ERR_INVALID_ARGUMENT, "FP8 scales must be finite and > 0");
+  } else if (q->format == PKV_KV_BF16K_FP8V) {
+    PKV_CHECK(std::isfinite(q->v_scale) && q->v_scale > 0.f, PKV_ERR_INVALID_ARGUMENT,
+              "the FP8 V scale must be finite and > 0");
   } else if (need_token_scales) {
     PKV_CHECK(q->k_token_scales && q->v_token_scales, PKV_ERR_INVALID_ARGUMENT,
               "INT8 pools need per-token scale arrays");
@@ -923,6 +938,9 @@ pkv_status pkv_kv_append_quant(const void* k, const void* v, const int32_t* bloc
                       ks, vs, kts, vts, slot_mapping_out))
   if (quant->format == PKV_KV_FP8_E4M3) {
     if (in_dtype == PKV_BF16) PKV_LAUNCH_AQ(__nv_bfloat16, 1); else PKV_LAUNCH_AQ(float, 1);
+  } else if (quant->format == PKV_KV_BF16K_FP8V) {
+    PKV_CHECK(aligned(k_cache, 2), PKV_ERR_INVALID_ARGUMENT, "misaligned bf16 K pool");
+    if (in_dtype == PKV_BF16) PKV_LAUNCH_AQ(__nv_bfloat16, 3); else PKV_LAUNCH_AQ(float, 3);
   } else {
     if (in_dtype == PKV_BF16) PKV_LAUNCH_AQ(__nv_bfloat16, 2); else PKV_LAUNCH_AQ(float, 2);
   }
@@ -943,6 +961,14 @@ pkv_status pkv_kv_block_copy_quant(void* k_cache, void* v_cache, const int64_t* 
   PKV_CHECK(k_cache && v_cache && src_dst_pairs, PKV_ERR_INVALID_ARGUMENT, "null pointer");
   const int64_t blk = (int64_t)block_size * num_kv_heads * head_dim;
   cudaStream_t strm = as_stream(stream);
+  if (quant->format == PKV_KV_BF16K_FP8V) {
+    // two pools of different block sizes: K (2 bytes per element), then V
+    st = move_blocks(k_cache, nullptr, num_blocks, k_cache, nullptr, num_blocks, src_dst_pairs,
+                     num_pairs, 2 * blk, strm);
+    if (st != PKV_OK) return st;
+    return move_blocks(v_cache, nullptr, num_blocks, v_cache, nullptr, num_blocks,
+                       src_dst_pairs, num_pairs, blk, strm);
+  }
   st = copy_blocks(k_cache, v_cache, src_dst_pairs, num_pairs, num_blocks, blk, strm);
   if (st != PKV_OK) return st;
   if (quant->format == PKV_KV_INT8_TOKEN) {
@@ -1024,7 +1050,8 @@ pkv_status attention_impl(const void* q, const void* k_cache, const void* v_cach
   PKV_CHECK(aligned(workspace, 256), PKV_ERR_INVALID_ARGUMENT, "workspace must be 256-byte aligned");
   const size_t eb = elem_bytes(dtype);
   const size_t pool_eb = quant ? 1 : eb;
-  PKV_CHECK(aligned(q, eb) && aligned(out, eb) && aligned(k_cache, pool_eb) &&
+  const size_t k_eb = quant && quant->format == PKV_KV_BF16K_FP8V ? 2 : pool_eb;
+  PKV_CHECK(aligned(q, eb) && aligned(out, eb) && aligned(k_cache, k_eb) &&
                 aligned(v_cache, pool_eb),
             PKV_ERR_INVALID_ARGUMENT, "misaligned q/out/pool");
   PKV_CHECK((int64_t)max_blocks_per_seq * block_size <= 2147483647, PKV_ERR_UNSUPPORTED,
@@ -1042,14 +1069,16 @@ pkv_status attention_impl(const void* q, const void* k_cache, const void* v_cach
     st = device_facts(&dev, &sms);
     if (st != PKV_OK) return st;
     memset(&prm, 0, sizeof(prm));
+    // one-byte tiles for quantized pools, except the bf16 K pool of the pair
+    const bool k16 = quant != nullptr && quant->format == PKV_KV_BF16K_FP8V;
     st = encode_pool_map_heads(&prm.tmap_k, k_cache, num_blocks, block_size, H_kv, D, plan.hpc,
-                               quant != nullptr);
+                               quant != nullptr && !k16);
     if (st != PKV_OK) return st;
     st = encode_pool_map_heads(&prm.tmap_v, v_cache, num_blocks, block_size, H_kv, D, plan.hpc,
                                quant != nullptr);
     if (st != PKV_OK) return st;
     if (quant) {
-      prm.v_scale = quant->format == PKV_KV_FP8_E4M3 ? quant->v_scale : 1.f;
+      prm.v_scale = quant->format == PKV_KV_INT8_TOKEN ? 1.f : quant->v_scale;
       prm.k_ts = quant->k_token_scales;
       prm.v_ts = quant->v_token_scales;
     }
@@ -1094,6 +1123,9 @@ pkv_status attention_impl(const void* q, const void* k_cache, const void* v_cach
       } else if (quant->format == PKV_KV_FP8_E4M3) {
         prm.scale_log2 = (float)((double)scale * log2e * (double)quant->k_scale);
         st = launch_tc_d<128, 1>(plan.hpc, block_size, prm, plan.n_per_group, plan.groups, strm,
+                                 dev);
+      } else if (quant->format == PKV_KV_BF16K_FP8V) {
+        st = launch_tc_d<128, 3>(plan.hpc, block_size, prm, plan.n_per_group, plan.groups, strm,
                                  dev);
       } else {
         st = launch_tc_d<128, 2>(plan.hpc, block_size, prm, plan.n_per_group, plan.groups, strm,

@@ -36,6 +36,15 @@ struct KvFp8 {            // e4m3 codes, one scale per tensor
     return e4m3_to_f32(v[i]) * v_scale;
   }
 };
+struct KvBf16Fp8 {        // bf16 K pool, e4m3 V codes with one scale
+  const __nv_bfloat16* k;
+  const uint8_t* v;
+  float v_scale;
+  __device__ __forceinline__ float ld_k(int64_t i, int64_t) const { return __bfloat162float(k[i]); }
+  __device__ __forceinline__ float ld_v(int64_t i, int64_t) const {
+    return e4m3_to_f32(v[i]) * v_scale;
+  }
+};
 struct KvInt8 {           // int8 codes, one scale per token slot
   const int8_t* k;
   const int8_t* v;

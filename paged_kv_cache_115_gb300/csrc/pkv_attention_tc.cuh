@@ -41,8 +41,9 @@ constexpr int kTcMaxSeqs = 2048;
 constexpr int kTcMaxShareSeqs = 1024;
 constexpr int kBoxBytes = kTile * 128;
 
-// tokens per stream-K chunk for a pool format (0 bf16, 1 FP8, 2 INT8)
-constexpr int tc_chunk_tokens(int ct) { return ct ? 2 * kTile : kTile; }
+// tokens per stream-K chunk for a pool format (0 bf16, 1 FP8, 2 INT8,
+// 3 bf16 K with FP8 V)
+constexpr int tc_chunk_tokens(int ct) { return ct == 1 || ct == 2 ? 2 * kTile : kTile; }
 
 struct TcParams {
   CUtensorMap tmap_k;
@@ -79,7 +80,8 @@ struct TcParams {
 };
 
 // Pool formats of the kernel: CT 0 = bf16, 1 = FP8 e4m3 (per-tensor scale),
-// 2 = INT8 (per-slot scale).  A head's row is one 128-byte column group in a
+// 2 = INT8 (per-slot scale), 3 = bf16 K pool with an FP8 e4m3 V pool
+// (per-tensor V scale).  A head's row is one 128-byte column group in a
 // one-byte pool of D = 128, D / 64 groups in a bf16 pool.  One-byte tiles are read straight
 // into f16 mma fragments (e4m3 and int8 codes are exact in f16); bf16 tiles
 // go through ldmatrix into bf16 mma fragments.
@@ -141,29 +143,38 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
 
 template <int D, int HPC, int NS, int CT = 0, bool B8 = false>
 struct TcCfg {
-  static constexpr int TL = CT ? 2 : 1;                   // 16-row tiles per chunk
+  static constexpr bool KB = CT == 0 || CT == 3;          // K tiles in bf16
+  static constexpr bool VB = CT == 0;                     // V tiles in bf16
+  static constexpr int TL = CT == 1 || CT == 2 ? 2 : 1;   // 16-row tiles per chunk
   static constexpr int CH = kTile * TL;                   // tokens per chunk
-  static constexpr int NH = CT ? 1 : D / 64;              // boxes per head row
-  static constexpr int KPART = HPC * TL * NH * kBoxBytes;
-  static constexpr int SCALE_OFF = 2 * KPART;
+  static constexpr int NHK = KB ? D / 64 : 1;             // boxes per head row, K
+  static constexpr int NHV = VB ? D / 64 : 1;             // boxes per head row, V
+  static constexpr int NH = NHV;                          // (V tile rows, zeroed past the end)
+  static constexpr int KPART = HPC * TL * NHK * kBoxBytes;
+  static constexpr int VPART = HPC * TL * NHV * kBoxBytes;
+  static constexpr int SCALE_OFF = KPART + VPART;
   static constexpr int SCALE_BYTES = CT == 2 ? 2 * TL * kTile * 4 : 0;
-  static constexpr int STAGE = ((2 * KPART + SCALE_BYTES + 1023) / 1024) * 1024;
+  static constexpr int STAGE = ((KPART + VPART + SCALE_BYTES + 1023) / 1024) * 1024;
   static constexpr int THREADS = (HPC + 1) * 32;
   static constexpr int BAR_OFF = NS * STAGE;
   static constexpr int CSTART_OFF = BAR_OFF + 2 * NS * 8 + 16;
   static constexpr int SMEM = CSTART_OFF + (kTcMaxSeqs + 1) * 4 + 1024;  // + alignment slack
-  static constexpr uint32_t TX = 2 * KPART + SCALE_BYTES;  // bytes landing per stage
+  static constexpr uint32_t TX = KPART + VPART + SCALE_BYTES;  // bytes landing per stage
   static_assert(CT == 0 || D == 128, "one-byte pools need head_dim 128");
+  static_assert(CT != 3 || !B8, "the bf16-K / FP8-V pair needs 16-token tiles of one block");
   static_assert(tc_chunk_tokens(CT) == CH, "chunk size");
-  static constexpr int TBOX = HPC * NH * kBoxBytes;  // one tile, all heads of the CTA
-  static constexpr int UST = HPC * NH * 1024;        // B8: one block half of a tile, all heads
-  static constexpr int RSTEP8 = B8 ? UST : 1024;     // rows 8..15 relative to rows 0..7
-  static constexpr int HSTR = B8 ? 1024 : kBoxBytes; // column group stride
+  static constexpr int TBOXK = HPC * NHK * kBoxBytes;  // one tile, all heads of the CTA
+  static constexpr int TBOXV = HPC * NHV * kBoxBytes;
+  static constexpr int TBOX = TBOXK;                   // (formats with equal K and V tiles)
+  static constexpr int UST = HPC * NHK * 1024;         // B8: one block half of a tile, all heads
+  static constexpr int RSTEP8 = B8 ? UST : 1024;       // rows 8..15 relative to rows 0..7
+  static constexpr int HSTR = B8 ? 1024 : kBoxBytes;   // column group stride
   // smem offset of row 0 of head h's box (tile t, column group half) of K
-  // (kv 0) or V
+  // (kv 0) or V; the B8 layout exists for formats whose K and V tiles match
   __host__ __device__ static constexpr int box_off(int kv, int h, int t, int half) {
-    return B8 ? kv * KPART + t * 2 * UST + (h * NH + half) * 1024
-              : kv * KPART + t * TBOX + (h * NH + half) * kBoxBytes;
+    return B8 ? kv * KPART + t * 2 * UST + (h * NHK + half) * 1024
+              : (kv ? KPART + t * TBOXV + (h * NHV + half) * kBoxBytes
+                    : t * TBOXK + (h * NHK + half) * kBoxBytes);
   }
   // offset of row r (0..15) inside a box
   __host__ __device__ static constexpr int row_off(int r) { return (r & 7) * 128 + (r >> 3) * RSTEP8; }
@@ -476,7 +487,7 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
             const int kv = j / TL, t = j - kv * TL;
             const int rr = t ? r[TL - 1][0] : r[0][0];
             if (i < NB) {
-              tma_load_4d(smem_u32(sb + kv * C::KPART + t * C::TBOX), kv ? &p.tmap_v : &p.tmap_k,
+              tma_load_4d(smem_u32(sb + C::box_off(kv, 0, t, 0)), kv ? &p.tmap_v : &p.tmap_k,
                           bar_full + 8 * stage, 0, rr, 0, head0, policy);
             } else if constexpr (CT == 2) {
               // a tile with no rows reads slot 0's scales, which meet zero codes
@@ -537,7 +548,7 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
 #pragma unroll
       for (int nb = 0; nb < NB; ++nb)
         ulim = min(ulim, min(col_lim(8 * nb + 2 * tq), col_lim(8 * nb + 2 * tq + 1)));
-      if constexpr (CT == 0) {
+      if constexpr (C::KB) {
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb) {
           // this lane's B-fragment column 8 nb + g
@@ -652,7 +663,7 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
     for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
       for (int t = 0; t < TL; ++t) sacc[nb][t][0] = sacc[nb][t][1] = sacc[nb][t][2] = sacc[nb][t][3] = 0.f;
-    if constexpr (CT == 0) {
+    if constexpr (C::KB) {
       const int r = (lane & 7) + ((lane >> 3) & 1) * 8;
       const int chs = lane >> 4;
       const uint8_t* kt = sb + C::box_off(0, w, 0, 0);
@@ -739,7 +750,7 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
       }
       float pr[TL][4];
       float ps0 = 0.f, ps1 = 0.f;
-      if constexpr (CT == 0) {
+      if constexpr (CT == 0 || CT == 3) {
         const float mn0 = fmaxf(m0[nb], mx0), mn1 = fmaxf(m1[nb], mx1);
         // a column may have seen no visible key yet (several query rows): keep
         // its state (-inf, 0, 0) instead of forming -inf - -inf
@@ -811,7 +822,7 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
 #pragma unroll
       for (int t = 0; t < TL; ++t) {
         uint32_t ph01, pl01, ph23, pl23;
-        if constexpr (CT == 0) {
+        if constexpr (C::VB) {
           split_bf16x2(pr[t][0], pr[t][1], ph01, pl01);
           split_bf16x2(pr[t][2], pr[t][3], ph23, pl23);
         } else {
@@ -832,7 +843,7 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
     }
     // ---- O^T[D x 8] += V^T[D x 16 tok] . P^T[16 tok x 8], per tile and
     // column block (one V fragment feeds every column block)
-    if constexpr (CT != 0) {
+    if constexpr (!C::VB) {
       // byte tiles; the rows of each 16-row m tile are permuted: row g -> d =
       // 16 mt + 2g, row g + 8 -> d = 16 mt + 2g + 1.  ldmatrix.trans over 8
       // token rows x 16 bytes (byte pairs as 16-bit elements) hands this
@@ -851,7 +862,7 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
 #pragma unroll
           for (int uu = 0; uu < 2; ++uu) {
             // r[2uu]: tokens 2tq, 2tq+1 of m tile mt + uu; r[2uu+1]: tokens + 8
-            if constexpr (CT == 1) {
+            if constexpr (CT == 1 || CT == 3) {
               // one permute makes both pairs: bytes (0, 2) low, (1, 3) high
               e4m3x4_to_f16x2x2(__byte_perm(r[2 * uu], 0u, 0x3120), af[uu][0], af[uu][1]);
               e4m3x4_to_f16x2x2(__byte_perm(r[2 * uu + 1], 0u, 0x3120), af[uu][2], af[uu][3]);
@@ -912,7 +923,7 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
     if (c == ce - 1 || c == b - 1) {
       // ---- end of partition: write the final output or a partial state of
       // each valid column
-      if constexpr (CT == 1) {
+      if constexpr (CT == 1 || CT == 3) {
 #pragma unroll
         for (int mt = 0; mt < D / 16; ++mt)
 #pragma unroll
@@ -960,8 +971,8 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
 #pragma unroll
             for (int mt = 0; mt < D / 16; ++mt) {
               // O^T rows g and g+8 of tile mt are d0 and d1 (see the PV product)
-              const int d0 = CT == 0 ? mt * 16 + g : mt * 16 + 2 * g;
-              const int d1 = CT == 0 ? d0 + 8 : d0 + 1;
+              const int d0 = C::VB ? mt * 16 + g : mt * 16 + 2 * g;
+              const int d1 = C::VB ? d0 + 8 : d0 + 1;
               orow[d0] = __float2bfloat16_rn(o[nb][mt][col] * inv);
               orow[d1] = __float2bfloat16_rn(o[nb][mt][2 + col] * inv);
             }
@@ -971,8 +982,8 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
             float* orow = p.ws.o + pa * D;
 #pragma unroll
             for (int mt = 0; mt < D / 16; ++mt) {
-              const int d0 = CT == 0 ? mt * 16 + g : mt * 16 + 2 * g;
-              const int d1 = CT == 0 ? d0 + 8 : d0 + 1;
+              const int d0 = C::VB ? mt * 16 + g : mt * 16 + 2 * g;
+              const int d1 = C::VB ? d0 + 8 : d0 + 1;
               orow[d0] = o[nb][mt][col];
               orow[d1] = o[nb][mt][2 + col];
             }

@@ -164,7 +164,8 @@ __global__ void kv_append_varlen_kernel(const uint8_t* __restrict__ k,
 // a1 + a2 into a quantized pool.  grid = (tokens, 2 for K/V), 128 threads.
 // FMT 1: e4m3(x / scale) per element (per-tensor scale).  FMT 2: the token's
 // row (all heads) gets scale = max|x| / 127 and codes rint(x / scale), the
-// scale stored at the token's slot.  Divisions are IEEE float32 (__fdiv_rn).
+// scale stored at the token's slot.  FMT 3: K rows as bfloat16 (rounded to
+// nearest even), V rows as FMT 1.  Divisions are IEEE float32 (__fdiv_rn).
 constexpr int kQuantThreads = 128;
 
 template <typename TIN, int FMT>
@@ -202,7 +203,11 @@ kv_append_quant_kernel(const TIN* __restrict__ k, const TIN* __restrict__ v,
   if (slot < 0) return;
   const TIN* src = (z ? v : k) + i * row_elems;
   uint8_t* dst = (z ? v_cache : k_cache) + slot * row_elems;
-  if constexpr (FMT == 1) {
+  if (FMT == 3 && z == 0) {
+    __nv_bfloat16* kd = reinterpret_cast<__nv_bfloat16*>(k_cache) + slot * row_elems;
+    for (int64_t e = threadIdx.x; e < row_elems; e += blockDim.x)
+      kd[e] = __float2bfloat16_rn(to_f32(src[e]));
+  } else if constexpr (FMT == 1 || FMT == 3) {
     const float sc = z ? v_scale : k_scale;
     for (int64_t e = threadIdx.x; e < row_elems; e += blockDim.x)
       dst[e] = f32_to_e4m3(__fdiv_rn(to_f32(src[e]), sc));

@@ -50,7 +50,7 @@ class KvQuant(ctypes.Structure):
                 ("k_token_scales", c_vp), ("v_token_scales", c_vp)]
 
 
-KV_FP8_E4M3, KV_INT8_TOKEN = 1, 2
+KV_FP8_E4M3, KV_INT8_TOKEN, KV_BF16K_FP8V = 1, 2, 3
 
 
 def _sig(name, restype, *argtypes):
@@ -433,13 +433,17 @@ def get_device_error(device=None) -> int:
 def kv_quant(fmt: str, k_scale: float = 1.0, v_scale: float = 1.0,
              k_token_scales: Optional[torch.Tensor] = None,
              v_token_scales: Optional[torch.Tensor] = None) -> KvQuant:
-    """Describe a quantized pool: ``fmt`` "fp8" (scales per tensor) or "int8"
-    (float32 CUDA tensors of one scale per token slot).  The description
-    holds references to the scale tensors, so that their memory lives as
-    long as it does."""
+    """Describe a quantized pool: ``fmt`` "fp8" (scales per tensor), "int8"
+    (float32 CUDA tensors of one scale per token slot) or "k16v8" (a bf16 K
+    pool with an FP8 V pool of scale ``v_scale``).  The description holds
+    references to the scale tensors, so that their memory lives as long as
+    it does."""
     qd = KvQuant()
+    qd.fmt = fmt
     if fmt == "fp8":
         qd.format, qd.k_scale, qd.v_scale = KV_FP8_E4M3, float(k_scale), float(v_scale)
+    elif fmt == "k16v8":
+        qd.format, qd.k_scale, qd.v_scale = KV_BF16K_FP8V, 1.0, float(v_scale)
     elif fmt == "int8":
         for name, t in (("k_token_scales", k_token_scales), ("v_token_scales", v_token_scales)):
             if t is None:
@@ -454,8 +458,12 @@ def kv_quant(fmt: str, k_scale: float = 1.0, v_scale: float = 1.0,
     return qd
 
 
-def _need_pool(t: torch.Tensor, name: str) -> None:
+def _need_pool(t: torch.Tensor, name: str, quant: Optional[KvQuant] = None) -> None:
     _need(t, name, None, 4)
+    if quant is not None and quant.format == KV_BF16K_FP8V and name == "k_cache":
+        if t.dtype != torch.bfloat16:
+            raise TypeError("k_cache of a k16v8 pool pair must be bfloat16")
+        return
     if t.dtype not in (torch.uint8, torch.int8, getattr(torch, "float8_e4m3fn", torch.uint8)):
         raise TypeError(f"{name} must hold one-byte codes (uint8 / int8 / float8_e4m3fn)")
 
@@ -466,7 +474,7 @@ def paged_kv_append_quant(k: torch.Tensor, v: torch.Tensor, block_tables: torch.
                           quant: KvQuant,
                           slot_mapping_out: Optional[torch.Tensor] = None) -> None:
     """Slot mapping + quantized KV write in one launch (rows k, v in bf16/fp32)."""
-    _need_pool(k_cache, "k_cache")
+    _need_pool(k_cache, "k_cache", quant)
     _need_pool(v_cache, "v_cache")
     nb, K, H, D = k_cache.shape
     _need(k, "k", None, 3)
@@ -491,7 +499,7 @@ def paged_kv_append_quant(k: torch.Tensor, v: torch.Tensor, block_tables: torch.
 def kv_block_copy_quant(k_cache: torch.Tensor, v_cache: torch.Tensor,
                         src_dst_pairs: torch.Tensor, quant: KvQuant) -> None:
     """Copy-on-write block copy of a quantized pool (codes and, for INT8, scales)."""
-    _need_pool(k_cache, "k_cache")
+    _need_pool(k_cache, "k_cache", quant)
     _need_pool(v_cache, "v_cache")
     _need(src_dst_pairs, "src_dst_pairs", torch.int64, 2)
     nb, K, H, D = k_cache.shape
@@ -522,7 +530,7 @@ def paged_attention_decode_quant(q: torch.Tensor, k_cache: torch.Tensor, v_cache
                                  kernel: int = 0, num_splits: int = 0) -> torch.Tensor:
     """Decode attention over a quantized pool (values read back as code * scale)."""
     _need(q, "q", None, 3)
-    _need_pool(k_cache, "k_cache")
+    _need_pool(k_cache, "k_cache", quant)
     _need_pool(v_cache, "v_cache")
     _need(block_tables, "block_tables", torch.int32, 2)
     _need(context_lens, "context_lens", torch.int32, 1)

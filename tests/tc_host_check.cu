@@ -33,7 +33,7 @@
 template <int D, int HPC, int CT, bool B8>
 int check_layout() {
   using C = pkv::TcCfg<D, HPC, 2, CT, B8>;
-  constexpr int TL = C::TL, NH = C::NH;
+  constexpr int TL = C::TL;
   constexpr int box_rows = B8 ? 8 : 16;
   constexpr int parts = B8 ? 2 : 1;   // copies per (tensor, tile)
   int errors = 0;
@@ -48,7 +48,11 @@ int check_layout() {
   for (int kv = 0; kv < 2; ++kv)
     for (int t = 0; t < TL; ++t)
       for (int u = 0; u < parts; ++u) {
-        const int dst = B8 ? kv * C::KPART + (2 * t + u) * C::UST : kv * C::KPART + t * C::TBOX;
+        // K boxes, then V boxes (a V tile is smaller than a K tile when V is
+        // one-byte and K bf16)
+        const int NH = kv ? C::NHV : C::NHK;
+        const int dst = B8 ? kv * C::KPART + (2 * t + u) * C::UST
+                           : (kv ? C::KPART + t * C::TBOXV : t * C::TBOXK);
         for (int h = 0; h < HPC; ++h)
           for (int hf = 0; hf < NH; ++hf)
             for (int rr = 0; rr < box_rows; ++rr) {
@@ -222,10 +226,11 @@ int main() {
   errors += check_hpc<128, 0, false>() + check_hpc<128, 0, true>();
   errors += check_hpc<128, 1, false>() + check_hpc<128, 1, true>();
   errors += check_hpc<128, 2, false>() + check_hpc<128, 2, true>();
+  errors += check_hpc<128, 3, false>();
   if (errors) {
     std::printf("errors: %d\n", errors);
     return 1;
   }
-  std::printf("layout ok: 32 configurations; stream-K ok; shared-prefix units ok\n");
+  std::printf("layout ok: 36 configurations; stream-K ok; shared-prefix units ok\n");
   return 0;
 }

@@ -36,18 +36,21 @@ def ops():
     return o
 
 
-@pytest.mark.parametrize("fmt", ["fp8", "int8"])
+@pytest.mark.parametrize("fmt", ["fp8", "int8", "k16v8"])
 def test_quant_full_size(ops, fmt):
     w = wl.build("mistral_7b")
     rng = np.random.default_rng(17)
     nb, K, H, D = w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim
     shape = (nb, K, H, D)
-    if fmt == "fp8":
+    if fmt in ("fp8", "k16v8"):
         kc = rng.integers(0, 256, size=shape, dtype=np.uint8)
         vc = rng.integers(0, 256, size=shape, dtype=np.uint8)
         kc[(kc & 0x7F) == 0x7F] -= 1                    # no NaN codes
         vc[(vc & 0x7F) == 0x7F] -= 1
         kts = vts = None
+        if fmt == "k16v8":    # K: bf16 patterns of N(0, 1) draws
+            kc = (rng.standard_normal(shape, dtype=np.float32).view(np.uint32) >> 16).astype(
+                np.uint16)
     else:
         kc = rng.integers(-127, 128, size=shape, dtype=np.int8)
         vc = rng.integers(-127, 128, size=shape, dtype=np.int8)
@@ -60,7 +63,9 @@ def test_quant_full_size(ops, fmt):
     dk, dv = torch.from_numpy(kc).to(DEV), torch.from_numpy(vc).to(DEV)
     if fmt == "fp8":
         qd = ops.kv_quant("fp8", 0.05, 0.07)
-        scales = dict(k_scale=0.05, v_scale=0.07)
+    elif fmt == "k16v8":
+        dk = torch.from_numpy(kc.view(np.int16)).view(torch.bfloat16).to(DEV)
+        qd = ops.kv_quant("k16v8", v_scale=0.07)
     else:
         dkt, dvt = torch.from_numpy(kts.copy()).to(DEV), torch.from_numpy(vts.copy()).to(DEV)
         qd = ops.kv_quant("int8", k_token_scales=dkt, v_token_scales=dvt)
@@ -79,19 +84,25 @@ def test_quant_full_size(ops, fmt):
     if fmt == "fp8":
         sk = np.zeros((w.num_seqs, 1, H, D), np.uint8)
         okc, ovc = Q.kv_write_fp8(sk, sk.copy(), kf, vf, idx, 0.05, 0.07)
+    elif fmt == "k16v8":
+        okc, ovc = Q.kv_write_k16v8(np.zeros((w.num_seqs, 1, H, D), np.uint16),
+                                    np.zeros((w.num_seqs, 1, H, D), np.uint8), kf, vf, idx, 0.07)
     else:
         sk = np.zeros((w.num_seqs, 1, H, D), np.int8)
         okc, ovc, okts, ovts = Q.kv_write_int8(sk, sk.copy(), np.zeros(w.num_seqs, np.float32),
                                                np.zeros(w.num_seqs, np.float32), kf, vf, idx)
-    got_k = dk.view(-1, H, D)[torch.from_numpy(slots).to(DEV)].cpu().numpy()
+    got_k = storage(dk.view(-1, H, D)[torch.from_numpy(slots).to(DEV)])
     got_v = dv.view(-1, H, D)[torch.from_numpy(slots).to(DEV)].cpu().numpy()
     assert np.array_equal(got_k, okc[:, 0]) and np.array_equal(got_v, ovc[:, 0])
-    kc_now = dk.cpu().numpy()
-    vc_now = dv.cpu().numpy()
+    # the pool as the oracle's own write leaves it (the rows just checked)
+    kc_now, vc_now = kc.copy(), vc.copy()
+    kc_now.reshape(-1, H, D)[slots] = okc[:, 0]
+    vc_now.reshape(-1, H, D)[slots] = ovc[:, 0]
     if fmt == "int8":
         assert np.array_equal(dkt.cpu().numpy()[slots], okts)
         assert np.array_equal(dvt.cpu().numpy()[slots], ovts)
-        kts_now, vts_now = dkt.cpu().numpy(), dvt.cpu().numpy()
+        kts_now, vts_now = kts.copy(), vts.copy()
+        kts_now[slots], vts_now[slots] = okts, ovts
     outf = as_f64(out)
     assert np.all(np.isfinite(outf))
     # every output row against the oracle over the pool as it now stands
@@ -99,6 +110,9 @@ def test_quant_full_size(ops, fmt):
     if fmt == "fp8":
         ref = Q.paged_attention_decode_quant(qn, kc_now, vc_now, w.block_tables, w.context_lens,
                                              w.scale, "bf16", "fp8", k_scale=0.05, v_scale=0.07)
+    elif fmt == "k16v8":
+        ref = Q.paged_attention_decode_quant(qn, kc_now, vc_now, w.block_tables, w.context_lens,
+                                             w.scale, "bf16", "k16v8", v_scale=0.07)
     else:
         ref = Q.paged_attention_decode_quant(qn, kc_now, vc_now, w.block_tables, w.context_lens,
                                              w.scale, "bf16", "int8", k_tok_scales=kts_now,

@@ -1,6 +1,7 @@
 """GPU parity of the quantized KV cache (FP8 e4m3 per-tensor scale, INT8 per
-token) against the oracle: quantized writes and copies bit-exact (codes and
-scales), attention within the tolerance of the plain path."""
+token, and the pair that keeps K in bf16 with V in FP8) against the oracle:
+quantized writes and copies bit-exact (codes, bf16 patterns and scales),
+attention within the tolerance of the plain path."""
 
 import numpy as np
 import pytest
@@ -95,10 +96,21 @@ def test_int8_append_bit_exact(ops, in_dtype):
     assert np.array_equal(d[3].cpu().numpy().view(np.uint32), evt.view(np.uint32))
 
 
-@pytest.mark.parametrize("fmt", ["fp8", "int8"])
+@pytest.mark.parametrize("fmt", ["fp8", "int8", "k16v8"])
 def test_quant_block_copy(ops, fmt):
     rng = np.random.default_rng(2)
     nb, K, H, D = 12, 16, 8, 128
+    if fmt == "k16v8":        # bf16 K pool (2 bytes per element), one-byte V pool
+        kc = torch.from_numpy(rng.integers(0, 2**16, size=(nb, K, H, D), dtype=np.uint16)
+                              .view(np.int16)).view(torch.bfloat16)
+        vc = torch.from_numpy(rng.integers(0, 256, size=(nb, K, H, D), dtype=np.uint8))
+        pairs = np.array([[0, 5], [3, 9], [11, 2]], dtype=np.int64)
+        dk, dv = kc.to(DEV), vc.to(DEV)
+        ops.kv_block_copy_quant(dk, dv, torch.from_numpy(pairs).to(DEV), ops.kv_quant("k16v8"))
+        assert ops.get_device_error() == 0
+        ek, ev = oracle.kv_block_copy(storage(kc), vc.numpy(), pairs)
+        assert np.array_equal(storage(dk), ek) and np.array_equal(dv.cpu().numpy(), ev)
+        return
     kc = torch.from_numpy(rng.integers(0, 256, size=(nb, K, H, D), dtype=np.uint8))
     vc = torch.from_numpy(rng.integers(0, 256, size=(nb, K, H, D), dtype=np.uint8))
     kts = torch.from_numpy(rng.standard_normal(nb * K).astype(np.float32))
@@ -129,7 +141,7 @@ def quant_problem(fmt, lens, H_q, H_kv, D, K, q_dtype, seed):
     nb, hist = w.num_blocks, w.history_mask
     shape = (nb, K, H_kv, D)
     c = wl.materialize(w, seed=seed, canary=False)
-    if fmt == "fp8":
+    if fmt in ("fp8", "k16v8"):
         vals = Q.e4m3_values()
         ok = np.array([i for i in range(256) if np.isfinite(vals[i]) and abs(vals[i]) <= 8],
                       np.uint8)
@@ -137,6 +149,10 @@ def quant_problem(fmt, lens, H_q, H_kv, D, K, q_dtype, seed):
         vc = rng.choice(ok, size=shape).astype(np.uint8)
         kc[~hist] = 0x7F
         vc[~hist] = 0x7F
+        if fmt == "k16v8":    # K: bf16 patterns of N(0, 1) draws, NaN without history
+            kc = (rng.standard_normal(shape).astype(np.float32).view(np.uint32) >> 16).astype(
+                np.uint16)
+            kc[~hist] = 0x7FC1
         return w, c, kc, vc, None, None
     kc = rng.integers(-127, 128, size=shape).astype(np.int8)
     vc = rng.integers(-127, 128, size=shape).astype(np.int8)
@@ -150,7 +166,7 @@ def quant_problem(fmt, lens, H_q, H_kv, D, K, q_dtype, seed):
 SHAPES = [(128, 4, 16), (64, 2, 4), (128, 8, 32)]
 
 
-@pytest.mark.parametrize("fmt", ["fp8", "int8"])
+@pytest.mark.parametrize("fmt", ["fp8", "int8", "k16v8"])
 @pytest.mark.parametrize("q_dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("D,G,K", SHAPES)
 @pytest.mark.parametrize("num_splits", [0, 64])
@@ -159,7 +175,7 @@ def test_quant_step_matches_oracle(ops, fmt, q_dtype, D, G, K, num_splits):
                    num_splits=num_splits)
 
 
-@pytest.mark.parametrize("fmt", ["fp8", "int8"])
+@pytest.mark.parametrize("fmt", ["fp8", "int8", "k16v8"])
 @pytest.mark.parametrize("kernel", [1, 2])
 @pytest.mark.parametrize("num_splits", [0, 3, 40])
 def test_quant_tensor_core_and_cuda_core(ops, fmt, kernel, num_splits):
@@ -168,10 +184,35 @@ def test_quant_tensor_core_and_cuda_core(ops, fmt, kernel, num_splits):
                    num_splits=num_splits)
 
 
-@pytest.mark.parametrize("fmt", ["fp8", "int8"])
+@pytest.mark.parametrize("fmt", ["fp8", "int8", "k16v8"])
 @pytest.mark.parametrize("G,K,H_kv", [(8, 32, 8), (2, 64, 4), (1, 16, 1), (4, 8, 8), (2, 8, 2)])
 def test_quant_tensor_core_shapes(ops, fmt, G, K, H_kv):
-    run_quant_step(ops, fmt, "bf16", 128, G, K, [5, 130, 1000, 64], H_kv=H_kv, kernel=1)
+    # the bf16-K / FP8-V pair has no 8-token-block tiles: automatic plan there
+    kern = 0 if fmt == "k16v8" and K == 8 else 1
+    run_quant_step(ops, fmt, "bf16", 128, G, K, [5, 130, 1000, 64], H_kv=H_kv, kernel=kern)
+
+
+@pytest.mark.parametrize("in_dtype", [torch.bfloat16, torch.float32])
+def test_k16v8_append_bit_exact(ops, in_dtype):
+    """K rows stored as bfloat16 (float32 input rounded to nearest even, bf16
+    input copied), V rows as e4m3 codes of x / v_scale."""
+    rng = np.random.default_rng(5)
+    T, H, D, K, nb = 150, 8, 128, 16, 170
+    mags = 10.0 ** rng.uniform(-3, 3, size=(T, 1, 1))
+    k = torch.from_numpy((rng.standard_normal((T, H, D)) * mags).astype(np.float32)).to(in_dtype)
+    v = torch.from_numpy((rng.standard_normal((T, H, D)) * mags).astype(np.float32)).to(in_dtype)
+    bt, pos = identity_tables(T, K, nb, rng)
+    pos[4] = -1
+    kc = torch.full((nb, K, H, D), float("nan"), dtype=torch.bfloat16)
+    vc = torch.full((nb, K, H, D), 0x7F, dtype=torch.uint8)
+    dk, dv = kc.to(DEV), vc.to(DEV)
+    qd = ops.kv_quant("k16v8", v_scale=0.3)
+    ops.paged_kv_append_quant(k.to(DEV), v.to(DEV), torch.from_numpy(bt).to(DEV),
+                              torch.from_numpy(pos).to(DEV), dk, dv, qd)
+    assert ops.get_device_error() == 0
+    slots = oracle.slot_mapping(bt, pos, K)
+    ek, ev = Q.kv_write_k16v8(storage(kc), vc.numpy(), f32_rows(k), f32_rows(v), slots, 0.3)
+    assert np.array_equal(storage(dk), ek) and np.array_equal(dv.cpu().numpy(), ev)
 
 
 def run_quant_step(ops, fmt, q_dtype, D, G, K, lens, H_kv=2, **attn_kw):
@@ -181,6 +222,10 @@ def run_quant_step(ops, fmt, q_dtype, D, G, K, lens, H_kv=2, **attn_kw):
     if fmt == "fp8":
         qd = ops.kv_quant("fp8", 0.5, 1.5)
         scales = dict(k_scale=0.5, v_scale=1.5)
+    elif fmt == "k16v8":
+        dkc = torch.from_numpy(kc.view(np.int16)).view(torch.bfloat16).to(DEV)
+        qd = ops.kv_quant("k16v8", v_scale=1.5)
+        scales = dict(v_scale=1.5)
     else:
         dkt, dvt = torch.from_numpy(kts.copy()).to(DEV), torch.from_numpy(vts.copy()).to(DEV)
         qd = ops.kv_quant("int8", k_token_scales=dkt, v_token_scales=dvt)
@@ -197,13 +242,17 @@ def run_quant_step(ops, fmt, q_dtype, D, G, K, lens, H_kv=2, **attn_kw):
         okc, ovc = Q.kv_write_fp8(kc, vc, f32_rows(c["k_new"]), f32_rows(c["v_new"]), slots,
                                   0.5, 1.5)
         tok = {}
+    elif fmt == "k16v8":
+        okc, ovc = Q.kv_write_k16v8(kc, vc, f32_rows(c["k_new"]), f32_rows(c["v_new"]), slots,
+                                    1.5)
+        tok = {}
     else:
         okc, ovc, okt, ovt = Q.kv_write_int8(kc, vc, kts, vts, f32_rows(c["k_new"]),
                                              f32_rows(c["v_new"]), slots)
         scales = {}
         tok = dict(k_tok_scales=okt, v_tok_scales=ovt)
         assert np.array_equal(dkt.cpu().numpy().view(np.uint32), okt.view(np.uint32))
-    assert np.array_equal(dkc.cpu().numpy(), okc) and np.array_equal(dvc.cpu().numpy(), ovc)
+    assert np.array_equal(storage(dkc), okc) and np.array_equal(dvc.cpu().numpy(), ovc)
     ref = Q.paged_attention_decode_quant(storage(c["q"]), okc, ovc, w.block_tables,
                                          w.context_lens, w.scale, q_dtype, fmt, **scales, **tok)
     check_attention(as_f64(out), ref, q_dtype, f"{fmt} {q_dtype} D{D} G{G} K{K} {attn_kw}")
