@@ -138,7 +138,10 @@ struct AttnPlan {
   int hpc = 0, groups = 0, n_per_group = 0;  // tensor-core kernel
   int ps = 0;                                // CUDA-core kernel: tokens per partition
   int share_m = 1;                           // tensor-core kernel: sequences per shared-prefix group
-  int pmax = 1;
+  int pmax = 1;                              // partials per row (CUDA-core / multi-query layout)
+  int64_t slots = 0;                         // partial slots of the workspace
+  int64_t slot_stride = 0;                   // tensor-core kernel: slots per member region
+  bool reduce = false;                       // a split-K reduce launch follows
   int seq_batch = 0;
   size_t ws_bytes = 0;
 };
@@ -156,6 +159,23 @@ int tc_hpc(int H_kv) {
   for (int h : {8, 4, 2, 1})
     if (H_kv % h == 0) return h;
   return 1;
+}
+
+// Workspace layout of a decode plan: meta (one int4 per row of a launch
+// batch), the partial (m, l) pairs and outputs per slot, then (shared-prefix
+// groups) the groups' shared lengths.
+struct WsLayout {
+  size_t ml, o, glen, total;
+};
+WsLayout ws_layout(const AttnPlan& p, int H_q, int H_kv, int D) {
+  const size_t sb = (size_t)std::max(p.seq_batch, 1);
+  WsLayout l;
+  l.ml = align256(sb * sizeof(int4));
+  l.o = l.ml + align256((size_t)p.slots * H_q * sizeof(float2));
+  l.glen = l.o + align256((size_t)p.slots * H_q * (size_t)D * sizeof(float));
+  l.total = l.glen + (p.share_m > 1 ? align256(ceil_div((int64_t)sb, p.share_m) * 4) : 0);
+  (void)H_kv;
+  return l;
 }
 
 pkv_status plan_attention(int S, int H_q, int H_kv, int D, int K, int max_len, int64_t num_blocks,
@@ -193,9 +213,13 @@ pkv_status plan_attention(int S, int H_q, int H_kv, int D, int K, int max_len, i
       // groups of 16 / G sequences fill the kernel's two 8-column blocks; a
       // sequence's partials are its group's shared unit's, then its own's
       p.share_m = 16 / G;
-      p.pmax *= 2;
       p.seq_batch = std::min(S, pkv::kTcMaxShareSeqs);
     }
+    // decode partials: slot CTA + unit (one region per member of a shared
+    // unit); any sequence of two or more chunks may be split
+    p.slot_stride = (int64_t)p.n_per_group + pkv::tc_num_units(std::max(p.seq_batch, 1), p.share_m);
+    p.slots = p.slot_stride * p.share_m;   // a region per member of a shared unit
+    p.reduce = max_chunks > 1;
   } else {
     PKV_CHECK(simt_shape_ok(G, D), PKV_ERR_UNSUPPORTED,
               "unsupported shape: head_dim must be 32/64/128/256 and G <= 16");
@@ -206,11 +230,10 @@ pkv_status plan_attention(int S, int H_q, int H_kv, int D, int K, int max_len, i
     p.pmax = std::max<int>(1, (int)ceil_div(max_len, p.ps));
     PKV_CHECK(p.pmax <= 2147483647 / 2, PKV_ERR_UNSUPPORTED, "too many partitions");
     p.seq_batch = std::min(S, 65535);
+    p.slots = (int64_t)std::max(p.seq_batch, 1) * p.pmax;
+    p.reduce = p.pmax > 1;
   }
-  const size_t sb = (size_t)std::max(p.seq_batch, 1);
-  p.ws_bytes = align256(sb * 4) + align256(sb * p.pmax * H_q * sizeof(float2)) +
-               align256(sb * p.pmax * H_q * (size_t)D * sizeof(float));
-  if (p.share_m > 1) p.ws_bytes += align256(ceil_div((int64_t)sb, p.share_m) * 4);
+  p.ws_bytes = ws_layout(p, H_q, H_kv, D).total;
   *plan = p;
   return PKV_OK;
 }
@@ -249,25 +272,20 @@ pkv_status plan_attention_quant(int S, int H_q, int H_kv, int D, int K, int max_
   return plan_attention(S, H_q, H_kv, D, K, max_len, 1, q_dt, &c, false, plan);
 }
 
-pkv::Workspace carve_workspace(void* ws, const AttnPlan& p, int H_q, int D) {
-  const size_t sb = (size_t)std::max(p.seq_batch, 1);
+pkv::Workspace carve_workspace(void* ws, const AttnPlan& p, int H_q, int H_kv, int D) {
+  const WsLayout l = ws_layout(p, H_q, H_kv, D);
   uint8_t* b = static_cast<uint8_t*>(ws);
   pkv::Workspace w;
-  w.nparts = reinterpret_cast<int*>(b);
-  b += align256(sb * 4);
-  w.ml = reinterpret_cast<float2*>(b);
-  b += align256(sb * p.pmax * H_q * sizeof(float2));
-  w.o = reinterpret_cast<float*>(b);
+  w.meta = reinterpret_cast<int4*>(b);
+  w.ml = reinterpret_cast<float2*>(b + l.ml);
+  w.o = reinterpret_cast<float*>(b + l.o);
   w.pmax = p.pmax;
   return w;
 }
 
 // Shared-prefix mode: the per-group shared lengths follow the partial outputs.
-int* carve_glen(void* ws, const AttnPlan& p, int H_q, int D) {
-  const size_t sb = (size_t)std::max(p.seq_batch, 1);
-  return reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + align256(sb * 4) +
-                                align256(sb * p.pmax * H_q * sizeof(float2)) +
-                                align256(sb * p.pmax * H_q * (size_t)D * sizeof(float)));
+int* carve_glen(void* ws, const AttnPlan& p, int H_q, int H_kv, int D) {
+  return reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + ws_layout(p, H_q, H_kv, D).glen);
 }
 
 // ---- tensor-core kernel dispatch ------------------------------------------------
@@ -396,7 +414,7 @@ pkv_status plan_prefill(int num_seqs, int num_tokens, int max_query_len, int max
     if (st != PKV_OK) return st;
     p.dec = true;
     const size_t T = (size_t)num_tokens;
-    p.ws_bytes = align256(T * 4) + align256(T * p.ap.pmax * H_q * sizeof(float2)) +
+    p.ws_bytes = align256(T * sizeof(int4)) + align256(T * p.ap.pmax * H_q * sizeof(float2)) +
                  align256(T * p.ap.pmax * H_q * (size_t)D * sizeof(float));
     *out = p;
     return PKV_OK;
@@ -437,7 +455,7 @@ pkv_status plan_prefill(int num_seqs, int num_tokens, int max_query_len, int max
   PKV_CHECK(p.tiles * p.nsp <= 2147483647, PKV_ERR_UNSUPPORTED, "too many query rows");
   if (p.nsp > 1) {
     const size_t T = (size_t)num_tokens;
-    p.ws_bytes = align256(T * 4) + align256(T * p.nsp * H_q * sizeof(float2)) +
+    p.ws_bytes = align256(T * sizeof(int4)) + align256(T * p.nsp * H_q * sizeof(float2)) +
                  align256(T * p.nsp * H_q * (size_t)D * sizeof(float));
   }
   *out = p;
@@ -1015,7 +1033,8 @@ pkv_status pkv_attention_launch_count(int32_t num_seqs, int32_t num_q_heads,
                                  max_context_len, 1, dtype, config, true, &plan);
   if (st != PKV_OK) return st;
   const int batches = num_seqs == 0 ? 0 : (int)ceil_div(num_seqs, plan.seq_batch);
-  *launches = batches * ((plan.pmax > 1 ? 2 : 1) + (plan.share_m > 1 ? 1 : 0));
+  // partition (+ split-K reduce) (+ the table comparison of share_prefix)
+  *launches = batches * (1 + (plan.reduce ? 1 : 0) + (plan.share_m > 1 ? 1 : 0));
   return PKV_OK;
 }
 
@@ -1059,7 +1078,7 @@ pkv_status attention_impl(const void* q, const void* k_cache, const void* v_cach
   const double log2e = 1.4426950408889634;
   const float sl = (float)((double)scale * log2e);
   cudaStream_t strm = as_stream(stream);
-  pkv::Workspace ws = carve_workspace(workspace, plan, num_q_heads, head_dim);
+  pkv::Workspace ws = carve_workspace(workspace, plan, num_q_heads, num_kv_heads, head_dim);
   const int D = head_dim, H_q = num_q_heads, H_kv = num_kv_heads;
 
   pkv::TcParams prm;
@@ -1104,10 +1123,11 @@ pkv_status attention_impl(const void* q, const void* k_cache, const void* v_cach
       prm.block_size = block_size;
       prm.scale_log2 = sl;
       prm.share_m = plan.share_m;
+      prm.slot_stride = plan.share_m > 1 ? (int)plan.slot_stride : 0;
       prm.glen = nullptr;
       if (plan.share_m > 1) {
         // the groups' shared lengths, from the table rows
-        int* glen = carve_glen(workspace, plan, H_q, D);
+        int* glen = carve_glen(workspace, plan, H_q, H_kv, D);
         const int ngroups = (int)ceil_div(S, plan.share_m);
         PKV_CUDA(launch_pdl(pkv::share_prefix_kernel,
                             dim3((unsigned)ceil_div(ngroups, pkv::kShareWarps)),
@@ -1137,7 +1157,7 @@ pkv_status attention_impl(const void* q, const void* k_cache, const void* v_cach
       st = launch_simt_any(dtype, quant, D, qb, k_cache, v_cache, ob, a, strm);
     }
     if (st != PKV_OK) return st;
-    if (plan.pmax > 1) {
+    if (plan.reduce) {
       st = dtype == PKV_BF16
                ? launch_reduce<__nv_bfloat16>(D, ws, S, H_q, ob, strm)
                : launch_reduce<float>(D, ws, S, H_q, ob, strm);
@@ -1320,8 +1340,8 @@ pkv_status pkv_attention_prefill(const void* q, const void* k_cache, const void*
     tp.cu_seqlens = cu_seqlens;
     uint8_t* b = static_cast<uint8_t*>(workspace);
     const size_t T = (size_t)num_tokens;
-    tp.ws.nparts = reinterpret_cast<int*>(b);
-    b += align256(T * 4);
+    tp.ws.meta = reinterpret_cast<int4*>(b);
+    b += align256(T * sizeof(int4));
     tp.ws.ml = reinterpret_cast<float2*>(b);
     b += align256(T * plan.ap.pmax * num_q_heads * sizeof(float2));
     tp.ws.o = reinterpret_cast<float*>(b);
@@ -1349,8 +1369,8 @@ pkv_status pkv_attention_prefill(const void* q, const void* k_cache, const void*
   if (plan.nsp > 1) {
     uint8_t* b = static_cast<uint8_t*>(workspace);
     const size_t T = (size_t)num_tokens;
-    prm.ws.nparts = reinterpret_cast<int*>(b);
-    b += align256(T * 4);
+    prm.ws.meta = reinterpret_cast<int4*>(b);
+    b += align256(T * sizeof(int4));
     prm.ws.ml = reinterpret_cast<float2*>(b);
     b += align256(T * plan.nsp * num_q_heads * sizeof(float2));
     prm.ws.o = reinterpret_cast<float*>(b);

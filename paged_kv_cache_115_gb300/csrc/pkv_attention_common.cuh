@@ -12,11 +12,16 @@
 // (s, h) are merged by attn_reduce_kernel with
 //   M = max m_p,  l = sum l_p 2^(m_p - M),  out = sum o_p 2^(m_p - M) / l.
 //
-// Workspace layout (per launch batch of sequences, Pmax partials per seq):
-//   int    nparts[S]                   partials written for s (0: empty seq,
-//                                      1: output already final)
-//   float2 ml[S][Pmax][H_q]            (m, l) of each partial
-//   float  o [S][Pmax][H_q][D]         unnormalised partial outputs
+// Workspace (per launch batch): partial states live in slots, slot x holding
+// (m, l) at ml[x * H_q + h] and o at o[(x * H_q + h) * D]; meta[r] =
+// (base1, n1, base2, n2) says that output row r (a sequence, or a query row)
+// has its partials in slots base1 .. base1 + n1 - 1 and base2 .. base2 + n2 - 1
+// (n1 + n2 <= 1: the partition kernel wrote the output itself).
+//   CUDA-core kernel, multi-query launches: row r's partial p in slot
+//     r * pmax + p;
+//   tensor-core decode kernel: the partition of CTA i over unit u in slot
+//     i + u (a unit's CTAs are consecutive, so are its slots); a shared unit
+//     keeps one region of slots per member sequence.
 #pragma once
 
 #include "pkv_device.cuh"
@@ -24,7 +29,7 @@
 namespace pkv {
 
 struct Workspace {
-  int* nparts;
+  int4* meta;
   float2* ml;
   float* o;
   int pmax;

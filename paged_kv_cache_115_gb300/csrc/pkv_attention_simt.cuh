@@ -76,7 +76,7 @@ attn_simt_kernel(const T* __restrict__ q, KV kv, const int32_t* __restrict__ blo
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int L = effective_len(context_lens[s], max_len, max_blocks_per_seq * K);
   const int np = (L + PS - 1) / PS;
-  if (p == 0 && j == 0 && threadIdx.x == 0) ws.nparts[s] = np;
+  if (p == 0 && j == 0 && threadIdx.x == 0) ws.meta[s] = make_int4(s * ws.pmax, np, 0, 0);
   if (L == 0) {
     if (p == 0) {
       for (int i = threadIdx.x; i < G * D; i += blockDim.x)

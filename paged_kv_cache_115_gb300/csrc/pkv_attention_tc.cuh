@@ -77,6 +77,9 @@ struct TcParams {
   // of 16, written by share_prefix_kernel).  share_m = 1 otherwise.
   int share_m;
   const int* glen;
+  // decode: slot distance between the member regions of a shared unit (CTAs
+  // + units of the launch; 0 without shared-prefix groups)
+  int slot_stride;
 };
 
 // Pool formats of the kernel: CT 0 = bf16, 1 = FP8 e4m3 (per-tensor scale),
@@ -220,18 +223,22 @@ __host__ __device__ __forceinline__ int tc_unit_parts(const int* cstart, int u, 
   const int a = cstart[u], b = cstart[u + 1];
   return a < b ? cta_of_chunk(b - 1, T, n) - cta_of_chunk(a, T, n) + 1 : 0;
 }
-// Partial states of sequence s, and the slot CTA `cta` writes for it from
-// unit u (one of s's units, holding chunks in that CTA).
-__host__ __device__ __forceinline__ int tc_seq_parts(const int* cstart, int s, int m, long long T,
-                                                     int n) {
-  const int pu = tc_unit_parts(cstart, tc_private_unit(s, m), T, n);
-  return m == 1 ? pu : pu + tc_unit_parts(cstart, tc_shared_unit(s, m), T, n);
-}
-__host__ __device__ __forceinline__ int tc_part_slot(const int* cstart, int s, int u, int m,
-                                                     int cta, long long T, int n) {
-  const int base = (m > 1 && u != tc_shared_unit(s, m))
-                       ? tc_unit_parts(cstart, tc_shared_unit(s, m), T, n) : 0;
-  return base + cta - cta_of_chunk(cstart[u], T, n);
+// Partial slots of sequence s in decode (CTA i's partition over unit u
+// writes member r's partials to slot r * stride + i + u, r being s's index
+// among the unit's sequences: 0 but in a shared unit): (base, count) of its
+// private unit, then of its group's shared unit (count 0 in plain mode).
+__host__ __device__ __forceinline__ int4 tc_seq_meta(const int* cstart, int s, int m,
+                                                     long long T, int n, int stride) {
+  const int up = tc_private_unit(s, m);
+  const int np = tc_unit_parts(cstart, up, T, n);
+  int4 r = make_int4(np ? cta_of_chunk(cstart[up], T, n) + up : 0, np, 0, 0);
+  if (m > 1) {
+    const int us = tc_shared_unit(s, m);
+    const int ns = tc_unit_parts(cstart, us, T, n);
+    r.z = ns ? (s % m) * stride + cta_of_chunk(cstart[us], T, n) + us : 0;
+    r.w = ns;
+  }
+  return r;
 }
 
 template <int D, int HPC, int NS, int CT = 0, bool B8 = false, bool SH = false>
@@ -398,31 +405,24 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
   if (warp == HPC && cb < ce) tile_rows(cb, row);
   if constexpr (!SH) pdl_wait_primary();
 
-  // ---- bookkeeping: partial counts and zero outputs of empty sequences
-  for (int s = tid; s < S; s += C::THREADS) {
-    const int up = tc_private_unit(s, M);
-    const int a = cstart[up], b = cstart[up + 1];
-    const int np = SH ? tc_seq_parts(cstart, s, M, T, n) : (a < b ? 1 : 0);
-    if (np == 0) {
+  // ---- bookkeeping (sequence s by CTA s mod grid): partial slots of each
+  // output row, and zero outputs of empty sequences
+  for (int s = cta + tid * (int)gridDim.x; s < S; s += C::THREADS * (int)gridDim.x) {
+    const int4 mt = tc_seq_meta(cstart, s, M, T, n, p.slot_stride);
+    if (mt.y + mt.w == 0) {
       // empty context: zero output (decode); a sequence without query rows
       // has no output
-      const int owner = a < T ? cta_of_chunk(a, T, n) : n - 1;
-      if (owner == cta && cu == nullptr) {
-        if (group == 0) p.ws.nparts[s] = 0;
+      if (cu == nullptr) {
+        if (group == 0) p.ws.meta[s] = mt;
         __nv_bfloat16* o = p.out + ((int64_t)s * H_q + head0 * G) * D;
         for (int i = 0; i < HPC * G * D; ++i) o[i] = __float2bfloat16_rn(0.f);
       }
     } else if (group == 0) {
-      // written by the first CTA of the sequence's private unit (of its
-      // group's shared unit when the private one is empty)
-      const int uo = a < b ? up : tc_shared_unit(s, M);
-      if (cta_of_chunk(cstart[uo], T, n) == cta) {
-        const int parts = tc_seq_parts(cstart, s, M, T, n);
-        if (cu == nullptr) {
-          p.ws.nparts[s] = parts;
-        } else {
-          for (int r = cu[s]; r < cu[s + 1]; ++r) p.ws.nparts[r] = parts;
-        }
+      if (cu == nullptr) {
+        p.ws.meta[s] = mt;
+      } else {
+        // several query rows: row r's partial p in slot r * pmax + p
+        for (int r = cu[s]; r < cu[s + 1]; ++r) p.ws.meta[r] = make_int4(r * p.ws.pmax, mt.y, 0, 0);
       }
     }
   }
@@ -960,9 +960,19 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
           const int row = (qr0 + cc / G) * H_q + j * G + cc % G;
           // the column's sequence: its query row in decode; the unit's
           // sequence for several query tokens per sequence
-          const int sq = cu ? u : (int)(row / H_q);
-          const int np = tc_seq_parts(cstart, sq, M, T, n);
-          const int part = tc_part_slot(cstart, sq, u, M, cta, T, n);
+          // its partial slot: member * stride + CTA + unit in decode; query
+          // row * Pmax + the partition's index within the sequence for several
+          // query tokens
+          int np, slot;
+          if (cu == nullptr) {
+            const int4 mt = tc_seq_meta(cstart, row / H_q, M, T, n, p.slot_stride);
+            np = mt.y + mt.w;
+            slot = (row / H_q - qr0) * p.slot_stride + cta + u;
+          } else {
+            np = tc_unit_parts(cstart, u, T, n);
+            const int part = cta - cta_of_chunk(a, T, n);
+            slot = part < p.ws.pmax ? (row / H_q) * p.ws.pmax + part : -1;
+          }
           const float lt = col ? lt1 : lt0;
           const float mm = col ? m1[nb] : m0[nb];
           if (np == 1) {
@@ -976,9 +986,9 @@ attn_tc_kernel(const __grid_constant__ TcParams p) {
               orow[d0] = __float2bfloat16_rn(o[nb][mt][col] * inv);
               orow[d1] = __float2bfloat16_rn(o[nb][mt][2 + col] * inv);
             }
-          } else if (part < p.ws.pmax) {
-            // partial of (query row, head) at ((row * Pmax + part) * H_q + head)
-            const int64_t pa = ((int64_t)(row / H_q) * p.ws.pmax + part) * H_q + row % H_q;
+          } else if (slot >= 0) {
+            // partial of (slot, head) at slot * H_q + head
+            const int64_t pa = (int64_t)slot * H_q + row % H_q;
             float* orow = p.ws.o + pa * D;
 #pragma unroll
             for (int mt = 0; mt < D / 16; ++mt) {

@@ -324,8 +324,8 @@ attn_prefill_kernel(const __grid_constant__ PfParams p) {
     // partial state of this key range: unnormalised o, running max m (base
     // 2), row sum l; an empty range leaves (-inf, 0, 0), which merges as 0
     if (sp == 0 && t4 == 0) {
-      if (va) p.ws.nparts[q0 + ia] = nsp;
-      if (vb) p.ws.nparts[q0 + ib] = nsp;
+      if (va) p.ws.meta[q0 + ia] = make_int4((q0 + ia) * p.ws.pmax, nsp, 0, 0);
+      if (vb) p.ws.meta[q0 + ib] = make_int4((q0 + ib) * p.ws.pmax, nsp, 0, 0);
     }
     if (va) {
       const int64_t base = ((int64_t)(q0 + ia) * p.ws.pmax + sp) * p.H_q + ha;

@@ -6,8 +6,9 @@
 namespace pkv {
 
 // ===========================================================================
-// Split-K reduce: one warp per (sequence, query head); 8 warps per CTA.
-// For a sequence with P >= 2 partials (m_p, l_p, o_p):
+// Split-K reduce: one warp per (output row, query head); 8 warps per CTA.
+// For a row with P >= 2 partials (m_p, l_p, o_p), in the slots meta[row]
+// lists:
 //   M = max_p m_p,  l = sum_p l_p 2^(m_p - M),
 //   out = sum_p o_p 2^(m_p - M) / l
 // (the rescaling identity of the online softmax).  Lane i owns D/32
@@ -46,22 +47,22 @@ attn_reduce_kernel(Workspace ws, int S, int H_q, T* __restrict__ out) {
   const long long pair = (long long)blockIdx.x * kReduceWarps + warp;
   if (pair >= (long long)S * H_q) return;
   const int s = (int)(pair / H_q), h = (int)(pair - (long long)s * H_q);
-  int np = ws.nparts[s];
+  const int4 mt = ws.meta[s];          // partial slots: mt.x .. + mt.y, mt.z .. + mt.w
+  const int np = mt.y + mt.w;
   if (np <= 1) return;
-  if (np > ws.pmax) {   // cannot happen with lengths clamped to the bound; never read past it
-    if (lane == 0) record_error(PKV_DEVERR_CONTEXT_LEN);
-    np = ws.pmax;
-  }
-  const int64_t base = (int64_t)s * ws.pmax * H_q + h;   // partial p at base + p * H_q
+  // partial p of the row -> its (m, l) index; the output index is that * D
+  auto idx = [&](int p) -> int64_t {
+    return (int64_t)(p < mt.y ? mt.x + p : mt.z + (p - mt.y)) * H_q + h;
+  };
+  const int lv = lane * V;
   if (np <= kReduceFast) {
     // few partials (the common case): the (m, l) pairs and the partial
     // outputs are all loaded at once, so the merge costs one round trip
-    const float2 ml = lane < np ? ws.ml[base + (int64_t)lane * H_q] : make_float2(-INFINITY, 0.f);
+    const float2 ml = lane < np ? ws.ml[idx(lane)] : make_float2(-INFINITY, 0.f);
     float v[kReduceFast][V];
-    const float* o0 = ws.o + base * D + lane * V;
 #pragma unroll
     for (int u = 0; u < kReduceFast; ++u)
-      if (u < np) load_f<V>(o0 + (int64_t)u * H_q * D, v[u]);
+      if (u < np) load_f<V>(ws.o + idx(u) * D + lv, v[u]);
     const float M = warp_max(ml.x);
     const float w = lane < np ? exp2f(ml.x - M) : 0.f;
     const float inv = 1.f / warp_sum(ml.y * w);
@@ -76,17 +77,17 @@ attn_reduce_kernel(Workspace ws, int S, int H_q, T* __restrict__ out) {
         for (int e = 0; e < V; ++e) acc[e] = fmaf(wu, v[u][e], acc[e]);
       }
     }
-    T* dst = out + ((int64_t)s * H_q + h) * D + lane * V;
+    T* dst = out + ((int64_t)s * H_q + h) * D + lv;
 #pragma unroll
     for (int e = 0; e < V; ++e) dst[e] = from_f32<T>(acc[e]);
     return;
   }
   float M = -INFINITY;
-  for (int p = lane; p < np; p += 32) M = fmaxf(M, ws.ml[base + (int64_t)p * H_q].x);
+  for (int p = lane; p < np; p += 32) M = fmaxf(M, ws.ml[idx(p)].x);
   M = warp_max(M);
   float lsum = 0.f;
   for (int p = lane; p < np; p += 32) {
-    const float2 ml = ws.ml[base + (int64_t)p * H_q];
+    const float2 ml = ws.ml[idx(p)];
     lsum += ml.y * exp2f(ml.x - M);
   }
   lsum = warp_sum(lsum);
@@ -95,21 +96,20 @@ attn_reduce_kernel(Workspace ws, int S, int H_q, T* __restrict__ out) {
   float acc[V];
 #pragma unroll
   for (int e = 0; e < V; ++e) acc[e] = 0.f;
-  const float* o0 = ws.o + base * D + lane * V;
   for (int p0 = 0; p0 < np; p0 += 32) {
     const int pl = p0 + lane;
-    const float w = pl < np ? exp2f(ws.ml[base + (int64_t)pl * H_q].x - M) * inv : 0.f;
+    const float w = pl < np ? exp2f(ws.ml[idx(pl)].x - M) * inv : 0.f;
     const int cnt = min(32, np - p0);
 #pragma unroll 4
     for (int u = 0; u < cnt; ++u) {
       const float wu = __shfl_sync(0xffffffffu, w, u);
       float v[V];
-      load_f<V>(o0 + (int64_t)(p0 + u) * H_q * D, v);
+      load_f<V>(ws.o + idx(p0 + u) * D + lv, v);
 #pragma unroll
       for (int e = 0; e < V; ++e) acc[e] = fmaf(wu, v[e], acc[e]);
     }
   }
-  T* dst = out + ((int64_t)s * H_q + h) * D + lane * V;
+  T* dst = out + ((int64_t)s * H_q + h) * D + lv;
 #pragma unroll
   for (int e = 0; e < V; ++e) dst[e] = from_f32<T>(acc[e]);
 }

@@ -129,21 +129,23 @@ int check_stream_k() {
   return errors;
 }
 
-// Shared-prefix units: for random batches (groups of m = 16 / G sequences,
-// shared lengths glen[g] that are multiples of 16 and at most the shortest
-// member's length, 0 for a group of one) and grid sizes, every CTA's runs of
-// one unit are that CTA's partitions; each member of the unit gets the slot
-// `slot(...)`.  Checked: a sequence's slots are exactly 0 .. parts - 1, each
-// once; slots stay below the plan's Pmax (twice the plain bound); the tokens
-// the partitions cover add up to the sequence's length.  `slot` is
-// pkv::tc_part_slot, or a planted variant that must fail.
+// Partial slots: for random batches (plain, or groups of m = 16 / G
+// sequences with shared lengths glen[g] that are multiples of 16 and at most
+// the shortest member's length, 0 for a group of one) and random grids, every
+// run of one unit inside a CTA's chunk range is a partition, which gives each
+// member of the unit the slot `slot(cta, unit, member, stride)`.  Checked: the
+// slots of all partitions are distinct; a sequence's slots are exactly the
+// ranges tc_seq_meta lists; slots stay below the plan's bound ((items +
+// units) per member region); the tokens a sequence's partitions cover add up
+// to its length.  `slot` is member * stride + CTA + unit, or a planted
+// variant that must fail.
 template <typename Slot>
-int check_shared_units(Slot slot, int trials) {
+int check_partial_slots(Slot slot, int trials) {
   int errors = 0;
   std::mt19937 rng(11);
   for (int trial = 0; trial < trials; ++trial) {
     const int G = 1 << (rng() % 4);
-    const int m = trial % 5 == 0 ? 1 : 16 / G;    // plain mode too
+    const int m = trial % 3 == 0 ? 1 : 16 / G;
     const int S = 1 + (int)(rng() % 40);
     const int max_len = 1 + (int)(rng() % 2000);
     std::vector<int> len(S), glen((S + m - 1) / m, 0);
@@ -176,11 +178,13 @@ int check_shared_units(Slot slot, int trials) {
     if (T == 0) continue;
     const int grid = 1 + (int)(rng() % 160);
     const int n = (int)(T < grid ? T : grid);
-    const int pmax = std::max(1, std::min(grid, (max_len + 15) / 16)) * (m > 1 ? 2 : 1);
+    const int stride = grid + NU;   // slots per member region
+    const long long bound = (long long)stride * m;
     std::vector<std::vector<int>> slots(S);
     std::vector<long long> covered(S, 0);
-    for (int cta = 0; cta < n; ++cta) {
-      const int cb = (int)((long long)cta * T / n), ce = (int)((long long)(cta + 1) * T / n);
+    std::vector<int> seen;
+    for (int i = 0; i < n; ++i) {
+      const int cb = (int)((long long)i * T / n), ce = (int)((long long)(i + 1) * T / n);
       for (int c = cb; c < ce; ++c) {
         const int u = pkv::seq_of_chunk(cstart.data(), NU, c);
         if (c != cb && c != cstart[u]) continue;            // not a partition start
@@ -188,19 +192,25 @@ int check_shared_units(Slot slot, int trials) {
         const long long tok = std::min<long long>(uend[u], ut0[u] + (long long)(last - cstart[u]) * 16) -
                               (ut0[u] + (long long)(c - cstart[u]) * 16);
         for (int r = 0; r < urows[u]; ++r) {
-          const int s = us0[u] + r;
-          slots[s].push_back(slot(cstart.data(), s, u, m, cta, T, n));
-          covered[s] += tok;
+          const int x = slot(i, u, r, m > 1 ? stride : 0);
+          seen.push_back(x);
+          if (x < 0 || x >= bound) ++errors;
+          slots[us0[u] + r].push_back(x);
+          covered[us0[u] + r] += tok;
         }
       }
     }
+    std::sort(seen.begin(), seen.end());
+    if (std::adjacent_find(seen.begin(), seen.end()) != seen.end()) ++errors;   // shared slot
     for (int s = 0; s < S; ++s) {
-      const int parts = pkv::tc_seq_parts(cstart.data(), s, m, T, n);
+      const int4 mt = pkv::tc_seq_meta(cstart.data(), s, m, T, n, m > 1 ? stride : 0);
+      std::vector<int> want;
+      for (int q = 0; q < mt.y; ++q) want.push_back(mt.x + q);
+      for (int q = 0; q < mt.w; ++q) want.push_back(mt.z + q);
       std::vector<int> got = slots[s];
       std::sort(got.begin(), got.end());
-      bool ok = (int)got.size() == parts && covered[s] == len[s];
-      for (int i = 0; ok && i < (int)got.size(); ++i) ok = got[i] == i && got[i] < pmax;
-      if (!ok) ++errors;
+      std::sort(want.begin(), want.end());
+      if (got != want || covered[s] != len[s]) ++errors;
     }
   }
   return errors;
@@ -209,16 +219,17 @@ int check_shared_units(Slot slot, int trials) {
 int main() {
   int errors = check_stream_k();
   {
-    const int e = check_shared_units(
-        [](const int* cs, int s, int u, int m, int cta, long long T, int n) {
-          return pkv::tc_part_slot(cs, s, u, m, cta, T, n);
-        }, 6000);
-    // planted mistake: private-unit slots without the shared unit's offset
-    const int planted = check_shared_units(
-        [](const int* cs, int s, int u, int m, int cta, long long T, int n) {
-          return cta - pkv::cta_of_chunk(cs[u], T, n);
-        }, 600);
-    if (e) std::printf("shared-prefix unit errors: %d\n", e);
+    const int e = check_partial_slots(
+        [](int cta, int unit, int member, int stride) { return member * stride + cta + unit; },
+        6000);
+    // planted mistakes: the members of a shared unit in one slot; the CTA
+    // alone as the slot (units of one CTA collide)
+    const int planted1 = check_partial_slots(
+        [](int cta, int unit, int, int) { return cta + unit; }, 600);
+    const int planted2 = check_partial_slots(
+        [](int cta, int, int member, int stride) { return member * stride + cta; }, 600);
+    const int planted = planted1 && planted2;
+    if (e) std::printf("partial slot errors: %d\n", e);
     if (planted == 0) std::printf("planted slot mistake not caught\n");
     errors += e + (planted == 0);
   }
@@ -231,6 +242,6 @@ int main() {
     std::printf("errors: %d\n", errors);
     return 1;
   }
-  std::printf("layout ok: 36 configurations; stream-K ok; shared-prefix units ok\n");
+  std::printf("layout ok: 36 configurations; stream-K ok; partial slots ok\n");
   return 0;
 }

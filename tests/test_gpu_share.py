@@ -149,9 +149,14 @@ def test_shared_block_id_out_of_range_reported(ops):
 
 def test_workspace_and_launch_count(ops):
     S, H_q, H_kv, D, K, L = 1024, 32, 8, 128, 16, 3072
-    plain = ops.attention_workspace_bytes(S, H_q, H_kv, D, K, L, torch.bfloat16)
-    shared = ops.attention_workspace_bytes(S, H_q, H_kv, D, K, L, torch.bfloat16,
+    # the tensor-core plans (the automatic query also covers the CUDA-core
+    # plan a misaligned pool would take): shared units keep one region of
+    # partial slots per member, and the groups' shared lengths
+    plain = ops.attention_workspace_bytes(S, H_q, H_kv, D, K, L, torch.bfloat16, kernel=1)
+    shared = ops.attention_workspace_bytes(S, H_q, H_kv, D, K, L, torch.bfloat16, kernel=1,
                                            share_prefix=True)
     assert shared > plain
+    assert ops.attention_workspace_bytes(S, H_q, H_kv, D, K, L, torch.bfloat16,
+                                         share_prefix=True) >= shared
     assert ops.attention_launch_count(S, H_q, H_kv, D, K, L, torch.bfloat16,
                                       share_prefix=True) == 3

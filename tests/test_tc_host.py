@@ -7,10 +7,10 @@ producer's 4-D TMA boxes land, that each row keeps its swizzle phase, and that
 the bytes a stage expects equal the bytes delivered; then, by brute force,
 that the chunk-to-CTA and chunk-to-sequence maps match their definitions and
 that no sequence spans more CTAs than the partial slots the plan reserves;
-and, for shared-prefix units (a group's shared tokens, then each member's
-own), that every sequence's partial slots are 0 .. parts - 1 exactly once,
-within the plan's bound, covering its whole context (a planted slot mistake
-must fail).
+and, over plain and shared-prefix units, that the partial slots of all
+partitions are distinct, match each sequence's listed ranges, stay within
+the workspace bound and cover its whole context (planted slot mistakes must
+fail).
 Built with nvcc for the host; no GPU is needed.
 """
 
@@ -44,4 +44,4 @@ def test_stage_layout_and_stream_k_bookkeeping(tmp_path):
     r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
     assert r.returncode == 0, r.stdout + r.stderr
     assert "layout ok" in r.stdout and "stream-K ok" in r.stdout
-    assert "shared-prefix units ok" in r.stdout
+    assert "partial slots ok" in r.stdout

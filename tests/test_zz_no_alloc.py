@@ -63,8 +63,10 @@ def test_noalloc_matches_regular_entry_point(ops, case):
 
 
 def test_noalloc_refuses_sizes_beyond_its_scratch(ops):
-    S, H_q, H_kv, D, K, L = 128, 32, 8, 128, 16, 8192
-    need = ops.attention_workspace_bytes(S, H_q, H_kv, D, K, L, torch.bfloat16)
+    # the CUDA-core kernel keeps one slot per 512-token partition of every
+    # sequence: 128 sequences of 131072 tokens need far more than the array
+    S, H_q, H_kv, D, K, L = 128, 32, 8, 128, 16, 131072
+    need = ops.attention_workspace_bytes(S, H_q, H_kv, D, K, L, torch.bfloat16, kernel=2)
     assert need > ops.NOALLOC_SCRATCH_BYTES
     dev = torch.device("cuda", 0)
     q = torch.zeros((S, H_q, D), dtype=torch.bfloat16, device=dev)
@@ -72,4 +74,5 @@ def test_noalloc_refuses_sizes_beyond_its_scratch(ops):
     bt = torch.zeros((S, L // K), dtype=torch.int32, device=dev)
     lens = torch.full((S,), L, dtype=torch.int32, device=dev)
     with pytest.raises(ops.PagedKVError, match="scratch"):
-        ops.paged_attention_decode_noalloc(q, kc, kc, bt, lens, 0.1, torch.empty_like(q), 8192)
+        ops.paged_attention_decode_noalloc(q, kc, kc, bt, lens, 0.1, torch.empty_like(q), L,
+                                           kernel=2)
